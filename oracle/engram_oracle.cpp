@@ -171,6 +171,12 @@ int oracle_gate_fwd(const double* x, const double* kv, const double* w,
 // those quantities, as the API does, and applies the chain rule through
 //   out = X + gate*v, gate = sigmoid(sq), sq = signed sqrt with clamp,
 //   dot = sum_i xh_i w_i kh_i, xh = x*rstd_X, kh = k*rstd_key.
+// The saved gate is the factor that multiplied v (it enters grad_v and
+// dgate = sum g*v); the gate's own derivative sigmoid'(sq) =
+// sigmoid(sq)*sigmoid(-sq) is evaluated at sq recomputed from the saved dot,
+// because a saved fp32 gate near 1 keeps too few bits of 1 - gate (and is
+// exactly 1 once |sq| > ~17).  A zero saved gate is a masked token: its gate
+// path carries no gradient (out = X there).
 // The clamp's derivative is 1 where |dot| >= clamp and 0 below (a tie passes
 // through, as a clamp_min does under autograd).  The RMS-norm backward is the
 // generic one: dx = rstd*(dxh - xh*mean(dxh*xh)), exact also for eps > 0.
@@ -201,10 +207,10 @@ int oracle_gate_bwd(const double* x, const double* kv, const double* w,
             double dgate = 0.0;
             for (int64_t i = 0; i < d; ++i) dgate += g[i] * v[i];
             for (int64_t i = 0; i < d; ++i) gv[i] += gate * g[i];
-            // gate = sigmoid(sq)
-            const double dsq = dgate * gate * (1.0 - gate);
-            // sq = sign(dot) * sqrt(max(|dot|, clamp))
+            // gate = sigmoid(sq), sq = sign(dot) * sqrt(max(|dot|, clamp))
             const double ad = std::fabs(dot);
+            const double sq = sgn(dot) * std::sqrt(std::fmax(ad, clamp));
+            const double dsq = (gate == 0.0) ? 0.0 : dgate * sigmoid(sq) * sigmoid(-sq);
             const double ddot = (ad >= clamp) ? dsq * 0.5 / std::sqrt(ad) : 0.0;
             ddot_all[static_cast<size_t>(n * S + s)] = ddot;
             // dot = sum xh * w * kh

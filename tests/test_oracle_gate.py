@@ -268,3 +268,31 @@ def test_clamped_region_has_zero_gate_derivative():
     assert np.array_equal(gx, g)
     assert np.all(gkv[:, :4 * d] == 0.0)
     assert np.all(gw == 0.0)
+
+
+def test_saturated_gate_keeps_its_derivative_through_fp32_saved_state():
+    # a key close to X at d = 64 gives dot ~ 60, sq ~ 7.8, 1 - gate ~ 4e-4.
+    # An fp32 saved gate keeps 1 - gate only to ~1e-4 relative; the backward
+    # evaluates sigmoid'(sq) from the saved dot, so fp32 and fp64 saved state
+    # give the same gradients to fp32 precision of dot and rstd.
+    d = 64
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((3, 4, d))
+    kv = rng.standard_normal((3, 5 * d))
+    for s in range(4):
+        kv[:, s * d:(s + 1) * d] = x[:, s] + 0.3 * rng.standard_normal((3, d))
+    w = 1.0 + 0.1 * rng.standard_normal((4, d))
+    g = rng.standard_normal((3, 4, d))
+    _, saved = oracle.gate_fwd(x, kv, w)
+    assert np.all(saved[..., 1] > 40)
+    saved32 = saved.astype(np.float32).astype(np.float64)
+    lost = np.abs((1.0 - saved32[..., 0]) / (1.0 - saved[..., 0]) - 1.0)
+    assert np.max(lost) > 1e-5   # fp32 lost those bits
+    r64 = oracle.gate_bwd(x, kv, w, saved, g)
+    r32 = oracle.gate_bwd(x, kv, w, saved32, g)
+    # compared on the scale of each tensor (the gate path of grad_x is
+    # grad_x - grad_out); the old 1 - gate form would be off by `lost`
+    pairs = [(r64[0] - g, r32[0] - g), (r64[1][:, :4 * d], r32[1][:, :4 * d]),
+             (r64[1][:, 4 * d:], r32[1][:, 4 * d:]), (r64[2], r32[2])]
+    for a, b in pairs:
+        assert np.max(np.abs(a - b)) <= 2e-6 * np.max(np.abs(a))
