@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of the Engram gate on GB300 through the C ABI (libengram.so).
+
+Workload (one step): saved-state gate forward + backward, N = 8192 tokens
+(the backward's maximum), S = 4 streams, d = 5120, bf16 X/KV ~N(0,1), fused
+fp32 weight 1 + 0.1 N(0,1), mask ~Bernoulli(0.9), grad_out ~N(0,1), eps
+1e-20, seed 1.  Inputs stay resident in HBM; one step reads and writes
+1.85 GB, larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `value` is tokens/s over all ranks (replicas:
+every rank runs the full workload on its own GPU, no collective on the data
+path).  `--impl reference` times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+N_TOK, S, D = 8192, 4, 5120
+FWD_BYTES_PER_TOKEN = 4 * D * 2 + 5 * D * 2 + 1 + 4 * D * 2 + 64      # 133,185
+BWD_BYTES_PER_TOKEN = 4 * D * 2 + 5 * D * 2 + 64 + 4 * D * 2 + 4 * D * 2 + 5 * D * 2  # 225,344
+FWD_FIXED = 4 * D * 4                 # weight
+BWD_FIXED = 2 * 4 * D * 4             # weight + grad_weight
+METRIC = "Engram gate fwd+bwd tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+WORKLOAD = ("saved-state gate fwd+bwd, N=8192, S=4, d=5120, bf16 X/KV ~N(0,1), "
+            "weight 1+0.1N(0,1), mask~Bernoulli(0.9), grad_out ~N(0,1), eps 1e-20, seed 1")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(profile_md, sources):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current sources; else None."""
+    path = os.path.join(ROOT, "profiles", profile_md)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not m or not t or m.group(1) != source_hash(sources):
+        return None
+    return int(t.group(1))
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append(parts)
+            except ValueError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        smax = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def time_region(torch, fn, reps, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(reps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / reps
+
+
+def graph_of(torch, fn, stream):
+    fn()  # one-time per-device set-up happens outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def op_entry(ms, nbytes, peak):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 5), "algorithmic_bytes": int(nbytes), "GB_s": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / peak, 4)}
+
+
+def extra_ops(torch, eg, inputs_mod, stream, peak):
+    """Each hot-path op at its own configuration, CUDA-graph replayed, inputs
+    larger than L2 (no flush needed)."""
+    ops = {}
+    s = stream
+    # forward sweep, N = 262144, per-token sigma ~ LogUniform(1e-2, 1e2), mask Bernoulli(0.5)
+    N = 262144
+    inp = inputs_mod.gate_inputs(N, 103, device="cuda", mask="bern0.5", sigma="loguniform",
+                                 with_grad=False)
+    out = torch.empty_like(inp["x"])
+    saved = torch.empty((N, 4, 4), device="cuda", dtype=torch.float32)
+    fn = lambda: eg.engram_gate_fwd(inp["x"], inp["kv"], inp["weight"], inp["mask"], out, saved,
+                                    stream=s)
+    g = graph_of(torch, fn, s)
+    for _ in range(3):
+        g.replay()
+    ms = time_region(torch, g.replay, 10, s)
+    ops["gate_fwd_N262144"] = op_entry(ms, N * FWD_BYTES_PER_TOKEN + FWD_FIXED, peak)
+    del inp, out, saved, g
+    torch.cuda.empty_cache()
+    # GateConv, two configurations
+    for (M, T, d, hs, vs, name) in ((4, 4096, 4096, 1.0, 1.0, "gateconv_M4_T4096_d4096"),
+                                    (8, 8192, 7168, 10.0, 0.1 ** 0.5, "gateconv_M8_T8192_d7168")):
+        ci = inputs_mod.gateconv_inputs(M, T, d, 31, device="cuda", h_scale=hs, v_std=vs)
+        res = [torch.empty_like(ci["H"]), torch.empty_like(ci["H"])] + \
+            [torch.empty((M, T), device="cuda", dtype=torch.float32) for _ in range(4)]
+        grads = [torch.empty_like(ci["H"]) for _ in range(3)] + \
+            [torch.empty(d, device="cuda"), torch.empty(d, device="cuda"),
+             torch.empty((4, d), device="cuda")]
+        ws = torch.empty(eg.engram_gateconv_bwd_workspace_size(M, T, d), device="cuda",
+                         dtype=torch.uint8)
+        f = lambda: eg.engram_gateconv_fwd(ci["H"], ci["k"], ci["v"], ci["rms_w_h"],
+                                           ci["rms_w_v"], ci["conv_w"], *res, stream=s)
+        b = lambda: eg.engram_gateconv_bwd(ci["dY"], ci["H"], ci["k"], ci["v"], ci["rms_w_h"],
+                                           ci["rms_w_v"], ci["conv_w"], *res[1:], *grads, ws,
+                                           stream=s)
+        gf, gb = graph_of(torch, f, s), graph_of(torch, b, s)
+        for _ in range(3):
+            gf.replay()
+            gb.replay()
+        tok = M * T
+        ops[name + "_fwd"] = op_entry(time_region(torch, gf.replay, 10, s),
+                                      tok * (10 * d + 16) + 24 * d, peak)
+        ops[name + "_bwd"] = op_entry(time_region(torch, gb.replay, 10, s),
+                                      tok * (16 * d + 16) + 48 * d, peak)
+        del ci, res, grads, ws, gf, gb
+        torch.cuda.empty_cache()
+    return ops
+
+
+def cpu_baseline(seconds=10.0):
+    """The fp64 oracle (as it stands) on a bounded sample of the workload."""
+    import oracle
+    from engram_memory_gating_gb300.inputs import gate_inputs
+    oracle.build()
+
+    def run(n):
+        inp = gate_inputs(n, 1, mask="bern0.9")
+        x, kv, w, m, g = f64_inputs(inp)
+        t0 = time.perf_counter()
+        _, saved = oracle.gate_fwd(x, kv, w, m)
+        oracle.gate_bwd(x, kv, w, saved, g)
+        return time.perf_counter() - t0
+
+    t = run(16)
+    n = int(max(16, min(4096, 16 * seconds / max(t, 1e-6))))
+    t = run(n)
+    return {"value": round(n / t, 2), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} tokens of the N=8192 workload (fwd+bwd, fp64), {t:.1f} s"}
+
+
+def f64_inputs(inp):
+    """bf16 / fp32 host tensors -> exact float64 arrays (plus the mask bytes)."""
+    f = lambda t: t.double().numpy()
+    return (f(inp["x"]), f(inp["kv"]), f(inp["weight"]),
+            inp["mask"].numpy().astype("uint8"), f(inp["grad_out"]))
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from engram_memory_gating_gb300.inputs import gate_inputs
+    oracle.build()
+    inp = gate_inputs(64, 1, mask="bern0.9")
+    x, kv, w, m, g = f64_inputs(inp)
+
+    def step(n):
+        _, saved = oracle.gate_fwd(x[:n], kv[:n], w, m[:n])
+        oracle.gate_bwd(x[:n], kv[:n], w, saved, g[:n])
+
+    t0 = time.perf_counter()
+    step(4)
+    per_tok = (time.perf_counter() - t0) / 4
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(64, budget / max(per_tok, 1e-9))))
+    for _ in range(args.warmup):
+        step(n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(n)
+    el = time.perf_counter() - t0
+    value = args.steps * n / el
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "N": N_TOK, "S": S, "d": D,
+                       "sample_tokens_per_step": n},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s",
+                             "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{n} tokens of the workload per step"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-op sweep")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    import engram_memory_gating_gb300 as eg
+    from engram_memory_gating_gb300 import inputs as inputs_mod
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    eg.load()
+    peak, peak_kind = peaks()
+    stream = torch.cuda.Stream()
+
+    inp = inputs_mod.gate_inputs(N_TOK, 1, device="cuda", mask="bern0.9")
+    x, kv, w, mask, gout = inp["x"], inp["kv"], inp["weight"], inp["mask"], inp["grad_out"]
+    out = torch.empty_like(x)
+    saved = torch.empty((N_TOK, S, 4), device="cuda", dtype=torch.float32)
+    gx, gkv, gw = torch.empty_like(x), torch.empty_like(kv), torch.empty_like(w)
+    ws = torch.empty(eg.engram_gate_bwd_workspace_size(N_TOK), device="cuda", dtype=torch.uint8)
+
+    def fwd():
+        eg.engram_gate_fwd(x, kv, w, mask, out, saved, stream=stream)
+
+    def bwd():
+        eg.engram_gate_bwd(x, kv, w, saved, gout, gx, gkv, gw, ws, stream=stream)
+
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t_start.record(stream)
+        for i in range(K):
+            evs[i][0].record(stream)
+            fwd()
+            evs[i][1].record(stream)
+            bwd()
+            evs[i][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end) / K
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * N_TOK / (ms * 1e-3)
+    step_bytes = N_TOK * (FWD_BYTES_PER_TOKEN + BWD_BYTES_PER_TOKEN) + FWD_FIXED + BWD_FIXED
+    fwd_bytes = N_TOK * FWD_BYTES_PER_TOKEN + FWD_FIXED
+    bwd_bytes = N_TOK * BWD_BYTES_PER_TOKEN + BWD_FIXED
+    bwd_gbs = bwd_bytes / (bwd_ms * 1e-3) / 1e9
+    fwd_gbs = fwd_bytes / (fwd_ms * 1e-3) / 1e9
+    csrc = "engram_memory_gating_gb300/csrc/"
+    traffic = profile_traffic("gate_bwd_n8192.md",
+                              [csrc + "gate_bwd.cu", csrc + "common.cuh", csrc + "engram_abi.cu"])
+
+    # ---- end to end through the public API with host buffers (pinned)
+    h = {k: v.cpu().pin_memory() for k, v in inp.items()}
+    ho = {"out": torch.empty_like(h["x"]).pin_memory(),
+          "saved": torch.empty((N_TOK, S, 4), dtype=torch.float32).pin_memory(),
+          "gx": torch.empty_like(h["x"]).pin_memory(), "gkv": torch.empty_like(h["kv"]).pin_memory(),
+          "gw": torch.empty_like(h["weight"]).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for t in ho.values())
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for k in ("x", "kv", "weight", "mask", "grad_out"):
+                inp[k].copy_(h[k], non_blocking=True)
+        fwd()
+        bwd()
+        with torch.cuda.stream(stream):
+            ho["out"].copy_(out, non_blocking=True)
+            ho["saved"].copy_(saved, non_blocking=True)
+            ho["gx"].copy_(gx, non_blocking=True)
+            ho["gkv"].copy_(gkv, non_blocking=True)
+            ho["gw"].copy_(gw, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    Ke = max(5, min(50, K // 20))
+    e2e_ms = time_region(torch, e2e_step, Ke, stream)
+    if dist:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    launch = {"fwd": eg.engram_launch_info(0, N_TOK), "bwd": eg.engram_launch_info(1, N_TOK)}
+    ops = None
+    if not args.no_extra and rank == 0:
+        ops = {"gate_fwd_N8192": op_entry(fwd_ms, fwd_bytes, peak),
+               "gate_bwd_N8192": op_entry(bwd_ms, bwd_bytes, peak)}
+        del h, ho
+        ops.update(extra_ops(torch, eg, inputs_mod, stream, peak))
+    err = eg.engram_device_error()
+    if dist:
+        dist.barrier()
+    if rank != 0:
+        return
+    cpu = None if (args.no_cpu or world > 1) else cpu_baseline()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "N": N_TOK, "S": S, "d": D,
+                   "l2": "inputs larger than L2 (1.85 GB read+written per step); no flush",
+                   "parallelism": f"replicas x{world}", "launch": launch},
+        "hbm_GB_s": round(step_bytes / (ms * 1e-3) / 1e9, 1),
+        "roofline": {"kernel": "engram_gate_bwd (gate_bwd_kernel + wreduce_kernel), N=8192",
+                     "bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(bwd_gbs / peak, 4),
+                     "traffic": traffic},
+        "roofline_fwd": {"kernel": "engram_gate_fwd (gate_fwd_kernel), N=8192", "bound": "hbm",
+                         "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(fwd_gbs / peak, 4)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * N_TOK / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+        "device_error_flags": err,
+    }
+    if ops is not None:
+        line["ops"] = ops
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

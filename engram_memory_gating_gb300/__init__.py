@@ -1,0 +1,260 @@
+"""Python binding of libengram.so (the GB300 Engram gate library).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in include/engram.h.  PyTorch provides
+device memory and the current stream.  There is no CPU fallback: if the
+library is missing or the device is not sm_103, calls raise.
+
+Entry points (same names as the C ABI):
+  engram_gate_fwd, engram_gate_bwd, engram_gate_bwd_workspace_size,
+  engram_gateconv_fwd, engram_gateconv_bwd, engram_gateconv_bwd_workspace_size,
+  engram_device_error, engram_launch_info.
+Convenience wrappers that allocate their outputs (like the eager wrappers of
+the cuDNN Frontend page): gate_forward, gate_backward, gateconv_forward,
+gateconv_backward.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from ._build import LIB as _LIB_PATH
+from ._build import build as _build_lib
+
+__all__ = [
+    "EngramError", "load", "build",
+    "engram_gate_fwd", "engram_gate_bwd", "engram_gate_bwd_workspace_size",
+    "engram_gateconv_fwd", "engram_gateconv_bwd", "engram_gateconv_bwd_workspace_size",
+    "engram_device_error", "engram_launch_info",
+    "gate_forward", "gate_backward", "gateconv_forward", "gateconv_backward",
+    "GATE_EPS", "GATECONV_EPS", "EXPORTED_SYMBOLS",
+]
+
+GATE_EPS = 1e-20     # default RMS-norm epsilon of the saved-state gate
+GATECONV_EPS = 1e-6  # default RMSNorm epsilon of GateConv
+D_GATE = 5120
+S_GATE = 4
+
+EXPORTED_SYMBOLS = (
+    "engram_status_string", "engram_gate_fwd", "engram_gate_bwd_workspace_size",
+    "engram_gate_bwd", "engram_gateconv_fwd", "engram_gateconv_bwd_workspace_size",
+    "engram_gateconv_bwd", "engram_device_error", "engram_launch_info",
+)
+
+_STATUS = {0: "ok", 1: "null pointer", 2: "misaligned pointer", 3: "size out of range",
+           4: "overlap", 5: "workspace too small", 6: "no usable sm_103 device",
+           7: "kernel launch failed"}
+
+
+class EngramError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: status {code} ({_STATUS.get(code, 'unknown')})")
+        self.code = code
+
+
+class _LaunchInfo(ctypes.Structure):
+    _fields_ = [("cluster", ctypes.c_int), ("threads", ctypes.c_int),
+                ("clusters", ctypes.c_int), ("stages", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libengram.so for sm_103a (nvcc) and return its path."""
+    return _build_lib(force=force)
+
+
+def load(path: str | None = None):
+    """Load libengram.so (building it first if it is absent or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _LIB_PATH
+        if path is None:
+            _build_lib()
+        if not os.path.exists(p):
+            raise RuntimeError(f"libengram.so not found at {p}")
+        lib = ctypes.CDLL(p)
+        P, I64, F, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        lib.engram_status_string.restype = ctypes.c_char_p
+        lib.engram_status_string.argtypes = [ctypes.c_int]
+        lib.engram_gate_fwd.argtypes = [P, P, P, P, P, P, I64, F, P]
+        lib.engram_gate_bwd_workspace_size.argtypes = [I64]
+        lib.engram_gate_bwd_workspace_size.restype = SZ
+        lib.engram_gate_bwd.argtypes = [P, P, P, P, P, P, P, P, P, SZ, I64, P]
+        lib.engram_gateconv_fwd.argtypes = [P] * 12 + [I64, I64, I64, F, P]
+        lib.engram_gateconv_bwd_workspace_size.argtypes = [I64, I64, I64]
+        lib.engram_gateconv_bwd_workspace_size.restype = SZ
+        lib.engram_gateconv_bwd.argtypes = [P] * 19 + [SZ, I64, I64, I64, F, P]
+        lib.engram_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        lib.engram_launch_info.argtypes = [ctypes.c_int, I64, I64, I64,
+                                           ctypes.POINTER(_LaunchInfo)]
+        for name in ("engram_gate_fwd", "engram_gate_bwd", "engram_gateconv_fwd",
+                     "engram_gateconv_bwd", "engram_device_error", "engram_launch_info"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        return ctypes.c_void_p(int(t))
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(fn, code):
+    if code != 0:
+        raise EngramError(fn, code)
+
+
+def _need(t, dtype, shape, name):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+# ------------------------------------------------------------ C ABI wrappers
+
+def engram_gate_fwd(x, kv, weight, mask, out, saved, eps: float = GATE_EPS, stream=None):
+    N = x.shape[0]
+    _need(x, torch.bfloat16, (N, S_GATE, D_GATE), "x")
+    _need(kv, torch.bfloat16, (N, (S_GATE + 1) * D_GATE), "kv")
+    _need(weight, torch.float32, (S_GATE, D_GATE), "weight")
+    _need(out, torch.bfloat16, (N, S_GATE, D_GATE), "out")
+    if mask is not None:
+        _need(mask, torch.bool, (N,), "mask")
+    if saved is not None:
+        _need(saved, torch.float32, (N, S_GATE, 4), "saved")
+    _check("engram_gate_fwd", load().engram_gate_fwd(
+        _ptr(x), _ptr(kv), _ptr(weight), _ptr(mask), _ptr(out), _ptr(saved), N,
+        float(eps), _stream(stream)))
+
+
+def engram_gate_bwd_workspace_size(N: int) -> int:
+    return int(load().engram_gate_bwd_workspace_size(int(N)))
+
+
+def engram_gate_bwd(x, kv, weight, saved, grad_out, grad_x, grad_kv, grad_weight, workspace,
+                    stream=None):
+    N = x.shape[0]
+    _need(saved, torch.float32, (N, S_GATE, 4), "saved")
+    _need(grad_out, torch.bfloat16, (N, S_GATE, D_GATE), "grad_out")
+    _need(grad_x, torch.bfloat16, (N, S_GATE, D_GATE), "grad_x")
+    _need(grad_kv, torch.bfloat16, (N, (S_GATE + 1) * D_GATE), "grad_kv")
+    _need(grad_weight, torch.float32, (S_GATE, D_GATE), "grad_weight")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("engram_gate_bwd", load().engram_gate_bwd(
+        _ptr(x), _ptr(kv), _ptr(weight), _ptr(saved), _ptr(grad_out), _ptr(grad_x),
+        _ptr(grad_kv), _ptr(grad_weight), _ptr(workspace), nbytes, N, _stream(stream)))
+
+
+def engram_gateconv_fwd(H, k, v, rms_w_h, rms_w_v, conv_w, Y, vhat, alpha, rrms_h, rrms_k,
+                        rrms_v, eps: float = GATECONV_EPS, stream=None):
+    M, T, d = H.shape
+    for t, n in ((H, "H"), (k, "k"), (v, "v"), (Y, "Y"), (vhat, "vhat")):
+        _need(t, torch.bfloat16, (M, T, d), n)
+    for t, n in ((alpha, "alpha"), (rrms_h, "rrms_h"), (rrms_k, "rrms_k"), (rrms_v, "rrms_v")):
+        _need(t, torch.float32, (M, T), n)
+    _need(rms_w_h, torch.float32, (d,), "rms_w_h")
+    _need(rms_w_v, torch.float32, (d,), "rms_w_v")
+    _need(conv_w, torch.float32, (4, d), "conv_w")
+    _check("engram_gateconv_fwd", load().engram_gateconv_fwd(
+        _ptr(H), _ptr(k), _ptr(v), _ptr(rms_w_h), _ptr(rms_w_v), _ptr(conv_w), _ptr(Y),
+        _ptr(vhat), _ptr(alpha), _ptr(rrms_h), _ptr(rrms_k), _ptr(rrms_v), M, T, d,
+        float(eps), _stream(stream)))
+
+
+def engram_gateconv_bwd_workspace_size(M: int, T: int, d: int) -> int:
+    return int(load().engram_gateconv_bwd_workspace_size(int(M), int(T), int(d)))
+
+
+def engram_gateconv_bwd(dY, H, k, v, rms_w_h, rms_w_v, conv_w, vhat, alpha, rrms_h, rrms_k,
+                        rrms_v, dH, dk, dv, drms_w_h, drms_w_v, dconv_w, workspace,
+                        eps: float = GATECONV_EPS, stream=None):
+    M, T, d = H.shape
+    for t, n in ((dY, "dY"), (k, "k"), (v, "v"), (vhat, "vhat"), (dH, "dH"), (dk, "dk"),
+                 (dv, "dv")):
+        _need(t, torch.bfloat16, (M, T, d), n)
+    _need(drms_w_h, torch.float32, (d,), "drms_w_h")
+    _need(drms_w_v, torch.float32, (d,), "drms_w_v")
+    _need(dconv_w, torch.float32, (4, d), "dconv_w")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("engram_gateconv_bwd", load().engram_gateconv_bwd(
+        _ptr(dY), _ptr(H), _ptr(k), _ptr(v), _ptr(rms_w_h), _ptr(rms_w_v), _ptr(conv_w),
+        _ptr(vhat), _ptr(alpha), _ptr(rrms_h), _ptr(rrms_k), _ptr(rrms_v), _ptr(dH), _ptr(dk),
+        _ptr(dv), _ptr(drms_w_h), _ptr(drms_w_v), _ptr(dconv_w), _ptr(workspace), nbytes,
+        M, T, d, float(eps), _stream(stream)))
+
+
+def engram_device_error() -> int:
+    v = ctypes.c_uint32(0)
+    _check("engram_device_error", load().engram_device_error(ctypes.byref(v)))
+    return int(v.value)
+
+
+def engram_launch_info(op: int, n0: int, n1: int = 0, n2: int = 0) -> dict:
+    info = _LaunchInfo()
+    _check("engram_launch_info", load().engram_launch_info(int(op), int(n0), int(n1), int(n2),
+                                                           ctypes.byref(info)))
+    return {f: getattr(info, f) for f, _ in _LaunchInfo._fields_}
+
+
+# ------------------------------------------------- allocating convenience API
+
+def gate_forward(x, kv, weight, mask=None, eps: float = GATE_EPS, save: bool = True):
+    out = torch.empty_like(x)
+    saved = torch.empty((x.shape[0], S_GATE, 4), device=x.device, dtype=torch.float32) \
+        if save else None
+    engram_gate_fwd(x, kv, weight, mask, out, saved, eps)
+    return out, saved
+
+
+def gate_backward(x, kv, weight, saved, grad_out):
+    N = x.shape[0]
+    gx = torch.empty_like(x)
+    gkv = torch.empty_like(kv)
+    gw = torch.empty_like(weight)
+    ws = torch.empty(engram_gate_bwd_workspace_size(N), device=x.device, dtype=torch.uint8)
+    engram_gate_bwd(x, kv, weight, saved, grad_out, gx, gkv, gw, ws)
+    return gx, gkv, gw
+
+
+def gateconv_forward(H, k, v, rms_w_h, rms_w_v, conv_w, eps: float = GATECONV_EPS):
+    M, T, d = H.shape
+    Y = torch.empty_like(H)
+    vhat = torch.empty_like(H)
+    sc = [torch.empty((M, T), device=H.device, dtype=torch.float32) for _ in range(4)]
+    engram_gateconv_fwd(H, k, v, rms_w_h, rms_w_v, conv_w, Y, vhat, *sc, eps=eps)
+    return (Y, vhat, *sc)
+
+
+def gateconv_backward(dY, H, k, v, rms_w_h, rms_w_v, conv_w, vhat, alpha, rrms_h, rrms_k,
+                      rrms_v, eps: float = GATECONV_EPS):
+    M, T, d = H.shape
+    dH, dk, dv = torch.empty_like(H), torch.empty_like(H), torch.empty_like(H)
+    dwh = torch.empty(d, device=H.device, dtype=torch.float32)
+    dwv = torch.empty(d, device=H.device, dtype=torch.float32)
+    dcw = torch.empty((4, d), device=H.device, dtype=torch.float32)
+    ws = torch.empty(engram_gateconv_bwd_workspace_size(M, T, d), device=H.device,
+                     dtype=torch.uint8)
+    engram_gateconv_bwd(dY, H, k, v, rms_w_h, rms_w_v, conv_w, vhat, alpha, rrms_h, rrms_k,
+                        rrms_v, dH, dk, dv, dwh, dwv, dcw, ws, eps=eps)
+    return dH, dk, dv, dwh, dwv, dcw

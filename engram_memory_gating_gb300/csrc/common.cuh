@@ -1,0 +1,231 @@
+// Device-side building blocks shared by the Engram kernels (sm_103a).
+//
+// Every kernel here follows one pattern, "cluster row split": a token row of
+// d columns is cut into C contiguous column slices, one per CTA of a thread
+// block cluster.  Each CTA streams its slice of consecutive token rows into a
+// ring of shared-memory stages with 1-D bulk asynchronous copies (TMA engine)
+// completing on mbarriers, reduces its slice, and exchanges the per-token
+// partial sums with the other CTAs of the cluster through distributed shared
+// memory.  Each thread owns 8 consecutive columns (one 16-byte vector of bf16)
+// of every stream of its slice for the whole kernel, so per-column weights
+// live in registers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define EG_DEV __device__ __forceinline__
+
+namespace eg {
+
+constexpr uint32_t kFullMask = 0xffffffffu;
+constexpr uint32_t kErrTimeout = 1u;                  // sticky device error bit
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr uint32_t kWaitMaxIters = 1u << 30;
+
+// ------------------------------------------------------------------ PTX glue
+
+EG_DEV uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+EG_DEV unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+EG_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes mbarrier initialisation visible to the async proxy and the cluster.
+EG_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+// Orders this thread's earlier generic-proxy shared accesses before later
+// async-proxy (bulk copy) accesses.
+EG_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+EG_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+EG_DEV bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Gives up after
+// kWaitLimitNs of wall time (or kWaitMaxIters polls) and returns false; the
+// caller records the failure and carries on without hanging the GPU.
+EG_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_addr(bar);
+    if (mbar_try_wait(addr, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 0; it < kWaitMaxIters; ++it) {
+        if (mbar_try_wait(addr, parity)) return true;
+        if ((it & 63u) == 63u && globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+EG_DEV void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+EG_DEV uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+EG_DEV uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+EG_DEV uint32_t cluster_index() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+EG_DEV uint32_t cluster_count() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Cluster-wide barrier with release/acquire semantics on shared memory.  Every
+// thread of every CTA of the cluster must reach it (uniform control flow).
+EG_DEV void cluster_sync() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::
+            : "memory");
+}
+
+// Address of the same shared variable in CTA `rank` of this cluster.
+EG_DEV uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+EG_DEV float2 ld_cluster_f2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+EG_DEV float ld_cluster_f(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Streaming 16-byte global store (evict-first in L1/L2).
+EG_DEV void stg_cs(void* p, const uint4& v) {
+    asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+EG_DEV void stg_f4(float* p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+
+EG_DEV uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// ------------------------------------------------------------------ bf16
+
+EG_DEV float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+EG_DEV float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+EG_DEV void unpack8(const uint4& q, float (&f)[8]) {
+    f[0] = bf_lo(q.x);
+    f[1] = bf_hi(q.x);
+    f[2] = bf_lo(q.y);
+    f[3] = bf_hi(q.y);
+    f[4] = bf_lo(q.z);
+    f[5] = bf_hi(q.z);
+    f[6] = bf_lo(q.w);
+    f[7] = bf_hi(q.w);
+}
+
+// Two fp32 values -> packed bf16x2, round-to-nearest-even (lo in the low half).
+EG_DEV uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+EG_DEV uint4 pack8(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+// ------------------------------------------------- error-free transformations
+// Knuth's TwoSum: s + e == a + b exactly.  Explicit _rn intrinsics keep the
+// compiler from contracting or reassociating these operations.
+EG_DEV void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float aa = __fsub_rn(s, bb);
+    e = __fadd_rn(__fsub_rn(a, aa), __fsub_rn(b, bb));
+}
+
+// (hi, lo) += t with the rounding error of the addition kept in lo.
+EG_DEV void cacc_add(float& hi, float& lo, float t) {
+    float s, e;
+    two_sum(hi, t, s, e);
+    hi = s;
+    lo = __fadd_rn(lo, e);
+}
+
+// (hi, lo) += a * b with both the product's and the sum's rounding errors
+// kept in lo (the product error is exact via FMA).
+EG_DEV void cacc_prod(float& hi, float& lo, float a, float b) {
+    const float t = __fmul_rn(a, b);
+    const float pe = __fmaf_rn(a, b, -t);
+    float s, e;
+    two_sum(hi, t, s, e);
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(e, pe));
+}
+
+// (hi, lo) += (ah + al) * b, with ah + al an unevaluated double-float factor.
+EG_DEV void cacc_prod2(float& hi, float& lo, float ah, float al, float b) {
+    const float t = __fmul_rn(ah, b);
+    float pe = __fmaf_rn(ah, b, -t);
+    pe = __fmaf_rn(al, b, pe);
+    float s, e;
+    two_sum(hi, t, s, e);
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(e, pe));
+}
+
+// (hi, lo) += (hi2, lo2)
+EG_DEV void cacc_merge(float& hi, float& lo, float hi2, float lo2) {
+    float s, e;
+    two_sum(hi, hi2, s, e);
+    hi = s;
+    lo = __fadd_rn(__fadd_rn(lo, lo2), e);
+}
+
+}  // namespace eg

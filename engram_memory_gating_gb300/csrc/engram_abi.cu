@@ -1,0 +1,554 @@
+// C ABI of libengram.so: host-side argument validation, per-device one-time
+// set-up and kernel launches.  No allocation, copy or synchronisation happens
+// on the execute path (cuDNN Frontend "Engram saved-state gate": plan/execute
+// paragraph -- execute does no allocation, conversion, compilation or sync).
+#include <cmath>
+#include <mutex>
+
+#include "engram.h"
+#include "engram_internal.h"
+
+// Sticky device error word (bit 0: an asynchronous copy timed out).  Host code
+// passes its device address, obtained with cudaGetSymbolAddress, to kernels.
+__device__ unsigned int eg_error_word = 0u;
+
+namespace eg {
+
+int pick_cluster(int64_t groups_total, int max_groups) {
+    for (int c = 1; c <= 8; ++c)
+        if (groups_total % c == 0 && groups_total / c <= max_groups) return c;
+    return 0;
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kGateD = ENGRAM_GATE_HIDDEN;
+constexpr int kGateFwdStages = 4;
+constexpr int kGateBwdStages = 3;
+constexpr int kGcFwdStages = 6;
+constexpr int kGcBwdStages = 6;  // >= 5: rows of tokens tau-3 .. tau+1 stay resident
+static_assert(kGcBwdStages >= 5 && kGcBwdStages <= kMaxStages, "ring too short");
+static_assert(kGateFwdStages <= kMaxStages && kGateBwdStages <= kMaxStages, "too many stages");
+constexpr int kGcFwdMinRange = 32;  // tokens; bounds the 3-token halo overhead
+
+struct OccKey {
+    int op, cluster, threads, smem;
+};
+
+struct DeviceState {
+    bool init = false;
+    bool ok = false;
+    int sm_count = 0;
+    unsigned int* err = nullptr;
+    static constexpr int kCache = 64;
+    OccKey keys[kCache];
+    int vals[kCache];
+    int n = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+// Occupancy-limited number of co-resident clusters for a kernel shape.
+int max_clusters(DeviceState& st, int op, int cluster, int threads, int smem) {
+    for (int i = 0; i < st.n; ++i)
+        if (st.keys[i].op == op && st.keys[i].cluster == cluster &&
+            st.keys[i].threads == threads && st.keys[i].smem == smem)
+            return st.vals[i];
+    int v = 0;
+    cudaError_t e = cudaSuccess;
+    switch (op) {
+        case 0:
+            e = gate_fwd_prepare(smem);
+            if (e == cudaSuccess) e = gate_fwd_max_clusters(cluster, threads, smem, &v);
+            break;
+        case 1:
+            e = gate_bwd_prepare(smem);
+            if (e == cudaSuccess) e = gate_bwd_max_clusters(cluster, threads, smem, &v);
+            break;
+        case 2:
+            e = gateconv_fwd_prepare(smem);
+            if (e == cudaSuccess) e = gateconv_fwd_max_clusters(cluster, threads, smem, &v);
+            break;
+        default:
+            e = gateconv_bwd_prepare(smem);
+            if (e == cudaSuccess) e = gateconv_bwd_max_clusters(cluster, threads, smem, &v);
+            break;
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        v = 0;
+    }
+    if (st.n < DeviceState::kCache) {
+        st.keys[st.n] = OccKey{op, cluster, threads, smem};
+        st.vals[st.n] = v;
+        ++st.n;
+    }
+    return v;
+}
+
+// Returns the calling thread's current-device state, initialising it once.
+DeviceState* device_state() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    DeviceState& st = g_dev[dev];
+    if (!st.init) {
+        st.init = true;
+        st.ok = false;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err), eg_error_word) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        // the library is built for sm_103a only
+        if (!(major == 10 && minor == 3)) return nullptr;
+        st.ok = true;
+    }
+    return st.ok ? &st : nullptr;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    const void* p;
+    size_t n;
+};
+
+bool overlaps(const Range& a, const Range& b) {
+    if (a.p == nullptr || b.p == nullptr || a.n == 0 || b.n == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+// Every output range against every input and every other output range.
+bool any_overlap(const Range* outs, int nout, const Range* ins, int nin) {
+    for (int i = 0; i < nout; ++i) {
+        for (int j = 0; j < nin; ++j)
+            if (overlaps(outs[i], ins[j])) return true;
+        for (int j = i + 1; j < nout; ++j)
+            if (overlaps(outs[i], outs[j])) return true;
+    }
+    return false;
+}
+
+engram_status_t launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return ENGRAM_OK;
+    (void)cudaGetLastError();
+    return ENGRAM_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------- geometry
+
+bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngroups) {
+    const int C = pick_cluster(kGateD / 8, 160);
+    ncols = kGateD / C;
+    ngroups = ncols / 8;
+    c.cluster = C;
+    c.threads = round_up(ngroups, 32);
+    c.stages = kGateFwdStages;
+    c.smem = kSmemRingOff + c.stages * 9 * ncols * 2;
+    const int mc = max_clusters(st, 0, C, c.threads, c.smem);
+    if (mc <= 0) return false;
+    c.clusters = static_cast<int>(N < mc ? N : mc);
+    return true;
+}
+
+bool gate_bwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngroups) {
+    const int C = pick_cluster(kGateD / 8, 160);
+    ncols = kGateD / C;
+    ngroups = ncols / 8;
+    c.cluster = C;
+    c.threads = round_up(ngroups, 32);
+    c.stages = kGateBwdStages;
+    c.smem = kSmemRingOff + c.stages * (13 * ncols * 2 + 64);
+    const int mc = max_clusters(st, 1, C, c.threads, c.smem);
+    if (mc <= 0) return false;
+    // at most half as many clusters as 64-token blocks, so each cluster's
+    // (hi, lo) grad_weight pair fits two of the workspace's block slots
+    const int64_t nb = N / 64;
+    const int64_t lim = nb >= 2 ? nb / 2 : 1;
+    c.clusters = static_cast<int>(lim < mc ? lim : mc);
+    return true;
+}
+
+bool gc_shape_ok(int64_t M, int64_t T, int64_t d) {
+    if (M < 1 || T < 1 || d < 8 || d > 65536 || d % 8 != 0) return false;
+    if (M * T > 2147483647LL) return false;
+    // forward: <= 256 groups of 8 columns per CTA; backward: <= 128 groups of
+    // 8 columns (256 threads of 4 columns).  Slices are whole 8-column groups
+    // so that every row slice is a multiple of 16 bytes (bulk-copy rule).
+    if (pick_cluster(d / 8, 256) == 0 || pick_cluster(d / 8, 128) == 0) return false;
+    return true;
+}
+
+bool gc_fwd_cfg(DeviceState& st, int64_t M, int64_t T, int64_t d, LaunchCfg& c, int& ncols,
+                int& ngroups, int& range_len, int& rpr) {
+    int C = pick_cluster(d / 8, 160);
+    if (C == 0) C = pick_cluster(d / 8, 256);
+    ncols = static_cast<int>(d / C);
+    ngroups = ncols / 8;
+    c.cluster = C;
+    c.threads = round_up(ngroups, 32);
+    c.stages = kGcFwdStages;
+    c.smem = kSmemRingOff + c.stages * 3 * ncols * 2;
+    const int mc = max_clusters(st, 2, C, c.threads, c.smem);
+    if (mc <= 0) return false;
+    // as many ranges as clusters fit, none shorter than kGcFwdMinRange tokens
+    int64_t per_row = (mc + M - 1) / M;
+    const int64_t max_per_row = (T + kGcFwdMinRange - 1) / kGcFwdMinRange;
+    if (per_row > max_per_row) per_row = max_per_row;
+    if (per_row < 1) per_row = 1;
+    range_len = static_cast<int>((T + per_row - 1) / per_row);
+    rpr = static_cast<int>((T + range_len - 1) / range_len);
+    c.clusters = static_cast<int>(M * rpr);
+    return true;
+}
+
+// Range length of the backward depends on (M, T) only, so that the workspace
+// size does not depend on the device: about 512 ranges, 128..T tokens each.
+void gc_bwd_ranges(int64_t M, int64_t T, int& range_len, int& rpr) {
+    int64_t L = (M * T + 511) / 512;
+    L = (L + 31) / 32 * 32;
+    if (L < 128) L = 128;
+    if (L > T) L = T;
+    range_len = static_cast<int>(L);
+    rpr = static_cast<int>((T + L - 1) / L);
+}
+
+bool gc_bwd_cfg(DeviceState& st, int64_t M, int64_t T, int64_t d, LaunchCfg& c, int& ncols,
+                int& ngroups, int& range_len, int& rpr) {
+    const int C = pick_cluster(d / 8, 128);
+    ncols = static_cast<int>(d / C);
+    ngroups = ncols / 4;
+    c.cluster = C;
+    c.threads = round_up(ngroups, 32);
+    c.stages = kGcBwdStages;
+    c.smem = kSmemRingOff + c.stages * 5 * ncols * 2;
+    if (max_clusters(st, 3, C, c.threads, c.smem) <= 0) return false;
+    gc_bwd_ranges(M, T, range_len, rpr);
+    c.clusters = static_cast<int>(M * rpr);
+    return true;
+}
+
+}  // namespace
+}  // namespace eg
+
+using namespace eg;
+
+extern "C" {
+
+const char* engram_status_string(engram_status_t s) {
+    switch (s) {
+        case ENGRAM_OK: return "ok";
+        case ENGRAM_ERR_NULL: return "null pointer";
+        case ENGRAM_ERR_ALIGN: return "misaligned pointer (16 bytes required)";
+        case ENGRAM_ERR_SHAPE: return "size out of range";
+        case ENGRAM_ERR_OVERLAP: return "output overlaps another buffer";
+        case ENGRAM_ERR_WORKSPACE: return "workspace too small";
+        case ENGRAM_ERR_DEVICE: return "no usable sm_103 device";
+        case ENGRAM_ERR_LAUNCH: return "kernel launch failed";
+    }
+    return "unknown status";
+}
+
+size_t engram_gate_bwd_workspace_size(int64_t N) {
+    if (N < 64 || N > ENGRAM_GATE_BWD_MAX_TOKENS || N % 64 != 0) return 0;
+    return static_cast<size_t>(4) *
+           (16 * static_cast<size_t>(N) + 4 * static_cast<size_t>(kGateD) * static_cast<size_t>(N / 64));
+}
+
+engram_status_t engram_gate_fwd(const void* x, const void* kv, const float* weight,
+                                const uint8_t* mask, void* out, float* saved, int64_t N,
+                                float eps, cudaStream_t stream) {
+    if (!x || !kv || !weight || !out) return ENGRAM_ERR_NULL;
+    if (N < 1 || N > ENGRAM_GATE_MAX_TOKENS) return ENGRAM_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(kv) || !aligned16(weight) || !aligned16(out) ||
+        (saved && !aligned16(saved)))
+        return ENGRAM_ERR_ALIGN;
+    const size_t n = static_cast<size_t>(N);
+    const Range ins[] = {{x, n * 4 * kGateD * 2}, {kv, n * 5 * kGateD * 2},
+                         {weight, 4 * kGateD * 4}, {mask, mask ? n : 0}};
+    const Range outs[] = {{out, n * 4 * kGateD * 2}, {saved, saved ? n * 64 : 0}};
+    if (any_overlap(outs, 2, ins, 4)) return ENGRAM_ERR_OVERLAP;
+
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st = device_state();
+    if (!st) return ENGRAM_ERR_DEVICE;
+    LaunchCfg c;
+    int ncols, ngroups;
+    if (!gate_fwd_cfg(*st, N, c, ncols, ngroups)) return ENGRAM_ERR_DEVICE;
+    GateFwdParams p;
+    p.x = static_cast<const uint16_t*>(x);
+    p.kv = static_cast<const uint16_t*>(kv);
+    p.w = weight;
+    p.mask = mask;
+    p.out = static_cast<uint16_t*>(out);
+    p.saved = saved;
+    p.err = st->err;
+    p.N = N;
+    p.d = kGateD;
+    p.ncols = ncols;
+    p.ngroups = ngroups;
+    p.stages = c.stages;
+    p.eps = eps;
+    return launch_status(gate_fwd_launch(p, c, stream));
+}
+
+engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weight,
+                                const float* saved, const void* grad_out, void* grad_x,
+                                void* grad_kv, float* grad_weight, void* workspace,
+                                size_t workspace_bytes, int64_t N, cudaStream_t stream) {
+    if (!x || !kv || !weight || !saved || !grad_out || !grad_x || !grad_kv || !grad_weight ||
+        !workspace)
+        return ENGRAM_ERR_NULL;
+    if (N < 64 || N > ENGRAM_GATE_BWD_MAX_TOKENS || N % 64 != 0) return ENGRAM_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(kv) || !aligned16(weight) || !aligned16(saved) ||
+        !aligned16(grad_out) || !aligned16(grad_x) || !aligned16(grad_kv) ||
+        !aligned16(grad_weight) || !aligned16(workspace))
+        return ENGRAM_ERR_ALIGN;
+    const size_t need = engram_gate_bwd_workspace_size(N);
+    if (workspace_bytes < need) return ENGRAM_ERR_WORKSPACE;
+    const size_t n = static_cast<size_t>(N);
+    const Range ins[] = {{x, n * 4 * kGateD * 2}, {kv, n * 5 * kGateD * 2},
+                         {weight, 4 * kGateD * 4}, {saved, n * 64}, {grad_out, n * 4 * kGateD * 2}};
+    const Range outs[] = {{grad_x, n * 4 * kGateD * 2}, {grad_kv, n * 5 * kGateD * 2},
+                          {grad_weight, 4 * kGateD * 4}, {workspace, need}};
+    if (any_overlap(outs, 4, ins, 5)) return ENGRAM_ERR_OVERLAP;
+
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st = device_state();
+    if (!st) return ENGRAM_ERR_DEVICE;
+    LaunchCfg c;
+    int ncols, ngroups;
+    if (!gate_bwd_cfg(*st, N, c, ncols, ngroups)) return ENGRAM_ERR_DEVICE;
+    // workspace: [16N floats, unused scratch | (N/64, 4, 5120) fp32 partials]
+    float* partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + 64 * n);
+    GateBwdParams p;
+    p.x = static_cast<const uint16_t*>(x);
+    p.kv = static_cast<const uint16_t*>(kv);
+    p.w = weight;
+    p.saved = saved;
+    p.gout = static_cast<const uint16_t*>(grad_out);
+    p.gx = static_cast<uint16_t*>(grad_x);
+    p.gkv = static_cast<uint16_t*>(grad_kv);
+    p.partial = partial;
+    p.err = st->err;
+    p.N = N;
+    p.d = kGateD;
+    p.ncols = ncols;
+    p.ngroups = ngroups;
+    p.stages = c.stages;
+    p.pair_slots = (N / 64) >= 2 ? 1 : 0;
+    engram_status_t s = launch_status(gate_bwd_launch(p, c, stream));
+    if (s != ENGRAM_OK) return s;
+    GateWReduceParams r;
+    r.partial = partial;
+    r.out = grad_weight;
+    r.nblocks = p.pair_slots ? 2 * c.clusters : c.clusters;
+    r.n = 4 * kGateD;
+    r.stride = 4 * kGateD;
+    r.pairs = p.pair_slots;
+    return launch_status(gate_wreduce_launch(r, stream));
+}
+
+engram_status_t engram_gateconv_fwd(const void* H, const void* k, const void* v,
+                                    const float* rms_w_h, const float* rms_w_v,
+                                    const float* conv_w, void* Y, void* vhat, float* alpha,
+                                    float* rrms_h, float* rrms_k, float* rrms_v, int64_t M,
+                                    int64_t T, int64_t d, float eps, cudaStream_t stream) {
+    if (!H || !k || !v || !rms_w_h || !rms_w_v || !conv_w || !Y || !vhat || !alpha || !rrms_h ||
+        !rrms_k || !rrms_v)
+        return ENGRAM_ERR_NULL;
+    if (!gc_shape_ok(M, T, d)) return ENGRAM_ERR_SHAPE;
+    const void* all[] = {H, k, v, rms_w_h, rms_w_v, conv_w, Y, vhat, alpha, rrms_h, rrms_k, rrms_v};
+    for (const void* ptr : all)
+        if (!aligned16(ptr)) return ENGRAM_ERR_ALIGN;
+    const size_t t = static_cast<size_t>(M * T), dd = static_cast<size_t>(d);
+    const Range ins[] = {{H, t * dd * 2}, {k, t * dd * 2}, {v, t * dd * 2},
+                         {rms_w_h, dd * 4}, {rms_w_v, dd * 4}, {conv_w, 4 * dd * 4}};
+    const Range outs[] = {{Y, t * dd * 2}, {vhat, t * dd * 2}, {alpha, t * 4},
+                          {rrms_h, t * 4}, {rrms_k, t * 4}, {rrms_v, t * 4}};
+    if (any_overlap(outs, 6, ins, 6)) return ENGRAM_ERR_OVERLAP;
+
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st = device_state();
+    if (!st) return ENGRAM_ERR_DEVICE;
+    LaunchCfg c;
+    int ncols, ngroups, range_len, rpr;
+    if (!gc_fwd_cfg(*st, M, T, d, c, ncols, ngroups, range_len, rpr)) return ENGRAM_ERR_DEVICE;
+    GateConvFwdParams p;
+    p.H = static_cast<const uint16_t*>(H);
+    p.k = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.wh = rms_w_h;
+    p.wv = rms_w_v;
+    p.cw = conv_w;
+    p.Y = static_cast<uint16_t*>(Y);
+    p.vhat = static_cast<uint16_t*>(vhat);
+    p.alpha = alpha;
+    p.rh = rrms_h;
+    p.rk = rrms_k;
+    p.rv = rrms_v;
+    p.err = st->err;
+    p.M = static_cast<int>(M);
+    p.T = static_cast<int>(T);
+    p.d = static_cast<int>(d);
+    p.ncols = ncols;
+    p.ngroups = ngroups;
+    p.stages = c.stages;
+    p.range_len = range_len;
+    p.ranges_per_row = rpr;
+    p.eps = eps;
+    p.inv_sqrt_d = static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
+    return launch_status(gateconv_fwd_launch(p, c, stream));
+}
+
+size_t engram_gateconv_bwd_workspace_size(int64_t M, int64_t T, int64_t d) {
+    if (!gc_shape_ok(M, T, d)) return 0;
+    int range_len, rpr;
+    gc_bwd_ranges(M, T, range_len, rpr);
+    return static_cast<size_t>(M) * static_cast<size_t>(rpr) * 6 * static_cast<size_t>(d) * 4;
+}
+
+engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k,
+                                    const void* v, const float* rms_w_h,
+                                    const float* rms_w_v, const float* conv_w,
+                                    const void* vhat, const float* alpha,
+                                    const float* rrms_h, const float* rrms_k,
+                                    const float* rrms_v, void* dH, void* dk, void* dv,
+                                    float* drms_w_h, float* drms_w_v, float* dconv_w,
+                                    void* workspace, size_t workspace_bytes, int64_t M,
+                                    int64_t T, int64_t d, float eps, cudaStream_t stream) {
+    if (!dY || !H || !k || !v || !rms_w_h || !rms_w_v || !conv_w || !vhat || !alpha || !rrms_h ||
+        !rrms_k || !rrms_v || !dH || !dk || !dv || !drms_w_h || !drms_w_v || !dconv_w ||
+        !workspace)
+        return ENGRAM_ERR_NULL;
+    if (!gc_shape_ok(M, T, d)) return ENGRAM_ERR_SHAPE;
+    const void* all[] = {dY, H, k, v, rms_w_h, rms_w_v, conv_w, vhat, alpha, rrms_h, rrms_k,
+                         rrms_v, dH, dk, dv, drms_w_h, drms_w_v, dconv_w, workspace};
+    for (const void* ptr : all)
+        if (!aligned16(ptr)) return ENGRAM_ERR_ALIGN;
+    const size_t need = engram_gateconv_bwd_workspace_size(M, T, d);
+    if (workspace_bytes < need) return ENGRAM_ERR_WORKSPACE;
+    const size_t t = static_cast<size_t>(M * T), dd = static_cast<size_t>(d);
+    const Range ins[] = {{dY, t * dd * 2}, {H, t * dd * 2}, {k, t * dd * 2}, {v, t * dd * 2},
+                         {rms_w_h, dd * 4}, {rms_w_v, dd * 4}, {conv_w, 4 * dd * 4},
+                         {vhat, t * dd * 2}, {alpha, t * 4}, {rrms_h, t * 4}, {rrms_k, t * 4},
+                         {rrms_v, t * 4}};
+    const Range outs[] = {{dH, t * dd * 2}, {dk, t * dd * 2}, {dv, t * dd * 2},
+                          {drms_w_h, dd * 4}, {drms_w_v, dd * 4}, {dconv_w, 4 * dd * 4},
+                          {workspace, need}};
+    if (any_overlap(outs, 7, ins, 12)) return ENGRAM_ERR_OVERLAP;
+
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st = device_state();
+    if (!st) return ENGRAM_ERR_DEVICE;
+    LaunchCfg c;
+    int ncols, ngroups, range_len, rpr;
+    if (!gc_bwd_cfg(*st, M, T, d, c, ncols, ngroups, range_len, rpr)) return ENGRAM_ERR_DEVICE;
+    float* partial = static_cast<float*>(workspace);
+    GateConvBwdParams p;
+    p.dY = static_cast<const uint16_t*>(dY);
+    p.H = static_cast<const uint16_t*>(H);
+    p.k = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.wh = rms_w_h;
+    p.wv = rms_w_v;
+    p.cw = conv_w;
+    p.vhat = static_cast<const uint16_t*>(vhat);
+    p.alpha = alpha;
+    p.rh = rrms_h;
+    p.rk = rrms_k;
+    p.rv = rrms_v;
+    p.dH = static_cast<uint16_t*>(dH);
+    p.dk = static_cast<uint16_t*>(dk);
+    p.dv = static_cast<uint16_t*>(dv);
+    p.partial = partial;
+    p.err = st->err;
+    p.M = static_cast<int>(M);
+    p.T = static_cast<int>(T);
+    p.d = static_cast<int>(d);
+    p.ncols = ncols;
+    p.ngroups = ngroups;
+    p.stages = c.stages;
+    p.range_len = range_len;
+    p.ranges_per_row = rpr;
+    p.eps = eps;
+    p.inv_sqrt_d = static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
+    engram_status_t s = launch_status(gateconv_bwd_launch(p, c, stream));
+    if (s != ENGRAM_OK) return s;
+    const int R = c.clusters;
+    float* outs3[3] = {drms_w_h, drms_w_v, dconv_w};
+    const int offs[3] = {0, 1, 2};
+    const int lens[3] = {1, 1, 4};
+    for (int i = 0; i < 3; ++i) {
+        GateWReduceParams r;
+        r.partial = partial + static_cast<size_t>(offs[i]) * dd;
+        r.out = outs3[i];
+        r.nblocks = R;
+        r.n = lens[i] * static_cast<int>(d);
+        r.stride = 6 * static_cast<int>(d);
+        r.pairs = 0;
+        s = launch_status(gateconv_wreduce_launch(r, stream));
+        if (s != ENGRAM_OK) return s;
+    }
+    return ENGRAM_OK;
+}
+
+engram_status_t engram_device_error(uint32_t* flags) {
+    if (!flags) return ENGRAM_ERR_NULL;
+    unsigned int v = 0u, zero = 0u;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(&v, eg_error_word, sizeof(v)) != cudaSuccess ||
+        cudaMemcpyToSymbol(eg_error_word, &zero, sizeof(zero)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ENGRAM_ERR_DEVICE;
+    }
+    *flags = v;
+    return ENGRAM_OK;
+}
+
+engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
+                                   engram_launch_info_t* info) {
+    if (!info) return ENGRAM_ERR_NULL;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st = device_state();
+    if (!st) return ENGRAM_ERR_DEVICE;
+    LaunchCfg c;
+    int ncols, ngroups, range_len, rpr;
+    bool ok = false;
+    switch (op) {
+        case 0:
+            ok = n0 >= 1 && n0 <= ENGRAM_GATE_MAX_TOKENS && gate_fwd_cfg(*st, n0, c, ncols, ngroups);
+            break;
+        case 1:
+            ok = engram_gate_bwd_workspace_size(n0) > 0 && gate_bwd_cfg(*st, n0, c, ncols, ngroups);
+            break;
+        case 2:
+            ok = gc_shape_ok(n0, n1, n2) && gc_fwd_cfg(*st, n0, n1, n2, c, ncols, ngroups, range_len, rpr);
+            break;
+        case 3:
+            ok = gc_shape_ok(n0, n1, n2) && gc_bwd_cfg(*st, n0, n1, n2, c, ncols, ngroups, range_len, rpr);
+            break;
+        default:
+            return ENGRAM_ERR_SHAPE;
+    }
+    if (!ok) return ENGRAM_ERR_SHAPE;
+    info->cluster = c.cluster;
+    info->threads = c.threads;
+    info->clusters = c.clusters;
+    info->stages = c.stages;
+    info->smem_bytes = c.smem;
+    return ENGRAM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,210 @@
+/*
+ * engram.h -- C ABI of the GB300 (sm_103a) Engram gate library, libengram.so.
+ *
+ * Two fused, memory-bound operators:
+ *
+ *  1. The four-stream saved-state gate (cuDNN Frontend, "Engram saved-state
+ *     gate": semantics, layout and saved-state paragraphs, and its
+ *     plan/execute example).  Per token n and stream s < 4, X[n,s,:] and its
+ *     key KV[n, s*5120 : (s+1)*5120] are RMS-normalised separately
+ *     (rstd = 1/sqrt(mean(x^2) + eps)); dot = sum_i xh_i * weight[s,i] * kh_i
+ *     in FP32; sq = sign(dot) * sqrt(max(|dot|, 1e-6)); gate = sigmoid(sq);
+ *     out = X + gate * v with v = KV[n, 20480:25600], rounded once to BF16.
+ *     A false mask gives out == X bit for bit.
+ *
+ *  2. GateConv (TileOPs "Engram Operators", GateConv section,
+ *     EngramGateConvFwdOp / EngramGateConvBwdOp): RMSNorm gating of H and k,
+ *     a causal depthwise conv1d with 4 taps over the RMS-normalised gated
+ *     value, then SiLU plus the gated value as residual.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers are DEVICE pointers to contiguous, row-major tensors.  BF16
+ *    tensors are passed as `void*` holding IEEE bfloat16 values (the upper
+ *    half of a binary32 word).  Floating tensors and workspaces must be
+ *    16-byte aligned; the mask is a byte array with no alignment rule.
+ *  - The caller allocates and owns every buffer.  The library keeps no
+ *    pointer after the call returns.  Outputs and workspaces must not
+ *    overlap any input or one another (checked on the host by address
+ *    range; overlap returns ENGRAM_ERR_OVERLAP).
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream):
+ *    it validates its arguments on the host, then enqueues kernels.  It
+ *    performs no allocation, no host<->device copy and no synchronisation,
+ *    so it may be captured in a CUDA graph.  The first call on a device also
+ *    performs one-time, per-device set-up (kernel attributes and occupancy
+ *    queries); make that first call before any stream capture.
+ *  - A non-OK status means nothing was enqueued, except ENGRAM_ERR_LAUNCH
+ *    (the launch itself failed; the stream state is then the CUDA runtime's).
+ *    The library never prints, traps or aborts.
+ *  - Kernels that wait on asynchronous copies give up after a bounded time
+ *    and raise a sticky device flag instead of hanging; read it with
+ *    engram_device_error().
+ */
+#ifndef ENGRAM_H_
+#define ENGRAM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ENGRAM_OK = 0,
+    ENGRAM_ERR_NULL = 1,      /* a required pointer is NULL                  */
+    ENGRAM_ERR_ALIGN = 2,     /* a floating tensor / workspace not 16-B aligned */
+    ENGRAM_ERR_SHAPE = 3,     /* a size is out of the supported range        */
+    ENGRAM_ERR_OVERLAP = 4,   /* an output or workspace overlaps another buffer */
+    ENGRAM_ERR_WORKSPACE = 5, /* workspace_bytes below the required size     */
+    ENGRAM_ERR_DEVICE = 6,    /* no usable sm_103 device / set-up failed     */
+    ENGRAM_ERR_LAUNCH = 7     /* the kernel launch returned an error         */
+} engram_status_t;
+
+/* Human-readable name of a status code (static string). */
+const char* engram_status_string(engram_status_t s);
+
+/* Fixed layout of the saved-state gate (cuDNN "Engram saved-state gate",
+ * layout paragraph): 4 streams of hidden size 5120; packed KV is 4 keys then
+ * one shared value, 25600 columns. */
+#define ENGRAM_GATE_STREAMS 4
+#define ENGRAM_GATE_HIDDEN 5120
+#define ENGRAM_GATE_KV_COLS 25600
+#define ENGRAM_GATE_MAX_TOKENS 4194240   /* forward: 1 <= N <= 65535*64     */
+#define ENGRAM_GATE_BWD_MAX_TOKENS 8192  /* backward: N % 64 == 0, N <= 8192 */
+
+/*
+ * Saved-state gate, forward (cuDNN "Engram saved-state gate", semantics and
+ * saved-state paragraphs).
+ *   x      bf16 (N, 4, 5120)     input streams X
+ *   kv     bf16 (N, 25600)       keys s = 0..3 in columns [s*5120, (s+1)*5120),
+ *                                shared value in [20480, 25600)
+ *   weight fp32 (4, 5120)        fused weight: product of the q/k norm weights
+ *   mask   uint8 (N)             nonzero = true (torch.bool layout); a false
+ *                                token gives out == X bit for bit; NULL = all true
+ *   out    bf16 (N, 4, 5120)     X + gate * v, one round-to-nearest-even
+ *   saved  fp32 (N, 4, 4) / NULL per (n, s): gate, dot, rstd_X, rstd_key.
+ *                                A false token stores gate = 0 (dot and both
+ *                                rstd as usual), which makes the backward the
+ *                                derivative of out = X.  NULL skips the write;
+ *                                `out` is bit-identical either way.
+ *   N      1 <= N <= ENGRAM_GATE_MAX_TOKENS
+ *   eps    RMS-norm epsilon (the pages' default is 1e-20)
+ * Keep `saved` and the matching x / kv / weight alive and unmodified until the
+ * backward that consumes them has run; each outstanding forward needs its
+ * own `saved`.  The library cannot check that identity.
+ * Workspace: none.
+ */
+engram_status_t engram_gate_fwd(const void* x, const void* kv, const float* weight,
+                                const uint8_t* mask, void* out, float* saved,
+                                int64_t N, float eps, cudaStream_t stream);
+
+/* Bytes of workspace the backward needs: 4*(16*N + 4*5120*(N/64)) (cuDNN
+ * "Engram saved-state gate", workspace paragraph).  0 for invalid N. */
+size_t engram_gate_bwd_workspace_size(int64_t N);
+
+/*
+ * Saved-state gate, backward (cuDNN "Engram saved-state gate", layout and
+ * saved-state paragraphs; tile-kernels test_engram_gate_bwd.py).
+ *   x, kv, weight   the forward's inputs
+ *   saved    fp32 (N, 4, 4)   the forward's saved state (gate, dot, rstd_X, rstd_key)
+ *   grad_out bf16 (N, 4, 5120)
+ *   grad_x   bf16 (N, 4, 5120)  out: grad_out + gate-path term, rounded once
+ *   grad_kv  bf16 (N, 25600)    out: key grads in the key columns; the shared
+ *                               value's grad = sum over the 4 streams of
+ *                               gate_s * grad_out_s, summed in FP32 (stream
+ *                               order 0..3) before its one BF16 rounding
+ *   grad_weight fp32 (4, 5120)  out: sum over tokens of ddot * xh * kh, formed
+ *                               as per-64-token partials in the workspace and
+ *                               reduced in ascending block order (bitwise
+ *                               reproducible run to run)
+ *   workspace  >= engram_gate_bwd_workspace_size(N) bytes, 16-B aligned,
+ *              contents need no initialisation and are left undefined
+ *   N        64 <= N <= 8192, N % 64 == 0
+ * Two kernels on `stream`, no host synchronisation between them.
+ */
+engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weight,
+                                const float* saved, const void* grad_out, void* grad_x,
+                                void* grad_kv, float* grad_weight, void* workspace,
+                                size_t workspace_bytes, int64_t N, cudaStream_t stream);
+
+/*
+ * GateConv, forward (TileOPs "Engram Operators", EngramGateConvFwdOp).
+ *   H, k, v   bf16 (M, T, d)   hidden states, key and value projections
+ *   rms_w_h   fp32 (d)         RMSNorm weight shared by H and k
+ *   rms_w_v   fp32 (d)         RMSNorm weight of the gated value (conv input)
+ *   conv_w    fp32 (4, d)      depthwise causal taps; tap 3 multiplies the
+ *                              current token, tap j the token 3-j steps back
+ *   Y         bf16 (M, T, d)   out: SiLU(conv(u)) + vhat (to be added to H
+ *                              by the caller as a residual)
+ *   vhat      bf16 (M, T, d)   out: alpha * v, saved for the backward
+ *   alpha, rrms_h, rrms_k, rrms_v  fp32 (M, T)  out: scalar gate and the
+ *                              reciprocal RMS of H, k and vhat
+ * with rrms_x = 1/sqrt(mean(x^2) + eps), alpha = sigmoid(sum_i (H rrms_h w_h)_i
+ * (k rrms_k w_h)_i / sqrt(d)), u = vhat * rrms_v * rms_w_v, conv zero-padded
+ * at the start of each batch row.  Y and vhat are rounded once to BF16; the
+ * forward uses the unrounded vhat for rrms_v, u and Y.
+ *   1 <= M, 1 <= T, 8 <= d <= 65536, d % 8 == 0, M*T <= 2^31 - 1.
+ * Workspace: none.
+ */
+engram_status_t engram_gateconv_fwd(const void* H, const void* k, const void* v,
+                                    const float* rms_w_h, const float* rms_w_v,
+                                    const float* conv_w, void* Y, void* vhat, float* alpha,
+                                    float* rrms_h, float* rrms_k, float* rrms_v, int64_t M,
+                                    int64_t T, int64_t d, float eps, cudaStream_t stream);
+
+/* Bytes of workspace engram_gateconv_bwd needs for (M, T, d); 0 if invalid. */
+size_t engram_gateconv_bwd_workspace_size(int64_t M, int64_t T, int64_t d);
+
+/*
+ * GateConv, backward (TileOPs "Engram Operators", EngramGateConvBwdOp).
+ *   dY, H, k, v, rms_w_h, rms_w_v, conv_w   as in the forward
+ *   vhat, alpha, rrms_h, rrms_k, rrms_v     the forward's saved tensors
+ *   dH, dk, dv          bf16 (M, T, d)      out
+ *   drms_w_h, drms_w_v  fp32 (d)            out, summed over all M*T tokens
+ *   dconv_w             fp32 (4, d)         out, summed over all M*T tokens
+ *   workspace  >= engram_gateconv_bwd_workspace_size(M, T, d) bytes, 16-B
+ *              aligned: per-range fp32 weight-gradient partials, reduced in a
+ *              fixed order by a second kernel (bitwise reproducible)
+ * The backward reads the saved bf16 vhat (not alpha * v) wherever the forward
+ * used the gated value, and recomputes the gate's logit from H, k, rrms_h and
+ * rrms_k.  Same size limits as the forward.
+ */
+engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k,
+                                    const void* v, const float* rms_w_h,
+                                    const float* rms_w_v, const float* conv_w,
+                                    const void* vhat, const float* alpha,
+                                    const float* rrms_h, const float* rrms_k,
+                                    const float* rrms_v, void* dH, void* dk, void* dv,
+                                    float* drms_w_h, float* drms_w_v, float* dconv_w,
+                                    void* workspace, size_t workspace_bytes, int64_t M,
+                                    int64_t T, int64_t d, float eps, cudaStream_t stream);
+
+/*
+ * Diagnostics (not part of the pages' API).
+ * engram_device_error: synchronises the current device, copies the sticky
+ * device error word into *flags (0 = none; bit 0 = an asynchronous copy did
+ * not complete within its time limit) and clears it.  Returns ENGRAM_OK or
+ * ENGRAM_ERR_DEVICE.  Not for use inside a stream capture.
+ */
+engram_status_t engram_device_error(uint32_t* flags);
+
+/* Launch geometry chosen for a call, for tests and benchmarks: cluster size
+ * (CTAs per token row), threads per CTA, number of clusters, ring stages and
+ * dynamic shared memory bytes.  `op`: 0 gate fwd, 1 gate bwd, 2 gateconv fwd,
+ * 3 gateconv bwd.  n0, n1, n2 = (N) for the gate, (M, T, d) for GateConv. */
+typedef struct {
+    int cluster;
+    int threads;
+    int clusters;
+    int stages;
+    int smem_bytes;
+} engram_launch_info_t;
+engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
+                                   engram_launch_info_t* info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENGRAM_H_ */

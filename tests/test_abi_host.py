@@ -1,0 +1,141 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+The library must load and export every function include/engram.h declares,
+and argument validation must reject bad calls before any device work.  The
+fake pointers used here are never valid for a kernel: every call below fails
+validation, so nothing is enqueued even on a machine with a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import engram_memory_gating_gb300 as eg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HDR = os.path.join(ROOT, "include", "engram.h")
+
+OK, ENULL, EALIGN, ESHAPE, EOVERLAP, EWS, EDEV = 0, 1, 2, 3, 4, 5, 6
+
+
+def declared_functions():
+    text = open(HDR).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(engram_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = eg.load()
+    names = declared_functions()
+    assert len(names) >= 9
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(names) == set(eg.EXPORTED_SYMBOLS)
+
+
+def test_status_strings():
+    lib = eg.load()
+    for code in range(8):
+        assert lib.engram_status_string(code)
+
+
+def test_gate_bwd_workspace_size_formula():
+    # 4 * (16 N + 4 * 5120 * (N // 64)) bytes
+    for N in (64, 128, 4096, 8192):
+        assert eg.engram_gate_bwd_workspace_size(N) == 4 * (16 * N + 4 * 5120 * (N // 64))
+    assert eg.engram_gate_bwd_workspace_size(8192) == 11010048
+    for N in (0, 1, 63, 100, 8256, -64):
+        assert eg.engram_gate_bwd_workspace_size(N) == 0
+
+
+def test_gateconv_bwd_workspace_size():
+    assert eg.engram_gateconv_bwd_workspace_size(4, 4096, 4096) > 0
+    assert eg.engram_gateconv_bwd_workspace_size(8, 8192, 7168) > 0
+    assert eg.engram_gateconv_bwd_workspace_size(1, 1, 8) > 0
+    for shape in ((0, 4, 64), (1, 0, 64), (1, 4, 12), (1, 4, 0), (1, 4, 8 * 1031)):
+        assert eg.engram_gateconv_bwd_workspace_size(*shape) == 0
+
+
+A = 1 << 20  # fake, 16-byte aligned, never dereferenced
+
+
+def p(v):
+    return ctypes.c_void_p(v)
+
+
+def gate_fwd(x=A, kv=2 * A * 1024, w=3 * A * 2048, mask=None, out=4 * A * 4096, saved=None,
+             N=4, eps=1e-20):
+    return eg.load().engram_gate_fwd(p(x), p(kv), p(w), p(mask) if mask else None, p(out),
+                                     p(saved) if saved else None, N, eps, None)
+
+
+def test_gate_fwd_validation():
+    assert gate_fwd(x=0) == ENULL
+    assert gate_fwd(out=0) == ENULL
+    assert gate_fwd(x=A + 8) == EALIGN
+    assert gate_fwd(saved=5 * A * 8192 + 4) == EALIGN
+    assert gate_fwd(N=0) == ESHAPE
+    assert gate_fwd(N=4194241) == ESHAPE
+    assert gate_fwd(out=A) == EOVERLAP                       # out aliases x
+    assert gate_fwd(out=A + 4 * 40960 - 16) == EOVERLAP      # partial overlap
+    assert gate_fwd(saved=4 * A * 4096 + 16) == EOVERLAP     # saved inside out
+
+
+def gate_bwd(N=64, ws_bytes=None, **kw):
+    lib = eg.load()
+    args = dict(x=A, kv=A * 100, w=A * 200, saved=A * 300, g=A * 400, gx=A * 500,
+                gkv=A * 600, gw=A * 700, ws=A * 800)
+    args.update(kw)
+    wsb = eg.engram_gate_bwd_workspace_size(N) if ws_bytes is None else ws_bytes
+    return lib.engram_gate_bwd(*(p(args[k]) for k in ("x", "kv", "w", "saved", "g", "gx",
+                                                      "gkv", "gw", "ws")), wsb, N, None)
+
+
+def test_gate_bwd_validation():
+    assert gate_bwd(ws=0) == ENULL
+    assert gate_bwd(N=100, ws_bytes=1 << 30) == ESHAPE
+    assert gate_bwd(N=8256, ws_bytes=1 << 30) == ESHAPE
+    assert gate_bwd(N=0, ws_bytes=1 << 30) == ESHAPE
+    assert gate_bwd(gx=A * 500 + 2) == EALIGN
+    assert gate_bwd(ws_bytes=eg.engram_gate_bwd_workspace_size(64) - 16) == EWS
+    assert gate_bwd(gkv=A * 100) == EOVERLAP                 # grad_kv aliases kv
+    assert gate_bwd(ws=A * 700 + 1024) == EOVERLAP           # workspace inside grad_weight
+
+
+def test_gateconv_validation():
+    lib = eg.load()
+    base = [A * i for i in range(1, 13)]
+
+    def call(ptrs, M=2, T=8, d=64):
+        return lib.engram_gateconv_fwd(*(p(v) for v in ptrs), M, T, d, 1e-6, None)
+
+    assert call([0] + base[1:]) == ENULL
+    assert call(base, d=12) == ESHAPE
+    assert call(base, M=0) == ESHAPE
+    assert call(base, d=8 * 1031) == ESHAPE
+    bad = list(base)
+    bad[7] = base[7] + 4
+    assert call(bad) == EALIGN
+    ov = list(base)
+    ov[6] = base[0]                                          # Y aliases H
+    assert call(ov) == EOVERLAP
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="needs a host without a GPU")
+def test_valid_arguments_without_a_device_report_device_error():
+    assert gate_fwd() == EDEV
+    info = eg._LaunchInfo()
+    assert eg.load().engram_launch_info(0, 64, 0, 0, ctypes.byref(info)) == EDEV
+
+
+def test_binding_has_no_cpu_fallback():
+    # the product package never imports the oracle
+    import engram_memory_gating_gb300 as pkg
+    src_dir = os.path.dirname(pkg.__file__)
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle|from\s+\.\.\s*import\s+oracle)",
+                     re.M)
+    for name in os.listdir(src_dir):
+        if name.endswith(".py"):
+            assert not pat.search(open(os.path.join(src_dir, name)).read()), name

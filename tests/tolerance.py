@@ -1,0 +1,61 @@
+"""Comparison rules between the CUDA path and the fp64 oracle.
+
+bf16 tensors (out, grad_x, grad_kv, Y, vhat, dH, dk, dv):
+    |gpu - exact| <= 2^-7 |exact| + 2^-16 rms(row of exact)
+  2^-7 = 7.8e-3 is "within one bf16 ulp" (the ulp of a bf16 value is at most
+  2^-7 of it).  The second term is the near-zero allowance: a value formed in
+  fp32 from terms of the row's magnitude that cancel cannot be resolved below
+  about 2^-23 of those terms; 2^-16 of the row's RMS leaves a 100x margin and
+  is still far below one ulp of any typical element.  A row whose exact
+  values are all zero must match exactly.
+fp32 tensors (saved gate/dot/rstd, grad_weight, alpha, rrms_*):
+    |gpu - exact| <= 1e-4 |exact| + 1e-6
+fp32 weight gradients of GateConv, summed over up to 65536 tokens:
+    |gpu - exact| <= 1e-4 |exact| + 1e-6 max(1, max|exact|)
+  (the near-zero allowance scales with the magnitude of the summed vector,
+  because fp32 partial sums of that magnitude carry rounding of that order).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BF16_REL = 2.0 ** -7
+ROW_FLOOR = 2.0 ** -16
+F32_REL = 1e-4
+F32_ABS = 1e-6
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits).view(np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def _report(name, got, exact, tol, bad):
+    idx = np.argwhere(bad)[:5]
+    lines = [f"{name}: {int(bad.sum())} of {bad.size} elements out of tolerance"]
+    for i in idx:
+        t = tuple(int(v) for v in i)
+        lines.append(f"  at {t}: got {got[t]!r} exact {exact[t]!r} tol {tol[t]!r}")
+    return "\n".join(lines)
+
+
+def check_bf16(name, got_bits, exact, row_axis=-1):
+    got = bf16_bits_to_f64(got_bits).reshape(exact.shape)
+    rms = np.sqrt(np.mean(exact * exact, axis=row_axis, keepdims=True))
+    tol = BF16_REL * np.abs(exact) + ROW_FLOOR * rms
+    diff = np.abs(got - exact)
+    bad = ~(diff <= tol)
+    assert not bad.any(), _report(name, got, exact, tol, bad)
+    return float(np.max(diff / np.maximum(tol, 1e-300))) if diff.size else 0.0
+
+
+def check_f32(name, got, exact, rel=F32_REL, abs_=F32_ABS):
+    got = np.asarray(got, dtype=np.float64).reshape(exact.shape)
+    tol = rel * np.abs(exact) + abs_
+    bad = ~(np.abs(got - exact) <= tol)
+    assert not bad.any(), _report(name, got, exact, tol, bad)
+
+
+def check_f32_sum(name, got, exact):
+    scale = max(1.0, float(np.max(np.abs(exact)))) if exact.size else 1.0
+    check_f32(name, got, exact, F32_REL, F32_ABS * scale)
