@@ -122,13 +122,16 @@ class Clocks:
 
 
 def time_region(torch, fn, reps, stream):
+    """Mean ms of fn() over reps, CUDA events on `stream`; fn's work (graph
+    replays included) is issued on that same stream."""
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    start.record(stream)
-    for _ in range(reps):
-        fn()
-    end.record(stream)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            fn()
+        end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / reps
 
@@ -164,8 +167,7 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
     fn = lambda: eg.engram_gate_fwd(inp["x"], inp["kv"], inp["weight"], inp["mask"], out, saved,
                                     stream=s)
     g = graph_of(torch, fn, s)
-    for _ in range(3):
-        g.replay()
+    time_region(torch, g.replay, 3, s)
     ms = time_region(torch, g.replay, 10, s)
     ops["gate_fwd_N262144"] = op_entry(ms, N * FWD_BYTES_PER_TOKEN + FWD_FIXED, peak)
     del inp, out, saved, g
@@ -187,9 +189,7 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
                                            ci["rms_w_v"], ci["conv_w"], *res[1:], *grads, ws,
                                            stream=s)
         gf, gb = graph_of(torch, f, s), graph_of(torch, b, s)
-        for _ in range(3):
-            gf.replay()
-            gb.replay()
+        time_region(torch, lambda: (gf.replay(), gb.replay()), 3, s)
         tok = M * T
         ops[name + "_fwd"] = op_entry(time_region(torch, gf.replay, 10, s),
                                       tok * (10 * d + 16) + 24 * d, peak)
