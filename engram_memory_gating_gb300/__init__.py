@@ -28,7 +28,7 @@ __all__ = [
     "EngramError", "load", "build",
     "engram_gate_fwd", "engram_gate_bwd", "engram_gate_bwd_workspace_size",
     "engram_gateconv_fwd", "engram_gateconv_bwd", "engram_gateconv_bwd_workspace_size",
-    "engram_device_error", "engram_launch_info",
+    "engram_device_error", "engram_launch_info", "engram_gate_bwd_noalloc",
     "gate_forward", "gate_backward", "gateconv_forward", "gateconv_backward",
     "GATE_EPS", "GATECONV_EPS", "EXPORTED_SYMBOLS",
 ]
@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "engram_status_string", "engram_gate_fwd", "engram_gate_bwd_workspace_size",
     "engram_gate_bwd", "engram_gateconv_fwd", "engram_gateconv_bwd_workspace_size",
     "engram_gateconv_bwd", "engram_device_error", "engram_launch_info",
+    "engram_gate_bwd_noalloc",
 )
 
 _STATUS = {0: "ok", 1: "null pointer", 2: "misaligned pointer", 3: "size out of range",
@@ -89,6 +90,7 @@ def load(path: str | None = None):
         lib.engram_gate_bwd_workspace_size.argtypes = [I64]
         lib.engram_gate_bwd_workspace_size.restype = SZ
         lib.engram_gate_bwd.argtypes = [P, P, P, P, P, P, P, P, P, SZ, I64, P]
+        lib.engram_gate_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I64, P]
         lib.engram_gateconv_fwd.argtypes = [P] * 12 + [I64, I64, I64, F, P]
         lib.engram_gateconv_bwd_workspace_size.argtypes = [I64, I64, I64]
         lib.engram_gateconv_bwd_workspace_size.restype = SZ
@@ -96,7 +98,8 @@ def load(path: str | None = None):
         lib.engram_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         lib.engram_launch_info.argtypes = [ctypes.c_int, I64, I64, I64,
                                            ctypes.POINTER(_LaunchInfo)]
-        for name in ("engram_gate_fwd", "engram_gate_bwd", "engram_gateconv_fwd",
+        for name in ("engram_gate_fwd", "engram_gate_bwd", "engram_gate_bwd_noalloc",
+                     "engram_gateconv_fwd",
                      "engram_gateconv_bwd", "engram_device_error", "engram_launch_info"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -164,6 +167,22 @@ def engram_gate_bwd(x, kv, weight, saved, grad_out, grad_x, grad_kv, grad_weight
     _check("engram_gate_bwd", load().engram_gate_bwd(
         _ptr(x), _ptr(kv), _ptr(weight), _ptr(saved), _ptr(grad_out), _ptr(grad_x),
         _ptr(grad_kv), _ptr(grad_weight), _ptr(workspace), nbytes, N, _stream(stream)))
+
+
+def engram_gate_bwd_noalloc(x, kv, weight, saved, grad_out, grad_x, grad_kv, grad_weight,
+                            stream=None):
+    """engram_gate_bwd without a workspace argument, for callers that cannot
+    allocate: the library's own fixed device array serves as the workspace
+    (N <= 2048).  Calls that can overlap on the GPU must be serialised."""
+    N = x.shape[0]
+    _need(saved, torch.float32, (N, S_GATE, 4), "saved")
+    _need(grad_out, torch.bfloat16, (N, S_GATE, D_GATE), "grad_out")
+    _need(grad_x, torch.bfloat16, (N, S_GATE, D_GATE), "grad_x")
+    _need(grad_kv, torch.bfloat16, (N, (S_GATE + 1) * D_GATE), "grad_kv")
+    _need(grad_weight, torch.float32, (S_GATE, D_GATE), "grad_weight")
+    _check("engram_gate_bwd_noalloc", load().engram_gate_bwd_noalloc(
+        _ptr(x), _ptr(kv), _ptr(weight), _ptr(saved), _ptr(grad_out), _ptr(grad_x),
+        _ptr(grad_kv), _ptr(grad_weight), N, _stream(stream)))
 
 
 def engram_gateconv_fwd(H, k, v, rms_w_h, rms_w_v, conv_w, Y, vhat, alpha, rrms_h, rrms_k,

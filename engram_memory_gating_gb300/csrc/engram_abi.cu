@@ -504,6 +504,50 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
     return ENGRAM_OK;
 }
 
+}  // extern "C"
+
+// Workspace of engram_gate_bwd_noalloc: a file-scope device array, so that
+// callers without an allocator can run the backward.  Host code never uses
+// the symbol itself as a pointer: its device address is looked up once per
+// device, with that device current, and that address is what the kernels get.
+static __device__ __align__(256) unsigned char g_gate_bwd_scratch[ENGRAM_GATE_BWD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+bool g_scratch_ready[eg::kMaxDevices] = {};
+void* g_scratch_addr[eg::kMaxDevices] = {};
+}  // namespace
+
+extern "C" {
+
+engram_status_t engram_gate_bwd_noalloc(const void* x, const void* kv, const float* weight,
+                                        const float* saved, const void* grad_out, void* grad_x,
+                                        void* grad_kv, float* grad_weight, int64_t N,
+                                        cudaStream_t stream) {
+    if (N < 64 || N > ENGRAM_GATE_BWD_NOALLOC_MAX_TOKENS || N % 64 != 0) return ENGRAM_ERR_SHAPE;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= eg::kMaxDevices) {
+            (void)cudaGetLastError();
+            return ENGRAM_ERR_DEVICE;
+        }
+        if (!g_scratch_ready[dev]) {
+            void* ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_gate_bwd_scratch) != cudaSuccess || ptr == nullptr) {
+                (void)cudaGetLastError();
+                return ENGRAM_ERR_DEVICE;
+            }
+            g_scratch_addr[dev] = ptr;
+            g_scratch_ready[dev] = true;
+        }
+        scratch = g_scratch_addr[dev];
+    }
+    // the regular backward, with the library's array as its workspace
+    return engram_gate_bwd(x, kv, weight, saved, grad_out, grad_x, grad_kv, grad_weight, scratch,
+                           ENGRAM_GATE_BWD_NOALLOC_SCRATCH_BYTES, N, stream);
+}
+
 engram_status_t engram_device_error(uint32_t* flags) {
     if (!flags) return ENGRAM_ERR_NULL;
     unsigned int v = 0u, zero = 0u;

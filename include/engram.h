@@ -181,6 +181,41 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
                                     int64_t T, int64_t d, float eps, cudaStream_t stream);
 
 /*
+ * Saved-state gate, backward, for callers that cannot allocate.  The pages
+ * have no counterpart to this entry point.
+ *
+ * Some callers cannot call cudaMalloc (or any allocator, PyTorch's included)
+ * at the point where they run the backward: code that runs while a stream
+ * is being captured into a CUDA graph, plug-ins embedded in a host framework
+ * that owns all device memory and forbids outside allocations, and runtimes
+ * that work from a fixed, pre-planned memory budget.  They can pass inputs
+ * and outputs they already own, but no workspace.  This call is
+ * engram_gate_bwd with its workspace taken from a fixed array inside the
+ * library (ENGRAM_GATE_BWD_NOALLOC_SCRATCH_BYTES, enough for N up to
+ * ENGRAM_GATE_BWD_NOALLOC_MAX_TOKENS).  Every GPU that loads the library
+ * holds that array until the process exits.
+ *   Arguments: as engram_gate_bwd, without the workspace pair.
+ *   N: 64 <= N <= ENGRAM_GATE_BWD_NOALLOC_MAX_TOKENS, N % 64 == 0; a larger N
+ *      returns ENGRAM_ERR_SHAPE and enqueues nothing (use engram_gate_bwd
+ *      with a caller-provided workspace instead).
+ *   The first call on each device looks up the array's device address with
+ *   that device current (one-time set-up); make that first call before any
+ *   stream capture.  The call itself allocates nothing.
+ *   All calls share the one array, which keeps the previous call's contents;
+ *   nothing in it needs to start at zero (each call writes every slot it
+ *   reads before reading it).  Calls whose kernels can overlap on the GPU
+ *   (different streams without ordering between them) race on the array and
+ *   give undefined results: serialise them.
+ */
+#define ENGRAM_GATE_BWD_NOALLOC_MAX_TOKENS 2048
+#define ENGRAM_GATE_BWD_NOALLOC_SCRATCH_BYTES \
+    (4 * (16 * ENGRAM_GATE_BWD_NOALLOC_MAX_TOKENS + 4 * 5120 * (ENGRAM_GATE_BWD_NOALLOC_MAX_TOKENS / 64)))
+engram_status_t engram_gate_bwd_noalloc(const void* x, const void* kv, const float* weight,
+                                        const float* saved, const void* grad_out, void* grad_x,
+                                        void* grad_kv, float* grad_weight, int64_t N,
+                                        cudaStream_t stream);
+
+/*
  * Diagnostics (not part of the pages' API).
  * engram_device_error: synchronises the current device, copies the sticky
  * device error word into *flags (0 = none; bit 0 = an asynchronous copy did
