@@ -53,6 +53,20 @@ EG_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
                  : "memory");
 }
 
+// Same, with acquire at cluster scope: for phases completed by other CTAs'
+// st.async writes into this CTA's shared memory.
+EG_DEV bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 EG_DEV bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -77,6 +91,27 @@ EG_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
         if ((it & 63u) == 63u && globaltimer() - t0 > kWaitLimitNs) return false;
     }
     return false;
+}
+
+EG_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_addr(bar);
+    if (mbar_try_wait_cluster(addr, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 0; it < kWaitMaxIters; ++it) {
+        if (mbar_try_wait_cluster(addr, parity)) return true;
+        if ((it & 63u) == 63u && globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+// Asynchronous 8-byte store into the shared memory of a CTA of this cluster
+// (addresses from map_to_rank), completing `bytes` on that CTA's mbarrier.
+EG_DEV void st_async_f2(uint32_t remote_addr, float a, float b, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+            remote_addr),
+        "f"(a), "f"(b), "r"(remote_bar)
+        : "memory");
 }
 
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
@@ -178,6 +213,54 @@ EG_DEV uint32_t pack_bf16x2(float lo, float hi) {
 EG_DEV uint4 pack8(const float (&f)[8]) {
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                       pack_bf16x2(f[6], f[7]));
+}
+
+// ------------------------------------------------------- packed fp32 pairs
+// Blackwell executes two fp32 lanes per instruction on float2 operands.
+EG_DEV float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+EG_DEV float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+EG_DEV float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+// a - b with one rounding (b * -1 + a)
+EG_DEV float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.f, -1.f), a); }
+EG_DEV float2 splat2(float a) { return make_float2(a, a); }
+EG_DEV float2 bf2(uint32_t u) { return make_float2(bf_lo(u), bf_hi(u)); }
+EG_DEV uint32_t pack2(float2 v) { return pack_bf16x2(v.x, v.y); }
+
+// TwoSum on both lanes: s + e == a + b exactly, lane by lane.
+EG_DEV void two_sum2(float2 a, float2 b, float2& s, float2& e) {
+    s = add2(a, b);
+    const float2 bb = sub2(s, a);
+    const float2 aa = sub2(s, bb);
+    e = add2(sub2(a, aa), sub2(b, bb));
+}
+
+// (hi, lo) += a * b on both lanes, product and sum errors kept in lo.
+EG_DEV void cacc_prod_x2(float2& hi, float2& lo, float2 a, float2 b) {
+    const float2 t = mul2(a, b);
+    const float2 pe = fma2(a, b, make_float2(-t.x, -t.y));
+    float2 s, e;
+    two_sum2(hi, t, s, e);
+    hi = s;
+    lo = add2(lo, add2(e, pe));
+}
+
+// (hi, lo) += t on both lanes.
+EG_DEV void cacc_add_x2(float2& hi, float2& lo, float2 t) {
+    float2 s, e;
+    two_sum2(hi, t, s, e);
+    hi = s;
+    lo = add2(lo, e);
+}
+
+// (hi, lo) += (ah + al) * b on both lanes, ah + al a double-float factor.
+EG_DEV void cacc_prod2_x2(float2& hi, float2& lo, float2 ah, float2 al, float2 b) {
+    const float2 t = mul2(ah, b);
+    float2 pe = fma2(ah, b, make_float2(-t.x, -t.y));
+    pe = fma2(al, b, pe);
+    float2 s, e;
+    two_sum2(hi, t, s, e);
+    hi = s;
+    lo = add2(lo, add2(e, pe));
 }
 
 // ------------------------------------------------- error-free transformations

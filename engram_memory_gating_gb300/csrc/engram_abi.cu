@@ -24,7 +24,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kGateD = ENGRAM_GATE_HIDDEN;
-constexpr int kGateFwdStages = 4;
+constexpr int kGateFwdStages = 3;
 constexpr int kGateBwdStages = 3;
 constexpr int kGcFwdStages = 6;
 constexpr int kGcBwdStages = 6;  // >= 5: rows of tokens tau-3 .. tau+1 stay resident
@@ -149,7 +149,7 @@ engram_status_t launch_status(cudaError_t e) {
 // ---------------------------------------------------------------- geometry
 
 bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngroups) {
-    const int C = pick_cluster(kGateD / 8, 160);
+    const int C = pick_cluster(kGateD / 8, 128);
     ncols = kGateD / C;
     ngroups = ncols / 8;
     c.cluster = C;
@@ -163,7 +163,7 @@ bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngr
 }
 
 bool gate_bwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngroups) {
-    const int C = pick_cluster(kGateD / 8, 160);
+    const int C = pick_cluster(kGateD / 8, 128);
     ncols = kGateD / C;
     ngroups = ncols / 8;
     c.cluster = C;

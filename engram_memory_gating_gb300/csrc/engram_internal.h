@@ -11,13 +11,16 @@ namespace eg {
 // equal slices of at most `max_groups` groups; 0 if none does.
 int pick_cluster(int64_t d, int max_groups);
 
-// Shared-memory layout common to the row-split kernels: mbarriers, per-warp
-// partials, the cluster exchange slots, then the ring of stages.
-constexpr int kSmemBarOff = 0;      // up to 16 mbarriers (8 B each)
-constexpr int kSmemRedOff = 128;    // 32 warps x 16 floats
-constexpr int kSmemXchOff = 128 + 32 * 16 * 4;  // 2 slots x 16 floats
-constexpr int kSmemRingOff = kSmemXchOff + 2 * 16 * 4 + 64;  // 16-byte aligned
+// Shared-memory layout common to the row-split kernels: mbarriers (ring
+// stages, then the two exchange slots), per-warp partials (two buffers), the
+// cluster exchange slots (2 x 8 ranks x 16 floats), then the ring of stages.
 constexpr int kMaxStages = 16;
+constexpr int kSmemBarOff = 0;                         // 16 stage + 2 exchange mbarriers
+constexpr int kSmemRxBarOff = kMaxStages * 8;
+constexpr int kSmemRedOff = 256;                       // 2 x 32 warps x 16 floats
+constexpr int kSmemXchOff = kSmemRedOff + 2 * 32 * 16 * 4;  // 2 x 8 ranks x 16 floats
+constexpr int kSmemRingOff = kSmemXchOff + 2 * 8 * 16 * 4;  // 128-byte aligned
+static_assert(kSmemRingOff % 128 == 0, "ring alignment");
 
 struct GateFwdParams {
     const uint16_t* x;

@@ -24,8 +24,12 @@
 // Layout of the work: a cluster of C CTAs owns whole 64-token blocks; each CTA
 // a column slice of every stream.  Per token the slice rows of X, the keys, v
 // and grad_out plus the 64-byte saved record are bulk-copied into a ring of
-// shared-memory stages; dgate (4 full-row reductions, compensated) is reduced
-// across the warp, the CTA and the cluster; each thread then writes its 8
+// shared-memory stages; dgate (4 full-row reductions, compensated, packed
+// fp32x2) is reduced across the warp and the CTA, and each CTA pushes its 4
+// (hi, lo) pairs into every CTA of the cluster with st.async (mbarrier
+// completion, no cluster barrier per token).  The loop is software-pipelined:
+// token j+1's dgate pass runs while token j's partials travel.  Each thread
+// then writes its 8
 // columns of grad_x, grad_key and grad_v and accumulates grad_w for its
 // columns over all tokens of the cluster as an unevaluated (hi, lo) pair.
 // With at least two 64-token blocks there are at most half as many clusters
@@ -75,11 +79,12 @@ EG_DEV void warp_reduce_pairs4(const float (&acc)[8], int lane, float& v0, float
     v1 = p1;
 }
 
-__global__ void __launch_bounds__(256) gate_bwd_kernel(const GateBwdParams p) {
+__global__ void __launch_bounds__(128, 2) gate_bwd_kernel(const GateBwdParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBarOff);
-    float* red = reinterpret_cast<float*>(smem + kSmemRedOff);
-    float* xch = reinterpret_cast<float*>(smem + kSmemXchOff);
+    uint64_t* rxbar = reinterpret_cast<uint64_t*>(smem + kSmemRxBarOff);
+    float* red = reinterpret_cast<float*>(smem + kSmemRedOff);  // [2][warps][8]
+    float* rx = reinterpret_cast<float*>(smem + kSmemXchOff);   // [2][8 ranks][16]
     unsigned char* ring = smem + kSmemRingOff;
 
     const int tid = threadIdx.x;
@@ -96,18 +101,21 @@ __global__ void __launch_bounds__(256) gate_bwd_kernel(const GateBwdParams p) {
     const uint32_t row_bytes = static_cast<uint32_t>(p.ncols) * 2u;
     const uint32_t stage_bytes = kRows * row_bytes + 64u;
     const int stages = p.stages;
+    const uint32_t xbytes = C * 8u * 4u;  // 4 streams x (hi, lo) from every CTA
 
-    float w[kS][8];
+    float2 w2[kS][4];
 #pragma unroll
     for (int s = 0; s < kS; ++s) {
         if (active) {
             const float4 a = __ldg(reinterpret_cast<const float4*>(p.w + s * d + col0 + 8 * tid));
             const float4 b = __ldg(reinterpret_cast<const float4*>(p.w + s * d + col0 + 8 * tid + 4));
-            w[s][0] = a.x; w[s][1] = a.y; w[s][2] = a.z; w[s][3] = a.w;
-            w[s][4] = b.x; w[s][5] = b.y; w[s][6] = b.z; w[s][7] = b.w;
+            w2[s][0] = make_float2(a.x, a.y);
+            w2[s][1] = make_float2(a.z, a.w);
+            w2[s][2] = make_float2(b.x, b.y);
+            w2[s][3] = make_float2(b.z, b.w);
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[s][e] = 0.f;
+            for (int e = 0; e < 4; ++e) w2[s][e] = make_float2(0.f, 0.f);
         }
     }
 
@@ -120,9 +128,13 @@ __global__ void __launch_bounds__(256) gate_bwd_kernel(const GateBwdParams p) {
 
     if (tid == 0) {
         for (int st = 0; st < stages; ++st) mbar_init(&full[st], 1);
+        mbar_init(&rxbar[0], 1);
+        mbar_init(&rxbar[1], 1);
         fence_mbar_init();
+        if (ntok > 0) mbar_arrive_expect_tx(&rxbar[0], xbytes);
+        if (ntok > 1) mbar_arrive_expect_tx(&rxbar[1], xbytes);
     }
-    __syncthreads();
+    cluster_sync();
 
     auto issue = [&](long long j) {
         const long long n = token_of(j);
@@ -147,71 +159,86 @@ __global__ void __launch_bounds__(256) gate_bwd_kernel(const GateBwdParams p) {
         for (long long j = 0; j < pro; ++j) issue(j);
     }
 
-    float phi[kS][8], plo[kS][8];  // grad_w of this thread's columns, hi + lo
+    float2 phi[kS][4], plo[kS][4];  // grad_w of this thread's columns, hi + lo
 #pragma unroll
     for (int s = 0; s < kS; ++s)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) phi[s][e] = plo[s][e] = 0.f;
+        for (int e = 0; e < 4; ++e) phi[s][e] = plo[s][e] = make_float2(0.f, 0.f);
 
     bool failed = false;
-    for (long long j = 0; j < ntok; ++j) {
-        const long long n = token_of(j);
+
+    // dgate_s = sum_i g_{s,i} v_i (g*v exact in fp32; compensated sum); the
+    // warp's 4 (hi, lo) pairs go to red[j & 1]
+    auto reduce_pass = [&](long long j) {
         const int st = static_cast<int>(j % stages);
         if (!failed && !mbar_wait(&full[st], static_cast<uint32_t>((j / stages) & 1))) failed = true;
         const unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
-        const float* sv = reinterpret_cast<const float*>(b + kRows * row_bytes);
-
-        // ---- dgate_s = sum_i g_{s,i} v_i (g*v exact in fp32; compensated sum)
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
         if (active) {
-            float vf[8];
-            unpack8(lds128(b + 2 * kS * row_bytes + 16 * tid), vf);
+            const uint4 vq = lds128(b + 2 * kS * row_bytes + 16 * tid);
+            const float2 v2[4] = {bf2(vq.x), bf2(vq.y), bf2(vq.z), bf2(vq.w)};
 #pragma unroll
             for (int s = 0; s < kS; ++s) {
-                float gf[8];
-                unpack8(lds128(b + (2 * kS + 1 + s) * row_bytes + 16 * tid), gf);
-                float hi = 0.f, lo = 0.f;
+                const uint4 gq = lds128(b + (2 * kS + 1 + s) * row_bytes + 16 * tid);
+                const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+                float2 hi = make_float2(0.f, 0.f), lo = hi;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) cacc_add(hi, lo, __fmul_rn(gf[e], vf[e]));
-                acc[2 * s] = hi;
-                acc[2 * s + 1] = lo;
+                for (int e = 0; e < 4; ++e) cacc_add_x2(hi, lo, mul2(bf2(gw[e]), v2[e]));
+                float h = hi.x, l = lo.x;
+                cacc_merge(h, l, hi.y, lo.y);
+                acc[2 * s] = h;
+                acc[2 * s + 1] = l;
             }
         }
         float v0, v1;
         warp_reduce_pairs4(acc, lane, v0, v1);
         if ((lane & 7) == 0) {
             const int sidx = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-            *reinterpret_cast<float2*>(red + warp * 8 + sidx * 2) = make_float2(v0, v1);
+            *reinterpret_cast<float2*>(red + (j & 1) * (32 * 8) + warp * 8 + sidx * 2) =
+                make_float2(v0, v1);
         }
-        __syncthreads();
-        if (tid == 0 && j >= 1 && j - 1 + stages < ntok) {
-            fence_proxy_async();
-            issue(j - 1 + stages);
-        }
-        float* slot = xch + (j & 1) * 8;
-        if (warp == 0 && lane < kS) {
-            float a0 = red[2 * lane], a1 = red[2 * lane + 1];
+    };
+
+    auto push = [&](long long j) {
+        if (lane < kS) {
+            const float* r = red + (j & 1) * (32 * 8);
+            float a0 = r[2 * lane], a1 = r[2 * lane + 1];
             for (int wi = 1; wi < nwarps; ++wi)
-                cacc_merge(a0, a1, red[wi * 8 + 2 * lane], red[wi * 8 + 2 * lane + 1]);
-            *reinterpret_cast<float2*>(slot + 2 * lane) = make_float2(a0, a1);
+                cacc_merge(a0, a1, r[wi * 8 + 2 * lane], r[wi * 8 + 2 * lane + 1]);
+            const int slot = static_cast<int>(j & 1);
+            const uint32_t dst = smem_addr(rx + (slot * 8 + rank) * 16 + 2 * lane);
+            const uint32_t bar = smem_addr(&rxbar[slot]);
+            for (uint32_t r2 = 0; r2 < C; ++r2)
+                st_async_f2(map_to_rank(dst, r2), a0, a1, map_to_rank(bar, r2));
         }
-        cluster_sync();
-        // ---- per-stream coefficients from the cluster totals (rank order)
+    };
+
+    if (ntok > 0) reduce_pass(0);
+    __syncthreads();
+    if (warp == 0 && ntok > 0) push(0);
+
+    for (long long j = 0; j < ntok; ++j) {
+        const long long n = token_of(j);
+        const int slot = static_cast<int>(j & 1);
+        const int st = static_cast<int>(j % stages);
+        const unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
+        if (j + 1 < ntok) reduce_pass(j + 1);
+
+        // ---- per-stream coefficients of token j from the cluster totals
+        if (!failed && !mbar_wait_cluster(&rxbar[slot], static_cast<uint32_t>((j >> 1) & 1)))
+            failed = true;
         float cA = 0.f, cAl = 0.f, cB = 0.f, cC = 0.f, cG = 0.f;
         if (lane < kS) {
-            const uint32_t a = smem_addr(slot + 2 * lane);
-            const float2 r0 = ld_cluster_f2(map_to_rank(a, 0));
-            float hi = r0.x, lo = r0.y;
-            for (uint32_t r = 1; r < C; ++r) {
-                const float2 rr = ld_cluster_f2(map_to_rank(a, r));
-                cacc_merge(hi, lo, rr.x, rr.y);
-            }
+            const float* r = rx + slot * 8 * 16 + 2 * lane;
+            float hi = r[0], lo = r[1];
+            for (uint32_t rr = 1; rr < C; ++rr) cacc_merge(hi, lo, r[rr * 16], r[rr * 16 + 1]);
+            const float* sv = reinterpret_cast<const float*>(b + kRows * row_bytes);
             const double dgate = static_cast<double>(hi) + static_cast<double>(lo);
             const float gate = sv[4 * lane + 0];
             const double dot = sv[4 * lane + 1];
-            const double rx = sv[4 * lane + 2];
+            const double rx_ = sv[4 * lane + 2];
             const double rk = sv[4 * lane + 3];
             const double ad = fabs(dot);
             const double sqm = sqrt(fmax(ad, 1e-6));
@@ -220,48 +247,60 @@ __global__ void __launch_bounds__(256) gate_bwd_kernel(const GateBwdParams p) {
             const double qd = (ad >= 1e-6) ? 0.5 / sqm : 0.0;
             const double ddot = (gate == 0.f) ? 0.0 : dgate * dsig * qd;
             const double dd = dot / static_cast<double>(d);
-            const double av = ddot * rx * rk;
+            const double av = ddot * rx_ * rk;
             cA = static_cast<float>(av);
             cAl = static_cast<float>(av - static_cast<double>(cA));
-            cB = static_cast<float>(ddot * rx * rx * dd);
+            cB = static_cast<float>(ddot * rx_ * rx_ * dd);
             cC = static_cast<float>(ddot * rk * rk * dd);
             cG = gate;
         }
-        float A[kS], Al[kS], B[kS], Ck[kS], Gt[kS];
-#pragma unroll
-        for (int s = 0; s < kS; ++s) {
-            A[s] = __shfl_sync(kFullMask, cA, s);
-            Al[s] = __shfl_sync(kFullMask, cAl, s);
-            B[s] = __shfl_sync(kFullMask, cB, s);
-            Ck[s] = __shfl_sync(kFullMask, cC, s);
-            Gt[s] = __shfl_sync(kFullMask, cG, s);
-        }
 
-        // ---- elementwise: grad_x, grad_key, grad_v, grad_w partial
+        // ---- elementwise: grad_x, grad_key, grad_v, grad_w (packed pairs)
         if (active) {
-            float gv[8];
+            float2 gv[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) gv[e] = 0.f;
+            for (int e = 0; e < 4; ++e) gv[e] = make_float2(0.f, 0.f);
             uint16_t* gxo = p.gx + n * kS * d + col0 + 8 * tid;
             uint16_t* gko = p.gkv + n * (kS + 1) * d + col0 + 8 * tid;
 #pragma unroll
             for (int s = 0; s < kS; ++s) {
-                float xf[8], kf[8], gf[8], ox[8], ok[8];
-                unpack8(lds128(b + s * row_bytes + 16 * tid), xf);
-                unpack8(lds128(b + (kS + s) * row_bytes + 16 * tid), kf);
-                unpack8(lds128(b + (2 * kS + 1 + s) * row_bytes + 16 * tid), gf);
+                const float2 A2 = splat2(__shfl_sync(kFullMask, cA, s));
+                const float2 Al2 = splat2(__shfl_sync(kFullMask, cAl, s));
+                const float2 nB2 = splat2(-__shfl_sync(kFullMask, cB, s));
+                const float2 nC2 = splat2(-__shfl_sync(kFullMask, cC, s));
+                const float2 G2 = splat2(__shfl_sync(kFullMask, cG, s));
+                const uint4 xq = lds128(b + s * row_bytes + 16 * tid);
+                const uint4 kq = lds128(b + (kS + s) * row_bytes + 16 * tid);
+                const uint4 gq = lds128(b + (2 * kS + 1 + s) * row_bytes + 16 * tid);
+                const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w};
+                const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
+                const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+                uint32_t ox[4], ok[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float aw = A[s] * w[s][e];
-                    ox[e] = fmaf(aw, kf[e], fmaf(-B[s], xf[e], gf[e]));
-                    ok[e] = fmaf(aw, xf[e], -Ck[s] * kf[e]);
-                    gv[e] = fmaf(Gt[s], gf[e], gv[e]);
-                    cacc_prod2(phi[s][e], plo[s][e], A[s], Al[s], __fmul_rn(xf[e], kf[e]));
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x2 = bf2(xw[e]), k2 = bf2(kw[e]), g2 = bf2(gw[e]);
+                    const float2 aw = mul2(A2, w2[s][e]);
+                    ox[e] = pack2(fma2(aw, k2, fma2(nB2, x2, g2)));
+                    ok[e] = pack2(fma2(aw, x2, mul2(nC2, k2)));
+                    gv[e] = fma2(G2, g2, gv[e]);
+                    cacc_prod2_x2(phi[s][e], plo[s][e], A2, Al2, mul2(x2, k2));
                 }
-                stg_cs(gxo + s * d, pack8(ox));
-                stg_cs(gko + s * d, pack8(ok));
+                stg_cs(gxo + s * d, make_uint4(ox[0], ox[1], ox[2], ox[3]));
+                stg_cs(gko + s * d, make_uint4(ok[0], ok[1], ok[2], ok[3]));
             }
-            stg_cs(gko + kS * d, pack8(gv));
+            stg_cs(gko + kS * d, make_uint4(pack2(gv[0]), pack2(gv[1]), pack2(gv[2]), pack2(gv[3])));
+        }
+        __syncthreads();
+        if (tid == 0) {
+            if (j + 2 < ntok) mbar_arrive_expect_tx(&rxbar[slot], xbytes);
+            if (j + stages < ntok) {
+                fence_proxy_async();
+                issue(j + stages);
+            }
+        }
+        if (warp == 0) {
+            __syncwarp();
+            if (j + 1 < ntok) push(j + 1);
         }
     }
     // ---- this cluster's grad_w for the slice: (hi, lo) in slots 2q, 2q+1, or
@@ -272,14 +311,17 @@ __global__ void __launch_bounds__(256) gate_bwd_kernel(const GateBwdParams p) {
             float* o = p.partial + ((p.pair_slots ? 2 * q : q) * kS + s) * d + col0 + 8 * tid;
             if (p.pair_slots) {
                 float* ol = o + static_cast<long long>(kS) * d;
-                stg_f4(o, phi[s][0], phi[s][1], phi[s][2], phi[s][3]);
-                stg_f4(o + 4, phi[s][4], phi[s][5], phi[s][6], phi[s][7]);
-                stg_f4(ol, plo[s][0], plo[s][1], plo[s][2], plo[s][3]);
-                stg_f4(ol + 4, plo[s][4], plo[s][5], plo[s][6], plo[s][7]);
+                stg_f4(o, phi[s][0].x, phi[s][0].y, phi[s][1].x, phi[s][1].y);
+                stg_f4(o + 4, phi[s][2].x, phi[s][2].y, phi[s][3].x, phi[s][3].y);
+                stg_f4(ol, plo[s][0].x, plo[s][0].y, plo[s][1].x, plo[s][1].y);
+                stg_f4(ol + 4, plo[s][2].x, plo[s][2].y, plo[s][3].x, plo[s][3].y);
             } else {
                 float r[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) r[e] = __fadd_rn(phi[s][e], plo[s][e]);
+                for (int e = 0; e < 4; ++e) {
+                    r[2 * e] = __fadd_rn(phi[s][e].x, plo[s][e].x);
+                    r[2 * e + 1] = __fadd_rn(phi[s][e].y, plo[s][e].y);
+                }
                 stg_f4(o, r[0], r[1], r[2], r[3]);
                 stg_f4(o + 4, r[4], r[5], r[6], r[7]);
             }
@@ -323,8 +365,11 @@ __global__ void __launch_bounds__(256) wreduce_kernel(const GateWReduceParams p)
 }  // namespace
 
 cudaError_t gate_bwd_prepare(int smem_bytes) {
-    return cudaFuncSetAttribute(gate_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                smem_bytes);
+    cudaError_t e = cudaFuncSetAttribute(gate_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gate_bwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
 }
 
 cudaError_t gate_bwd_max_clusters(int cluster, int threads, int smem, int* out) {

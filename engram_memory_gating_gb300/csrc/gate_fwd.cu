@@ -7,17 +7,21 @@
 //   gate   = sigmoid(sign(dot) sqrt(max(|dot|, 1e-6)))
 //   out    = bf16_rn(x + gate v)            (false mask: out = x, gate saved as 0)
 //
-// One pass over X and KV: a cluster of C CTAs owns a token row, each CTA a
-// slice of ncols = d/C columns of every stream.  The slice rows of successive
-// tokens (X: 4 rows, keys: 4 rows, v: 1 row) are bulk-copied into a ring of
-// shared-memory stages.  The three per-stream reductions (sum x^2, sum k^2,
-// sum x w k) are formed per thread, reduced across the warp, the CTA and the
-// cluster (distributed shared memory), and every CTA then writes its slice of
-// `out` from the X values still in registers.
+// One pass over X and KV.  A cluster of C CTAs owns a token row, each CTA a
+// slice of d/C columns of every stream; each thread 8 columns.  The slice
+// rows of successive tokens (X: 4 rows, keys: 4 rows, v: 1 row) arrive by
+// 1-D bulk copies in a ring of shared-memory stages.  Per token the three
+// per-stream sums (sum x^2, sum k^2, sum x w k) are formed per thread with
+// packed fp32x2 arithmetic, reduced across the warp and the CTA, and every
+// CTA pushes its 16 partials into the shared memory of every CTA of the
+// cluster with st.async, completing on a per-slot mbarrier there: no cluster
+// barrier per token.  The loop is software-pipelined: while the partials of
+// token j travel, the CTA already reduces token j+1, then finishes token j
+// (gates, out from the X values kept in registers).
 //
-// sum x w k is accumulated with error-free transformations (TwoProd via FMA,
-// TwoSum) so that the dot product keeps its accuracy when the terms cancel;
-// the squares are summed in plain fp32 (all terms positive).
+// sum x w k uses error-free transformations (TwoProd via FMA, TwoSum) so the
+// dot product keeps its accuracy when the terms cancel; the squares are
+// summed in plain fp32 (all terms positive).
 #include "common.cuh"
 #include "engram_internal.h"
 
@@ -87,11 +91,12 @@ EG_DEV void warp_reduce16(const float (&acc)[kVals], int lane, float& v0, float&
     v1 = p1;
 }
 
-__global__ void __launch_bounds__(256) gate_fwd_kernel(const GateFwdParams p) {
+__global__ void __launch_bounds__(128, 3) gate_fwd_kernel(const GateFwdParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBarOff);
-    float* red = reinterpret_cast<float*>(smem + kSmemRedOff);
-    float* xch = reinterpret_cast<float*>(smem + kSmemXchOff);
+    uint64_t* rxbar = reinterpret_cast<uint64_t*>(smem + kSmemRxBarOff);
+    float* red = reinterpret_cast<float*>(smem + kSmemRedOff);  // [2][warps][16]
+    float* rx = reinterpret_cast<float*>(smem + kSmemXchOff);   // [2][8 ranks][16]
     unsigned char* ring = smem + kSmemRingOff;
 
     const int tid = threadIdx.x;
@@ -108,28 +113,36 @@ __global__ void __launch_bounds__(256) gate_fwd_kernel(const GateFwdParams p) {
     const uint32_t row_bytes = static_cast<uint32_t>(p.ncols) * 2u;
     const uint32_t stage_bytes = 9u * row_bytes;
     const int stages = p.stages;
+    const uint32_t xbytes = C * 16u * 4u;  // partial bytes arriving per token
 
-    // fused weight of this thread's 8 columns, all streams, kept in registers
-    float w[kS][8];
+    // fused weight of this thread's 8 columns, all streams, as 4 pairs each
+    float2 w2[kS][4];
 #pragma unroll
     for (int s = 0; s < kS; ++s) {
         if (active) {
             const float4 a = __ldg(reinterpret_cast<const float4*>(p.w + s * d + col0 + 8 * tid));
             const float4 b = __ldg(reinterpret_cast<const float4*>(p.w + s * d + col0 + 8 * tid + 4));
-            w[s][0] = a.x; w[s][1] = a.y; w[s][2] = a.z; w[s][3] = a.w;
-            w[s][4] = b.x; w[s][5] = b.y; w[s][6] = b.z; w[s][7] = b.w;
+            w2[s][0] = make_float2(a.x, a.y);
+            w2[s][1] = make_float2(a.z, a.w);
+            w2[s][2] = make_float2(b.x, b.y);
+            w2[s][3] = make_float2(b.z, b.w);
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[s][e] = 0.f;
+            for (int e = 0; e < 4; ++e) w2[s][e] = make_float2(0.f, 0.f);
         }
     }
 
     const long long ntok = (p.N > q) ? (p.N - 1 - q) / G + 1 : 0;
     if (tid == 0) {
         for (int st = 0; st < stages; ++st) mbar_init(&full[st], 1);
+        mbar_init(&rxbar[0], 1);
+        mbar_init(&rxbar[1], 1);
         fence_mbar_init();
+        if (ntok > 0) mbar_arrive_expect_tx(&rxbar[0], xbytes);
+        if (ntok > 1) mbar_arrive_expect_tx(&rxbar[1], xbytes);
     }
-    __syncthreads();
+    // every CTA's exchange barriers are initialised and armed before any push
+    cluster_sync();
 
     auto issue = [&](long long j) {
         const long long n = q + j * G;
@@ -150,15 +163,14 @@ __global__ void __launch_bounds__(256) gate_fwd_kernel(const GateFwdParams p) {
     }
 
     bool failed = false;
-    for (long long j = 0; j < ntok; ++j) {
-        const long long n = q + j * G;
+
+    // reduction pass of token j: keeps its X words in xq, leaves the warp's
+    // 16 partials in red[j & 1]
+    auto reduce_pass = [&](long long j, uint4 (&xq)[kS]) {
         const int st = static_cast<int>(j % stages);
         if (!failed && !mbar_wait(&full[st], static_cast<uint32_t>((j / stages) & 1))) failed = true;
         const unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
-
-        // ---- one pass: sum x^2, sum k^2, sum x w k (compensated) per stream
         float acc[kVals];
-        uint4 xq[kS];
 #pragma unroll
         for (int i = 0; i < kVals; ++i) acc[i] = 0.f;
         if (active) {
@@ -166,21 +178,24 @@ __global__ void __launch_bounds__(256) gate_fwd_kernel(const GateFwdParams p) {
             for (int s = 0; s < kS; ++s) {
                 xq[s] = lds128(b + s * row_bytes + 16 * tid);
                 const uint4 kq = lds128(b + (kS + s) * row_bytes + 16 * tid);
-                float xf[8], kf[8];
-                unpack8(xq[s], xf);
-                unpack8(kq, kf);
-                float ssx = 0.f, ssk = 0.f, hi = 0.f, lo = 0.f;
+                const uint32_t xw[4] = {xq[s].x, xq[s].y, xq[s].z, xq[s].w};
+                const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
+                float2 ssx = make_float2(0.f, 0.f), ssk = ssx, hi = ssx, lo = ssx;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    ssx = fmaf(xf[e], xf[e], ssx);
-                    ssk = fmaf(kf[e], kf[e], ssk);
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x2 = bf2(xw[e]);
+                    const float2 k2 = bf2(kw[e]);
+                    ssx = fma2(x2, x2, ssx);
+                    ssk = fma2(k2, k2, ssk);
                     // x*k is exact in fp32 (two 8-bit significands)
-                    cacc_prod(hi, lo, __fmul_rn(xf[e], kf[e]), w[s][e]);
+                    cacc_prod_x2(hi, lo, mul2(x2, k2), w2[s][e]);
                 }
-                acc[4 * s + 0] = ssx;
-                acc[4 * s + 1] = ssk;
-                acc[4 * s + 2] = hi;
-                acc[4 * s + 3] = lo;
+                float h = hi.x, l = lo.x;
+                cacc_merge(h, l, hi.y, lo.y);
+                acc[4 * s + 0] = __fadd_rn(ssx.x, ssx.y);
+                acc[4 * s + 1] = __fadd_rn(ssk.x, ssk.y);
+                acc[4 * s + 2] = h;
+                acc[4 * s + 3] = l;
             }
         } else {
 #pragma unroll
@@ -191,20 +206,19 @@ __global__ void __launch_bounds__(256) gate_fwd_kernel(const GateFwdParams p) {
         if ((lane & 3) == 0) {
             const int sidx = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
             const int kind = (lane >> 2) & 1;
-            *reinterpret_cast<float2*>(red + warp * 16 + (sidx * 2 + kind) * 2) = make_float2(v0, v1);
+            float* r = red + (j & 1) * (32 * 16) + warp * 16 + (sidx * 2 + kind) * 2;
+            *reinterpret_cast<float2*>(r) = make_float2(v0, v1);
         }
-        __syncthreads();
-        // every thread is past token j-1: its stage can be refilled
-        if (tid == 0 && j >= 1 && j - 1 + stages < ntok) {
-            fence_proxy_async();
-            issue(j - 1 + stages);
-        }
-        float* slot = xch + (j & 1) * 16;
-        if (warp == 0 && lane < 8) {
+    };
+
+    // warp 0: CTA total of token j's partials, pushed to every CTA's slot j&1
+    auto push = [&](long long j) {
+        if (lane < 8) {
             const int kind = lane & 1;
-            float a0 = red[2 * lane], a1 = red[2 * lane + 1];
+            const float* r = red + (j & 1) * (32 * 16);
+            float a0 = r[2 * lane], a1 = r[2 * lane + 1];
             for (int wi = 1; wi < nwarps; ++wi) {
-                const float b0 = red[wi * 16 + 2 * lane], b1 = red[wi * 16 + 2 * lane + 1];
+                const float b0 = r[wi * 16 + 2 * lane], b1 = r[wi * 16 + 2 * lane + 1];
                 if (kind) {
                     cacc_merge(a0, a1, b0, b1);
                 } else {
@@ -212,30 +226,47 @@ __global__ void __launch_bounds__(256) gate_fwd_kernel(const GateFwdParams p) {
                     a1 = __fadd_rn(a1, b1);
                 }
             }
-            *reinterpret_cast<float2*>(slot + 2 * lane) = make_float2(a0, a1);
+            const int slot = static_cast<int>(j & 1);
+            const uint32_t dst = smem_addr(rx + (slot * 8 + rank) * 16 + 2 * lane);
+            const uint32_t bar = smem_addr(&rxbar[slot]);
+            for (uint32_t r2 = 0; r2 < C; ++r2)
+                st_async_f2(map_to_rank(dst, r2), a0, a1, map_to_rank(bar, r2));
         }
-        cluster_sync();
-        // ---- cluster totals, in rank order (identical in every CTA and warp)
+    };
+
+    uint4 xq_cur[kS], xq_nxt[kS];
+    if (ntok > 0) reduce_pass(0, xq_cur);
+    __syncthreads();
+    if (warp == 0 && ntok > 0) push(0);
+
+    for (long long j = 0; j < ntok; ++j) {
+        const long long n = q + j * G;
+        const int slot = static_cast<int>(j & 1);
+        const uint8_t mval = (p.mask == nullptr) ? 1 : __ldg(p.mask + n);
+        if (j + 1 < ntok) reduce_pass(j + 1, xq_nxt);
+
+        // ---- finish token j: cluster totals in rank order (same in every warp)
+        if (!failed && !mbar_wait_cluster(&rxbar[slot], static_cast<uint32_t>((j >> 1) & 1)))
+            failed = true;
         float t0 = 0.f, t1 = 0.f;
         if (lane < 8) {
             const int kind = lane & 1;
-            const uint32_t a = smem_addr(slot + 2 * lane);
-            const float2 r0 = ld_cluster_f2(map_to_rank(a, 0));
-            t0 = r0.x;
-            t1 = r0.y;
-            for (uint32_t r = 1; r < C; ++r) {
-                const float2 rr = ld_cluster_f2(map_to_rank(a, r));
+            const float* r = rx + slot * 8 * 16 + 2 * lane;
+            t0 = r[0];
+            t1 = r[1];
+            for (uint32_t rr = 1; rr < C; ++rr) {
+                const float b0 = r[rr * 16], b1 = r[rr * 16 + 1];
                 if (kind) {
-                    cacc_merge(t0, t1, rr.x, rr.y);
+                    cacc_merge(t0, t1, b0, b1);
                 } else {
-                    t0 = __fadd_rn(t0, rr.x);
-                    t1 = __fadd_rn(t1, rr.y);
+                    t0 = __fadd_rn(t0, b0);
+                    t1 = __fadd_rn(t1, b1);
                 }
             }
         }
         const float hi = __shfl_sync(kFullMask, t0, lane | 1);
         const float lo = __shfl_sync(kFullMask, t1, lane | 1);
-        const bool on = (p.mask == nullptr) || (p.mask[n] != 0);
+        const bool on = mval != 0;
         float gate = 0.f;
         if (lane < 8 && (lane & 1) == 0) {
             const float inv_d = 1.0f / static_cast<float>(d);
@@ -254,36 +285,62 @@ __global__ void __launch_bounds__(256) gate_fwd_kernel(const GateFwdParams p) {
 #pragma unroll
         for (int s = 0; s < kS; ++s) gs[s] = __shfl_sync(kFullMask, gate, 2 * s);
 
-        // ---- out = x + gate * v, one rounding; false mask copies X's bits
+        // ---- out = x + gate * v, one rounding; a false mask copies X's bits
         if (active) {
             uint16_t* o = p.out + n * kS * d + col0 + 8 * tid;
             if (on) {
-                float vf[8];
-                unpack8(lds128(b + 2 * kS * row_bytes + 16 * tid), vf);
+                const int st = static_cast<int>(j % stages);
+                const uint4 vq = lds128(ring + static_cast<size_t>(st) * stage_bytes +
+                                        2 * kS * row_bytes + 16 * tid);
+                const float2 v2[4] = {bf2(vq.x), bf2(vq.y), bf2(vq.z), bf2(vq.w)};
 #pragma unroll
                 for (int s = 0; s < kS; ++s) {
-                    float xf[8];
-                    unpack8(xq[s], xf);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) xf[e] = fmaf(gs[s], vf[e], xf[e]);
-                    stg_cs(o + s * d, pack8(xf));
+                    const float2 g2 = splat2(gs[s]);
+                    const uint32_t xw[4] = {xq_cur[s].x, xq_cur[s].y, xq_cur[s].z, xq_cur[s].w};
+                    uint4 ov;
+                    ov.x = pack2(fma2(g2, v2[0], bf2(xw[0])));
+                    ov.y = pack2(fma2(g2, v2[1], bf2(xw[1])));
+                    ov.z = pack2(fma2(g2, v2[2], bf2(xw[2])));
+                    ov.w = pack2(fma2(g2, v2[3], bf2(xw[3])));
+                    stg_cs(o + s * d, ov);
                 }
             } else {
 #pragma unroll
-                for (int s = 0; s < kS; ++s) stg_cs(o + s * d, xq[s]);
+                for (int s = 0; s < kS; ++s) stg_cs(o + s * d, xq_cur[s]);
             }
         }
+        // every thread is done with token j: its stage, its exchange slot and
+        // red[(j + 1) & 1] are settled
+        __syncthreads();
+        if (tid == 0) {
+            // re-arm this slot for token j + 2 before this CTA's push of token
+            // j + 1, which every peer needs before it can push token j + 2
+            if (j + 2 < ntok) mbar_arrive_expect_tx(&rxbar[slot], xbytes);
+            if (j + stages < ntok) {
+                fence_proxy_async();
+                issue(j + stages);
+            }
+        }
+        if (warp == 0) {
+            __syncwarp();
+            if (j + 1 < ntok) push(j + 1);
+        }
+#pragma unroll
+        for (int s = 0; s < kS; ++s) xq_cur[s] = xq_nxt[s];
     }
     if (failed) atomicOr(p.err, kErrTimeout);
-    // no CTA may leave while a peer can still read its exchange slots
+    // no CTA may leave while a peer can still push into its shared memory
     cluster_sync();
 }
 
 }  // namespace
 
 cudaError_t gate_fwd_prepare(int smem_bytes) {
-    return cudaFuncSetAttribute(gate_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                smem_bytes);
+    cudaError_t e = cudaFuncSetAttribute(gate_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gate_fwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
 }
 
 cudaError_t gate_fwd_max_clusters(int cluster, int threads, int smem, int* out) {
