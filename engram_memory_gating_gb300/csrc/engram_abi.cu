@@ -25,11 +25,12 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kGateD = ENGRAM_GATE_HIDDEN;
 constexpr int kGateFwdStages = 3;
-constexpr int kGateBwdStages = 3;
+constexpr int kGateBwdStages = 4;  // >= 3: a stage is refilled one token after its last use
 constexpr int kGcFwdStages = 6;
 constexpr int kGcBwdStages = 6;  // >= 5: rows of tokens tau-3 .. tau+1 stay resident
 static_assert(kGcBwdStages >= 5 && kGcBwdStages <= kMaxStages, "ring too short");
 static_assert(kGateFwdStages <= kMaxStages && kGateBwdStages <= kMaxStages, "too many stages");
+static_assert(kGateBwdStages >= 3 && kGateFwdStages >= 2, "ring too short");
 constexpr int kGcFwdMinRange = 32;  // tokens; bounds the 3-token halo overhead
 
 struct OccKey {

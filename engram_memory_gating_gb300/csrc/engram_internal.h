@@ -19,7 +19,8 @@ constexpr int kSmemBarOff = 0;                         // 16 stage + 2 exchange 
 constexpr int kSmemRxBarOff = kMaxStages * 8;
 constexpr int kSmemRedOff = 256;                       // 2 x 32 warps x 16 floats
 constexpr int kSmemXchOff = kSmemRedOff + 2 * 32 * 16 * 4;  // 2 x 8 ranks x 16 floats
-constexpr int kSmemRingOff = kSmemXchOff + 2 * 8 * 16 * 4;  // 128-byte aligned
+constexpr int kSmemCoefOff = kSmemXchOff + 2 * 8 * 16 * 4;  // 2 x 32 floats per-token scalars
+constexpr int kSmemRingOff = kSmemCoefOff + 2 * 32 * 4;     // 128-byte aligned
 static_assert(kSmemRingOff % 128 == 0, "ring alignment");
 
 struct GateFwdParams {

@@ -28,8 +28,9 @@
 // fp32x2) is reduced across the warp and the CTA, and each CTA pushes its 4
 // (hi, lo) pairs into every CTA of the cluster with st.async (mbarrier
 // completion, no cluster barrier per token).  The loop is software-pipelined:
-// token j+1's dgate pass runs while token j's partials travel.  Each thread
-// then writes its 8
+// token j+1's dgate pass runs while token j's partials travel, and one warp
+// turns token j's totals into per-stream scalars (shared memory).  Each
+// thread then writes its 8
 // columns of grad_x, grad_key and grad_v and accumulates grad_w for its
 // columns over all tokens of the cluster as an unevaluated (hi, lo) pair.
 // With at least two 64-token blocks there are at most half as many clusters
@@ -215,6 +216,50 @@ __global__ void __launch_bounds__(128, 2) gate_bwd_kernel(const GateBwdParams p)
         }
     };
 
+    // warp 0, lanes 0..3 (stream s = lane): per-stream scalars of token j in
+    // fp64 from the cluster totals and the saved record, into cbuf[j & 1]:
+    // A (hi, lo), -B, -Ck, gate.  rsqrt and the reciprocal start from fp32
+    // estimates refined by one Newton step in fp64; exp is the fp64 routine.
+    float* cbuf = reinterpret_cast<float*>(smem + kSmemCoefOff);  // [2][32]
+    auto coefficients = [&](long long j, const unsigned char* b) {
+        const int slot = static_cast<int>(j & 1);
+        if (!failed && !mbar_wait_cluster(&rxbar[slot], static_cast<uint32_t>((j >> 1) & 1)))
+            failed = true;
+        if (lane < kS) {
+            const float* r = rx + slot * 8 * 16 + 2 * lane;
+            float hi = r[0], lo = r[1];
+            for (uint32_t rr = 1; rr < C; ++rr) cacc_merge(hi, lo, r[rr * 16], r[rr * 16 + 1]);
+            const float* sv = reinterpret_cast<const float*>(b + kRows * row_bytes);
+            const float gate = sv[4 * lane + 0];
+            const float dotf = sv[4 * lane + 1];
+            const double rx_ = sv[4 * lane + 2];
+            const double rk = sv[4 * lane + 3];
+            const double dot = dotf;
+            const double ad = fabs(dot);
+            double ddot = 0.0;
+            if (ad >= 1e-6 && gate != 0.f) {
+                double y = rsqrtf(fabsf(dotf));
+                y = y * (1.5 - 0.5 * ad * y * y);           // 1/sqrt(|dot|)
+                const double sqm = ad * y;                  // sqrt(|dot|) = |sq|
+                const double ex = exp(-sqm);
+                const double den = 1.0 + ex;
+                double rc = __frcp_rn(static_cast<float>(den));
+                rc = rc * (2.0 - den * rc);                 // 1/(1 + e^-|sq|)
+                const double dsig = ex * rc * rc;           // sigmoid(sq) sigmoid(-sq)
+                const double dgate = static_cast<double>(hi) + static_cast<double>(lo);
+                ddot = dgate * dsig * (0.5 * y);            // d sq / d dot = 0.5/sqrt(|dot|)
+            }
+            const double dd = dot / static_cast<double>(d);
+            const double av = ddot * rx_ * rk;
+            float* c = cbuf + slot * 32 + lane * 5;
+            c[0] = static_cast<float>(av);
+            c[1] = static_cast<float>(av - static_cast<double>(c[0]));
+            c[2] = static_cast<float>(-(ddot * rx_ * rx_ * dd));
+            c[3] = static_cast<float>(-(ddot * rk * rk * dd));
+            c[4] = gate;
+        }
+    };
+
     if (ntok > 0) reduce_pass(0);
     __syncthreads();
     if (warp == 0 && ntok > 0) push(0);
@@ -225,34 +270,22 @@ __global__ void __launch_bounds__(128, 2) gate_bwd_kernel(const GateBwdParams p)
         const int st = static_cast<int>(j % stages);
         const unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
         if (j + 1 < ntok) reduce_pass(j + 1);
-
-        // ---- per-stream coefficients of token j from the cluster totals
-        if (!failed && !mbar_wait_cluster(&rxbar[slot], static_cast<uint32_t>((j >> 1) & 1)))
-            failed = true;
-        float cA = 0.f, cAl = 0.f, cB = 0.f, cC = 0.f, cG = 0.f;
-        if (lane < kS) {
-            const float* r = rx + slot * 8 * 16 + 2 * lane;
-            float hi = r[0], lo = r[1];
-            for (uint32_t rr = 1; rr < C; ++rr) cacc_merge(hi, lo, r[rr * 16], r[rr * 16 + 1]);
-            const float* sv = reinterpret_cast<const float*>(b + kRows * row_bytes);
-            const double dgate = static_cast<double>(hi) + static_cast<double>(lo);
-            const float gate = sv[4 * lane + 0];
-            const double dot = sv[4 * lane + 1];
-            const double rx_ = sv[4 * lane + 2];
-            const double rk = sv[4 * lane + 3];
-            const double ad = fabs(dot);
-            const double sqm = sqrt(fmax(ad, 1e-6));
-            const double ex = exp(-sqm);
-            const double dsig = ex / ((1.0 + ex) * (1.0 + ex));  // sigmoid(sq) sigmoid(-sq)
-            const double qd = (ad >= 1e-6) ? 0.5 / sqm : 0.0;
-            const double ddot = (gate == 0.f) ? 0.0 : dgate * dsig * qd;
-            const double dd = dot / static_cast<double>(d);
-            const double av = ddot * rx_ * rk;
-            cA = static_cast<float>(av);
-            cAl = static_cast<float>(av - static_cast<double>(cA));
-            cB = static_cast<float>(ddot * rx_ * rx_ * dd);
-            cC = static_cast<float>(ddot * rk * rk * dd);
-            cG = gate;
+        if (warp == 0) coefficients(j, b);
+        // token j's scalars are published, red[(j+1)&1] is complete, and every
+        // thread is done with token j-1 (its stage can be refilled)
+        __syncthreads();
+        if (tid == 0) {
+            // re-arm this slot for token j + 2 before this CTA's push of token
+            // j + 1, which every peer needs before it can push token j + 2
+            if (j + 2 < ntok) mbar_arrive_expect_tx(&rxbar[slot], xbytes);
+            if (j >= 1 && j - 1 + stages < ntok) {
+                fence_proxy_async();
+                issue(j - 1 + stages);
+            }
+        }
+        if (warp == 0) {
+            __syncwarp();
+            if (j + 1 < ntok) push(j + 1);
         }
 
         // ---- elementwise: grad_x, grad_key, grad_v, grad_w (packed pairs)
@@ -262,13 +295,14 @@ __global__ void __launch_bounds__(128, 2) gate_bwd_kernel(const GateBwdParams p)
             for (int e = 0; e < 4; ++e) gv[e] = make_float2(0.f, 0.f);
             uint16_t* gxo = p.gx + n * kS * d + col0 + 8 * tid;
             uint16_t* gko = p.gkv + n * (kS + 1) * d + col0 + 8 * tid;
+            const float* cb = cbuf + slot * 32;
 #pragma unroll
             for (int s = 0; s < kS; ++s) {
-                const float2 A2 = splat2(__shfl_sync(kFullMask, cA, s));
-                const float2 Al2 = splat2(__shfl_sync(kFullMask, cAl, s));
-                const float2 nB2 = splat2(-__shfl_sync(kFullMask, cB, s));
-                const float2 nC2 = splat2(-__shfl_sync(kFullMask, cC, s));
-                const float2 G2 = splat2(__shfl_sync(kFullMask, cG, s));
+                const float2 A2 = splat2(cb[s * 5 + 0]);
+                const float2 Al2 = splat2(cb[s * 5 + 1]);
+                const float2 nB2 = splat2(cb[s * 5 + 2]);
+                const float2 nC2 = splat2(cb[s * 5 + 3]);
+                const float2 G2 = splat2(cb[s * 5 + 4]);
                 const uint4 xq = lds128(b + s * row_bytes + 16 * tid);
                 const uint4 kq = lds128(b + (kS + s) * row_bytes + 16 * tid);
                 const uint4 gq = lds128(b + (2 * kS + 1 + s) * row_bytes + 16 * tid);
@@ -289,18 +323,6 @@ __global__ void __launch_bounds__(128, 2) gate_bwd_kernel(const GateBwdParams p)
                 stg_cs(gko + s * d, make_uint4(ok[0], ok[1], ok[2], ok[3]));
             }
             stg_cs(gko + kS * d, make_uint4(pack2(gv[0]), pack2(gv[1]), pack2(gv[2]), pack2(gv[3])));
-        }
-        __syncthreads();
-        if (tid == 0) {
-            if (j + 2 < ntok) mbar_arrive_expect_tx(&rxbar[slot], xbytes);
-            if (j + stages < ntok) {
-                fence_proxy_async();
-                issue(j + stages);
-            }
-        }
-        if (warp == 0) {
-            __syncwarp();
-            if (j + 1 < ntok) push(j + 1);
         }
     }
     // ---- this cluster's grad_w for the slice: (hi, lo) in slots 2q, 2q+1, or

@@ -16,8 +16,10 @@
 // CTA pushes its 16 partials into the shared memory of every CTA of the
 // cluster with st.async, completing on a per-slot mbarrier there: no cluster
 // barrier per token.  The loop is software-pipelined: while the partials of
-// token j travel, the CTA already reduces token j+1, then finishes token j
-// (gates, out from the X values kept in registers).
+// token j travel, the CTA already reduces token j+1; one warp then turns the
+// cluster totals of token j into gates (shared memory), and every thread
+// writes its slice of token j's `out` from the X and v words it kept in
+// registers, so a stage is refilled as soon as its reduction pass is done.
 //
 // sum x w k uses error-free transformations (TwoProd via FMA, TwoSum) so the
 // dot product keeps its accuracy when the terms cancel; the squares are
@@ -163,10 +165,11 @@ __global__ void __launch_bounds__(128, 3) gate_fwd_kernel(const GateFwdParams p)
     }
 
     bool failed = false;
+    float* gbuf = reinterpret_cast<float*>(smem + kSmemCoefOff);  // [2][8]: 4 gates, on flag
 
-    // reduction pass of token j: keeps its X words in xq, leaves the warp's
-    // 16 partials in red[j & 1]
-    auto reduce_pass = [&](long long j, uint4 (&xq)[kS]) {
+    // reduction pass of token j: keeps its X and v words in registers (the
+    // stage is free afterwards), leaves the warp's 16 partials in red[j & 1]
+    auto reduce_pass = [&](long long j, uint4 (&xq)[kS], uint4& vq) {
         const int st = static_cast<int>(j % stages);
         if (!failed && !mbar_wait(&full[st], static_cast<uint32_t>((j / stages) & 1))) failed = true;
         const unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(128, 3) gate_fwd_kernel(const GateFwdParams p)
 #pragma unroll
         for (int i = 0; i < kVals; ++i) acc[i] = 0.f;
         if (active) {
+            vq = lds128(b + 2 * kS * row_bytes + 16 * tid);
 #pragma unroll
             for (int s = 0; s < kS; ++s) {
                 xq[s] = lds128(b + s * row_bytes + 16 * tid);
@@ -200,6 +204,7 @@ __global__ void __launch_bounds__(128, 3) gate_fwd_kernel(const GateFwdParams p)
         } else {
 #pragma unroll
             for (int s = 0; s < kS; ++s) xq[s] = make_uint4(0, 0, 0, 0);
+            vq = make_uint4(0, 0, 0, 0);
         }
         float v0, v1;
         warp_reduce16(acc, lane, v0, v1);
@@ -234,18 +239,10 @@ __global__ void __launch_bounds__(128, 3) gate_fwd_kernel(const GateFwdParams p)
         }
     };
 
-    uint4 xq_cur[kS], xq_nxt[kS];
-    if (ntok > 0) reduce_pass(0, xq_cur);
-    __syncthreads();
-    if (warp == 0 && ntok > 0) push(0);
-
-    for (long long j = 0; j < ntok; ++j) {
+    // warp 0: gates of token j from the cluster totals (rank order) -> gbuf
+    auto gates = [&](long long j, bool on) {
         const long long n = q + j * G;
         const int slot = static_cast<int>(j & 1);
-        const uint8_t mval = (p.mask == nullptr) ? 1 : __ldg(p.mask + n);
-        if (j + 1 < ntok) reduce_pass(j + 1, xq_nxt);
-
-        // ---- finish token j: cluster totals in rank order (same in every warp)
         if (!failed && !mbar_wait_cluster(&rxbar[slot], static_cast<uint32_t>((j >> 1) & 1)))
             failed = true;
         float t0 = 0.f, t1 = 0.f;
@@ -266,8 +263,6 @@ __global__ void __launch_bounds__(128, 3) gate_fwd_kernel(const GateFwdParams p)
         }
         const float hi = __shfl_sync(kFullMask, t0, lane | 1);
         const float lo = __shfl_sync(kFullMask, t1, lane | 1);
-        const bool on = mval != 0;
-        float gate = 0.f;
         if (lane < 8 && (lane & 1) == 0) {
             const float inv_d = 1.0f / static_cast<float>(d);
             const float rstd_x = 1.0f / sqrtf(fmaf(t0, inv_d, p.eps));
@@ -277,25 +272,64 @@ __global__ void __launch_bounds__(128, 3) gate_fwd_kernel(const GateFwdParams p)
             float sq = sqrtf(fmaxf(fabsf(dot), 1e-6f));
             sq = dot > 0.f ? sq : (dot < 0.f ? -sq : 0.f);
             const float g = 1.0f / (1.0f + expf(-sq));
-            gate = on ? g : 0.f;
-            if (rank == 0 && warp == 0 && p.saved != nullptr)
+            const float gate = on ? g : 0.f;
+            gbuf[slot * 8 + (lane >> 1)] = gate;
+            if (rank == 0 && p.saved != nullptr)
                 stg_f4(p.saved + (n * kS + (lane >> 1)) * 4, gate, dot, rstd_x, rstd_k);
         }
-        float gs[kS];
-#pragma unroll
-        for (int s = 0; s < kS; ++s) gs[s] = __shfl_sync(kFullMask, gate, 2 * s);
+        if (lane == 0) gbuf[slot * 8 + 4] = on ? 1.f : 0.f;
+    };
+
+    uint4 xq_cur[kS], xq_nxt[kS], vq_cur, vq_nxt;
+    uint8_t m_cur = 1, m_nxt = 1;
+    if (ntok > 0) {
+        if (p.mask != nullptr && warp == 0) m_cur = __ldg(p.mask + q);
+        reduce_pass(0, xq_cur, vq_cur);
+    }
+    __syncthreads();
+    if (tid == 0 && stages < ntok) {
+        fence_proxy_async();
+        issue(stages);
+    }
+    if (warp == 0 && ntok > 0) {
+        __syncwarp();
+        push(0);
+    }
+
+    for (long long j = 0; j < ntok; ++j) {
+        const long long n = q + j * G;
+        const int slot = static_cast<int>(j & 1);
+        if (j + 1 < ntok) {
+            if (p.mask != nullptr && warp == 0) m_nxt = __ldg(p.mask + n + G);
+            reduce_pass(j + 1, xq_nxt, vq_nxt);
+        }
+        if (warp == 0) gates(j, m_cur != 0);
+        // gates of token j are published; red[(j+1)&1] is complete; token
+        // j+1's stage has been read by every thread
+        __syncthreads();
+        if (tid == 0) {
+            // re-arm this slot for token j + 2 before this CTA's push of token
+            // j + 1, which every peer needs before it can push token j + 2
+            if (j + 2 < ntok) mbar_arrive_expect_tx(&rxbar[slot], xbytes);
+            if (j + 1 + stages < ntok) {
+                fence_proxy_async();
+                issue(j + 1 + stages);
+            }
+        }
+        if (warp == 0) {
+            __syncwarp();
+            if (j + 1 < ntok) push(j + 1);
+        }
 
         // ---- out = x + gate * v, one rounding; a false mask copies X's bits
         if (active) {
             uint16_t* o = p.out + n * kS * d + col0 + 8 * tid;
-            if (on) {
-                const int st = static_cast<int>(j % stages);
-                const uint4 vq = lds128(ring + static_cast<size_t>(st) * stage_bytes +
-                                        2 * kS * row_bytes + 16 * tid);
-                const float2 v2[4] = {bf2(vq.x), bf2(vq.y), bf2(vq.z), bf2(vq.w)};
+            const float* gb = gbuf + slot * 8;
+            if (gb[4] != 0.f) {
+                const float2 v2[4] = {bf2(vq_cur.x), bf2(vq_cur.y), bf2(vq_cur.z), bf2(vq_cur.w)};
 #pragma unroll
                 for (int s = 0; s < kS; ++s) {
-                    const float2 g2 = splat2(gs[s]);
+                    const float2 g2 = splat2(gb[s]);
                     const uint32_t xw[4] = {xq_cur[s].x, xq_cur[s].y, xq_cur[s].z, xq_cur[s].w};
                     uint4 ov;
                     ov.x = pack2(fma2(g2, v2[0], bf2(xw[0])));
@@ -309,24 +343,10 @@ __global__ void __launch_bounds__(128, 3) gate_fwd_kernel(const GateFwdParams p)
                 for (int s = 0; s < kS; ++s) stg_cs(o + s * d, xq_cur[s]);
             }
         }
-        // every thread is done with token j: its stage, its exchange slot and
-        // red[(j + 1) & 1] are settled
-        __syncthreads();
-        if (tid == 0) {
-            // re-arm this slot for token j + 2 before this CTA's push of token
-            // j + 1, which every peer needs before it can push token j + 2
-            if (j + 2 < ntok) mbar_arrive_expect_tx(&rxbar[slot], xbytes);
-            if (j + stages < ntok) {
-                fence_proxy_async();
-                issue(j + stages);
-            }
-        }
-        if (warp == 0) {
-            __syncwarp();
-            if (j + 1 < ntok) push(j + 1);
-        }
 #pragma unroll
         for (int s = 0; s < kS; ++s) xq_cur[s] = xq_nxt[s];
+        vq_cur = vq_nxt;
+        m_cur = m_nxt;
     }
     if (failed) atomicOr(p.err, kErrTimeout);
     // no CTA may leave while a peer can still push into its shared memory
