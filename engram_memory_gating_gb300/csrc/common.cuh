@@ -79,6 +79,24 @@ EG_DEV bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of a phase (acquire at CTA scope).
+EG_DEV bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// One arrival (release at CTA scope), no transaction bytes.
+EG_DEV void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // kWaitLimitNs of wall time (or kWaitMaxIters polls) and returns false; the
 // caller records the failure and carries on without hanging the GPU.

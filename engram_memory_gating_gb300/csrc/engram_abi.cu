@@ -24,13 +24,12 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kGateD = ENGRAM_GATE_HIDDEN;
-constexpr int kGateFwdStages = 3;
 constexpr int kGateBwdStages = 4;  // >= 3: a stage is refilled one token after its last use
 constexpr int kGcFwdStages = 6;
 constexpr int kGcBwdStages = 6;  // >= 5: rows of tokens tau-3 .. tau+1 stay resident
 static_assert(kGcBwdStages >= 5 && kGcBwdStages <= kMaxStages, "ring too short");
-static_assert(kGateFwdStages <= kMaxStages && kGateBwdStages <= kMaxStages, "too many stages");
-static_assert(kGateBwdStages >= 3 && kGateFwdStages >= 2, "ring too short");
+static_assert(kGateBwdStages <= kMaxStages, "too many stages");
+static_assert(kGateBwdStages >= 3, "ring too short");
 constexpr int kGcFwdMinRange = 32;  // tokens; bounds the 3-token halo overhead
 
 struct OccKey {
@@ -149,17 +148,19 @@ engram_status_t launch_status(cudaError_t e) {
 
 // ---------------------------------------------------------------- geometry
 
+// Forward: one warp per (token, stream) row, 8 warps per CTA, as many CTAs
+// as fit on the device (persistent), fewer if there are fewer rows.
 bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngroups) {
-    const int C = pick_cluster(kGateD / 8, 128);
-    ncols = kGateD / C;
-    ngroups = ncols / 8;
-    c.cluster = C;
-    c.threads = round_up(ngroups, 32);
-    c.stages = kGateFwdStages;
-    c.smem = kSmemRingOff + c.stages * 9 * ncols * 2;
-    const int mc = max_clusters(st, 0, C, c.threads, c.smem);
+    ncols = kGateD;
+    ngroups = 0;
+    c.cluster = 1;
+    c.threads = 256;
+    c.stages = 0;
+    c.smem = 0;
+    const int mc = max_clusters(st, 0, 1, c.threads, 0);
     if (mc <= 0) return false;
-    c.clusters = static_cast<int>(N < mc ? N : mc);
+    const int64_t need = (N * 4 + 7) / 8;
+    c.clusters = static_cast<int>(need < mc ? need : mc);
     return true;
 }
 

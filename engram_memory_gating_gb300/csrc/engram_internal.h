@@ -15,12 +15,17 @@ int pick_cluster(int64_t d, int max_groups);
 // stages, then the two exchange slots), per-warp partials (two buffers), the
 // cluster exchange slots (2 x 8 ranks x 16 floats), then the ring of stages.
 constexpr int kMaxStages = 16;
-constexpr int kSmemBarOff = 0;                         // 16 stage + 2 exchange mbarriers
-constexpr int kSmemRxBarOff = kMaxStages * 8;
-constexpr int kSmemRedOff = 256;                       // 2 x 32 warps x 16 floats
-constexpr int kSmemXchOff = kSmemRedOff + 2 * 32 * 16 * 4;  // 2 x 8 ranks x 16 floats
-constexpr int kSmemCoefOff = kSmemXchOff + 2 * 8 * 16 * 4;  // 2 x 32 floats per-token scalars
+constexpr int kSmemBarOff = 0;                         // 16 stage ("full") mbarriers
+constexpr int kSmemRxBarOff = kMaxStages * 8;          // 4 exchange mbarriers
+constexpr int kSmemEmptyBarOff = kSmemRxBarOff + 4 * 8;  // 16 stage-release mbarriers
+constexpr int kRedWarps = 8;                           // per-warp partial buffers
+constexpr int kSmemRedOff = 512;                       // 2 x 8 warps x 16 floats
+constexpr int kSmemXchOff = kSmemRedOff + 2 * kRedWarps * 16 * 4;  // exchange slots
+constexpr int kXchSlots = 4;                           // tokens in flight per exchange
+constexpr int kXchMaxParts = 20;                       // cluster CTAs x warps per token
+constexpr int kSmemCoefOff = kSmemXchOff + kXchSlots * kXchMaxParts * 16 * 4;
 constexpr int kSmemRingOff = kSmemCoefOff + 2 * 32 * 4;     // 128-byte aligned
+static_assert(kSmemEmptyBarOff + kMaxStages * 8 <= kSmemRedOff, "barrier area");
 static_assert(kSmemRingOff % 128 == 0, "ring alignment");
 
 struct GateFwdParams {

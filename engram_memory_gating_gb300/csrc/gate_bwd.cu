@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(128, 2) gate_bwd_kernel(const GateBwdParams p)
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBarOff);
     uint64_t* rxbar = reinterpret_cast<uint64_t*>(smem + kSmemRxBarOff);
-    float* red = reinterpret_cast<float*>(smem + kSmemRedOff);  // [2][warps][8]
+    float* red = reinterpret_cast<float*>(smem + kSmemRedOff);  // [2][8 warps][8]
     float* rx = reinterpret_cast<float*>(smem + kSmemXchOff);   // [2][8 ranks][16]
     unsigned char* ring = smem + kSmemRingOff;
 
@@ -197,14 +197,14 @@ __global__ void __launch_bounds__(128, 2) gate_bwd_kernel(const GateBwdParams p)
         warp_reduce_pairs4(acc, lane, v0, v1);
         if ((lane & 7) == 0) {
             const int sidx = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-            *reinterpret_cast<float2*>(red + (j & 1) * (32 * 8) + warp * 8 + sidx * 2) =
+            *reinterpret_cast<float2*>(red + (j & 1) * (kRedWarps * 8) + warp * 8 + sidx * 2) =
                 make_float2(v0, v1);
         }
     };
 
     auto push = [&](long long j) {
         if (lane < kS) {
-            const float* r = red + (j & 1) * (32 * 8);
+            const float* r = red + (j & 1) * (kRedWarps * 8);
             float a0 = r[2 * lane], a1 = r[2 * lane + 1];
             for (int wi = 1; wi < nwarps; ++wi)
                 cacc_merge(a0, a1, r[wi * 8 + 2 * lane], r[wi * 8 + 2 * lane + 1]);

@@ -248,9 +248,13 @@ def test_bwd_graph_capture_matches_eager():
     assert torch.equal(gw, ref[2])
 
 
-def test_launch_geometry_is_cluster_split():
+def test_launch_geometry():
+    # forward: one warp per (token, stream) row, persistent CTAs
     fwd = eg.engram_launch_info(0, 65536)
-    assert fwd["cluster"] >= 2 and 5120 % (8 * fwd["cluster"]) == 0
-    assert fwd["clusters"] >= 1 and fwd["smem_bytes"] > 0
+    assert fwd["cluster"] == 1 and fwd["threads"] % 32 == 0 and fwd["clusters"] >= 1
+    assert eg.engram_launch_info(0, 1)["clusters"] == 1
+    # backward: token rows split across a cluster; at most one cluster per two
+    # 64-token blocks, so each cluster's (hi, lo) grad_weight pair fits
     bwd = eg.engram_launch_info(1, 8192)
-    assert bwd["clusters"] <= 8192 // 64
+    assert bwd["cluster"] >= 2 and 5120 % (8 * bwd["cluster"]) == 0
+    assert bwd["clusters"] <= 8192 // 128 and bwd["smem_bytes"] > 0
