@@ -164,21 +164,29 @@ bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngr
     return true;
 }
 
-bool gate_bwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngroups) {
+// Backward: kernel 1 (per-token scalars) on a persistent grid of 256-thread
+// CTAs; kernel 2 on a grid of (column slices) x (token groups).  A group
+// covers at least two 64-token blocks, so its (hi, lo) grad_weight pair fits
+// two of the workspace's block slots; a single-block problem uses one slot.
+bool gate_bwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngroups,
+                  int& group_tokens) {
     const int C = pick_cluster(kGateD / 8, 128);
     ncols = kGateD / C;
     ngroups = ncols / 8;
-    c.cluster = C;
+    c.cluster = 1;
     c.threads = round_up(ngroups, 32);
     c.stages = kGateBwdStages;
-    c.smem = kSmemRingOff + c.stages * (13 * ncols * 2 + 64);
-    const int mc = max_clusters(st, 1, C, c.threads, c.smem);
-    if (mc <= 0) return false;
-    // at most half as many clusters as 64-token blocks, so each cluster's
-    // (hi, lo) grad_weight pair fits two of the workspace's block slots
+    c.smem = 256 + c.stages * (12 * ncols * 2 + 128);
+    if (max_clusters(st, 1, 1, c.threads, c.smem) <= 0) return false;
+    const int mc1 = max_clusters(st, 1, 1, 256, 0);
+    if (mc1 <= 0) return false;
     const int64_t nb = N / 64;
-    const int64_t lim = nb >= 2 ? nb / 2 : 1;
-    c.clusters = static_cast<int>(lim < mc ? lim : mc);
+    const int64_t groups0 = nb >= 2 ? nb / 2 : 1;
+    group_tokens = static_cast<int>(64 * ((nb + groups0 - 1) / groups0));
+    c.clusters = C;
+    c.grid_y = static_cast<int>((N + group_tokens - 1) / group_tokens);
+    const int64_t need1 = (N + 7) / 8;
+    c.aux_blocks = static_cast<int>(need1 < mc1 ? need1 : mc1);
     return true;
 }
 
@@ -285,7 +293,7 @@ engram_status_t engram_gate_fwd(const void* x, const void* kv, const float* weig
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
-    LaunchCfg c;
+    LaunchCfg c = {};
     int ncols, ngroups;
     if (!gate_fwd_cfg(*st, N, c, ncols, ngroups)) return ENGRAM_ERR_DEVICE;
     GateFwdParams p;
@@ -329,10 +337,12 @@ engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weig
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
-    LaunchCfg c;
+    LaunchCfg c = {};
     int ncols, ngroups;
-    if (!gate_bwd_cfg(*st, N, c, ncols, ngroups)) return ENGRAM_ERR_DEVICE;
-    // workspace: [16N floats, unused scratch | (N/64, 4, 5120) fp32 partials]
+    int group_tokens = 0;
+    if (!gate_bwd_cfg(*st, N, c, ncols, ngroups, group_tokens)) return ENGRAM_ERR_DEVICE;
+    // workspace: [(N, 4, 4) per-token scalars | (N/64, 4, 5120) fp32 partial slots]
+    float* coef = static_cast<float*>(workspace);
     float* partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + 64 * n);
     GateBwdParams p;
     p.x = static_cast<const uint16_t*>(x);
@@ -342,6 +352,7 @@ engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weig
     p.gout = static_cast<const uint16_t*>(grad_out);
     p.gx = static_cast<uint16_t*>(grad_x);
     p.gkv = static_cast<uint16_t*>(grad_kv);
+    p.coef = coef;
     p.partial = partial;
     p.err = st->err;
     p.N = N;
@@ -349,13 +360,14 @@ engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weig
     p.ncols = ncols;
     p.ngroups = ngroups;
     p.stages = c.stages;
+    p.group_tokens = group_tokens;
     p.pair_slots = (N / 64) >= 2 ? 1 : 0;
     engram_status_t s = launch_status(gate_bwd_launch(p, c, stream));
     if (s != ENGRAM_OK) return s;
     GateWReduceParams r;
     r.partial = partial;
     r.out = grad_weight;
-    r.nblocks = p.pair_slots ? 2 * c.clusters : c.clusters;
+    r.nblocks = p.pair_slots ? 2 * c.grid_y : c.grid_y;
     r.n = 4 * kGateD;
     r.stride = 4 * kGateD;
     r.pairs = p.pair_slots;
@@ -384,7 +396,7 @@ engram_status_t engram_gateconv_fwd(const void* H, const void* k, const void* v,
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
-    LaunchCfg c;
+    LaunchCfg c = {};
     int ncols, ngroups, range_len, rpr;
     if (!gc_fwd_cfg(*st, M, T, d, c, ncols, ngroups, range_len, rpr)) return ENGRAM_ERR_DEVICE;
     GateConvFwdParams p;
@@ -454,7 +466,7 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
-    LaunchCfg c;
+    LaunchCfg c = {};
     int ncols, ngroups, range_len, rpr;
     if (!gc_bwd_cfg(*st, M, T, d, c, ncols, ngroups, range_len, rpr)) return ENGRAM_ERR_DEVICE;
     float* partial = static_cast<float*>(workspace);
@@ -569,16 +581,23 @@ engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
-    LaunchCfg c;
+    LaunchCfg c = {};
     int ncols, ngroups, range_len, rpr;
     bool ok = false;
     switch (op) {
         case 0:
             ok = n0 >= 1 && n0 <= ENGRAM_GATE_MAX_TOKENS && gate_fwd_cfg(*st, n0, c, ncols, ngroups);
             break;
-        case 1:
-            ok = engram_gate_bwd_workspace_size(n0) > 0 && gate_bwd_cfg(*st, n0, c, ncols, ngroups);
+        case 1: {
+            int gt = 0;
+            ok = engram_gate_bwd_workspace_size(n0) > 0 && gate_bwd_cfg(*st, n0, c, ncols, ngroups, gt);
+            // CTAs sharing a token row = column slices; "clusters" = token groups
+            if (ok) {
+                c.cluster = c.clusters;
+                c.clusters = c.grid_y;
+            }
             break;
+        }
         case 2:
             ok = gc_shape_ok(n0, n1, n2) && gc_fwd_cfg(*st, n0, n1, n2, c, ncols, ngroups, range_len, rpr);
             break;

@@ -52,14 +52,16 @@ struct GateBwdParams {
     const uint16_t* gout;
     uint16_t* gx;
     uint16_t* gkv;
-    float* partial;  // (N/64, 4, d) fp32 slots for per-cluster grad_weight
+    float* coef;     // (N, 4, 4) fp32 per-token scalars: A hi, A lo, -B, -Ck
+    float* partial;  // (N/64, 4, d) fp32 slots for per-group grad_weight
     unsigned int* err;
     long long N;
     int d;
-    int ncols;
-    int ngroups;
+    int ncols;        // columns per CTA slice
+    int ngroups;      // 8-column groups per slice (<= threads)
     int stages;
-    int pair_slots;  // 1: cluster q writes (hi, lo) to slots 2q, 2q+1
+    int group_tokens; // tokens per token group (one grad_weight partial each)
+    int pair_slots;   // 1: group g writes (hi, lo) to slots 2g, 2g+1
 };
 
 struct GateWReduceParams {
@@ -122,9 +124,11 @@ struct GateConvBwdParams {
 struct LaunchCfg {
     int cluster;
     int threads;
-    int clusters;
+    int clusters;   // grid size in clusters (CTAs when cluster == 1)
     int stages;
     int smem;
+    int grid_y;     // second grid dimension (1 unless stated)
+    int aux_blocks; // CTAs of a preceding helper kernel, if any
 };
 
 // Kernel launchers (defined next to their kernels).  Each returns the launch

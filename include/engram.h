@@ -224,9 +224,10 @@ engram_status_t engram_gate_bwd_noalloc(const void* x, const void* kv, const flo
  */
 engram_status_t engram_device_error(uint32_t* flags);
 
-/* Launch geometry chosen for a call, for tests and benchmarks: cluster size
- * (CTAs per token row), threads per CTA, number of clusters, ring stages and
- * dynamic shared memory bytes.  `op`: 0 gate fwd, 1 gate bwd, 2 gateconv fwd,
+/* Launch geometry chosen for a call, for tests and benchmarks: CTAs that
+ * share one token row (thread-block cluster size, or column slices), threads
+ * per CTA, number of such CTA groups, ring stages and dynamic shared memory
+ * bytes of the main kernel.  `op`: 0 gate fwd, 1 gate bwd, 2 gateconv fwd,
  * 3 gateconv bwd.  n0, n1, n2 = (N) for the gate, (M, T, d) for GateConv. */
 typedef struct {
     int cluster;
