@@ -170,11 +170,13 @@ bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngr
 // two of the workspace's block slots; a single-block problem uses one slot.
 bool gate_bwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngroups,
                   int& group_tokens) {
-    const int C = pick_cluster(kGateD / 8, 128);
+    // slices of 64 column groups: 8 warps x (8 groups x 4 streams)
+    static_assert((kGateD / 8) % 64 == 0, "whole slices");
+    const int C = kGateD / 8 / 64;
     ncols = kGateD / C;
     ngroups = ncols / 8;
     c.cluster = 1;
-    c.threads = round_up(ngroups, 32);
+    c.threads = 4 * ngroups;
     c.stages = kGateBwdStages;
     c.smem = 256 + c.stages * (12 * ncols * 2 + 128);
     if (max_clusters(st, 1, 1, c.threads, c.smem) <= 0) return false;

@@ -10,7 +10,7 @@
 //   A = ddot rstd_X rstd_key,  B = ddot rstd_X^2 dot / d,  Ck = ddot rstd_key^2 dot / d:
 //   grad_x_i   = g_i + A w_i k_i - B x_i
 //   grad_key_i = A w_i x_i - Ck k_i
-//   grad_v_i   = sum_{s=0..3} gate_s g_{s,i}      (fp32, one rounding)
+//   grad_v_i   = (gate_0 g_0 + gate_1 g_1) + (gate_2 g_2 + gate_3 g_3)  (fp32, one rounding)
 //   grad_w_i  += A x_i k_i                         (= ddot * xh_i * kh_i)
 // These are the chain rule through the RMS norms written with the saved dot
 // (sum_i xh_i w_i kh_i): d dot/d x_i = rstd_X (w_i kh_i - xh_i dot/d).
@@ -19,15 +19,18 @@
 //  1. coefficients: one warp per token reads the token's grad_out rows and v
 //     (16-byte loads), reduces the four dgate sums with error-free
 //     accumulation and shuffles, and lanes 0..3 turn them into the per-stream
-//     scalars (A as a double-float pair, -B, -Ck) in fp64, written to the
-//     workspace's 16 floats per token;
-//  2. elementwise: a CTA owns a 1024-column slice of every stream over a
+//     scalars in fp64 (A split as an 8-significant-bit head plus a float
+//     tail, -B, -Ck), written to the workspace's 16 floats per token;
+//  2. elementwise: a CTA owns a 512-column slice of every stream over a
 //     group of consecutive tokens; the slice rows of X, the keys and grad_out
 //     plus the token's scalars and saved record stream through a ring of
-//     shared-memory stages (1-D bulk copies); each thread writes its 8
-//     columns of grad_x, grad_key and grad_v and accumulates grad_w for its
+//     shared-memory stages (1-D bulk copies); each thread owns 8 columns of
+//     one stream, writes grad_x and grad_key there, forms grad_v with two
+//     shuffles across the four stream lanes, and accumulates grad_w for its
 //     columns over the group as an unevaluated (hi, lo) pair, stored in the
-//     workspace's block slots (group g: slots 2g and 2g+1);
+//     workspace's block slots (group g: slots 2g and 2g+1).  The warps never
+//     wait for one another: each counts itself out of a stage in shared
+//     memory and the last one to leave it issues its refill;
 //  3. the pairs are merged in ascending group order (bitwise reproducible).
 // The per-token scalars are evaluated in fp64 because a relative error of a
 // few fp32 ulps in A, summed over 8192 tokens, would exceed the 1e-6
@@ -64,31 +67,33 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
     const int lane = threadIdx.x & 31;
     const long long gwarp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-    for (long long n = gwarp; n < p.N; n += nwarps) {
+    static_assert((kChunks / kCG) % 2 == 0, "group 0 of every token uses buffer 0");
+    uint4 vb[2][kCG], gb[2][kS][kCG];
+    auto load_group = [&](long long n, int grp, int buf) {
         const uint4* vr = reinterpret_cast<const uint4*>(p.kv + (n * (kS + 1) + kS) * kD) + lane;
         const uint4* gr = reinterpret_cast<const uint4*>(p.gout + n * kS * kD) + lane;
+#pragma unroll
+        for (int c = 0; c < kCG; ++c) {
+            const int m = grp * kCG + c;
+            vb[buf][c] = ldg16_na(vr + 32 * m);
+#pragma unroll
+            for (int s = 0; s < kS; ++s) gb[buf][s][c] = ldg16_na(gr + s * (kD / 8) + 32 * m);
+        }
+    };
+    if (gwarp < p.N) load_group(gwarp, 0, 0);
+    for (long long n = gwarp; n < p.N; n += nwarps) {
         float2 hi[kS], lo[kS];
 #pragma unroll
         for (int s = 0; s < kS; ++s) hi[s] = lo[s] = make_float2(0.f, 0.f);
-        uint4 vb[2][kCG], gb[2][kS][kCG];
-#pragma unroll
-        for (int c = 0; c < kCG; ++c) {
-            vb[0][c] = ldg16_na(vr + 32 * c);
-#pragma unroll
-            for (int s = 0; s < kS; ++s) gb[0][s][c] = ldg16_na(gr + s * (kD / 8) + 32 * c);
-        }
 #pragma unroll
         for (int grp = 0; grp < kChunks / kCG; ++grp) {
             const int cur = grp & 1;
-            if (grp + 1 < kChunks / kCG) {
-#pragma unroll
-                for (int c = 0; c < kCG; ++c) {
-                    const int m = (grp + 1) * kCG + c;
-                    vb[cur ^ 1][c] = ldg16_na(vr + 32 * m);
-#pragma unroll
-                    for (int s = 0; s < kS; ++s) gb[cur ^ 1][s][c] = ldg16_na(gr + s * (kD / 8) + 32 * m);
-                }
-            }
+            // next group of this token, or the first group of the next token
+            // (its loads then overlap this token's reduction and fp64 work)
+            if (grp + 1 < kChunks / kCG)
+                load_group(n, grp + 1, cur ^ 1);
+            else if (n + nwarps < p.N)
+                load_group(n + nwarps, 0, cur ^ 1);
 #pragma unroll
             for (int c = 0; c < kCG; ++c) {
                 const float2 v2[4] = {bf2(vb[cur][c].x), bf2(vb[cur][c].y), bf2(vb[cur][c].z),
@@ -136,26 +141,37 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
             }
             const double dd = dot / static_cast<double>(kD);
             const double av = ddot * rx * rk;
-            const float a_hi = static_cast<float>(av);
-            const float a_lo = static_cast<float>(av - static_cast<double>(a_hi));
-            stg_f4(p.coef + (n * kS + lane) * 4, a_hi, a_lo, static_cast<float>(-(ddot * rx * rx * dd)),
+            // A = a8 + arest: a8 keeps 8 significant bits, so a8 * (x*k) is exact
+            // in fp32 (8 + 16 bits); arest carries the next 24 bits
+            const float a8 = __uint_as_float(__float_as_uint(static_cast<float>(av)) & 0xffff0000u);
+            const float arest = static_cast<float>(av - static_cast<double>(a8));
+            stg_f4(p.coef + (n * kS + lane) * 4, a8, arest, static_cast<float>(-(ddot * rx * rx * dd)),
                    static_cast<float>(-(ddot * rk * rk * dd)));
         }
     }
 }
 
 // ---------------------------------------------------------------- kernel 2
-constexpr int kRing2Off = 256;  // after the stage mbarriers
+constexpr int kRing2Off = 256;  // after the stage mbarriers and release counters
 
-__global__ void __launch_bounds__(128, 2) gate_bwd_main_kernel(const GateBwdParams p) {
+// Thread mapping: lane = 8 * stream + g, warp w; the thread owns the 8 columns
+// col0 + 8 * (8w + g) of one stream.  The four streams of a column group sit
+// in one warp, so grad_v (a sum over streams) is two shuffles.
+__global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);                            // [stages]
+    unsigned int* released = reinterpret_cast<unsigned int*>(smem + kMaxStages * 8);  // [stages]
     unsigned char* ring = smem + kRing2Off;
 
     const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int W = blockDim.x >> 5;
+    const int s = lane >> 3;                               // stream
+    const int cg = (tid >> 5) * 8 + (lane & 7);           // column group in the slice
     const int col0 = static_cast<int>(blockIdx.x) * p.ncols;
+    const int col = col0 + 8 * cg;
+    const bool active = cg < p.ngroups;
     const long long grp = blockIdx.y;
-    const bool active = tid < p.ngroups;
     const uint32_t row_bytes = static_cast<uint32_t>(p.ncols) * 2u;
     const uint32_t stage_bytes = kRows * row_bytes + 128u;
     const int stages = p.stages;
@@ -163,126 +179,150 @@ __global__ void __launch_bounds__(128, 2) gate_bwd_main_kernel(const GateBwdPara
     const long long t1 = (t0 + p.group_tokens < p.N) ? t0 + p.group_tokens : p.N;
     const long long ntok = t1 > t0 ? t1 - t0 : 0;
 
-    float2 w2[kS][4];
+    float2 w2[4];
+    if (active) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p.w + s * kD + col));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(p.w + s * kD + col + 4));
+        w2[0] = make_float2(a.x, a.y);
+        w2[1] = make_float2(a.z, a.w);
+        w2[2] = make_float2(b.x, b.y);
+        w2[3] = make_float2(b.z, b.w);
+    } else {
 #pragma unroll
-    for (int s = 0; s < kS; ++s) {
-        if (active) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(p.w + s * kD + col0 + 8 * tid));
-            const float4 b = __ldg(reinterpret_cast<const float4*>(p.w + s * kD + col0 + 8 * tid + 4));
-            w2[s][0] = make_float2(a.x, a.y);
-            w2[s][1] = make_float2(a.z, a.w);
-            w2[s][2] = make_float2(b.x, b.y);
-            w2[s][3] = make_float2(b.z, b.w);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) w2[s][e] = make_float2(0.f, 0.f);
-        }
+        for (int e = 0; e < 4; ++e) w2[e] = make_float2(0.f, 0.f);
     }
 
     if (tid == 0) {
-        for (int st = 0; st < stages; ++st) mbar_init(&full[st], 1);
+        for (int st = 0; st < stages; ++st) {
+            mbar_init(&full[st], 1);
+            released[st] = 0u;
+        }
         fence_mbar_init();
     }
     __syncthreads();
 
-    auto issue = [&](long long j) {
+    auto issue = [&](int j, int st) {
         const long long n = t0 + j;
-        const int st = static_cast<int>(j % stages);
         unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
         mbar_arrive_expect_tx(&full[st], stage_bytes);
 #pragma unroll
-        for (int s = 0; s < kS; ++s) {
-            bulk_g2s(b + s * row_bytes, p.x + (n * kS + s) * kD + col0, row_bytes, &full[st]);
-            bulk_g2s(b + (kS + s) * row_bytes, p.kv + (n * (kS + 1) + s) * kD + col0, row_bytes, &full[st]);
-            bulk_g2s(b + (2 * kS + s) * row_bytes, p.gout + (n * kS + s) * kD + col0, row_bytes, &full[st]);
+        for (int r = 0; r < kS; ++r) {
+            bulk_g2s(b + r * row_bytes, p.x + (n * kS + r) * kD + col0, row_bytes, &full[st]);
+            bulk_g2s(b + (kS + r) * row_bytes, p.kv + (n * (kS + 1) + r) * kD + col0, row_bytes, &full[st]);
+            bulk_g2s(b + (2 * kS + r) * row_bytes, p.gout + (n * kS + r) * kD + col0, row_bytes, &full[st]);
         }
         bulk_g2s(b + kRows * row_bytes, p.coef + n * kS * 4, 64u, &full[st]);
         bulk_g2s(b + kRows * row_bytes + 64, p.saved + n * kS * 4, 64u, &full[st]);
     };
     if (tid == 0) {
-        const long long pro = ntok < stages ? ntok : stages;
-        for (long long j = 0; j < pro; ++j) issue(j);
+        const int pro = ntok < stages ? static_cast<int>(ntok) : stages;
+        for (int j = 0; j < pro; ++j) issue(j, j);
     }
 
-    float2 phi[kS][4], plo[kS][4];  // grad_w of this thread's columns, hi + lo
+    float2 phi[4], plo[4];  // grad_w of this thread's columns, hi + lo
 #pragma unroll
-    for (int s = 0; s < kS; ++s)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) phi[s][e] = plo[s][e] = make_float2(0.f, 0.f);
+    for (int e = 0; e < 4; ++e) phi[e] = plo[e] = make_float2(0.f, 0.f);
 
     bool failed = false;
-    for (long long j = 0; j < ntok; ++j) {
+    int st = 0;
+    uint32_t phase = 0;
+    for (int j = 0; j < ntok; ++j) {
         const long long n = t0 + j;
-        const int st = static_cast<int>(j % stages);
-        if (!failed && !mbar_wait(&full[st], static_cast<uint32_t>((j / stages) & 1))) failed = true;
+        if (!failed && !mbar_wait(&full[st], phase)) failed = true;
         const unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
         const float* cf = reinterpret_cast<const float*>(b + kRows * row_bytes);  // [s][4]
-        const float* sv = cf + 16;                                                // [s][4]
+        const float4 c4 = *reinterpret_cast<const float4*>(cf + 4 * s);
+        const float2 A82 = splat2(c4.x), Ar2 = splat2(c4.y);
+        const float2 A2 = splat2(__fadd_rn(c4.x, c4.y));
+        const float2 nB2 = splat2(c4.z), nC2 = splat2(c4.w);
+        const float2 G2 = splat2(cf[16 + 4 * s]);  // saved gate of stream s
+        float2 gv[4];
+        uint32_t ox[4], ok[4];
         if (active) {
-            float2 gv[4];
+            const uint4 xq = lds128(b + s * row_bytes + 16 * cg);
+            const uint4 kq = lds128(b + (kS + s) * row_bytes + 16 * cg);
+            const uint4 gq = lds128(b + (2 * kS + s) * row_bytes + 16 * cg);
+            const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w};
+            const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
+            const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x2 = bf2(xw[e]), k2 = bf2(kw[e]), g2 = bf2(gw[e]);
+                const float2 aw = mul2(A2, w2[e]);
+                ox[e] = pack2(fma2(aw, k2, fma2(nB2, x2, g2)));
+                ok[e] = pack2(fma2(aw, x2, mul2(nC2, k2)));
+                gv[e] = mul2(G2, g2);
+                // grad_w += (a8 + arest) * (x*k): a8*(x*k) exact, error-free sum
+                const float2 xk = mul2(x2, k2);
+                float2 sum, err;
+                two_sum2(phi[e], mul2(A82, xk), sum, err);
+                phi[e] = sum;
+                plo[e] = fma2(Ar2, xk, add2(plo[e], err));
+            }
+        } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) gv[e] = make_float2(0.f, 0.f);
-            uint16_t* gxo = p.gx + n * kS * kD + col0 + 8 * tid;
-            uint16_t* gko = p.gkv + n * (kS + 1) * kD + col0 + 8 * tid;
-#pragma unroll
-            for (int s = 0; s < kS; ++s) {
-                const float4 c4 = *reinterpret_cast<const float4*>(cf + 4 * s);
-                const float2 A2 = splat2(c4.x), Al2 = splat2(c4.y);
-                const float2 nB2 = splat2(c4.z), nC2 = splat2(c4.w);
-                const float2 G2 = splat2(sv[4 * s]);
-                const uint4 xq = lds128(b + s * row_bytes + 16 * tid);
-                const uint4 kq = lds128(b + (kS + s) * row_bytes + 16 * tid);
-                const uint4 gq = lds128(b + (2 * kS + s) * row_bytes + 16 * tid);
-                const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w};
-                const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
-                const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
-                uint32_t ox[4], ok[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x2 = bf2(xw[e]), k2 = bf2(kw[e]), g2 = bf2(gw[e]);
-                    const float2 aw = mul2(A2, w2[s][e]);
-                    ox[e] = pack2(fma2(aw, k2, fma2(nB2, x2, g2)));
-                    ok[e] = pack2(fma2(aw, x2, mul2(nC2, k2)));
-                    gv[e] = fma2(G2, g2, gv[e]);
-                    cacc_prod2_x2(phi[s][e], plo[s][e], A2, Al2, mul2(x2, k2));
-                }
-                stg_cs(gxo + s * kD, make_uint4(ox[0], ox[1], ox[2], ox[3]));
-                stg_cs(gko + s * kD, make_uint4(ok[0], ok[1], ok[2], ok[3]));
-            }
-            stg_cs(gko + kS * kD, make_uint4(pack2(gv[0]), pack2(gv[1]), pack2(gv[2]), pack2(gv[3])));
         }
-        // every thread is done with this stage: refill it
-        __syncthreads();
-        if (tid == 0 && j + stages < ntok) {
-            fence_proxy_async();
-            issue(j + stages);
+        // this warp is done with the stage; the last warp to finish refills it
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&released[st], 1u) == static_cast<unsigned int>(W - 1)) {
+                released[st] = 0u;
+                if (j + stages < ntok) {
+                    fence_proxy_async();
+                    issue(j + stages, st);
+                }
+            }
+        }
+        if (++st == stages) {
+            st = 0;
+            phase ^= 1u;
+        }
+        // grad_v = (g0 + g1) + (g2 + g3) over the four streams' lanes
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            gv[e] = add2(gv[e], make_float2(__shfl_xor_sync(kFullMask, gv[e].x, 8),
+                                            __shfl_xor_sync(kFullMask, gv[e].y, 8)));
+            gv[e] = add2(gv[e], make_float2(__shfl_xor_sync(kFullMask, gv[e].x, 16),
+                                            __shfl_xor_sync(kFullMask, gv[e].y, 16)));
+        }
+        if (active) {
+            stg_cs(p.gx + (n * kS + s) * kD + col, make_uint4(ox[0], ox[1], ox[2], ox[3]));
+            stg_cs(p.gkv + (n * (kS + 1) + s) * kD + col, make_uint4(ok[0], ok[1], ok[2], ok[3]));
+            if (s == 0)
+                stg_cs(p.gkv + (n * (kS + 1) + kS) * kD + col,
+                       make_uint4(pack2(gv[0]), pack2(gv[1]), pack2(gv[2]), pack2(gv[3])));
         }
     }
-    // this group's grad_w for the slice: (hi, lo) in slots 2g, 2g+1, or
+    // this group's grad_w for the columns: (hi, lo) in slots 2g, 2g+1, or
     // hi + lo in slot 0 when a single group covers a single block
     if (active && ntok > 0) {
+        float* o = p.partial + ((p.pair_slots ? 2 * grp : grp) * kS + s) * kD + col;
+        if (p.pair_slots) {
+            float* ol = o + static_cast<long long>(kS) * kD;
+            stg_f4(o, phi[0].x, phi[0].y, phi[1].x, phi[1].y);
+            stg_f4(o + 4, phi[2].x, phi[2].y, phi[3].x, phi[3].y);
+            stg_f4(ol, plo[0].x, plo[0].y, plo[1].x, plo[1].y);
+            stg_f4(ol + 4, plo[2].x, plo[2].y, plo[3].x, plo[3].y);
+        } else {
+            float r[8];
 #pragma unroll
-        for (int s = 0; s < kS; ++s) {
-            float* o = p.partial + ((p.pair_slots ? 2 * grp : grp) * kS + s) * kD + col0 + 8 * tid;
-            if (p.pair_slots) {
-                float* ol = o + static_cast<long long>(kS) * kD;
-                stg_f4(o, phi[s][0].x, phi[s][0].y, phi[s][1].x, phi[s][1].y);
-                stg_f4(o + 4, phi[s][2].x, phi[s][2].y, phi[s][3].x, phi[s][3].y);
-                stg_f4(ol, plo[s][0].x, plo[s][0].y, plo[s][1].x, plo[s][1].y);
-                stg_f4(ol + 4, plo[s][2].x, plo[s][2].y, plo[s][3].x, plo[s][3].y);
-            } else {
-                float r[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    r[2 * e] = __fadd_rn(phi[s][e].x, plo[s][e].x);
-                    r[2 * e + 1] = __fadd_rn(phi[s][e].y, plo[s][e].y);
-                }
-                stg_f4(o, r[0], r[1], r[2], r[3]);
-                stg_f4(o + 4, r[4], r[5], r[6], r[7]);
+            for (int e = 0; e < 4; ++e) {
+                r[2 * e] = __fadd_rn(phi[e].x, plo[e].x);
+                r[2 * e + 1] = __fadd_rn(phi[e].y, plo[e].y);
             }
+            stg_f4(o, r[0], r[1], r[2], r[3]);
+            stg_f4(o + 4, r[4], r[5], r[6], r[7]);
         }
     }
-    if (failed) atomicOr(p.err, kErrTimeout);
+    if (failed) {
+        atomicOr(p.err, kErrTimeout);
+        // let the copies this CTA issued land before it leaves (bounded)
+        if (tid == 0)
+            for (int t = ntok > stages ? static_cast<int>(ntok) - stages : 0; t < ntok; ++t)
+                (void)mbar_wait(&full[t % stages], static_cast<uint32_t>((t / stages) & 1));
+    }
 }
 
 // ---------------------------------------------------------------- kernel 3

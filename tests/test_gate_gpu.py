@@ -257,4 +257,4 @@ def test_launch_geometry():
     # 64-token blocks, so each cluster's (hi, lo) grad_weight pair fits
     bwd = eg.engram_launch_info(1, 8192)
     assert bwd["cluster"] >= 2 and 5120 % (8 * bwd["cluster"]) == 0
-    assert bwd["clusters"] <= 8192 // 128 and bwd["smem_bytes"] > 0
+    assert bwd["clusters"] <= 8192 // 128
