@@ -201,25 +201,23 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
 
 
 def cpu_baseline(seconds=10.0):
-    """The fp64 oracle (as it stands) on a bounded sample of the workload."""
+    """The fp64 oracle (as it stands) on the N=8192 workload, fwd + bwd,
+    repeated until about `seconds` of CPU work have run."""
     import oracle
     from engram_memory_gating_gb300.inputs import gate_inputs
     oracle.build()
-
-    def run(n):
-        inp = gate_inputs(n, 1, mask="bern0.9")
-        x, kv, w, m, g = f64_inputs(inp)
+    inp = gate_inputs(N_TOK, 1, mask="bern0.9")
+    x, kv, w, m, g = f64_inputs(inp)
+    reps, el = 0, 0.0
+    while el < seconds and reps < 200:
         t0 = time.perf_counter()
         _, saved = oracle.gate_fwd(x, kv, w, m)
         oracle.gate_bwd(x, kv, w, saved, g)
-        return time.perf_counter() - t0
-
-    t = run(16)
-    n = int(max(16, min(4096, 16 * seconds / max(t, 1e-6))))
-    t = run(n)
-    return {"value": round(n / t, 2), "unit": "tokens/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{n} tokens of the N=8192 workload (fwd+bwd, fp64), {t:.1f} s"}
+        el += time.perf_counter() - t0
+        reps += 1
+    return {"value": round(reps * N_TOK / el, 2), "unit": "tokens/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{reps} x the full N=8192 workload (fwd+bwd, fp64), {el:.1f} s"}
 
 
 def f64_inputs(inp):
@@ -350,6 +348,8 @@ def main():
     csrc = "engram_memory_gating_gb300/csrc/"
     traffic = profile_traffic("gate_bwd_n8192.md",
                               [csrc + "gate_bwd.cu", csrc + "common.cuh", csrc + "engram_abi.cu"])
+    traffic_fwd = profile_traffic("gate_fwd_n8192.md",
+                                  [csrc + "gate_fwd.cu", csrc + "common.cuh", csrc + "engram_abi.cu"])
 
     # ---- end to end through the public API with host buffers (pinned)
     h = {k: v.cpu().pin_memory() for k, v in inp.items()}
@@ -410,7 +410,7 @@ def main():
                      "traffic": traffic},
         "roofline_fwd": {"kernel": "engram_gate_fwd (gate_fwd_kernel), N=8192", "bound": "hbm",
                          "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(fwd_gbs / peak, 4)},
+                         "frac": round(fwd_gbs / peak, 4), "traffic": traffic_fwd},
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * N_TOK / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
