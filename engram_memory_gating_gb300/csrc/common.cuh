@@ -204,6 +204,21 @@ EG_DEV void stg_f4(float* p, float a, float b, float c, float d) {
 }
 
 EG_DEV uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+EG_DEV uint2 lds64(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+
+// Streaming 8-byte global store.
+EG_DEV void stg_cs8(void* p, const uint2& v) {
+    asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// Asynchronous 4-byte store into the shared memory of a CTA of this cluster,
+// completing 4 bytes on that CTA's mbarrier.
+EG_DEV void st_async_f32(uint32_t remote_addr, float a, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr),
+        "f"(a), "r"(remote_bar)
+        : "memory");
+}
 
 // ------------------------------------------------------------------ bf16
 
@@ -221,11 +236,22 @@ EG_DEV void unpack8(const uint4& q, float (&f)[8]) {
     f[7] = bf_hi(q.w);
 }
 
+EG_DEV void unpack4(const uint2& q, float (&f)[4]) {
+    f[0] = bf_lo(q.x);
+    f[1] = bf_hi(q.x);
+    f[2] = bf_lo(q.y);
+    f[3] = bf_hi(q.y);
+}
+
 // Two fp32 values -> packed bf16x2, round-to-nearest-even (lo in the low half).
 EG_DEV uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+EG_DEV uint2 pack4(const float (&f)[4]) {
+    return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
 }
 
 EG_DEV uint4 pack8(const float (&f)[8]) {

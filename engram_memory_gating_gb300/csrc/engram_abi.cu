@@ -14,37 +14,49 @@ __device__ unsigned int eg_error_word = 0u;
 
 namespace eg {
 
-int pick_cluster(int64_t groups_total, int max_groups) {
-    for (int c = 1; c <= 8; ++c)
-        if (groups_total % c == 0 && groups_total / c <= max_groups) return c;
-    return 0;
-}
-
 namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kGateD = ENGRAM_GATE_HIDDEN;
 constexpr int kGateBwdStages = 4;  // >= 3: a stage is refilled one token after its last use
-constexpr int kGcFwdStages = 6;
-constexpr int kGcBwdStages = 6;  // >= 5: rows of tokens tau-3 .. tau+1 stay resident
-static_assert(kGcBwdStages >= 5 && kGcBwdStages <= kMaxStages, "ring too short");
 static_assert(kGateBwdStages <= kMaxStages, "too many stages");
 static_assert(kGateBwdStages >= 3, "ring too short");
-constexpr int kGcFwdMinRange = 32;  // tokens; bounds the 3-token halo overhead
+// GateConv: CTAs of 256 threads, 4 columns each, 16 one-token ring stages
+constexpr int kGcThreads = 256;
+constexpr int kGcStages = 16;
+constexpr int kGcMinRange = 16;    // tokens; bounds the 3-token halo overhead
+constexpr int kGcRangeCost = 8;    // per-range set-up, in token-steps, for the range split
+constexpr int64_t kGcBwdSlots = 256;  // backward weight-gradient slots (one per range)
 
 struct OccKey {
     int op, cluster, threads, smem;
+};
+
+// GateConv launch geometry for one (M, T, d).
+struct GcGeom {
+    LaunchCfg c;
+    int ncols;
+    int ring_off;
+    int range_len;
+    int rpr;  // ranges per batch row
+};
+
+struct GcCacheEntry {
+    int64_t M = -1, T = -1, d = -1;
+    GcGeom g;
 };
 
 struct DeviceState {
     bool init = false;
     bool ok = false;
     int sm_count = 0;
+    int smem_optin = 0;  // largest dynamic shared memory a CTA may opt in to
     unsigned int* err = nullptr;
     static constexpr int kCache = 64;
     OccKey keys[kCache];
     int vals[kCache];
     int n = 0;
+    GcCacheEntry gc_last[2];  // forward, backward
 };
 
 std::mutex g_mu;
@@ -60,23 +72,31 @@ int max_clusters(DeviceState& st, int op, int cluster, int threads, int smem) {
             return st.vals[i];
     int v = 0;
     cudaError_t e = cudaSuccess;
-    switch (op) {
-        case 0:
-            e = gate_fwd_prepare(smem);
-            if (e == cudaSuccess) e = gate_fwd_max_clusters(cluster, threads, smem, &v);
-            break;
-        case 1:
-            e = gate_bwd_prepare(smem);
-            if (e == cudaSuccess) e = gate_bwd_max_clusters(cluster, threads, smem, &v);
-            break;
-        case 2:
-            e = gateconv_fwd_prepare(smem);
-            if (e == cudaSuccess) e = gateconv_fwd_max_clusters(cluster, threads, smem, &v);
-            break;
-        default:
-            e = gateconv_bwd_prepare(smem);
-            if (e == cudaSuccess) e = gateconv_bwd_max_clusters(cluster, threads, smem, &v);
-            break;
+    // The dynamic shared-memory limit is an attribute of the kernel, shared by
+    // every shape launched with it: set it once to the device's opt-in maximum
+    // (the occupancy query below uses the shape's own size).
+    const int lim = smem > 0 ? st.smem_optin : 0;
+    if (smem > st.smem_optin) {
+        e = cudaErrorInvalidValue;
+    } else {
+        switch (op) {
+            case 0:
+                e = gate_fwd_prepare(lim);
+                if (e == cudaSuccess) e = gate_fwd_max_clusters(cluster, threads, smem, &v);
+                break;
+            case 1:
+                e = gate_bwd_prepare(lim);
+                if (e == cudaSuccess) e = gate_bwd_max_clusters(cluster, threads, smem, &v);
+                break;
+            case 2:
+                e = gateconv_fwd_prepare(lim);
+                if (e == cudaSuccess) e = gateconv_fwd_max_clusters(cluster, threads, smem, &v);
+                break;
+            default:
+                e = gateconv_bwd_prepare(lim);
+                if (e == cudaSuccess) e = gateconv_bwd_max_clusters(cluster, threads, smem, &v);
+                break;
+        }
     }
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
@@ -105,6 +125,8 @@ DeviceState* device_state() {
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
             cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err), eg_error_word) != cudaSuccess) {
             (void)cudaGetLastError();
             return nullptr;
@@ -150,9 +172,7 @@ engram_status_t launch_status(cudaError_t e) {
 
 // Forward: one warp per (token, stream) row, 8 warps per CTA, as many CTAs
 // as fit on the device (persistent), fewer if there are fewer rows.
-bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngroups) {
-    ncols = kGateD;
-    ngroups = 0;
+bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c) {
     c.cluster = 1;
     c.threads = 256;
     c.stages = 0;
@@ -193,62 +213,72 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngr
 }
 
 bool gc_shape_ok(int64_t M, int64_t T, int64_t d) {
-    if (M < 1 || T < 1 || d < 8 || d > 65536 || d % 8 != 0) return false;
-    if (M * T > 2147483647LL) return false;
-    // forward: <= 256 groups of 8 columns per CTA; backward: <= 128 groups of
-    // 8 columns (256 threads of 4 columns).  Slices are whole 8-column groups
-    // so that every row slice is a multiple of 16 bytes (bulk-copy rule).
-    if (pick_cluster(d / 8, 256) == 0 || pick_cluster(d / 8, 128) == 0) return false;
-    return true;
+    if (M < 1 || T < 1 || d < 8 || d > ENGRAM_GATECONV_MAX_D || d % 8 != 0) return false;
+    return M * T <= 2147483647LL;
 }
 
-bool gc_fwd_cfg(DeviceState& st, int64_t M, int64_t T, int64_t d, LaunchCfg& c, int& ncols,
-                int& ngroups, int& range_len, int& rpr) {
-    int C = pick_cluster(d / 8, 160);
-    if (C == 0) C = pick_cluster(d / 8, 256);
-    ncols = static_cast<int>(d / C);
-    ngroups = ncols / 8;
-    c.cluster = C;
-    c.threads = round_up(ngroups, 32);
-    c.stages = kGcFwdStages;
-    c.smem = kSmemRingOff + c.stages * 3 * ncols * 2;
-    const int mc = max_clusters(st, 2, C, c.threads, c.smem);
-    if (mc <= 0) return false;
-    // as many ranges as clusters fit, none shorter than kGcFwdMinRange tokens
-    int64_t per_row = (mc + M - 1) / M;
-    const int64_t max_per_row = (T + kGcFwdMinRange - 1) / kGcFwdMinRange;
-    if (per_row > max_per_row) per_row = max_per_row;
-    if (per_row < 1) per_row = 1;
-    range_len = static_cast<int>((T + per_row - 1) / per_row);
-    rpr = static_cast<int>((T + range_len - 1) / range_len);
-    c.clusters = static_cast<int>(M * rpr);
-    return true;
+// Weight-gradient slots of the backward's workspace: one per token range, at
+// most max(M, kGcBwdSlots) ranges (fixed by M and T alone, so the workspace
+// size does not depend on the device).
+int64_t gc_bwd_slots(int64_t M, int64_t T) {
+    const int64_t per_row = (T + kGcMinRange - 1) / kGcMinRange;
+    int64_t s = M * per_row;
+    if (s > kGcBwdSlots) s = kGcBwdSlots;
+    return s > M ? s : M;
 }
 
-// Range length of the backward depends on (M, T) only, so that the workspace
-// size does not depend on the device: about 512 ranges, 128..T tokens each.
-void gc_bwd_ranges(int64_t M, int64_t T, int& range_len, int& rpr) {
-    int64_t L = (M * T + 511) / 512;
-    L = (L + 31) / 32 * 32;
-    if (L < 128) L = 128;
-    if (L > T) L = T;
-    range_len = static_cast<int>(L);
-    rpr = static_cast<int>((T + L - 1) / L);
+// Column split: C = ceil(d / 1024) CTAs per row, each of `threads` (a multiple
+// of 32) threads owning 4 columns; every slice is a whole number of 8-column
+// groups, so every row slice is a multiple of 16 bytes (bulk-copy rule).
+void gc_split(int64_t d, int rows, GcGeom& g) {
+    const int C = static_cast<int>((d + 4 * kGcThreads - 1) / (4 * kGcThreads));
+    const int quads = static_cast<int>(d / 4);
+    g.c.cluster = C;
+    g.c.threads = round_up((quads + C - 1) / C, 32);
+    g.ncols = 4 * g.c.threads;
+    const int parts = C * (g.c.threads / 32);
+    g.ring_off = round_up(256 + 2 * parts * 16 * 4, 128);
+    g.c.stages = kGcStages;
+    g.c.smem = g.ring_off + kGcStages * rows * g.ncols * 2;
 }
 
-bool gc_bwd_cfg(DeviceState& st, int64_t M, int64_t T, int64_t d, LaunchCfg& c, int& ncols,
-                int& ngroups, int& range_len, int& rpr) {
-    const int C = pick_cluster(d / 8, 128);
-    ncols = static_cast<int>(d / C);
-    ngroups = ncols / 4;
-    c.cluster = C;
-    c.threads = round_up(ngroups, 32);
-    c.stages = kGcBwdStages;
-    c.smem = kSmemRingOff + c.stages * 5 * ncols * 2;
-    if (max_clusters(st, 3, C, c.threads, c.smem) <= 0) return false;
-    gc_bwd_ranges(M, T, range_len, rpr);
-    c.clusters = static_cast<int>(M * rpr);
-    return true;
+// Token ranges: ranges_per_row r minimising (waves of clusters) x (tokens of
+// the longest range + halo + set-up), with at most max_ranges ranges.
+void gc_ranges(int64_t M, int64_t T, int K, int64_t max_ranges, GcGeom& g) {
+    int64_t hi = (T + kGcMinRange - 1) / kGcMinRange;
+    if (hi > max_ranges / M) hi = max_ranges / M;
+    if (hi > 4096) hi = 4096;
+    if (hi < 1) hi = 1;
+    int64_t best_len = T, best_cost = -1;
+    for (int64_t r = 1; r <= hi; ++r) {
+        const int64_t len = (T + r - 1) / r;
+        const int64_t rr = (T + len - 1) / len;
+        const int64_t waves = (M * rr + K - 1) / K;
+        const int64_t cost = waves * (len + 3 + kGcRangeCost);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_len = len;
+        }
+    }
+    g.range_len = static_cast<int>(best_len);
+    g.rpr = static_cast<int>((T + best_len - 1) / best_len);
+    g.c.clusters = static_cast<int>(M * g.rpr);
+}
+
+// op 0: forward (3 rows per stage: H, k, v); op 1: backward (dY, vhat, v, H, k).
+const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
+    GcCacheEntry& e = st.gc_last[op];
+    if (e.M == M && e.T == T && e.d == d) return &e.g;
+    GcGeom g = {};
+    gc_split(d, op == 0 ? 3 : 5, g);
+    const int K = max_clusters(st, op == 0 ? 2 : 3, g.c.cluster, g.c.threads, g.c.smem);
+    if (K <= 0) return nullptr;
+    gc_ranges(M, T, K, op == 0 ? (int64_t(1) << 31) : gc_bwd_slots(M, T), g);
+    e.M = M;
+    e.T = T;
+    e.d = d;
+    e.g = g;
+    return &e.g;
 }
 
 }  // namespace
@@ -296,8 +326,7 @@ engram_status_t engram_gate_fwd(const void* x, const void* kv, const float* weig
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
     LaunchCfg c = {};
-    int ncols, ngroups;
-    if (!gate_fwd_cfg(*st, N, c, ncols, ngroups)) return ENGRAM_ERR_DEVICE;
+    if (!gate_fwd_cfg(*st, N, c)) return ENGRAM_ERR_DEVICE;
     GateFwdParams p;
     p.x = static_cast<const uint16_t*>(x);
     p.kv = static_cast<const uint16_t*>(kv);
@@ -307,10 +336,6 @@ engram_status_t engram_gate_fwd(const void* x, const void* kv, const float* weig
     p.saved = saved;
     p.err = st->err;
     p.N = N;
-    p.d = kGateD;
-    p.ncols = ncols;
-    p.ngroups = ngroups;
-    p.stages = c.stages;
     p.eps = eps;
     return launch_status(gate_fwd_launch(p, c, stream));
 }
@@ -398,9 +423,8 @@ engram_status_t engram_gateconv_fwd(const void* H, const void* k, const void* v,
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
-    LaunchCfg c = {};
-    int ncols, ngroups, range_len, rpr;
-    if (!gc_fwd_cfg(*st, M, T, d, c, ncols, ngroups, range_len, rpr)) return ENGRAM_ERR_DEVICE;
+    const GcGeom* g = gc_cfg(*st, 0, M, T, d);
+    if (!g) return ENGRAM_ERR_DEVICE;
     GateConvFwdParams p;
     p.H = static_cast<const uint16_t*>(H);
     p.k = static_cast<const uint16_t*>(k);
@@ -418,21 +442,18 @@ engram_status_t engram_gateconv_fwd(const void* H, const void* k, const void* v,
     p.M = static_cast<int>(M);
     p.T = static_cast<int>(T);
     p.d = static_cast<int>(d);
-    p.ncols = ncols;
-    p.ngroups = ngroups;
-    p.stages = c.stages;
-    p.range_len = range_len;
-    p.ranges_per_row = rpr;
+    p.ncols = g->ncols;
+    p.ring_off = g->ring_off;
+    p.range_len = g->range_len;
+    p.ranges_per_row = g->rpr;
     p.eps = eps;
     p.inv_sqrt_d = static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
-    return launch_status(gateconv_fwd_launch(p, c, stream));
+    return launch_status(gateconv_fwd_launch(p, g->c, stream));
 }
 
 size_t engram_gateconv_bwd_workspace_size(int64_t M, int64_t T, int64_t d) {
     if (!gc_shape_ok(M, T, d)) return 0;
-    int range_len, rpr;
-    gc_bwd_ranges(M, T, range_len, rpr);
-    return static_cast<size_t>(M) * static_cast<size_t>(rpr) * 6 * static_cast<size_t>(d) * 4;
+    return static_cast<size_t>(gc_bwd_slots(M, T)) * 6 * static_cast<size_t>(d) * 4;
 }
 
 engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k,
@@ -468,9 +489,8 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
-    LaunchCfg c = {};
-    int ncols, ngroups, range_len, rpr;
-    if (!gc_bwd_cfg(*st, M, T, d, c, ncols, ngroups, range_len, rpr)) return ENGRAM_ERR_DEVICE;
+    const GcGeom* g = gc_cfg(*st, 1, M, T, d);
+    if (!g) return ENGRAM_ERR_DEVICE;
     float* partial = static_cast<float*>(workspace);
     GateConvBwdParams p;
     p.dY = static_cast<const uint16_t*>(dY);
@@ -493,16 +513,15 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
     p.M = static_cast<int>(M);
     p.T = static_cast<int>(T);
     p.d = static_cast<int>(d);
-    p.ncols = ncols;
-    p.ngroups = ngroups;
-    p.stages = c.stages;
-    p.range_len = range_len;
-    p.ranges_per_row = rpr;
+    p.ncols = g->ncols;
+    p.ring_off = g->ring_off;
+    p.range_len = g->range_len;
+    p.ranges_per_row = g->rpr;
     p.eps = eps;
     p.inv_sqrt_d = static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
-    engram_status_t s = launch_status(gateconv_bwd_launch(p, c, stream));
+    engram_status_t s = launch_status(gateconv_bwd_launch(p, g->c, stream));
     if (s != ENGRAM_OK) return s;
-    const int R = c.clusters;
+    const int R = g->c.clusters;
     float* outs3[3] = {drms_w_h, drms_w_v, dconv_w};
     const int offs[3] = {0, 1, 2};
     const int lens[3] = {1, 1, 4};
@@ -584,11 +603,11 @@ engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
     LaunchCfg c = {};
-    int ncols, ngroups, range_len, rpr;
+    int ncols, ngroups;
     bool ok = false;
     switch (op) {
         case 0:
-            ok = n0 >= 1 && n0 <= ENGRAM_GATE_MAX_TOKENS && gate_fwd_cfg(*st, n0, c, ncols, ngroups);
+            ok = n0 >= 1 && n0 <= ENGRAM_GATE_MAX_TOKENS && gate_fwd_cfg(*st, n0, c);
             break;
         case 1: {
             int gt = 0;
@@ -601,11 +620,12 @@ engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
             break;
         }
         case 2:
-            ok = gc_shape_ok(n0, n1, n2) && gc_fwd_cfg(*st, n0, n1, n2, c, ncols, ngroups, range_len, rpr);
+        case 3: {
+            const GcGeom* g = gc_shape_ok(n0, n1, n2) ? gc_cfg(*st, op - 2, n0, n1, n2) : nullptr;
+            ok = g != nullptr;
+            if (ok) c = g->c;
             break;
-        case 3:
-            ok = gc_shape_ok(n0, n1, n2) && gc_bwd_cfg(*st, n0, n1, n2, c, ncols, ngroups, range_len, rpr);
-            break;
+        }
         default:
             return ENGRAM_ERR_SHAPE;
     }

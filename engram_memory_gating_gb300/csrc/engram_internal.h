@@ -7,26 +7,8 @@
 
 namespace eg {
 
-// Smallest cluster size C (1..8) that cuts the d/8 column groups of a row into
-// equal slices of at most `max_groups` groups; 0 if none does.
-int pick_cluster(int64_t d, int max_groups);
-
-// Shared-memory layout common to the row-split kernels: mbarriers (ring
-// stages, then the two exchange slots), per-warp partials (two buffers), the
-// cluster exchange slots (2 x 8 ranks x 16 floats), then the ring of stages.
+// Largest number of ring stages any kernel uses (mbarrier area sizing).
 constexpr int kMaxStages = 16;
-constexpr int kSmemBarOff = 0;                         // 16 stage ("full") mbarriers
-constexpr int kSmemRxBarOff = kMaxStages * 8;          // 4 exchange mbarriers
-constexpr int kSmemEmptyBarOff = kSmemRxBarOff + 4 * 8;  // 16 stage-release mbarriers
-constexpr int kRedWarps = 8;                           // per-warp partial buffers
-constexpr int kSmemRedOff = 512;                       // 2 x 8 warps x 16 floats
-constexpr int kSmemXchOff = kSmemRedOff + 2 * kRedWarps * 16 * 4;  // exchange slots
-constexpr int kXchSlots = 4;                           // tokens in flight per exchange
-constexpr int kXchMaxParts = 20;                       // cluster CTAs x warps per token
-constexpr int kSmemCoefOff = kSmemXchOff + kXchSlots * kXchMaxParts * 16 * 4;
-constexpr int kSmemRingOff = kSmemCoefOff + 2 * 32 * 4;     // 128-byte aligned
-static_assert(kSmemEmptyBarOff + kMaxStages * 8 <= kSmemRedOff, "barrier area");
-static_assert(kSmemRingOff % 128 == 0, "ring alignment");
 
 struct GateFwdParams {
     const uint16_t* x;
@@ -37,10 +19,6 @@ struct GateFwdParams {
     float* saved;
     unsigned int* err;
     long long N;
-    int d;        // hidden size of one stream
-    int ncols;    // columns per CTA slice
-    int ngroups;  // 8-column groups per CTA slice (<= threads)
-    int stages;
     float eps;
 };
 
@@ -73,6 +51,8 @@ struct GateWReduceParams {
     int pairs;  // slots come as (hi, lo) pairs
 };
 
+// GateConv: one cluster per token range (consecutive tokens of one batch
+// row); CTA `rank` of the cluster owns columns [rank * ncols, ...).
 struct GateConvFwdParams {
     const uint16_t* H;
     const uint16_t* k;
@@ -88,8 +68,9 @@ struct GateConvFwdParams {
     float* rv;
     unsigned int* err;
     int M, T, d;
-    int ncols, ngroups, stages;
-    int range_len;       // tokens per range (last range of a row may be shorter)
+    int ncols;           // columns per CTA slice (4 per thread); the last may be shorter
+    int ring_off;        // byte offset of the ring in shared memory
+    int range_len;       // tokens per range (the last range of a row may be shorter)
     int ranges_per_row;
     float eps;
     float inv_sqrt_d;
@@ -114,7 +95,9 @@ struct GateConvBwdParams {
     float* partial;  // (ranges, 6, d): dwh, dwv, dcw[0..3]
     unsigned int* err;
     int M, T, d;
-    int ncols, ngroups, stages;
+    int ncols;
+    int ring_off;
+    int du_off;      // byte offset of the du buffers in shared memory
     int range_len;
     int ranges_per_row;
     float eps;

@@ -72,6 +72,7 @@ const char* engram_status_string(engram_status_t s);
 #define ENGRAM_GATE_KV_COLS 25600
 #define ENGRAM_GATE_MAX_TOKENS 4194240   /* forward: 1 <= N <= 65535*64     */
 #define ENGRAM_GATE_BWD_MAX_TOKENS 8192  /* backward: N % 64 == 0, N <= 8192 */
+#define ENGRAM_GATECONV_MAX_D 8192       /* GateConv: 8 <= d <= 8192, d % 8 == 0 */
 
 /*
  * Saved-state gate, forward (cuDNN "Engram saved-state gate", semantics and
@@ -144,7 +145,8 @@ engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weig
  * (k rrms_k w_h)_i / sqrt(d)), u = vhat * rrms_v * rms_w_v, conv zero-padded
  * at the start of each batch row.  Y and vhat are rounded once to BF16; the
  * forward uses the unrounded vhat for rrms_v, u and Y.
- *   1 <= M, 1 <= T, 8 <= d <= 65536, d % 8 == 0, M*T <= 2^31 - 1.
+ *   1 <= M, 1 <= T, 8 <= d <= ENGRAM_GATECONV_MAX_D, d % 8 == 0,
+ *   M*T <= 2^31 - 1; otherwise ENGRAM_ERR_SHAPE.
  * Workspace: none.
  */
 engram_status_t engram_gateconv_fwd(const void* H, const void* k, const void* v,
@@ -164,8 +166,10 @@ size_t engram_gateconv_bwd_workspace_size(int64_t M, int64_t T, int64_t d);
  *   drms_w_h, drms_w_v  fp32 (d)            out, summed over all M*T tokens
  *   dconv_w             fp32 (4, d)         out, summed over all M*T tokens
  *   workspace  >= engram_gateconv_bwd_workspace_size(M, T, d) bytes, 16-B
- *              aligned: per-range fp32 weight-gradient partials, reduced in a
- *              fixed order by a second kernel (bitwise reproducible)
+ *              aligned: per-range fp32 weight-gradient partials (6 d floats
+ *              per token range, at most max(M, 256) ranges), summed in a fixed
+ *              order by a second kernel (bitwise reproducible); nothing in it
+ *              needs to start at zero
  * The backward reads the saved bf16 vhat (not alpha * v) wherever the forward
  * used the gated value, and recomputes the gate's logit from H, k, rrms_h and
  * rrms_k.  Same size limits as the forward.
