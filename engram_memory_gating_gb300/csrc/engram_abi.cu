@@ -179,7 +179,11 @@ bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c) {
     c.smem = 0;
     const int mc = max_clusters(st, 0, 1, c.threads, 0);
     if (mc <= 0) return false;
-    const int64_t need = (N * 4 + 7) / 8;
+    // rows per warp with every co-resident CTA busy, then the fewest CTAs that
+    // keep that count, so the last round of rows leaves few warps idle
+    const int64_t rows = N * 4;
+    const int64_t rpw = (rows + 8LL * mc - 1) / (8LL * mc);
+    const int64_t need = (rows + 8 * rpw - 1) / (8 * rpw);
     c.clusters = static_cast<int>(need < mc ? need : mc);
     return true;
 }
@@ -243,18 +247,19 @@ void gc_split(int64_t d, int rows, GcGeom& g) {
 }
 
 // Token ranges: ranges_per_row r minimising (waves of clusters) x (tokens of
-// the longest range + halo + set-up), with at most max_ranges ranges.
+// the longest range + halo + set-up), with at most max_ranges ranges.  Range
+// lengths are multiples of 4 tokens (the kernels' window slots rely on it).
 void gc_ranges(int64_t M, int64_t T, int K, int64_t max_ranges, GcGeom& g) {
     int64_t hi = (T + kGcMinRange - 1) / kGcMinRange;
     if (hi > max_ranges / M) hi = max_ranges / M;
     if (hi > 4096) hi = 4096;
     if (hi < 1) hi = 1;
-    int64_t best_len = T, best_cost = -1;
+    int64_t best_len = (T + 3) / 4 * 4, best_cost = -1;
     for (int64_t r = 1; r <= hi; ++r) {
-        const int64_t len = (T + r - 1) / r;
+        const int64_t len = ((T + r - 1) / r + 3) / 4 * 4;
         const int64_t rr = (T + len - 1) / len;
         const int64_t waves = (M * rr + K - 1) / K;
-        const int64_t cost = waves * (len + 3 + kGcRangeCost);
+        const int64_t cost = waves * (len + 4 + kGcRangeCost);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best_len = len;

@@ -326,34 +326,51 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
 }
 
 // ---------------------------------------------------------------- kernel 3
-// grad_weight[i] from the group partials, merged in ascending order with
-// error-free additions (bitwise reproducible).  pairs: slot 2g = hi, 2g+1 = lo.
-__global__ void __launch_bounds__(256) wreduce_kernel(const GateWReduceParams p) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= p.n) return;
-    const float* src = p.partial + i;
+// grad_weight[i] from the group partials with error-free additions, in a fixed
+// order (bitwise reproducible): warp g of a CTA merges the g-th eighth of the
+// slots for 32 consecutive columns, then warp 0 merges the eight results in
+// ascending g.  pairs: slot 2b = hi, 2b+1 = lo of group b.
+constexpr int kRedGroups = 8;
+
+__global__ void __launch_bounds__(32 * kRedGroups) wreduce_kernel(const GateWReduceParams p) {
+    __shared__ float shi[kRedGroups][32], slo[kRedGroups][32];
+    const int lane = threadIdx.x & 31;
+    const int g = threadIdx.x >> 5;
+    const int i = blockIdx.x * 32 + lane;
+    const int nslot = p.pairs ? p.nblocks / 2 : p.nblocks;
+    const int per = (nslot + kRedGroups - 1) / kRedGroups;
+    const int b0 = min(nslot, g * per), b1 = min(nslot, b0 + per);
     float hi = 0.f, lo = 0.f;
-    if (!p.pairs) {
-        for (int b = 0; b < p.nblocks; ++b) cacc_add(hi, lo, __ldg(src + static_cast<size_t>(b) * p.stride));
-        p.out[i] = __fadd_rn(hi, lo);
-        return;
-    }
-    const int np = p.nblocks / 2;
-    int b = 0;
-    for (; b + 4 <= np; b += 4) {
-        float h[4], l[4];
+    if (i < p.n) {
+        const float* src = p.partial + i;
+        if (p.pairs) {
+            int b = b0;
+            for (; b + 4 <= b1; b += 4) {
+                float h[4], l[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            h[u] = __ldg(src + static_cast<size_t>(2 * (b + u)) * p.stride);
-            l[u] = __ldg(src + static_cast<size_t>(2 * (b + u) + 1) * p.stride);
+                for (int u = 0; u < 4; ++u) {
+                    h[u] = __ldg(src + static_cast<size_t>(2 * (b + u)) * p.stride);
+                    l[u] = __ldg(src + static_cast<size_t>(2 * (b + u) + 1) * p.stride);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) cacc_merge(hi, lo, h[u], l[u]);
+            }
+            for (; b < b1; ++b)
+                cacc_merge(hi, lo, __ldg(src + static_cast<size_t>(2 * b) * p.stride),
+                           __ldg(src + static_cast<size_t>(2 * b + 1) * p.stride));
+        } else {
+            for (int b = b0; b < b1; ++b) cacc_add(hi, lo, __ldg(src + static_cast<size_t>(b) * p.stride));
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) cacc_merge(hi, lo, h[u], l[u]);
     }
-    for (; b < np; ++b)
-        cacc_merge(hi, lo, __ldg(src + static_cast<size_t>(2 * b) * p.stride),
-                   __ldg(src + static_cast<size_t>(2 * b + 1) * p.stride));
-    p.out[i] = __fadd_rn(hi, lo);
+    shi[g][lane] = hi;
+    slo[g][lane] = lo;
+    __syncthreads();
+    if (g == 0 && i < p.n) {
+        float h = shi[0][lane], l = slo[0][lane];
+#pragma unroll
+        for (int k = 1; k < kRedGroups; ++k) cacc_merge(h, l, shi[k][lane], slo[k][lane]);
+        p.out[i] = __fadd_rn(h, l);
+    }
 }
 
 }  // namespace
@@ -393,9 +410,7 @@ cudaError_t gate_bwd_launch(const GateBwdParams& p, const LaunchCfg& c, cudaStre
 }
 
 cudaError_t gate_wreduce_launch(const GateWReduceParams& p, cudaStream_t s) {
-    const int threads = 128;
-    const int blocks = (p.n + threads - 1) / threads;
-    wreduce_kernel<<<blocks, threads, 0, s>>>(p);
+    wreduce_kernel<<<(p.n + 31) / 32, 32 * kRedGroups, 0, s>>>(p);
     return cudaPeekAtLastError();
 }
 

@@ -29,6 +29,8 @@
 // a halo.  Weight gradients accumulate per thread over the range and go to
 // the workspace, one slot per range; a second kernel sums the slots in
 // ascending order.
+#include <type_traits>
+
 #include "common.cuh"
 #include "engram_internal.h"
 #include "gateconv_xch.cuh"
@@ -38,9 +40,68 @@ namespace {
 
 using gc::kChunk;
 constexpr int kRows = 5;  // dY, vhat, v, H, k
-constexpr int kMask = gc::kStages - 1;
-static_assert((gc::kStages & kMask) == 0, "stage count must be a power of two");
-static_assert(gc::kStages >= 3 * kChunk + 3, "ring too short for two chunks and the look-ahead");
+constexpr int kStages = gc::kStages;
+static_assert(kStages % kChunk == 0, "a chunk must not wrap around the ring");
+static_assert(kStages >= 3 * kChunk + 3, "ring too short for two chunks and the look-ahead");
+
+// Per-thread sliding windows of the conv and its transpose: u and dc of the
+// last four tokens, token tau in slot tau % 4 (each float2 = 2 columns).
+struct Windows {
+    float2 U[4][2];
+    float2 D[4][2];
+};
+
+struct Weights {
+    float2 wv[2], wh2[2], cw[4][2];
+};
+
+// Consumes token tau (S = tau % 4) from its stage row pointer `b` (this
+// thread's 8 bytes of the dY row): u_tau = vhat rrms_v w_v and, for tokens
+// of the range or after it (`dc`), c_tau and dc_tau = dY SiLU'(c_tau); `acc`
+// adds the dconv_w contributions dc_tau u_{tau-3+j} of tokens inside the
+// range.  A token that does not exist (`real` false: past the row end) gives
+// u = dc = 0; values read for it are discarded by selection, never scaled by
+// zero, so whatever the stage holds cannot leak in.
+template <int S>
+EG_DEV void consume(Windows& W, float2 (&gcw)[4][2], const Weights& P, const unsigned char* b,
+                    uint32_t pitch, float rv, bool real, bool dc, bool acc) {
+    const uint2 vq = lds64(b + pitch);
+    const uint2 yq = lds64(b);
+    const float2 rv2 = splat2(rv);
+    const float2 zero = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float2 u = mul2(mul2(bf2(i == 0 ? vq.x : vq.y), rv2), P.wv[i]);
+        u = real ? u : zero;
+        const float2 dy = bf2(i == 0 ? yq.x : yq.y);
+        const float2 cc = fma2(P.cw[0][i], W.U[(S + 1) & 3][i],
+                               fma2(P.cw[1][i], W.U[(S + 2) & 3][i],
+                                    fma2(P.cw[2][i], W.U[(S + 3) & 3][i], mul2(P.cw[3][i], u))));
+        const float2 sg = make_float2(__fdividef(1.0f, 1.0f + __expf(-cc.x)),
+                                      __fdividef(1.0f, 1.0f + __expf(-cc.y)));
+        // SiLU'(c) = s (1 + c (1 - s))
+        const float2 one = splat2(1.0f);
+        float2 d = mul2(mul2(dy, sg), fma2(cc, sub2(one, sg), one));
+        d = (real && dc) ? d : zero;
+        const float2 da = acc ? d : zero;
+        gcw[0][i] = fma2(da, W.U[(S + 1) & 3][i], gcw[0][i]);
+        gcw[1][i] = fma2(da, W.U[(S + 2) & 3][i], gcw[1][i]);
+        gcw[2][i] = fma2(da, W.U[(S + 3) & 3][i], gcw[2][i]);
+        gcw[3][i] = fma2(da, u, gcw[3][i]);
+        W.D[S][i] = d;
+        W.U[S][i] = u;
+    }
+}
+
+// du_t = sum_j cw_j dc_{t+3-j} for t in slot S (dc_{t+3} already consumed)
+template <int S>
+EG_DEV void conv_t(const Windows& W, const Weights& P, float2 (&du)[2]) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        du[i] = fma2(P.cw[3][i], W.D[S][i],
+                     fma2(P.cw[2][i], W.D[(S + 1) & 3][i],
+                          fma2(P.cw[1][i], W.D[(S + 2) & 3][i], mul2(P.cw[0][i], W.D[(S + 3) & 3][i]))));
+}
 
 __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const GateConvBwdParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -67,40 +128,52 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
     const uint32_t row_bytes = 2u * static_cast<uint32_t>(cols);
     const uint32_t pitch = 2u * static_cast<uint32_t>(p.ncols);
     const uint32_t stage_bytes = kRows * pitch;
-    constexpr int stages = gc::kStages;
 
+    // ranges start at multiples of kChunk, and so does the streamed halo, so
+    // token t sits in window slot t % 4 (known at compile time below)
     const int m = q / p.ranges_per_row;
     const int t_out = (q - m * p.ranges_per_row) * p.range_len;
     const int t_end = min(p.T, t_out + p.range_len);
-    const int t_first = t_out - min(3, t_out);
+    const int t_first = t_out >= kChunk ? t_out - kChunk : 0;
     const int t_last = min(p.T, t_end + 3);
     const int ntok = t_last - t_first;             // streamed tokens (halo included)
     const int nchunks = (t_end - t_out + kChunk - 1) / kChunk;
     const long long row0 = static_cast<long long>(m) * p.T;
     const uint32_t xbytes = static_cast<uint32_t>(parts) * gc::kVals * 4u;
 
-    float wh[4], wv[4], cw[4][4];
+    Weights P;
     if (active) {
         const float4 a = __ldg(reinterpret_cast<const float4*>(p.wh + c0));
         const float4 b = __ldg(reinterpret_cast<const float4*>(p.wv + c0));
-        wh[0] = a.x; wh[1] = a.y; wh[2] = a.z; wh[3] = a.w;
-        wv[0] = b.x; wv[1] = b.y; wv[2] = b.z; wv[3] = b.w;
+        P.wh2[0] = make_float2(a.x * a.x, a.y * a.y);
+        P.wh2[1] = make_float2(a.z * a.z, a.w * a.w);
+        P.wv[0] = make_float2(b.x, b.y);
+        P.wv[1] = make_float2(b.z, b.w);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float4 c = __ldg(reinterpret_cast<const float4*>(p.cw + static_cast<long long>(j) * d + c0));
-            cw[j][0] = c.x; cw[j][1] = c.y; cw[j][2] = c.z; cw[j][3] = c.w;
+            P.cw[j][0] = make_float2(c.x, c.y);
+            P.cw[j][1] = make_float2(c.z, c.w);
         }
     } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            wh[e] = wv[e] = 0.f;
+        for (int i = 0; i < 2; ++i) {
+            P.wh2[i] = P.wv[i] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) cw[j][e] = 0.f;
+            for (int j = 0; j < 4; ++j) P.cw[j][i] = make_float2(0.f, 0.f);
         }
+    }
+    float2 wh[2];  // w_h itself, for drms_w_h
+    if (active) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p.wh + c0));
+        wh[0] = make_float2(a.x, a.y);
+        wh[1] = make_float2(a.z, a.w);
+    } else {
+        wh[0] = wh[1] = make_float2(0.f, 0.f);
     }
 
     auto issue = [&](int j) {
-        const int st = j & kMask;
+        const int st = j % kStages;
         const long long off = (row0 + t_first + j) * d + col0;
         unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
         mbar_arrive_expect_tx(&full[st], kRows * row_bytes);
@@ -110,28 +183,34 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
         bulk_g2s(b + 3 * pitch, p.H + off, row_bytes, &full[st]);
         bulk_g2s(b + 4 * pitch, p.k + off, row_bytes, &full[st]);
     };
-    auto stage_of = [&](int t) -> const unsigned char* {
-        return ring + static_cast<size_t>((t - t_first) & kMask) * stage_bytes + 8 * tid;
+    auto row_of = [&](int t) -> const unsigned char* {
+        return ring + static_cast<size_t>((t - t_first) % kStages) * stage_bytes + 8 * tid;
     };
-    // this warp is done with token t's stage; the last warp refills it
-    auto release = [&](int t) {
+    // this warp is done with the stages of tokens t .. t+n-1 (one counter per
+    // group, at its first stage); the last warp refills them
+    auto release = [&](int t, int n) {
         const int j = t - t_first;
-        const int st = j & kMask;
+        const int st = j % kStages;
         __syncwarp();
         if (lane == 0) {
             __threadfence_block();
             if (atomicAdd(&released[st], 1u) == static_cast<unsigned int>(nw - 1)) {
                 released[st] = 0u;
-                if (j + stages < ntok) {
-                    fence_proxy_async();
-                    issue(j + stages);
-                }
+                fence_proxy_async();
+                for (int i = 0; i < n && j + kStages + i < ntok; ++i) issue(j + kStages + i);
             }
         }
     };
+    // waits for token tau's stage (a real token: t_first <= tau < t_last)
+    bool failed = false;
+    auto wait_tok = [&](int tau) {
+        const int j = tau - t_first;
+        if (!failed && !mbar_wait(&full[j % kStages], static_cast<uint32_t>((j / kStages) & 1)))
+            failed = true;
+    };
 
     if (tid == 0) {
-        for (int s = 0; s < stages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             released[s] = 0u;
         }
@@ -140,130 +219,145 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
         fence_mbar_init();
         mbar_arrive_expect_tx(&xbar[0], xbytes);
         if (nchunks > 1) mbar_arrive_expect_tx(&xbar[1], xbytes);
-        const int pro = ntok < stages ? ntok : stages;
+        const int pro = ntok < kStages ? ntok : kStages;
         for (int j = 0; j < pro; ++j) issue(j);
     }
     cluster_sync();
 
-    float u1[4], u2[4], u3[4];     // u at tau-1, tau-2, tau-3
-    float dc1[4], dc2[4], dc3[4];  // dc at tau-1, tau-2, tau-3
-    float gwh[4], gwv[4], gcw[4][4];
+    Windows W;
+    float2 gcw[4][2], gwh[2], gwv[2];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        u1[e] = u2[e] = u3[e] = dc1[e] = dc2[e] = dc3[e] = 0.f;
-        gwh[e] = gwv[e] = 0.f;
+    for (int i = 0; i < 2; ++i) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) gcw[j][e] = 0.f;
+        for (int s = 0; s < 4; ++s) W.U[s][i] = W.D[s][i] = gcw[s][i] = make_float2(0.f, 0.f);
+        gwh[i] = gwv[i] = make_float2(0.f, 0.f);
     }
-    bool failed = false;
 
-    // Step to token tau: u_tau, c_tau, dc_tau (zero outside [t_out, t_last)),
-    // the dconv_w contributions of tau inside the range; returns dc_tau.
-    auto advance = [&](int tau, float (&dcv)[4]) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dcv[e] = 0.f;
-        if (tau >= t_last) return;
-        const int j = tau - t_first;
-        if (!failed && !mbar_wait(&full[j & kMask], static_cast<uint32_t>((j / stages) & 1))) failed = true;
+    // Steps to token tau in slot S: real tokens are consumed (the halo before
+    // the range for u only, and released at once), tokens past the row end
+    // give dc = 0.
+    auto step = [&](auto slot, int tau) {
+        constexpr int S = decltype(slot)::value;
+        if (tau < 0) return;
+        if (tau >= t_last) {
+            W.D[S][0] = W.D[S][1] = make_float2(0.f, 0.f);
+            return;
+        }
+        wait_tok(tau);
         const float rv = __ldg(p.rv + row0 + tau);
-        if (active) {
-            const unsigned char* b = stage_of(tau);
-            float vh[4], u[4];
-            unpack4(lds64(b + pitch), vh);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) u[e] = vh[e] * rv * wv[e];
-            if (tau >= t_out) {
-                float dy[4];
-                unpack4(lds64(b), dy);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float cc =
-                        fmaf(cw[0][e], u3[e], fmaf(cw[1][e], u2[e], fmaf(cw[2][e], u1[e], cw[3][e] * u[e])));
-                    const float s = __frcp_rn(1.0f + __expf(-cc));
-                    dcv[e] = dy[e] * s * fmaf(cc, 1.0f - s, 1.0f);
-                    if (tau < t_end) {
-                        gcw[0][e] = fmaf(dcv[e], u3[e], gcw[0][e]);
-                        gcw[1][e] = fmaf(dcv[e], u2[e], gcw[1][e]);
-                        gcw[2][e] = fmaf(dcv[e], u1[e], gcw[2][e]);
-                        gcw[3][e] = fmaf(dcv[e], u[e], gcw[3][e]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                u3[e] = u2[e];
-                u2[e] = u1[e];
-                u1[e] = u[e];
-            }
-        }
-        // halo tokens are not needed after this step
-        if (tau < t_out || tau >= t_end) release(tau);
-    };
-    auto push_dc = [&](const float (&dcv)[4]) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            dc3[e] = dc2[e];
-            dc2[e] = dc1[e];
-            dc1[e] = dcv[e];
-        }
+        consume<S>(W, gcw, P, row_of(tau), pitch, rv, true, tau >= t_out, active && tau >= t_out && tau < t_end);
+        // the halo before the range is not needed again (the halo after it
+        // sits at the end of the stream, its stages are never refilled)
+        if (tau < t_out) release(tau, 1);
     };
 
-    // fill the windows: tokens before the range, and dc of its first 3 tokens
-    for (int tau = t_first; tau < t_out + 3; ++tau) {
-        float dcv[4];
-        advance(tau, dcv);
-        push_dc(dcv);
-    }
+    // fill the windows: the 4 tokens before the range, and dc of its first 3
+    step(std::integral_constant<int, 0>(), t_out - 4);
+    step(std::integral_constant<int, 1>(), t_out - 3);
+    step(std::integral_constant<int, 2>(), t_out - 2);
+    step(std::integral_constant<int, 3>(), t_out - 1);
+    step(std::integral_constant<int, 0>(), t_out);
+    step(std::integral_constant<int, 1>(), t_out + 1);
+    step(std::integral_constant<int, 2>(), t_out + 2);
 
     const float inv_d = 1.0f / static_cast<float>(d);
-    float duA[kChunk][4], duB[kChunk][4];  // du of chunk c and of chunk c - 1
+    float2 duA[kChunk][2], duB[kChunk][2];  // du of chunk c and of chunk c - 1
     float P_l = 0.f, Q_l = 0.f, a_l = 0.f, Ah_l = 0.f, Bh_l = 0.f, Bk_l = 0.f;
 
+    // one output token t = tc + S of chunk c: consume t + 3, then du_t, the
+    // partial sums and drms_w_v (branch-free: tokens past the range select 0)
+    auto out1 = [&](auto slot, int tc, const float (&rvt)[kChunk], const float (&rvc)[kChunk],
+                    float (&sums)[gc::kVals]) {
+        constexpr int S = decltype(slot)::value;
+        const int t = tc + S;
+        const bool vt = active && t < t_end;
+        consume<(S + 3) & 3>(W, gcw, P, row_of(t + 3), pitch, rvc[S], t + 3 < t_last, true,
+                             active && t + 3 < t_end);
+        float2 du[2];
+        conv_t<S>(W, P, du);
+        const unsigned char* b = row_of(t);
+        const uint2 yq = lds64(b), hq = lds64(b + pitch), vq = lds64(b + 2 * pitch);
+        const uint2 Hq = lds64(b + 3 * pitch), kq = lds64(b + 4 * pitch);
+        const float2 rv2 = splat2(rvt[S]);
+        const float2 zero = make_float2(0.f, 0.f);
+        float2 s1 = zero, s3 = zero, s4 = zero, s5 = zero;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float2 dy = bf2(i == 0 ? yq.x : yq.y), vh = bf2(i == 0 ? hq.x : hq.y);
+            const float2 vv = bf2(i == 0 ? vq.x : vq.y);
+            const float2 h = bf2(i == 0 ? Hq.x : Hq.y), kk = bf2(i == 0 ? kq.x : kq.y);
+            const float2 wdu = mul2(P.wv[i], du[i]);
+            s1 = fma2(fma2(rv2, wdu, dy), vv, s1);
+            s3 = fma2(vh, vv, s3);
+            s4 = fma2(wdu, vh, s4);
+            s5 = fma2(mul2(h, kk), P.wh2[i], s5);
+            const float2 g = mul2(du[i], mul2(vh, rv2));
+            gwv[i] = add2(gwv[i], vt ? g : zero);
+            duA[S][i] = du[i];
+        }
+        sums[4 * S + 0] = vt ? s1.x + s1.y : 0.f;
+        sums[4 * S + 1] = vt ? s3.x + s3.y : 0.f;
+        sums[4 * S + 2] = vt ? s4.x + s4.y : 0.f;
+        sums[4 * S + 3] = vt ? s5.x + s5.y : 0.f;
+    };
+
+    // one output token t of chunk c - 1 in slot S: dv, dH, dk, drms_w_h
+    auto out2 = [&](auto slot, int t) {
+        constexpr int S = decltype(slot)::value;
+        const float Pv = __shfl_sync(kFullMask, P_l, S);
+        const float Q = __shfl_sync(kFullMask, Q_l, S);
+        const float a = __shfl_sync(kFullMask, a_l, S);
+        const float Ah = __shfl_sync(kFullMask, Ah_l, S);
+        const float Bh = __shfl_sync(kFullMask, Bh_l, S);
+        const float Bk = __shfl_sync(kFullMask, Bk_l, S);
+        const bool vt = active && t < t_end;
+        const unsigned char* b = row_of(t);
+        const uint2 yq = lds64(b), hq = lds64(b + pitch);
+        const uint2 Hq = lds64(b + 3 * pitch), kq = lds64(b + 4 * pitch);
+        const float2 P2 = splat2(Pv), nQ2 = splat2(-Q), a2 = splat2(a);
+        const float2 Ah2 = splat2(Ah), nBh2 = splat2(-Bh), nBk2 = splat2(-Bk), Ah22 = splat2(2.0f * Ah);
+        const float2 zero = make_float2(0.f, 0.f);
+        uint32_t oh[2], ok[2], ov[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float2 dy = bf2(i == 0 ? yq.x : yq.y), vh = bf2(i == 0 ? hq.x : hq.y);
+            const float2 h = bf2(i == 0 ? Hq.x : Hq.y), kk = bf2(i == 0 ? kq.x : kq.y);
+            const float2 dvh = fma2(nQ2, vh, fma2(mul2(P2, P.wv[i]), duB[S][i], dy));
+            ov[i] = pack2(mul2(a2, dvh));
+            const float2 aw = mul2(Ah2, P.wh2[i]);
+            oh[i] = pack2(fma2(aw, kk, mul2(nBh2, h)));
+            ok[i] = pack2(fma2(aw, h, mul2(nBk2, kk)));
+            const float2 g = mul2(mul2(Ah22, wh[i]), mul2(h, kk));
+            gwh[i] = add2(gwh[i], vt ? g : zero);
+        }
+        if (vt) {
+            const long long off = (row0 + t) * d + c0;
+            stg_cs8(p.dH + off, make_uint2(oh[0], oh[1]));
+            stg_cs8(p.dk + off, make_uint2(ok[0], ok[1]));
+            stg_cs8(p.dv + off, make_uint2(ov[0], ov[1]));
+        }
+    };
+
     for (int c = 0; c <= nchunks; ++c) {
+        const int tc = t_out + c * kChunk;          // first token of chunk c
         // ---- 1: du and partial sums of chunk c
         float val = 0.f;
         if (c < nchunks) {
-            float sums[gc::kVals];
+            // all waits first, then branch-free arithmetic over the chunk
+#pragma unroll
+            for (int w = 0; w < kChunk; ++w)
+                if (tc + w < t_end && tc + w + 3 < t_last) wait_tok(tc + w + 3);
+            float rvt[kChunk], rvc[kChunk];
 #pragma unroll
             for (int w = 0; w < kChunk; ++w) {
-                const int t = t_out + c * kChunk + w;
-                float s1 = 0.f, s3 = 0.f, s4 = 0.f, s5 = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) duA[w][e] = 0.f;
-                if (t < t_end) {
-                    float dcv[4];
-                    advance(t + 3, dcv);
-                    float du[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        du[e] = fmaf(cw[3][e], dc3[e], fmaf(cw[2][e], dc2[e], fmaf(cw[1][e], dc1[e], cw[0][e] * dcv[e])));
-                    push_dc(dcv);
-                    const float rv = __ldg(p.rv + row0 + t);
-                    if (active) {
-                        const unsigned char* b = stage_of(t);
-                        float dy[4], vh[4], vv[4], h[4], kk[4];
-                        unpack4(lds64(b), dy);
-                        unpack4(lds64(b + pitch), vh);
-                        unpack4(lds64(b + 2 * pitch), vv);
-                        unpack4(lds64(b + 3 * pitch), h);
-                        unpack4(lds64(b + 4 * pitch), kk);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float wdu = wv[e] * du[e];
-                            s1 = fmaf(fmaf(rv, wdu, dy[e]), vv[e], s1);
-                            s3 = fmaf(vh[e], vv[e], s3);
-                            s4 = fmaf(wdu, vh[e], s4);
-                            s5 = fmaf(h[e] * kk[e], wh[e] * wh[e], s5);
-                            gwv[e] = fmaf(du[e], vh[e] * rv, gwv[e]);
-                            duA[w][e] = du[e];
-                        }
-                    }
-                }
-                sums[4 * w + 0] = s1;
-                sums[4 * w + 1] = s3;
-                sums[4 * w + 2] = s4;
-                sums[4 * w + 3] = s5;
+                rvt[w] = __ldg(p.rv + row0 + min(tc + w, t_end - 1));
+                rvc[w] = __ldg(p.rv + row0 + min(tc + w + 3, t_last - 1));
             }
+            float sums[gc::kVals];
+            out1(std::integral_constant<int, 0>(), tc, rvt, rvc, sums);
+            out1(std::integral_constant<int, 1>(), tc, rvt, rvc, sums);
+            out1(std::integral_constant<int, 2>(), tc, rvt, rvc, sums);
+            out1(std::integral_constant<int, 3>(), tc, rvt, rvc, sums);
             val = gc::warp_reduce16(sums, lane);
         }
         // ---- totals of chunk c - 1 -> coefficients of token (lane & 3)
@@ -278,7 +372,7 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
             const float S3 = __shfl_sync(kFullMask, tot, tw + 1);
             const float S4 = __shfl_sync(kFullMask, tot, tw + 2);
             const float S5 = __shfl_sync(kFullMask, tot, tw + 3);
-            const int t = min(t_out + (c - 1) * kChunk + (lane & 3), t_end - 1);
+            const int t = min(tc - kChunk + (lane & 3), t_end - 1);
             const long long r = row0 + t;
             const float rv = __ldg(p.rv + r), a = __ldg(p.alpha + r);
             const float rh = __ldg(p.rh + r), rk = __ldg(p.rk + r);
@@ -299,59 +393,31 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
         if (c < nchunks) gc::xch_send(xch, xbar, c & 1, parts, part, val, lane, C);
         // ---- 2: dv, dH, dk of chunk c - 1
         if (c >= 1) {
-#pragma unroll
-            for (int w = 0; w < kChunk; ++w) {
-                const int t = t_out + (c - 1) * kChunk + w;
-                if (t >= t_end) break;
-                const float P = __shfl_sync(kFullMask, P_l, w);
-                const float Q = __shfl_sync(kFullMask, Q_l, w);
-                const float a = __shfl_sync(kFullMask, a_l, w);
-                const float Ah = __shfl_sync(kFullMask, Ah_l, w);
-                const float Bh = __shfl_sync(kFullMask, Bh_l, w);
-                const float Bk = __shfl_sync(kFullMask, Bk_l, w);
-                if (active) {
-                    const unsigned char* b = stage_of(t);
-                    float dy[4], vh[4], h[4], kk[4], oh[4], ok[4], ov[4];
-                    unpack4(lds64(b), dy);
-                    unpack4(lds64(b + pitch), vh);
-                    unpack4(lds64(b + 3 * pitch), h);
-                    unpack4(lds64(b + 4 * pitch), kk);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float dvh = fmaf(-Q, vh[e], fmaf(P * wv[e], duB[w][e], dy[e]));
-                        ov[e] = a * dvh;
-                        const float aw = Ah * wh[e] * wh[e];
-                        oh[e] = fmaf(aw, kk[e], -Bh * h[e]);
-                        ok[e] = fmaf(aw, h[e], -Bk * kk[e]);
-                        gwh[e] = fmaf(2.0f * Ah * wh[e], h[e] * kk[e], gwh[e]);
-                    }
-                    const long long off = (row0 + t) * d + c0;
-                    stg_cs8(p.dH + off, pack4(oh));
-                    stg_cs8(p.dk + off, pack4(ok));
-                    stg_cs8(p.dv + off, pack4(ov));
-                }
-                release(t);
-            }
+            const int tp = tc - kChunk;
+            out2(std::integral_constant<int, 0>(), tp);
+            out2(std::integral_constant<int, 1>(), tp + 1);
+            out2(std::integral_constant<int, 2>(), tp + 2);
+            out2(std::integral_constant<int, 3>(), tp + 3);
+            release(tp, min(kChunk, t_end - tp));
         }
 #pragma unroll
-        for (int w = 0; w < kChunk; ++w)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) duB[w][e] = duA[w][e];
+        for (int w = 0; w < kChunk; ++w) duB[w][0] = duA[w][0], duB[w][1] = duA[w][1];
     }
 
     // per-range weight-gradient partial: [dwh | dwv | dcw0..3], each d wide
     if (active) {
         float* o = p.partial + static_cast<long long>(q) * 6 * d + c0;
-        stg_f4(o, gwh[0], gwh[1], gwh[2], gwh[3]);
-        stg_f4(o + d, gwv[0], gwv[1], gwv[2], gwv[3]);
+        stg_f4(o, gwh[0].x, gwh[0].y, gwh[1].x, gwh[1].y);
+        stg_f4(o + d, gwv[0].x, gwv[0].y, gwv[1].x, gwv[1].y);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) stg_f4(o + (2 + j) * d, gcw[j][0], gcw[j][1], gcw[j][2], gcw[j][3]);
+        for (int j = 0; j < 4; ++j)
+            stg_f4(o + (2 + j) * d, gcw[j][0].x, gcw[j][0].y, gcw[j][1].x, gcw[j][1].y);
     }
     if (failed) {
         atomicOr(p.err, kErrTimeout);
         if (tid == 0)
-            for (int j = ntok > stages ? ntok - stages : 0; j < ntok; ++j)
-                (void)mbar_wait(&full[j & kMask], static_cast<uint32_t>((j / stages) & 1));
+            for (int j = ntok > kStages ? ntok - kStages : 0; j < ntok; ++j)
+                (void)mbar_wait(&full[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
     }
     cluster_sync();
 }

@@ -19,8 +19,9 @@
 //   B  (one chunk behind) the totals give alpha and rrms_v; each thread runs
 //      the causal conv over its 4 columns with the last three u values kept
 //      in registers, and writes Y and vhat.
-// A range that does not start at t = 0 first runs the 3 tokens before it
+// A range that does not start at t = 0 first runs the 4 tokens before it
 // (the halo) through A and B without writing them, to fill the window.
+// Arithmetic on pairs of columns uses the packed fp32x2 instructions.
 #include "common.cuh"
 #include "engram_internal.h"
 #include "gateconv_xch.cuh"
@@ -56,37 +57,44 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
     const uint32_t pitch = 2u * static_cast<uint32_t>(p.ncols);
     const uint32_t stage_bytes = 3u * pitch;
     constexpr int stages = gc::kStages;
+    static_assert(stages % kChunk == 0, "a chunk must not wrap around the ring");
 
+    // ranges start at multiples of kChunk, and so does the streamed halo, so
+    // token t of the stream sits in window slot t % 4 = w for chunk position w
     const int m = q / p.ranges_per_row;
     const int t_out = (q - m * p.ranges_per_row) * p.range_len;
     const int t_end = min(p.T, t_out + p.range_len);
-    const int t_first = t_out - min(3, t_out);
+    const int t_first = t_out >= kChunk ? t_out - kChunk : 0;
     const int ntok = t_end - t_first;
     const int nchunks = (ntok + kChunk - 1) / kChunk;
     const long long row0 = static_cast<long long>(m) * p.T;
     const uint32_t xbytes = static_cast<uint32_t>(parts) * gc::kVals * 4u;
 
-    float wh2[4], wv[4], cw[4][4];
+    float2 wh2[2], wv[2], cw[4][2];
     if (active) {
         const float4 a = __ldg(reinterpret_cast<const float4*>(p.wh + c0));
         const float4 b = __ldg(reinterpret_cast<const float4*>(p.wv + c0));
-        wh2[0] = a.x * a.x; wh2[1] = a.y * a.y; wh2[2] = a.z * a.z; wh2[3] = a.w * a.w;
-        wv[0] = b.x; wv[1] = b.y; wv[2] = b.z; wv[3] = b.w;
+        wh2[0] = make_float2(a.x * a.x, a.y * a.y);
+        wh2[1] = make_float2(a.z * a.z, a.w * a.w);
+        wv[0] = make_float2(b.x, b.y);
+        wv[1] = make_float2(b.z, b.w);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float4 c = __ldg(reinterpret_cast<const float4*>(p.cw + static_cast<long long>(j) * d + c0));
-            cw[j][0] = c.x; cw[j][1] = c.y; cw[j][2] = c.z; cw[j][3] = c.w;
+            cw[j][0] = make_float2(c.x, c.y);
+            cw[j][1] = make_float2(c.z, c.w);
         }
     } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            wh2[e] = wv[e] = 0.f;
+        for (int i = 0; i < 2; ++i) {
+            wh2[i] = wv[i] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) cw[j][e] = 0.f;
+            for (int j = 0; j < 4; ++j) cw[j][i] = make_float2(0.f, 0.f);
         }
     }
 
-    auto issue = [&](int j, int st) {
+    auto issue = [&](int j) {
+        const int st = j % stages;
         const long long off = (row0 + t_first + j) * d + col0;
         unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
         mbar_arrive_expect_tx(&full[st], 3u * row_bytes);
@@ -107,54 +115,46 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
         mbar_arrive_expect_tx(&xbar[0], xbytes);
         if (nchunks > 1) mbar_arrive_expect_tx(&xbar[1], xbytes);
         const int pro = ntok < stages ? ntok : stages;
-        for (int j = 0; j < pro; ++j) issue(j, j);
+        for (int j = 0; j < pro; ++j) issue(j);
     }
     // every CTA's barriers exist before any peer stores into its slots
     cluster_sync();
 
-    float u1[4], u2[4], u3[4];  // u at t-1, t-2, t-3 (zero before the row start)
+    float2 U[kChunk][2];  // u of the last four tokens, slot t % 4 (zero before the row start)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) u1[e] = u2[e] = u3[e] = 0.f;
+    for (int w = 0; w < kChunk; ++w) U[w][0] = U[w][1] = make_float2(0.f, 0.f);
 
     const float inv_d = 1.0f / static_cast<float>(d);
     bool failed = false;
-    int stA = 0, stB = 0;
-    uint32_t phA = 0;
     float alpha_l = 0.f, rv_l = 0.f;  // scalars of token (lane & 3) of chunk c - 1
 
     for (int c = 0; c <= nchunks; ++c) {
-        // ---- A: partial sums of chunk c over this warp's columns
+        // ---- A: partial sums of chunk c over this warp's columns (all waits
+        // first, then branch-free arithmetic so the four tokens interleave)
         float val = 0.f;
         if (c < nchunks) {
             float sums[gc::kVals];
+            const int j0 = c * kChunk;
+            const unsigned char* b0 = ring + static_cast<size_t>(j0 % stages) * stage_bytes + 8 * tid;
+            const uint32_t par = static_cast<uint32_t>((j0 / stages) & 1);
+#pragma unroll
+            for (int w = 0; w < kChunk; ++w)
+                if (j0 + w < ntok && !failed && !mbar_wait(&full[j0 % stages + w], par)) failed = true;
 #pragma unroll
             for (int w = 0; w < kChunk; ++w) {
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-                if (c * kChunk + w < ntok) {
-                    if (!failed && !mbar_wait(&full[stA], phA)) failed = true;
-                    if (active) {
-                        const unsigned char* b = ring + static_cast<size_t>(stA) * stage_bytes + 8 * tid;
-                        float h[4], kk[4], vv[4];
-                        unpack4(lds64(b), h);
-                        unpack4(lds64(b + pitch), kk);
-                        unpack4(lds64(b + 2 * pitch), vv);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            s0 = fmaf(h[e], h[e], s0);
-                            s1 = fmaf(kk[e], kk[e], s1);
-                            s2 = fmaf(h[e] * kk[e], wh2[e], s2);
-                            s3 = fmaf(vv[e], vv[e], s3);
-                        }
-                    }
-                    if (++stA == stages) {
-                        stA = 0;
-                        phA ^= 1u;
-                    }
-                }
-                sums[4 * w + 0] = s0;
-                sums[4 * w + 1] = s1;
-                sums[4 * w + 2] = s2;
-                sums[4 * w + 3] = s3;
+                const unsigned char* b = b0 + static_cast<size_t>(w) * stage_bytes;
+                const uint2 hq = lds64(b), kq = lds64(b + pitch), vq = lds64(b + 2 * pitch);
+                const float2 h0 = bf2(hq.x), h1 = bf2(hq.y), k0 = bf2(kq.x), k1 = bf2(kq.y);
+                const float2 v0 = bf2(vq.x), v1 = bf2(vq.y);
+                const float2 hh = fma2(h1, h1, mul2(h0, h0));
+                const float2 kk = fma2(k1, k1, mul2(k0, k0));
+                const float2 hk = fma2(mul2(h1, k1), wh2[1], mul2(mul2(h0, k0), wh2[0]));
+                const float2 vv = fma2(v1, v1, mul2(v0, v0));
+                const bool ok = active && j0 + w < ntok;
+                sums[4 * w + 0] = ok ? hh.x + hh.y : 0.f;
+                sums[4 * w + 1] = ok ? kk.x + kk.y : 0.f;
+                sums[4 * w + 2] = ok ? hk.x + hk.y : 0.f;
+                sums[4 * w + 3] = ok ? vv.x + vv.y : 0.f;
             }
             val = gc::warp_reduce16(sums, lane);
         }
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
             const float rh = rsqrtf(fmaf(sh, inv_d, p.eps));
             const float rk = rsqrtf(fmaf(sk, inv_d, p.eps));
             const float z = rh * rk * shk * p.inv_sqrt_d;
-            alpha_l = 1.0f / (1.0f + __expf(-z));
+            alpha_l = __fdividef(1.0f, 1.0f + __expf(-z));
             rv_l = rsqrtf(fmaf(alpha_l * alpha_l * sv, inv_d, p.eps));
             const int j = (c - 1) * kChunk + lane;
             if (rank == 0 && warp == 0 && lane < kChunk && j < ntok && t_first + j >= t_out) {
@@ -186,49 +186,48 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
         }
         // ---- send chunk c (after this warp has read chunk c - 1)
         if (c < nchunks) gc::xch_send(xch, xbar, c & 1, parts, part, val, lane, C);
-        // ---- B: conv, SiLU and outputs of chunk c - 1
+        // ---- B: conv, SiLU and outputs of chunk c - 1 (branch-free; stores
+        // predicated)
         if (c >= 1) {
+            const int j0 = (c - 1) * kChunk;
+            const unsigned char* b0 =
+                ring + static_cast<size_t>(j0 % stages) * stage_bytes + 2 * pitch + 8 * tid;
+            const long long off0 = (row0 + t_first + j0) * d + c0;
 #pragma unroll
             for (int w = 0; w < kChunk; ++w) {
-                const int j = (c - 1) * kChunk + w;
-                if (j >= ntok) break;
                 const float alpha = __shfl_sync(kFullMask, alpha_l, w);
                 const float rv = __shfl_sync(kFullMask, rv_l, w);
-                const int t = t_first + j;
-                if (active) {
-                    const unsigned char* b = ring + static_cast<size_t>(stB) * stage_bytes + 2 * pitch + 8 * tid;
-                    float vv[4], y[4], vh[4];
-                    unpack4(lds64(b), vv);
+                const uint2 vq = lds64(b0 + static_cast<size_t>(w) * stage_bytes);
+                const float2 a2 = splat2(alpha), ar2 = splat2(alpha * rv);
+                float2 vh[2], y[2];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        vh[e] = alpha * vv[e];
-                        const float u = vh[e] * rv * wv[e];
-                        const float cc =
-                            fmaf(cw[0][e], u3[e], fmaf(cw[1][e], u2[e], fmaf(cw[2][e], u1[e], cw[3][e] * u)));
-                        y[e] = cc / (1.0f + __expf(-cc)) + vh[e];
-                        u3[e] = u2[e];
-                        u2[e] = u1[e];
-                        u1[e] = u;
-                    }
-                    if (t >= t_out) {
-                        const long long off = (row0 + t) * d + c0;
-                        stg_cs8(p.Y + off, pack4(y));
-                        stg_cs8(p.vhat + off, pack4(vh));
-                    }
+                for (int i = 0; i < 2; ++i) {
+                    const float2 v2 = bf2(i == 0 ? vq.x : vq.y);
+                    vh[i] = mul2(a2, v2);
+                    const float2 u = mul2(mul2(ar2, v2), wv[i]);
+                    const float2 cc =
+                        fma2(cw[0][i], U[(w + 1) & 3][i],
+                             fma2(cw[1][i], U[(w + 2) & 3][i], fma2(cw[2][i], U[(w + 3) & 3][i], mul2(cw[3][i], u))));
+                    const float2 den = make_float2(1.0f + __expf(-cc.x), 1.0f + __expf(-cc.y));
+                    y[i] = add2(make_float2(__fdividef(cc.x, den.x), __fdividef(cc.y, den.y)), vh[i]);
+                    U[w][i] = u;
                 }
-                // this warp is done with the stage; the last warp refills it
-                __syncwarp();
-                if (lane == 0) {
-                    __threadfence_block();
-                    if (atomicAdd(&released[stB], 1u) == static_cast<unsigned int>(nw - 1)) {
-                        released[stB] = 0u;
-                        if (j + stages < ntok) {
-                            fence_proxy_async();
-                            issue(j + stages, stB);
-                        }
-                    }
+                if (active && j0 + w < ntok && t_first + j0 + w >= t_out) {
+                    const long long off = off0 + static_cast<long long>(w) * d;
+                    stg_cs8(p.Y + off, make_uint2(pack2(y[0]), pack2(y[1])));
+                    stg_cs8(p.vhat + off, make_uint2(pack2(vh[0]), pack2(vh[1])));
                 }
-                if (++stB == stages) stB = 0;
+            }
+            // this warp is done with the chunk's stages; the last warp refills them
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                const int st0 = j0 % stages;
+                if (atomicAdd(&released[st0], 1u) == static_cast<unsigned int>(nw - 1)) {
+                    released[st0] = 0u;
+                    fence_proxy_async();
+                    for (int w = 0; w < kChunk && j0 + stages + w < ntok; ++w) issue(j0 + stages + w);
+                }
             }
         }
     }

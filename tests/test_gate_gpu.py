@@ -253,6 +253,11 @@ def test_launch_geometry():
     fwd = eg.engram_launch_info(0, 65536)
     assert fwd["cluster"] == 1 and fwd["threads"] % 32 == 0 and fwd["clusters"] >= 1
     assert eg.engram_launch_info(0, 1)["clusters"] == 1
+    # the grid is sized so that the last round of rows leaves under one CTA idle
+    f8 = eg.engram_launch_info(0, 8192)
+    warps, rows = 8 * f8["clusters"], 4 * 8192
+    rpw = -(-rows // warps)
+    assert warps * rpw - rows < 8 * rpw
     # backward: token rows split across a cluster; at most one cluster per two
     # 64-token blocks, so each cluster's (hi, lo) grad_weight pair fits
     bwd = eg.engram_launch_info(1, 8192)

@@ -172,3 +172,17 @@ def test_full_config_m8_t8192_d7168_windows():
                                  *(f64(sl(t)) for t in res[1:]))
         for name, got, e in (("dH", g[0], eb[0]), ("dk", g[1], eb[1]), ("dv", g[2], eb[2])):
             check_bf16(name, bf16_bits(got[m:m + 1, a:b]), e[:, o0:o1])
+
+
+def test_launch_geometry():
+    """C = ceil(d / 1024) CTAs of at most 256 threads (4 columns each) per row."""
+    for (M, T, d, C) in ((4, 4096, 4096, 4), (8, 8192, 7168, 7), (2, 45, 1032, 2), (1, 40, 8192, 8),
+                         (1, 5, 64, 1)):
+        for op in (2, 3):
+            info = eg.engram_launch_info(op, M, T, d)
+            assert info["cluster"] == C
+            assert info["threads"] % 32 == 0 and info["threads"] <= 256
+            assert 4 * info["threads"] * C >= d > 4 * info["threads"] * (C - 1)
+            assert info["clusters"] >= M
+    with pytest.raises(eg.EngramError):
+        eg.engram_launch_info(2, 1, 4, 8200)
