@@ -121,6 +121,21 @@ class Clocks:
                 "samples": len(rows)}
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 def time_region(torch, fn, reps, stream):
     """Mean ms of fn() over reps, CUDA events on `stream`; fn's work (graph
     replays included) is issued on that same stream."""
@@ -335,11 +350,8 @@ def main():
     ms = t_start.elapsed_time(t_end) / K
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * N_TOK / (ms * 1e-3)
+    ms = max_over_ranks(ms, dist, "cuda")
+    value = job_throughput(N_TOK, world, ms)
     step_bytes = N_TOK * (FWD_BYTES_PER_TOKEN + BWD_BYTES_PER_TOKEN) + FWD_FIXED + BWD_FIXED
     fwd_bytes = N_TOK * FWD_BYTES_PER_TOKEN + FWD_FIXED
     bwd_bytes = N_TOK * BWD_BYTES_PER_TOKEN + BWD_FIXED
@@ -376,11 +388,7 @@ def main():
     for _ in range(3):
         e2e_step()
     Ke = max(5, min(50, K // 20))
-    e2e_ms = time_region(torch, e2e_step, Ke, stream)
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(time_region(torch, e2e_step, Ke, stream), dist, "cuda")
 
     launch = {"fwd": eg.engram_launch_info(0, N_TOK), "bwd": eg.engram_launch_info(1, N_TOK)}
     ops = None
@@ -412,10 +420,10 @@ def main():
                          "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(fwd_gbs / peak, 4), "traffic": traffic_fwd},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * N_TOK / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(N_TOK, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 4 * K,  # forward + backward coefficients, elementwise, grad_weight merge
         "clocks": clk.summary(),
         "device_error_flags": err,
     }

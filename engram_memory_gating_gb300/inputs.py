@@ -96,3 +96,38 @@ def gateconv_inputs(M: int, T: int, d: int, seed: int = 0, *, device="cpu",
 def bf16_bits(t: torch.Tensor):
     """bf16 tensor -> numpy uint16 bit patterns (host copy)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
+
+
+def _formula(shape, a: float, b: float, c: float, scale: float = 1.0) -> torch.Tensor:
+    """Deterministic, generator-free values scale * sin(a*i + b*j + c) over the
+    flattened index i and the leading index j: the same on every machine."""
+    n = 1
+    for s in shape:
+        n *= s
+    i = torch.arange(n, dtype=torch.float64)
+    j = torch.div(i, n // shape[0], rounding_mode="floor")
+    return (scale * torch.sin(a * i + b * j + c)).reshape(shape)
+
+
+def gate_inputs_formula(N: int = 3) -> dict:
+    """Small gate inputs defined by formulas (no random generator), for the
+    stored fixtures: x, kv, grad_out bf16, weight fp32, mask [1, 0, 1, ...]."""
+    x = _formula((N, S_STREAMS, D_GATE), 0.37, 1.3, 0.1, 2.0).to(torch.bfloat16)
+    kv = _formula((N, (S_STREAMS + 1) * D_GATE), 0.23, 0.7, 0.5, 1.5).to(torch.bfloat16)
+    w = (1.0 + 0.1 * _formula((S_STREAMS, D_GATE), 0.11, 0.9, 0.3)).to(torch.float32)
+    mask = torch.tensor([n % 2 == 0 or n % 3 == 2 for n in range(N)], dtype=torch.bool)
+    g = _formula((N, S_STREAMS, D_GATE), 0.53, 0.4, 0.2).to(torch.bfloat16)
+    return {"x": x, "kv": kv, "weight": w.contiguous(), "mask": mask, "grad_out": g}
+
+
+def gateconv_inputs_formula(M: int = 2, T: int = 7, d: int = 16) -> dict:
+    """Small GateConv inputs defined by formulas (no random generator)."""
+    H = _formula((M, T, d), 0.31, 0.8, 0.2, 1.5).to(torch.bfloat16)
+    k = _formula((M, T, d), 0.17, 0.6, 0.9).to(torch.bfloat16)
+    v = _formula((M, T, d), 0.29, 1.1, 0.4).to(torch.bfloat16)
+    wh = (1.0 + 0.1 * _formula((d,), 0.7, 0.0, 0.1)).to(torch.float32)
+    wv = (1.0 + 0.1 * _formula((d,), 0.45, 0.0, 0.6)).to(torch.float32)
+    cw = (0.5 * _formula((4, d), 0.13, 1.7, 0.3)).to(torch.float32)
+    dY = _formula((M, T, d), 0.41, 0.5, 0.7).to(torch.bfloat16)
+    return {"H": H, "k": k, "v": v, "rms_w_h": wh.contiguous(), "rms_w_v": wv.contiguous(),
+            "conv_w": cw.contiguous(), "dY": dY}
