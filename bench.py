@@ -281,6 +281,53 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+GC_WORKLOADS = {"m4": (4, 4096, 4096, 1.0, 1.0), "m8": (8, 8192, 7168, 10.0, 0.1 ** 0.5)}
+
+
+def run_single_op(args):
+    """One entry point alone, `warmup` + `steps` plain calls on one stream, for
+    profiler captures: the gate at the step's N = 8192 inputs, GateConv at
+    --gc-workload (m4: M=4, T=4096, d=4096; m8: M=8, T=8192, d=7168).  Prints
+    the mean event-timed call.  Launches per call: gate_fwd 1, gate_bwd 3,
+    gateconv_fwd 1, gateconv_bwd 4."""
+    import torch
+    import engram_memory_gating_gb300 as eg
+    from engram_memory_gating_gb300 import inputs as inputs_mod
+    s = torch.cuda.Stream()
+    if args.op.startswith("gate_"):
+        inp = inputs_mod.gate_inputs(N_TOK, 1, device="cuda", mask="bern0.9")
+        out, saved = eg.gate_forward(inp["x"], inp["kv"], inp["weight"], inp["mask"])
+        gx, gkv, gw = (torch.empty_like(inp["x"]), torch.empty_like(inp["kv"]),
+                       torch.empty_like(inp["weight"]))
+        ws = torch.empty(eg.engram_gate_bwd_workspace_size(N_TOK), device="cuda", dtype=torch.uint8)
+        if args.op == "gate_fwd":
+            fn = lambda: eg.engram_gate_fwd(inp["x"], inp["kv"], inp["weight"], inp["mask"], out,
+                                            saved, stream=s)
+        else:
+            fn = lambda: eg.engram_gate_bwd(inp["x"], inp["kv"], inp["weight"], saved,
+                                            inp["grad_out"], gx, gkv, gw, ws, stream=s)
+    else:
+        M, T, d, hs, vs = GC_WORKLOADS[args.gc_workload]
+        ci = inputs_mod.gateconv_inputs(M, T, d, 31, device="cuda", h_scale=hs, v_std=vs)
+        res = eg.gateconv_forward(ci["H"], ci["k"], ci["v"], ci["rms_w_h"], ci["rms_w_v"], ci["conv_w"])
+        grads = [torch.empty_like(ci["H"]) for _ in range(3)] + \
+            [torch.empty(d, device="cuda"), torch.empty(d, device="cuda"), torch.empty((4, d), device="cuda")]
+        ws = torch.empty(eg.engram_gateconv_bwd_workspace_size(M, T, d), device="cuda", dtype=torch.uint8)
+        if args.op == "gateconv_fwd":
+            fn = lambda: eg.engram_gateconv_fwd(ci["H"], ci["k"], ci["v"], ci["rms_w_h"], ci["rms_w_v"],
+                                                ci["conv_w"], *res, stream=s)
+        else:
+            fn = lambda: eg.engram_gateconv_bwd(ci["dY"], ci["H"], ci["k"], ci["v"], ci["rms_w_h"],
+                                                ci["rms_w_v"], ci["conv_w"], *res[1:], *grads, ws, stream=s)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            fn()
+        ms = time_region(torch, fn, max(1, args.steps), s)
+    assert eg.engram_device_error() == 0
+    print(json.dumps({"op": args.op, "ms": round(ms, 5)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -289,12 +336,18 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-op sweep")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--op", choices=["step", "gate_fwd", "gate_bwd", "gateconv_fwd", "gateconv_bwd"],
+                    default="step", help="time one entry point alone (profiler captures)")
+    ap.add_argument("--gc-workload", choices=sorted(GC_WORKLOADS), default="m4")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.op != "step":
+        run_single_op(args)
         return
     args.warmup = max(args.warmup, 3)
 

@@ -27,6 +27,7 @@ constexpr int kGcStages = 16;
 constexpr int kGcMinRange = 16;    // tokens; bounds the 3-token halo overhead
 constexpr int kGcRangeCost = 8;    // per-range set-up, in token-steps, for the range split
 constexpr int64_t kGcBwdSlots = 256;  // backward weight-gradient slots (one per range)
+constexpr int kGcBwdMaxRange = 1024;  // backward range cap (its saved scalars sit in shared memory)
 
 struct OccKey {
     int op, cluster, threads, smem;
@@ -37,6 +38,7 @@ struct GcGeom {
     LaunchCfg c;
     int ncols;
     int ring_off;
+    int sc_off;  // backward: byte offset of the staged per-token scalars
     int range_len;
     int rpr;  // ranges per batch row
 };
@@ -228,7 +230,8 @@ int64_t gc_bwd_slots(int64_t M, int64_t T) {
     const int64_t per_row = (T + kGcMinRange - 1) / kGcMinRange;
     int64_t s = M * per_row;
     if (s > kGcBwdSlots) s = kGcBwdSlots;
-    return s > M ? s : M;
+    const int64_t least = M * ((T + kGcBwdMaxRange - 1) / kGcBwdMaxRange);
+    return s > least ? s : least;
 }
 
 // Column split: C = ceil(d / 1024) CTAs per row, each of `threads` (a multiple
@@ -249,13 +252,14 @@ void gc_split(int64_t d, int rows, GcGeom& g) {
 // Token ranges: ranges_per_row r minimising (waves of clusters) x (tokens of
 // the longest range + halo + set-up), with at most max_ranges ranges.  Range
 // lengths are multiples of 4 tokens (the kernels' window slots rely on it).
-void gc_ranges(int64_t M, int64_t T, int K, int64_t max_ranges, GcGeom& g) {
+void gc_ranges(int64_t M, int64_t T, int K, int64_t max_ranges, int64_t max_len, GcGeom& g) {
+    const int64_t lo = (T + max_len - 1) / max_len;
     int64_t hi = (T + kGcMinRange - 1) / kGcMinRange;
     if (hi > max_ranges / M) hi = max_ranges / M;
-    if (hi > 4096) hi = 4096;
-    if (hi < 1) hi = 1;
-    int64_t best_len = (T + 3) / 4 * 4, best_cost = -1;
-    for (int64_t r = 1; r <= hi; ++r) {
+    if (hi > lo + 4096) hi = lo + 4096;
+    if (hi < lo) hi = lo;
+    int64_t best_len = ((T + lo - 1) / lo + 3) / 4 * 4, best_cost = -1;
+    for (int64_t r = lo; r <= hi; ++r) {
         const int64_t len = ((T + r - 1) / r + 3) / 4 * 4;
         const int64_t rr = (T + len - 1) / len;
         const int64_t waves = (M * rr + K - 1) / K;
@@ -276,9 +280,16 @@ const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
     if (e.M == M && e.T == T && e.d == d) return &e.g;
     GcGeom g = {};
     gc_split(d, op == 0 ? 3 : 5, g);
+    if (op == 1) {
+        g.sc_off = g.c.smem;  // saved scalars of up to kGcBwdMaxRange + 7 streamed tokens
+        g.c.smem += 16 * (kGcBwdMaxRange + 8);
+    }
     const int K = max_clusters(st, op == 0 ? 2 : 3, g.c.cluster, g.c.threads, g.c.smem);
     if (K <= 0) return nullptr;
-    gc_ranges(M, T, K, op == 0 ? (int64_t(1) << 31) : gc_bwd_slots(M, T), g);
+    if (op == 0)
+        gc_ranges(M, T, K, int64_t(1) << 31, int64_t(1) << 31, g);
+    else
+        gc_ranges(M, T, K, gc_bwd_slots(M, T), kGcBwdMaxRange, g);
     e.M = M;
     e.T = T;
     e.d = d;
@@ -520,6 +531,7 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
     p.d = static_cast<int>(d);
     p.ncols = g->ncols;
     p.ring_off = g->ring_off;
+    p.sc_off = g->sc_off;
     p.range_len = g->range_len;
     p.ranges_per_row = g->rpr;
     p.eps = eps;

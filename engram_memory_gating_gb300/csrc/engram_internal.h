@@ -97,7 +97,7 @@ struct GateConvBwdParams {
     int M, T, d;
     int ncols;
     int ring_off;
-    int du_off;      // byte offset of the du buffers in shared memory
+    int sc_off;      // byte offset of the per-token saved scalars in shared memory
     int range_len;
     int ranges_per_row;
     float eps;

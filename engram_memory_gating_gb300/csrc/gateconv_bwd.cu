@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
     unsigned int* released = reinterpret_cast<unsigned int*>(smem + gc::kOffRel);
     float* xch = reinterpret_cast<float*>(smem + gc::kOffXch);
     unsigned char* ring = smem + p.ring_off;
+    float4* sc = reinterpret_cast<float4*>(smem + p.sc_off);  // (rrms_v, alpha, rrms_h, rrms_k)
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -222,6 +223,11 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
         const int pro = ntok < kStages ? ntok : kStages;
         for (int j = 0; j < pro; ++j) issue(j);
     }
+    // the saved per-token scalars of the streamed tokens, staged once
+    for (int i = tid; i < ntok; i += blockDim.x) {
+        const long long r = row0 + t_first + i;
+        sc[i] = make_float4(__ldg(p.rv + r), __ldg(p.alpha + r), __ldg(p.rh + r), __ldg(p.rk + r));
+    }
     cluster_sync();
 
     Windows W;
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
             return;
         }
         wait_tok(tau);
-        const float rv = __ldg(p.rv + row0 + tau);
+        const float rv = sc[tau - t_first].x;
         consume<S>(W, gcw, P, row_of(tau), pitch, rv, true, tau >= t_out, active && tau >= t_out && tau < t_end);
         // the halo before the range is not needed again (the halo after it
         // sits at the end of the stream, its stages are never refilled)
@@ -350,8 +356,8 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
             float rvt[kChunk], rvc[kChunk];
 #pragma unroll
             for (int w = 0; w < kChunk; ++w) {
-                rvt[w] = __ldg(p.rv + row0 + min(tc + w, t_end - 1));
-                rvc[w] = __ldg(p.rv + row0 + min(tc + w + 3, t_last - 1));
+                rvt[w] = sc[min(tc + w, t_end - 1) - t_first].x;
+                rvc[w] = sc[min(tc + w + 3, t_last - 1) - t_first].x;
             }
             float sums[gc::kVals];
             out1(std::integral_constant<int, 0>(), tc, rvt, rvc, sums);
@@ -373,9 +379,8 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
             const float S4 = __shfl_sync(kFullMask, tot, tw + 2);
             const float S5 = __shfl_sync(kFullMask, tot, tw + 3);
             const int t = min(tc - kChunk + (lane & 3), t_end - 1);
-            const long long r = row0 + t;
-            const float rv = __ldg(p.rv + r), a = __ldg(p.alpha + r);
-            const float rh = __ldg(p.rh + r), rk = __ldg(p.rk + r);
+            const float4 s4 = sc[t - t_first];
+            const float rv = s4.x, a = s4.y, rh = s4.z, rk = s4.w;
             const float mu = rv * S4 * inv_d;
             const float q2 = rv * rv * mu;
             const float dalpha = fmaf(-q2, S3, S1);

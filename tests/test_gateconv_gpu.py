@@ -62,7 +62,8 @@ def check_bwd(res, exact, sums=True):
 # 640 + 392 columns), the largest d (8 CTAs of 1024 columns), rows shorter
 # than the conv (T = 1, 2) and rows cut into several token ranges with halos
 SMALL = [(1, 1, 8, 0), (2, 37, 64, 1), (3, 129, 512, 2), (1, 1000, 64, 3), (2, 300, 4096, 4),
-         (1, 70, 7168, 5), (1, 5, 5120, 6), (2, 45, 1032, 7), (1, 40, 8192, 8), (3, 2, 264, 9)]
+         (1, 70, 7168, 5), (1, 5, 5120, 6), (2, 45, 1032, 7), (1, 40, 8192, 8), (3, 2, 264, 9),
+         (1, 2500, 64, 10)]
 
 
 @pytest.mark.parametrize("M,T,d,seed", SMALL)
