@@ -234,11 +234,11 @@ int64_t gc_bwd_slots(int64_t M, int64_t T) {
     return s > least ? s : least;
 }
 
-// Column split: C = ceil(d / 1024) CTAs per row, each of `threads` (a multiple
-// of 32) threads owning 4 columns; every slice is a whole number of 8-column
-// groups, so every row slice is a multiple of 16 bytes (bulk-copy rule).
-void gc_split(int64_t d, int rows, GcGeom& g) {
-    const int C = static_cast<int>((d + 4 * kGcThreads - 1) / (4 * kGcThreads));
+// Column split over C CTAs per row, each of `threads` (a multiple of 32,
+// at most 256) threads owning 4 columns; every slice is a whole number of
+// 8-column groups, so every row slice is a multiple of 16 bytes (bulk-copy
+// rule).
+void gc_split(int64_t d, int rows, int C, GcGeom& g) {
     const int quads = static_cast<int>(d / 4);
     g.c.cluster = C;
     g.c.threads = round_up((quads + C - 1) / C, 32);
@@ -278,8 +278,10 @@ void gc_ranges(int64_t M, int64_t T, int K, int64_t max_ranges, int64_t max_len,
 const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
     GcCacheEntry& e = st.gc_last[op];
     if (e.M == M && e.T == T && e.d == d) return &e.g;
+    // C = ceil(d / 1024): measured on GB300, larger clusters (more, smaller
+    // CTAs) did not run faster even where they packed onto more SMs.
     GcGeom g = {};
-    gc_split(d, op == 0 ? 3 : 5, g);
+    gc_split(d, op == 0 ? 3 : 5, static_cast<int>((d + 1023) / 1024), g);
     if (op == 1) {
         g.sc_off = g.c.smem;  // saved scalars of up to kGcBwdMaxRange + 7 streamed tokens
         g.c.smem += 16 * (kGcBwdMaxRange + 8);
@@ -652,6 +654,9 @@ engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
     info->clusters = c.clusters;
     info->stages = c.stages;
     info->smem_bytes = c.smem;
+    // co-resident CTA groups: CTAs for the gate kernels, clusters for GateConv
+    info->resident = op == 1 ? max_clusters(*st, op, 1, c.threads, c.smem) / c.cluster
+                             : max_clusters(*st, op, op >= 2 ? c.cluster : 1, c.threads, c.smem);
     return ENGRAM_OK;
 }
 
