@@ -210,6 +210,13 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
                                       tok * (10 * d + 16) + 24 * d, peak)
         ops[name + "_bwd"] = op_entry(time_region(torch, gb.replay, 10, s),
                                       tok * (16 * d + 16) + 48 * d, peak)
+        if M == 4:  # DRAM bytes per launch from the committed ncu summaries
+            csrc = "engram_memory_gating_gb300/csrc/"
+            common = [csrc + "gateconv_xch.cuh", csrc + "common.cuh", csrc + "engram_abi.cu"]
+            ops[name + "_fwd"]["traffic"] = profile_traffic(
+                "gateconv_fwd_m4_t4096_d4096.md", [csrc + "gateconv_fwd.cu"] + common)
+            ops[name + "_bwd"]["traffic"] = profile_traffic(
+                "gateconv_bwd_m4_t4096_d4096.md", [csrc + "gateconv_bwd.cu"] + common)
         del ci, res, grads, ws, gf, gb
         torch.cuda.empty_cache()
     return ops
