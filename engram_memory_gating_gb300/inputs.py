@@ -109,7 +109,7 @@ def _formula(shape, a: float, b: float, c: float, scale: float = 1.0) -> torch.T
     return (scale * torch.sin(a * i + b * j + c)).reshape(shape)
 
 
-def gate_inputs_formula(N: int = 3) -> dict:
+def gate_inputs_formula(N: int = 64) -> dict:
     """Small gate inputs defined by formulas (no random generator), for the
     stored fixtures: x, kv, grad_out bf16, weight fp32, mask [1, 0, 1, ...]."""
     x = _formula((N, S_STREAMS, D_GATE), 0.37, 1.3, 0.1, 2.0).to(torch.bfloat16)

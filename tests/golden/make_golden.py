@@ -55,12 +55,12 @@ def bits(a) -> list[int]:
 
 
 def gate_fixture() -> dict:
-    inp = gate_inputs_formula(3)
+    inp = gate_inputs_formula(64)
     x, kv, w, g = (f64(inp[k]) for k in ("x", "kv", "weight", "grad_out"))
     m = inp["mask"].numpy().astype(np.uint8)
     out, saved = oracle.gate_fwd(x, kv, w, m)
     gx, gkv, gw = oracle.gate_bwd(x, kv, w, saved, g)
-    fx = {"inputs": "gate_inputs_formula(3)",
+    fx = {"inputs": "gate_inputs_formula(64)",
           "inputs_sha256": digest([inp[k] for k in ("x", "kv", "weight", "mask", "grad_out")]),
           "saved": floats(saved)}
     for name, arr, kind in (("out", out, "bf16"), ("grad_x", gx, "bf16"), ("grad_kv", gkv, "bf16"),
@@ -95,7 +95,7 @@ def gateconv_fixture() -> dict:
 
 def main():
     oracle.build()
-    for name, fx in (("oracle_gate_n3.json", gate_fixture()), ("oracle_gateconv_m2_t7_d16.json", gateconv_fixture())):
+    for name, fx in (("oracle_gate_n64.json", gate_fixture()), ("oracle_gateconv_m2_t7_d16.json", gateconv_fixture())):
         fx["written_by"] = "tests/golden/make_golden.py (oracle only)"
         with open(os.path.join(HERE, name), "w") as f:
             # one key per line, each value compact

@@ -82,16 +82,16 @@ def test_gateconv_closed_forms():
 
 def test_formula_inputs_are_stable():
     gm = _gm()
-    g = gate_inputs_formula(3)
+    g = gate_inputs_formula(64)
     c = gateconv_inputs_formula(2, 7, 16)
     assert gm.digest([g[k] for k in ("x", "kv", "weight", "mask", "grad_out")]) == \
-        load("oracle_gate_n3.json")["inputs_sha256"]
+        load("oracle_gate_n64.json")["inputs_sha256"]
     assert gm.digest([c[k] for k in ("H", "k", "v", "rms_w_h", "rms_w_v", "conv_w", "dY")]) == \
         load("oracle_gateconv_m2_t7_d16.json")["inputs_sha256"]
 
 
 def test_oracle_reproduces_stored_gate_fixture():
-    fx = load("oracle_gate_n3.json")
+    fx = load("oracle_gate_n64.json")
     now = _gm().gate_fixture()
     assert np.allclose(now["saved"], fx["saved"], rtol=1e-13, atol=0)
     for name in ("out", "grad_x", "grad_kv"):
@@ -121,8 +121,8 @@ def _near(got, exact, floor):
 @pytest.mark.gpu
 def test_cuda_gate_matches_stored_fixture():
     import engram_memory_gating_gb300 as eg
-    fx = load("oracle_gate_n3.json")
-    inp = {k: v.cuda() for k, v in gate_inputs_formula(3).items()}
+    fx = load("oracle_gate_n64.json")
+    inp = {k: v.cuda() for k, v in gate_inputs_formula(64).items()}
     out, saved = eg.gate_forward(inp["x"], inp["kv"], inp["weight"], inp["mask"])
     gx, gkv, gw = eg.gate_backward(inp["x"], inp["kv"], inp["weight"], saved, inp["grad_out"])
     torch.cuda.synchronize()
