@@ -187,6 +187,28 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
     ops["gate_fwd_N262144"] = op_entry(ms, N * FWD_BYTES_PER_TOKEN + FWD_FIXED, peak)
     del inp, out, saved, g
     torch.cuda.empty_cache()
+    # separate-tensor gate (tile-kernels layout), N = 8192, H = 4096
+    N, H = 8192, 4096
+    inp = inputs_mod.gate_inputs(N, 105, device="cuda", d=H)
+    k = inp["kv"][:, :4 * H].reshape(N, 4, H).contiguous()
+    v = inp["kv"][:, 4 * H:].contiguous()
+    del inp["kv"]
+    out = torch.empty_like(inp["x"])
+    sv = [torch.empty((N, 4), device="cuda") for _ in range(4)]
+    gx, gk, gv = torch.empty_like(inp["x"]), torch.empty_like(k), torch.empty_like(v)
+    gwp = torch.empty(((N + 63) // 64, 4, H), device="cuda")
+    ws = torch.empty(eg.engram_gate_sep_bwd_workspace_size(N), device="cuda", dtype=torch.uint8)
+    f = lambda: eg.engram_gate_sep_fwd(inp["x"], k, v, inp["weight"], out, *sv, stream=s)
+    b = lambda: eg.engram_gate_sep_bwd(inp["grad_out"], inp["x"], k, v, inp["weight"], *sv, gx, gk, gv,
+                                       gwp, ws, stream=s)
+    gf, gb = graph_of(torch, f, s), graph_of(torch, b, s)
+    time_region(torch, lambda: (gf.replay(), gb.replay()), 3, s)
+    ops["gate_sep_fwd_N8192_H4096"] = op_entry(time_region(torch, gf.replay, 10, s),
+                                               N * (26 * H + 64) + 16 * H, peak)
+    ops["gate_sep_bwd_N8192_H4096"] = op_entry(time_region(torch, gb.replay, 10, s),
+                                               N * (44 * H + 64) + 16 * H + (N // 64) * 16 * H, peak)
+    del inp, k, v, out, sv, gx, gk, gv, gwp, ws, gf, gb
+    torch.cuda.empty_cache()
     # GateConv, two configurations
     for (M, T, d, hs, vs, name) in ((4, 4096, 4096, 1.0, 1.0, "gateconv_M4_T4096_d4096"),
                                     (8, 8192, 7168, 10.0, 0.1 ** 0.5, "gateconv_M8_T8192_d7168")):

@@ -29,11 +29,14 @@ __all__ = [
     "engram_gate_fwd", "engram_gate_bwd", "engram_gate_bwd_workspace_size",
     "engram_gateconv_fwd", "engram_gateconv_bwd", "engram_gateconv_bwd_workspace_size",
     "engram_device_error", "engram_launch_info", "engram_gate_bwd_noalloc",
+    "engram_gate_sep_fwd", "engram_gate_sep_bwd", "engram_gate_sep_bwd_workspace_size",
     "gate_forward", "gate_backward", "gateconv_forward", "gateconv_backward",
-    "GATE_EPS", "GATECONV_EPS", "EXPORTED_SYMBOLS",
+    "gate_sep_forward", "gate_sep_backward",
+    "GATE_EPS", "GATE_CLAMP", "GATECONV_EPS", "EXPORTED_SYMBOLS",
 ]
 
 GATE_EPS = 1e-20     # default RMS-norm epsilon of the saved-state gate
+GATE_CLAMP = 1e-6    # clamp of the gate's signed square root
 GATECONV_EPS = 1e-6  # default RMSNorm epsilon of GateConv
 D_GATE = 5120
 S_GATE = 4
@@ -42,7 +45,8 @@ EXPORTED_SYMBOLS = (
     "engram_status_string", "engram_gate_fwd", "engram_gate_bwd_workspace_size",
     "engram_gate_bwd", "engram_gateconv_fwd", "engram_gateconv_bwd_workspace_size",
     "engram_gateconv_bwd", "engram_device_error", "engram_launch_info",
-    "engram_gate_bwd_noalloc",
+    "engram_gate_bwd_noalloc", "engram_gate_sep_fwd", "engram_gate_sep_bwd_workspace_size",
+    "engram_gate_sep_bwd",
 )
 
 _STATUS = {0: "ok", 1: "null pointer", 2: "misaligned pointer", 3: "size out of range",
@@ -91,6 +95,10 @@ def load(path: str | None = None):
         lib.engram_gate_bwd_workspace_size.restype = SZ
         lib.engram_gate_bwd.argtypes = [P, P, P, P, P, P, P, P, P, SZ, I64, P]
         lib.engram_gate_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I64, P]
+        lib.engram_gate_sep_fwd.argtypes = [P] * 9 + [I64, I64, F, F, P]
+        lib.engram_gate_sep_bwd_workspace_size.argtypes = [I64]
+        lib.engram_gate_sep_bwd_workspace_size.restype = SZ
+        lib.engram_gate_sep_bwd.argtypes = [P] * 14 + [SZ, I64, I64, F, P]
         lib.engram_gateconv_fwd.argtypes = [P] * 12 + [I64, I64, I64, F, P]
         lib.engram_gateconv_bwd_workspace_size.argtypes = [I64, I64, I64]
         lib.engram_gateconv_bwd_workspace_size.restype = SZ
@@ -99,7 +107,7 @@ def load(path: str | None = None):
         lib.engram_launch_info.argtypes = [ctypes.c_int, I64, I64, I64,
                                            ctypes.POINTER(_LaunchInfo)]
         for name in ("engram_gate_fwd", "engram_gate_bwd", "engram_gate_bwd_noalloc",
-                     "engram_gateconv_fwd",
+                     "engram_gate_sep_fwd", "engram_gate_sep_bwd", "engram_gateconv_fwd",
                      "engram_gateconv_bwd", "engram_device_error", "engram_launch_info"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -185,6 +193,42 @@ def engram_gate_bwd_noalloc(x, kv, weight, saved, grad_out, grad_x, grad_kv, gra
         _ptr(grad_kv), _ptr(grad_weight), N, _stream(stream)))
 
 
+def engram_gate_sep_fwd(x, k, v, weight, out, dot=None, gate=None, rstd_x=None, rstd_k=None,
+                        eps: float = GATE_EPS, clamp: float = GATE_CLAMP, stream=None):
+    """Separate key / value tensors, any hidden size H (multiple of 8); the
+    saved state is four (N, 4) arrays, all given or all None."""
+    N, _, H = x.shape
+    _need(x, torch.bfloat16, (N, S_GATE, H), "x")
+    _need(k, torch.bfloat16, (N, S_GATE, H), "k")
+    _need(v, torch.bfloat16, (N, H), "v")
+    _need(weight, torch.float32, (S_GATE, H), "weight")
+    _need(out, torch.bfloat16, (N, S_GATE, H), "out")
+    for t, n in ((dot, "dot"), (gate, "gate"), (rstd_x, "rstd_x"), (rstd_k, "rstd_k")):
+        if t is not None:
+            _need(t, torch.float32, (N, S_GATE), n)
+    _check("engram_gate_sep_fwd", load().engram_gate_sep_fwd(
+        _ptr(x), _ptr(k), _ptr(v), _ptr(weight), _ptr(out), _ptr(dot), _ptr(gate), _ptr(rstd_x),
+        _ptr(rstd_k), N, H, float(eps), float(clamp), _stream(stream)))
+
+
+def engram_gate_sep_bwd_workspace_size(N: int) -> int:
+    return int(load().engram_gate_sep_bwd_workspace_size(int(N)))
+
+
+def engram_gate_sep_bwd(grad_out, x, k, v, weight, dot, gate, rstd_x, rstd_k, grad_x, grad_k,
+                        grad_v, grad_w_partial, workspace, clamp: float = GATE_CLAMP, stream=None):
+    N, _, H = x.shape
+    for t, n in ((grad_out, "grad_out"), (grad_x, "grad_x"), (grad_k, "grad_k")):
+        _need(t, torch.bfloat16, (N, S_GATE, H), n)
+    _need(grad_v, torch.bfloat16, (N, H), "grad_v")
+    _need(grad_w_partial, torch.float32, ((N + 63) // 64, S_GATE, H), "grad_w_partial")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("engram_gate_sep_bwd", load().engram_gate_sep_bwd(
+        _ptr(grad_out), _ptr(x), _ptr(k), _ptr(v), _ptr(weight), _ptr(dot), _ptr(gate),
+        _ptr(rstd_x), _ptr(rstd_k), _ptr(grad_x), _ptr(grad_k), _ptr(grad_v), _ptr(grad_w_partial),
+        _ptr(workspace), nbytes, N, H, float(clamp), _stream(stream)))
+
+
 def engram_gateconv_fwd(H, k, v, rms_w_h, rms_w_v, conv_w, Y, vhat, alpha, rrms_h, rrms_k,
                         rrms_v, eps: float = GATECONV_EPS, stream=None):
     M, T, d = H.shape
@@ -254,6 +298,28 @@ def gate_backward(x, kv, weight, saved, grad_out):
     ws = torch.empty(engram_gate_bwd_workspace_size(N), device=x.device, dtype=torch.uint8)
     engram_gate_bwd(x, kv, weight, saved, grad_out, gx, gkv, gw, ws)
     return gx, gkv, gw
+
+
+def gate_sep_forward(x, k, v, weight, eps: float = GATE_EPS, clamp: float = GATE_CLAMP,
+                     save: bool = True):
+    """Returns out and, with save, (dot, gate, rstd_x, rstd_k), each (N, 4)."""
+    out = torch.empty_like(x)
+    sv = [torch.empty((x.shape[0], S_GATE), device=x.device, dtype=torch.float32)
+          for _ in range(4)] if save else [None] * 4
+    engram_gate_sep_fwd(x, k, v, weight, out, *sv, eps=eps, clamp=clamp)
+    return (out, *sv) if save else (out,)
+
+
+def gate_sep_backward(grad_out, x, k, v, weight, dot, gate, rstd_x, rstd_k,
+                      clamp: float = GATE_CLAMP):
+    """Returns grad_x, grad_k, grad_v and grad_w_partial (ceil(N/64), 4, H)."""
+    N, _, H = x.shape
+    gx, gk, gv = torch.empty_like(x), torch.empty_like(k), torch.empty_like(v)
+    gwp = torch.empty(((N + 63) // 64, S_GATE, H), device=x.device, dtype=torch.float32)
+    ws = torch.empty(engram_gate_sep_bwd_workspace_size(N), device=x.device, dtype=torch.uint8)
+    engram_gate_sep_bwd(grad_out, x, k, v, weight, dot, gate, rstd_x, rstd_k, gx, gk, gv, gwp, ws,
+                        clamp=clamp)
+    return gx, gk, gv, gwp
 
 
 def gateconv_forward(H, k, v, rms_w_h, rms_w_v, conv_w, eps: float = GATECONV_EPS):

@@ -191,26 +191,30 @@ bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c) {
 }
 
 // Backward: kernel 1 (per-token scalars) on a persistent grid of 256-thread
-// CTAs; kernel 2 on a grid of (column slices) x (token groups).  A group
-// covers at least two 64-token blocks, so its (hi, lo) grad_weight pair fits
-// two of the workspace's block slots; a single-block problem uses one slot.
-bool gate_bwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c, int& ncols, int& ngroups,
+// CTAs; kernel 2 on a grid of (column slices of 512) x (token groups).  With
+// `blocks` set, every 64-token block is its own group and writes one
+// grad_weight partial (returned to the caller); otherwise a group covers at
+// least two 64-token blocks, so its (hi, lo) grad_weight pair fits two of the
+// workspace's block slots (a single-block problem uses one slot).
+bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg& c, int& ncols,
                   int& group_tokens) {
     // slices of 64 column groups: 8 warps x (8 groups x 4 streams)
-    static_assert((kGateD / 8) % 64 == 0, "whole slices");
-    const int C = kGateD / 8 / 64;
-    ncols = kGateD / C;
-    ngroups = ncols / 8;
+    ncols = 512;
+    const int C = static_cast<int>((d + ncols - 1) / ncols);
     c.cluster = 1;
-    c.threads = 4 * ngroups;
+    c.threads = 256;
     c.stages = kGateBwdStages;
     c.smem = 256 + c.stages * (12 * ncols * 2 + 128);
     if (max_clusters(st, 1, 1, c.threads, c.smem) <= 0) return false;
     const int mc1 = max_clusters(st, 1, 1, 256, 0);
     if (mc1 <= 0) return false;
-    const int64_t nb = N / 64;
-    const int64_t groups0 = nb >= 2 ? nb / 2 : 1;
-    group_tokens = static_cast<int>(64 * ((nb + groups0 - 1) / groups0));
+    const int64_t nb = (N + 63) / 64;
+    if (blocks) {
+        group_tokens = 64;
+    } else {
+        const int64_t groups0 = nb >= 2 ? nb / 2 : 1;
+        group_tokens = static_cast<int>(64 * ((nb + groups0 - 1) / groups0));
+    }
     c.clusters = C;
     c.grid_y = static_cast<int>((N + group_tokens - 1) / group_tokens);
     const int64_t need1 = (N + 7) / 8;
@@ -345,16 +349,21 @@ engram_status_t engram_gate_fwd(const void* x, const void* kv, const float* weig
     if (!st) return ENGRAM_ERR_DEVICE;
     LaunchCfg c = {};
     if (!gate_fwd_cfg(*st, N, c)) return ENGRAM_ERR_DEVICE;
-    GateFwdParams p;
+    GateFwdParams p = {};
     p.x = static_cast<const uint16_t*>(x);
-    p.kv = static_cast<const uint16_t*>(kv);
+    p.key = static_cast<const uint16_t*>(kv);
+    p.v = static_cast<const uint16_t*>(kv) + 4 * kGateD;
+    p.key_ts = p.v_ts = 5LL * kGateD;
     p.w = weight;
     p.mask = mask;
     p.out = static_cast<uint16_t*>(out);
     p.saved = saved;
     p.err = st->err;
     p.N = N;
+    p.d = kGateD;
+    p.packed = 1;
     p.eps = eps;
+    p.clamp = ENGRAM_GATE_CLAMP;
     return launch_status(gate_fwd_launch(p, c, stream));
 }
 
@@ -383,30 +392,35 @@ engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weig
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
     LaunchCfg c = {};
-    int ncols, ngroups;
+    int ncols;
     int group_tokens = 0;
-    if (!gate_bwd_cfg(*st, N, c, ncols, ngroups, group_tokens)) return ENGRAM_ERR_DEVICE;
+    if (!gate_bwd_cfg(*st, N, kGateD, false, c, ncols, group_tokens)) return ENGRAM_ERR_DEVICE;
     // workspace: [(N, 4, 4) per-token scalars | (N/64, 4, 5120) fp32 partial slots]
     float* coef = static_cast<float*>(workspace);
     float* partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + 64 * n);
-    GateBwdParams p;
+    GateBwdParams p = {};
     p.x = static_cast<const uint16_t*>(x);
-    p.kv = static_cast<const uint16_t*>(kv);
+    p.key = static_cast<const uint16_t*>(kv);
+    p.v = static_cast<const uint16_t*>(kv) + 4 * kGateD;
+    p.key_ts = p.v_ts = 5LL * kGateD;
     p.w = weight;
     p.saved = saved;
     p.gout = static_cast<const uint16_t*>(grad_out);
     p.gx = static_cast<uint16_t*>(grad_x);
-    p.gkv = static_cast<uint16_t*>(grad_kv);
+    p.gkey = static_cast<uint16_t*>(grad_kv);
+    p.gv = static_cast<uint16_t*>(grad_kv) + 4 * kGateD;
+    p.gkey_ts = p.gv_ts = 5LL * kGateD;
     p.coef = coef;
     p.partial = partial;
     p.err = st->err;
     p.N = N;
     p.d = kGateD;
     p.ncols = ncols;
-    p.ngroups = ngroups;
     p.stages = c.stages;
     p.group_tokens = group_tokens;
     p.pair_slots = (N / 64) >= 2 ? 1 : 0;
+    p.packed = 1;
+    p.clamp = ENGRAM_GATE_CLAMP;
     engram_status_t s = launch_status(gate_bwd_launch(p, c, stream));
     if (s != ENGRAM_OK) return s;
     GateWReduceParams r;
@@ -467,6 +481,117 @@ engram_status_t engram_gateconv_fwd(const void* H, const void* k, const void* v,
     p.eps = eps;
     p.inv_sqrt_d = static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
     return launch_status(gateconv_fwd_launch(p, g->c, stream));
+}
+
+engram_status_t engram_gate_sep_fwd(const void* x, const void* k, const void* v,
+                                    const float* weight, void* out, float* dot, float* gate,
+                                    float* rstd_x, float* rstd_k, int64_t N, int64_t H, float eps,
+                                    float clamp, cudaStream_t stream) {
+    if (!x || !k || !v || !weight || !out) return ENGRAM_ERR_NULL;
+    const int nsaved = (dot != nullptr) + (gate != nullptr) + (rstd_x != nullptr) + (rstd_k != nullptr);
+    if (nsaved != 0 && nsaved != 4) return ENGRAM_ERR_NULL;
+    if (N < 1 || N > ENGRAM_GATE_MAX_TOKENS || H < 8 || H > ENGRAM_GATE_SEP_MAX_HIDDEN || H % 8 != 0)
+        return ENGRAM_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(k) || !aligned16(v) || !aligned16(weight) || !aligned16(out) ||
+        (nsaved && (!aligned16(dot) || !aligned16(gate) || !aligned16(rstd_x) || !aligned16(rstd_k))))
+        return ENGRAM_ERR_ALIGN;
+    const size_t n = static_cast<size_t>(N), h = static_cast<size_t>(H);
+    const Range ins[] = {{x, n * 4 * h * 2}, {k, n * 4 * h * 2}, {v, n * h * 2}, {weight, 4 * h * 4}};
+    const Range outs[] = {{out, n * 4 * h * 2}, {dot, dot ? n * 16 : 0}, {gate, gate ? n * 16 : 0},
+                          {rstd_x, rstd_x ? n * 16 : 0}, {rstd_k, rstd_k ? n * 16 : 0}};
+    if (any_overlap(outs, 5, ins, 4)) return ENGRAM_ERR_OVERLAP;
+
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st = device_state();
+    if (!st) return ENGRAM_ERR_DEVICE;
+    LaunchCfg c = {};
+    if (!gate_fwd_cfg(*st, N, c)) return ENGRAM_ERR_DEVICE;
+    GateFwdParams p = {};
+    p.x = static_cast<const uint16_t*>(x);
+    p.key = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.key_ts = 4LL * H;
+    p.v_ts = H;
+    p.w = weight;
+    p.out = static_cast<uint16_t*>(out);
+    p.sv_gate = gate;
+    p.sv_dot = dot;
+    p.sv_rx = rstd_x;
+    p.sv_rk = rstd_k;
+    p.err = st->err;
+    p.N = N;
+    p.d = static_cast<int>(H);
+    p.eps = eps;
+    p.clamp = clamp;
+    return launch_status(gate_fwd_launch(p, c, stream));
+}
+
+size_t engram_gate_sep_bwd_workspace_size(int64_t N) {
+    if (N < 1 || N > ENGRAM_GATE_MAX_TOKENS) return 0;
+    return static_cast<size_t>(64) * static_cast<size_t>(N);
+}
+
+engram_status_t engram_gate_sep_bwd(const void* grad_out, const void* x, const void* k,
+                                    const void* v, const float* weight, const float* dot,
+                                    const float* gate, const float* rstd_x, const float* rstd_k,
+                                    void* grad_x, void* grad_k, void* grad_v, float* grad_w_partial,
+                                    void* workspace, size_t workspace_bytes, int64_t N, int64_t H,
+                                    float clamp, cudaStream_t stream) {
+    if (!grad_out || !x || !k || !v || !weight || !dot || !gate || !rstd_x || !rstd_k || !grad_x ||
+        !grad_k || !grad_v || !grad_w_partial || !workspace)
+        return ENGRAM_ERR_NULL;
+    if (N < 1 || N > ENGRAM_GATE_MAX_TOKENS || H < 8 || H > ENGRAM_GATE_SEP_MAX_HIDDEN || H % 8 != 0)
+        return ENGRAM_ERR_SHAPE;
+    const void* all[] = {grad_out, x, k, v, weight, dot, gate, rstd_x, rstd_k,
+                         grad_x, grad_k, grad_v, grad_w_partial, workspace};
+    for (const void* ptr : all)
+        if (!aligned16(ptr)) return ENGRAM_ERR_ALIGN;
+    const size_t need = engram_gate_sep_bwd_workspace_size(N);
+    if (workspace_bytes < need) return ENGRAM_ERR_WORKSPACE;
+    const size_t n = static_cast<size_t>(N), h = static_cast<size_t>(H);
+    const size_t nblk = (n + 63) / 64;
+    const Range ins[] = {{grad_out, n * 4 * h * 2}, {x, n * 4 * h * 2}, {k, n * 4 * h * 2},
+                         {v, n * h * 2}, {weight, 4 * h * 4}, {dot, n * 16}, {gate, n * 16},
+                         {rstd_x, n * 16}, {rstd_k, n * 16}};
+    const Range outs[] = {{grad_x, n * 4 * h * 2}, {grad_k, n * 4 * h * 2}, {grad_v, n * h * 2},
+                          {grad_w_partial, nblk * 4 * h * 4}, {workspace, need}};
+    if (any_overlap(outs, 5, ins, 9)) return ENGRAM_ERR_OVERLAP;
+
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st = device_state();
+    if (!st) return ENGRAM_ERR_DEVICE;
+    LaunchCfg c = {};
+    int ncols;
+    int group_tokens = 0;
+    if (!gate_bwd_cfg(*st, N, H, true, c, ncols, group_tokens)) return ENGRAM_ERR_DEVICE;
+    GateBwdParams p = {};
+    p.x = static_cast<const uint16_t*>(x);
+    p.key = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.key_ts = 4LL * H;
+    p.v_ts = H;
+    p.w = weight;
+    p.sv_gate = gate;
+    p.sv_dot = dot;
+    p.sv_rx = rstd_x;
+    p.sv_rk = rstd_k;
+    p.gout = static_cast<const uint16_t*>(grad_out);
+    p.gx = static_cast<uint16_t*>(grad_x);
+    p.gkey = static_cast<uint16_t*>(grad_k);
+    p.gv = static_cast<uint16_t*>(grad_v);
+    p.gkey_ts = 4LL * H;
+    p.gv_ts = H;
+    p.coef = static_cast<float*>(workspace);
+    p.partial = grad_w_partial;  // one slot per 64-token block, written directly
+    p.err = st->err;
+    p.N = N;
+    p.d = static_cast<int>(H);
+    p.ncols = ncols;
+    p.stages = c.stages;
+    p.group_tokens = group_tokens;
+    p.pair_slots = 0;
+    p.clamp = clamp;
+    return launch_status(gate_bwd_launch(p, c, stream));
 }
 
 size_t engram_gateconv_bwd_workspace_size(int64_t M, int64_t T, int64_t d) {
@@ -622,7 +747,7 @@ engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
     LaunchCfg c = {};
-    int ncols, ngroups;
+    int ncols;
     bool ok = false;
     switch (op) {
         case 0:
@@ -630,7 +755,7 @@ engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
             break;
         case 1: {
             int gt = 0;
-            ok = engram_gate_bwd_workspace_size(n0) > 0 && gate_bwd_cfg(*st, n0, c, ncols, ngroups, gt);
+            ok = engram_gate_bwd_workspace_size(n0) > 0 && gate_bwd_cfg(*st, n0, kGateD, false, c, ncols, gt);
             // CTAs sharing a token row = column slices; "clusters" = token groups
             if (ok) {
                 c.cluster = c.clusters;

@@ -7,39 +7,59 @@
 
 namespace eg {
 
+// Hidden size of the saved-state gate's packed-KV entry points.
+constexpr int kGateHidden = 5120;
+
 // Largest number of ring stages any kernel uses (mbarrier area sizing).
 constexpr int kMaxStages = 16;
 
+// Saved-state gate.  Row (n, s) of X is x + (n*4 + s)*d; the key row is
+// key + n*key_ts + s*d and the shared value row v + n*v_ts (packed KV:
+// key = kv, key_ts = 5d, v = kv + 4d, v_ts = 5d).  Saved state: packed
+// (gate, dot, rstd_X, rstd_key) records `saved` (N, 4, 4), or four separate
+// (N, 4) arrays sv_gate, sv_dot, sv_rx, sv_rk.
 struct GateFwdParams {
     const uint16_t* x;
-    const uint16_t* kv;
+    const uint16_t* key;
+    const uint16_t* v;
+    long long key_ts, v_ts;
     const float* w;
     const uint8_t* mask;
     uint16_t* out;
     float* saved;
+    float *sv_gate, *sv_dot, *sv_rx, *sv_rk;
     unsigned int* err;
     long long N;
+    int d;
+    int packed;   // 1: packed KV and saved records, d = 5120 (compile-time kernel)
     float eps;
+    float clamp;
 };
 
 struct GateBwdParams {
     const uint16_t* x;
-    const uint16_t* kv;
+    const uint16_t* key;
+    const uint16_t* v;
+    long long key_ts, v_ts;
     const float* w;
-    const float* saved;
+    const float* saved;        // packed records, or null with the four arrays below
+    const float *sv_gate, *sv_dot, *sv_rx, *sv_rk;
     const uint16_t* gout;
     uint16_t* gx;
-    uint16_t* gkv;
+    uint16_t* gkey;            // grad of key row (n, s) at gkey + n*gkey_ts + s*d
+    uint16_t* gv;              // grad of the shared value row n at gv + n*gv_ts
+    long long gkey_ts, gv_ts;
     float* coef;     // (N, 4, 4) fp32 per-token scalars: A hi, A lo, -B, -Ck
-    float* partial;  // (N/64, 4, d) fp32 slots for per-group grad_weight
+    float* partial;  // grad_weight slots (4, d) fp32 each
     unsigned int* err;
     long long N;
     int d;
-    int ncols;        // columns per CTA slice
-    int ngroups;      // 8-column groups per slice (<= threads)
+    int ncols;        // columns per CTA slice (the last slice may be shorter)
     int stages;
     int group_tokens; // tokens per token group (one grad_weight partial each)
     int pair_slots;   // 1: group g writes (hi, lo) to slots 2g, 2g+1
+    int packed;       // 1: packed KV / grad_kv and saved records, d = 5120
+    float clamp;
 };
 
 struct GateWReduceParams {

@@ -42,11 +42,8 @@ namespace eg {
 namespace {
 
 constexpr int kS = 4;
-constexpr int kD = 5120;
-constexpr int kChunks = kD / 256;   // 16-byte chunks per lane per row
 constexpr int kCG = 2;              // chunk indices per load group (kernel 1)
 constexpr int kRows = 3 * kS;       // X rows, key rows, grad_out rows (kernel 2)
-static_assert(kChunks % kCG == 0, "row must split into whole groups");
 
 EG_DEV uint4 ldg16_na(const uint4* p) {
     uint4 v;
@@ -63,51 +60,62 @@ EG_DEV void warp_sum_pair(float& hi, float& lo) {
 }
 
 // ---------------------------------------------------------------- kernel 1
+// kDFix = 5120: hidden size known at compile time, packed saved records;
+// kDFix = 0: any hidden size (a multiple of 8), separate saved arrays.
+template <int kDFix>
 __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdParams p) {
     const int lane = threadIdx.x & 31;
     const long long gwarp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-    static_assert((kChunks / kCG) % 2 == 0, "group 0 of every token uses buffer 0");
-    uint4 vb[2][kCG], gb[2][kS][kCG];
-    auto load_group = [&](long long n, int grp, int buf) {
-        const uint4* vr = reinterpret_cast<const uint4*>(p.kv + (n * (kS + 1) + kS) * kD) + lane;
-        const uint4* gr = reinterpret_cast<const uint4*>(p.gout + n * kS * kD) + lane;
+    const int d = kDFix ? kDFix : p.d;
+    const int nch = d >> 3;                                   // 16-byte chunks per row
+    const int ng = (((nch + 31) / 32 + kCG - 1) / kCG + 1) & ~1;  // even number of load groups
+    auto has = [&](int m) { return (kDFix != 0 && (kDFix / 8) % (32 * 2 * kCG) == 0) || lane + 32 * m < nch; };
+    uint4 v0[kCG], g0[kS][kCG], v1[kCG], g1[kS][kCG];
+    auto load_group = [&](long long n, int grp, uint4 (&vb)[kCG], uint4 (&gb)[kS][kCG]) {
+        const uint4* vr = reinterpret_cast<const uint4*>(p.v + n * (kDFix ? 5LL * kDFix : p.v_ts)) + lane;
+        const uint4* gr = reinterpret_cast<const uint4*>(p.gout + n * kS * d) + lane;
 #pragma unroll
         for (int c = 0; c < kCG; ++c) {
             const int m = grp * kCG + c;
-            vb[buf][c] = ldg16_na(vr + 32 * m);
+            const bool ok = has(m);
+            vb[c] = ok ? ldg16_na(vr + 32 * m) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int s = 0; s < kS; ++s) gb[buf][s][c] = ldg16_na(gr + s * (kD / 8) + 32 * m);
+            for (int s = 0; s < kS; ++s) gb[s][c] = ok ? ldg16_na(gr + s * (d / 8) + 32 * m) : make_uint4(0, 0, 0, 0);
         }
     };
-    if (gwarp < p.N) load_group(gwarp, 0, 0);
+    float2 hi[kS], lo[kS];
+    auto accumulate = [&](const uint4 (&vb)[kCG], const uint4 (&gb)[kS][kCG]) {
+#pragma unroll
+        for (int c = 0; c < kCG; ++c) {
+            const float2 v2[4] = {bf2(vb[c].x), bf2(vb[c].y), bf2(vb[c].z), bf2(vb[c].w)};
+#pragma unroll
+            for (int s = 0; s < kS; ++s) {
+                const uint4 gq = gb[s][c];
+                // g*v is exact in fp32 (two 8-bit significands)
+                cacc_add_x2(hi[s], lo[s], mul2(bf2(gq.x), v2[0]));
+                cacc_add_x2(hi[s], lo[s], mul2(bf2(gq.y), v2[1]));
+                cacc_add_x2(hi[s], lo[s], mul2(bf2(gq.z), v2[2]));
+                cacc_add_x2(hi[s], lo[s], mul2(bf2(gq.w), v2[3]));
+            }
+        }
+    };
+    if (gwarp < p.N) load_group(gwarp, 0, v0, g0);
     for (long long n = gwarp; n < p.N; n += nwarps) {
-        float2 hi[kS], lo[kS];
 #pragma unroll
         for (int s = 0; s < kS; ++s) hi[s] = lo[s] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int grp = 0; grp < kChunks / kCG; ++grp) {
-            const int cur = grp & 1;
-            // next group of this token, or the first group of the next token
-            // (its loads then overlap this token's reduction and fp64 work)
-            if (grp + 1 < kChunks / kCG)
-                load_group(n, grp + 1, cur ^ 1);
+        for (int grp = 0; grp < ng; grp += 2) {
+            // buffer 0 holds group grp; its successor goes to buffer 1, then
+            // buffer 0 takes group grp + 2 or the first group of the next
+            // token (whose loads then overlap this token's reduction and fp64 work)
+            load_group(n, grp + 1, v1, g1);
+            accumulate(v0, g0);
+            if (grp + 2 < ng)
+                load_group(n, grp + 2, v0, g0);
             else if (n + nwarps < p.N)
-                load_group(n + nwarps, 0, cur ^ 1);
-#pragma unroll
-            for (int c = 0; c < kCG; ++c) {
-                const float2 v2[4] = {bf2(vb[cur][c].x), bf2(vb[cur][c].y), bf2(vb[cur][c].z),
-                                      bf2(vb[cur][c].w)};
-#pragma unroll
-                for (int s = 0; s < kS; ++s) {
-                    const uint4 gq = gb[cur][s][c];
-                    // g*v is exact in fp32 (two 8-bit significands)
-                    cacc_add_x2(hi[s], lo[s], mul2(bf2(gq.x), v2[0]));
-                    cacc_add_x2(hi[s], lo[s], mul2(bf2(gq.y), v2[1]));
-                    cacc_add_x2(hi[s], lo[s], mul2(bf2(gq.z), v2[2]));
-                    cacc_add_x2(hi[s], lo[s], mul2(bf2(gq.w), v2[3]));
-                }
-            }
+                load_group(n + nwarps, 0, v0, g0);
+            accumulate(v1, g1);
         }
         float h[kS], l[kS];
 #pragma unroll
@@ -122,12 +130,17 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
             // fp32 estimates refined by one Newton step, exp is the fp64 routine
             const float hs = lane == 0 ? h[0] : lane == 1 ? h[1] : lane == 2 ? h[2] : h[3];
             const float ls = lane == 0 ? l[0] : lane == 1 ? l[1] : lane == 2 ? l[2] : l[3];
-            const float4 sv = __ldg(reinterpret_cast<const float4*>(p.saved + (n * kS + lane) * 4));
+            const long long rs = n * kS + lane;
+            float4 sv;
+            if (kDFix)
+                sv = __ldg(reinterpret_cast<const float4*>(p.saved + rs * 4));
+            else
+                sv = make_float4(__ldg(p.sv_gate + rs), __ldg(p.sv_dot + rs), __ldg(p.sv_rx + rs), __ldg(p.sv_rk + rs));
             const float gate = sv.x;
             const double dot = sv.y, rx = sv.z, rk = sv.w;
             const double ad = fabs(dot);
             double ddot = 0.0;
-            if (ad >= 1e-6 && gate != 0.f) {
+            if (ad >= static_cast<double>(p.clamp) && gate != 0.f) {
                 double y = rsqrtf(fabsf(sv.y));
                 y = y * (1.5 - 0.5 * ad * y * y);           // 1/sqrt(|dot|)
                 const double sqm = ad * y;                  // |sq| = sqrt(|dot|)
@@ -139,13 +152,13 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
                 const double dgate = static_cast<double>(hs) + static_cast<double>(ls);
                 ddot = dgate * dsig * (0.5 * y);            // d sq/d dot = 0.5/sqrt(|dot|)
             }
-            const double dd = dot / static_cast<double>(kD);
+            const double dd = dot / static_cast<double>(d);
             const double av = ddot * rx * rk;
             // A = a8 + arest: a8 keeps 8 significant bits, so a8 * (x*k) is exact
             // in fp32 (8 + 16 bits); arest carries the next 24 bits
             const float a8 = __uint_as_float(__float_as_uint(static_cast<float>(av)) & 0xffff0000u);
             const float arest = static_cast<float>(av - static_cast<double>(a8));
-            stg_f4(p.coef + (n * kS + lane) * 4, a8, arest, static_cast<float>(-(ddot * rx * rx * dd)),
+            stg_f4(p.coef + rs * 4, a8, arest, static_cast<float>(-(ddot * rx * rx * dd)),
                    static_cast<float>(-(ddot * rk * rk * dd)));
         }
     }
@@ -157,6 +170,9 @@ constexpr int kRing2Off = 256;  // after the stage mbarriers and release counter
 // Thread mapping: lane = 8 * stream + g, warp w; the thread owns the 8 columns
 // col0 + 8 * (8w + g) of one stream.  The four streams of a column group sit
 // in one warp, so grad_v (a sum over streams) is two shuffles.
+// kPacked: d = 5120, packed KV / grad_kv rows and saved records, all strides
+// known at compile time; otherwise runtime d and strides.
+template <bool kPacked>
 __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);                            // [stages]
@@ -168,11 +184,19 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     const int W = blockDim.x >> 5;
     const int s = lane >> 3;                               // stream
     const int cg = (tid >> 5) * 8 + (lane & 7);           // column group in the slice
+    const int d = kPacked ? kGateHidden : p.d;
+    const long long key_ts = kPacked ? 5LL * kGateHidden : p.key_ts;
+    const long long gkey_ts = kPacked ? 5LL * kGateHidden : p.gkey_ts;
+    const long long gv_ts = kPacked ? 5LL * kGateHidden : p.gv_ts;
     const int col0 = static_cast<int>(blockIdx.x) * p.ncols;
+    const int cols = min(p.ncols, d - col0);            // this slice (the last may be shorter)
     const int col = col0 + 8 * cg;
-    const bool active = cg < p.ngroups;
+    const bool active = 8 * cg < cols;
     const long long grp = blockIdx.y;
-    const uint32_t row_bytes = static_cast<uint32_t>(p.ncols) * 2u;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.ncols) * 2u;   // stage row pitch
+    const uint32_t copy_bytes = static_cast<uint32_t>(cols) * 2u;     // bytes copied per row
+    // saved gate of (n, s): packed records (stride 4 floats) or a (N, 4) array
+    const int gstride = (kPacked || p.saved != nullptr) ? 4 : 1;
     const uint32_t stage_bytes = kRows * row_bytes + 128u;
     const int stages = p.stages;
     const long long t0 = grp * p.group_tokens;
@@ -181,8 +205,8 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
 
     float2 w2[4];
     if (active) {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(p.w + s * kD + col));
-        const float4 b = __ldg(reinterpret_cast<const float4*>(p.w + s * kD + col + 4));
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p.w + s * d + col));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(p.w + s * d + col + 4));
         w2[0] = make_float2(a.x, a.y);
         w2[1] = make_float2(a.z, a.w);
         w2[2] = make_float2(b.x, b.y);
@@ -201,18 +225,21 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     }
     __syncthreads();
 
+    const uint32_t gate_bytes = 16u * static_cast<uint32_t>(gstride);
     auto issue = [&](int j, int st) {
         const long long n = t0 + j;
         unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
-        mbar_arrive_expect_tx(&full[st], stage_bytes);
+        mbar_arrive_expect_tx(&full[st], kRows * copy_bytes + 64u + gate_bytes);
 #pragma unroll
         for (int r = 0; r < kS; ++r) {
-            bulk_g2s(b + r * row_bytes, p.x + (n * kS + r) * kD + col0, row_bytes, &full[st]);
-            bulk_g2s(b + (kS + r) * row_bytes, p.kv + (n * (kS + 1) + r) * kD + col0, row_bytes, &full[st]);
-            bulk_g2s(b + (2 * kS + r) * row_bytes, p.gout + (n * kS + r) * kD + col0, row_bytes, &full[st]);
+            bulk_g2s(b + r * row_bytes, p.x + (n * kS + r) * d + col0, copy_bytes, &full[st]);
+            bulk_g2s(b + (kS + r) * row_bytes, p.key + n * key_ts + static_cast<long long>(r) * d + col0,
+                     copy_bytes, &full[st]);
+            bulk_g2s(b + (2 * kS + r) * row_bytes, p.gout + (n * kS + r) * d + col0, copy_bytes, &full[st]);
         }
         bulk_g2s(b + kRows * row_bytes, p.coef + n * kS * 4, 64u, &full[st]);
-        bulk_g2s(b + kRows * row_bytes + 64, p.saved + n * kS * 4, 64u, &full[st]);
+        const float* gsrc = p.saved != nullptr ? p.saved + n * kS * 4 : p.sv_gate + n * kS;
+        bulk_g2s(b + kRows * row_bytes + 64, gsrc, gate_bytes, &full[st]);
     };
     if (tid == 0) {
         const int pro = ntok < stages ? static_cast<int>(ntok) : stages;
@@ -235,7 +262,7 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
         const float2 A82 = splat2(c4.x), Ar2 = splat2(c4.y);
         const float2 A2 = splat2(__fadd_rn(c4.x, c4.y));
         const float2 nB2 = splat2(c4.z), nC2 = splat2(c4.w);
-        const float2 G2 = splat2(cf[16 + 4 * s]);  // saved gate of stream s
+        const float2 G2 = splat2(cf[16 + gstride * s]);  // saved gate of stream s
         float2 gv[4];
         uint32_t ox[4], ok[4];
         if (active) {
@@ -288,19 +315,20 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
                                             __shfl_xor_sync(kFullMask, gv[e].y, 16)));
         }
         if (active) {
-            stg_cs(p.gx + (n * kS + s) * kD + col, make_uint4(ox[0], ox[1], ox[2], ox[3]));
-            stg_cs(p.gkv + (n * (kS + 1) + s) * kD + col, make_uint4(ok[0], ok[1], ok[2], ok[3]));
+            stg_cs(p.gx + (n * kS + s) * d + col, make_uint4(ox[0], ox[1], ox[2], ox[3]));
+            stg_cs(p.gkey + n * gkey_ts + static_cast<long long>(s) * d + col,
+                   make_uint4(ok[0], ok[1], ok[2], ok[3]));
             if (s == 0)
-                stg_cs(p.gkv + (n * (kS + 1) + kS) * kD + col,
+                stg_cs(p.gv + n * gv_ts + col,
                        make_uint4(pack2(gv[0]), pack2(gv[1]), pack2(gv[2]), pack2(gv[3])));
         }
     }
     // this group's grad_w for the columns: (hi, lo) in slots 2g, 2g+1, or
     // hi + lo in slot 0 when a single group covers a single block
     if (active && ntok > 0) {
-        float* o = p.partial + ((p.pair_slots ? 2 * grp : grp) * kS + s) * kD + col;
+        float* o = p.partial + ((p.pair_slots ? 2 * grp : grp) * kS + s) * d + col;
         if (p.pair_slots) {
-            float* ol = o + static_cast<long long>(kS) * kD;
+            float* ol = o + static_cast<long long>(kS) * d;
             stg_f4(o, phi[0].x, phi[0].y, phi[1].x, phi[1].y);
             stg_f4(o + 4, phi[2].x, phi[2].y, phi[3].x, phi[3].y);
             stg_f4(ol, plo[0].x, plo[0].y, plo[1].x, plo[1].y);
@@ -378,13 +406,21 @@ __global__ void __launch_bounds__(32 * kRedGroups) wreduce_kernel(const GateWRed
 cudaError_t gate_bwd_prepare(int smem_bytes) {
     cudaError_t e = cudaSuccess;
     if (smem_bytes > 0)  // 0: only the coefficient kernel is being set up
-        e = cudaFuncSetAttribute(gate_bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gate_bwd_main_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes);
+    if (e == cudaSuccess && smem_bytes > 0)
+        e = cudaFuncSetAttribute(gate_bwd_main_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem_bytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gate_bwd_main_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(gate_bwd_main_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gate_bwd_coef_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
+    e = cudaFuncSetAttribute(gate_bwd_main_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gate_bwd_coef_kernel<kGateHidden>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gate_bwd_coef_kernel<0>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
 }
 
 // Co-resident CTAs: of the coefficient kernel (threads = 256) when smem == 0,
@@ -392,8 +428,8 @@ cudaError_t gate_bwd_prepare(int smem_bytes) {
 cudaError_t gate_bwd_max_clusters(int, int threads, int smem, int* out) {
     int per_sm = 0, dev = 0, sms = 0;
     cudaError_t e = smem == 0
-        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_bwd_coef_kernel, threads, 0)
-        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_bwd_main_kernel, threads, smem);
+        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_bwd_coef_kernel<kGateHidden>, threads, 0)
+        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_bwd_main_kernel<true>, threads, smem);
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     *out = per_sm * sms;
@@ -402,10 +438,17 @@ cudaError_t gate_bwd_max_clusters(int, int threads, int smem, int* out) {
 
 // kernel 1 then kernel 2 on the stream (kernel 3 is gate_wreduce_launch)
 cudaError_t gate_bwd_launch(const GateBwdParams& p, const LaunchCfg& c, cudaStream_t s) {
-    gate_bwd_coef_kernel<<<c.aux_blocks, 256, 0, s>>>(p);
+    // the compile-time specialisations serve the packed layout (d = 5120)
+    if (p.packed)
+        gate_bwd_coef_kernel<kGateHidden><<<c.aux_blocks, 256, 0, s>>>(p);
+    else
+        gate_bwd_coef_kernel<0><<<c.aux_blocks, 256, 0, s>>>(p);
     cudaError_t e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
-    gate_bwd_main_kernel<<<dim3(c.clusters, c.grid_y, 1), c.threads, c.smem, s>>>(p);
+    if (p.packed)
+        gate_bwd_main_kernel<true><<<dim3(c.clusters, c.grid_y, 1), c.threads, c.smem, s>>>(p);
+    else
+        gate_bwd_main_kernel<false><<<dim3(c.clusters, c.grid_y, 1), c.threads, c.smem, s>>>(p);
     return cudaPeekAtLastError();
 }
 

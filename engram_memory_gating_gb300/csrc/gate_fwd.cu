@@ -28,10 +28,7 @@ namespace eg {
 namespace {
 
 constexpr int kS = 4;       // streams
-constexpr int kD = 5120;    // hidden size of one stream
-constexpr int kChunks = kD / 256;  // 16-byte chunks per lane per row
-constexpr int kGroup = 4;          // chunks per lane per load group
-static_assert(kChunks % kGroup == 0, "row must split into whole groups");
+constexpr int kGroup = 4;   // 16-byte chunks per lane per load group
 
 // 16-byte loads: read-only path; `_na` does not allocate in L1 (data used once).
 EG_DEV uint4 ldg16(const uint4* p) {
@@ -60,49 +57,60 @@ EG_DEV void warp_sum_pair(float& hi, float& lo) {
         cacc_merge(hi, lo, __shfl_xor_sync(kFullMask, hi, off), __shfl_xor_sync(kFullMask, lo, off));
 }
 
+// kDFix = 5120: the packed layout (KV rows, saved state as (N, 4, 4) records)
+// with hidden size and strides known at compile time; kDFix = 0: any hidden
+// size d (a multiple of 8), key / value rows through runtime strides, saved
+// state as four (N, 4) arrays.
+template <int kDFix>
 __global__ void __launch_bounds__(256, 2) gate_fwd_kernel(const GateFwdParams p) {
     const int lane = threadIdx.x & 31;
     const long long gwarp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
     const long long rows = p.N * kS;
-    const float inv_d = 1.0f / static_cast<float>(kD);
+    const int d = kDFix ? kDFix : p.d;
+    const int nch = d >> 3;                         // 16-byte chunks per row
+    const int ng = ((nch + 31) / 32 + kGroup - 1) / kGroup;  // load groups per lane
+    const float inv_d = 1.0f / static_cast<float>(d);
+    // chunk m of this lane (chunk index lane + 32 m) exists
+    auto has = [&](int m) { return (kDFix != 0 && (kDFix / 8) % 32 == 0) || lane + 32 * m < nch; };
 
     for (long long row = gwarp; row < rows; row += nwarps) {
         const long long n = row >> 2;
         const int s = static_cast<int>(row & 3);
-        const uint4* xr = reinterpret_cast<const uint4*>(p.x + (n * kS + s) * kD) + lane;
-        const uint4* kr = reinterpret_cast<const uint4*>(p.kv + (n * (kS + 1) + s) * kD) + lane;
-        const uint4* vr = reinterpret_cast<const uint4*>(p.kv + (n * (kS + 1) + kS) * kD) + lane;
-        const float4* wr = reinterpret_cast<const float4*>(p.w + s * kD) + 2 * lane;
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x + (n * kS + s) * d) + lane;
+        const long long key_ts = kDFix ? 5LL * kDFix : p.key_ts;
+        const long long v_ts = kDFix ? 5LL * kDFix : p.v_ts;
+        const uint4* kr = reinterpret_cast<const uint4*>(p.key + n * key_ts + static_cast<long long>(s) * d) + lane;
+        const uint4* vr = reinterpret_cast<const uint4*>(p.v + n * v_ts) + lane;
+        const float4* wr = reinterpret_cast<const float4*>(p.w + static_cast<long long>(s) * d) + 2 * lane;
         const bool on = (p.mask == nullptr) || (__ldg(p.mask + n) != 0);
 
         // ---- pass 1: sum x^2, sum k^2, sum x w k (compensated)
         float2 ssx = make_float2(0.f, 0.f), ssk = ssx, hi = ssx, lo = ssx;
-        uint4 xb[2][kGroup], kb[2][kGroup];
-#pragma unroll
-        for (int c = 0; c < kGroup; ++c) {
-            xb[0][c] = ldg16(xr + 32 * c);
-            kb[0][c] = ldg16_na(kr + 32 * c);
-        }
-#pragma unroll
-        for (int g = 0; g < kChunks / kGroup; ++g) {
-            const int cur = g & 1;
-            if (g + 1 < kChunks / kGroup) {
-#pragma unroll
-                for (int c = 0; c < kGroup; ++c) {
-                    xb[cur ^ 1][c] = ldg16(xr + 32 * ((g + 1) * kGroup + c));
-                    kb[cur ^ 1][c] = ldg16_na(kr + 32 * ((g + 1) * kGroup + c));
-                }
-            }
+        uint4 xa[kGroup], ka[kGroup], xb[kGroup], kb[kGroup];
+        auto load = [&](int g, uint4 (&xq)[kGroup], uint4 (&kq)[kGroup]) {
 #pragma unroll
             for (int c = 0; c < kGroup; ++c) {
                 const int m = g * kGroup + c;
+                if (has(m)) {
+                    xq[c] = ldg16(xr + 32 * m);
+                    kq[c] = ldg16_na(kr + 32 * m);
+                } else {
+                    xq[c] = kq[c] = make_uint4(0, 0, 0, 0);
+                }
+            }
+        };
+        auto accum = [&](int g, const uint4 (&xq)[kGroup], const uint4 (&kq)[kGroup]) {
+#pragma unroll
+            for (int c = 0; c < kGroup; ++c) {
+                const int m = g * kGroup + c;
+                if (!has(m)) continue;
                 const float4 wa = __ldg(wr + 64 * m);
                 const float4 wb = __ldg(wr + 64 * m + 1);
                 const float2 w2[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w),
                                       make_float2(wb.x, wb.y), make_float2(wb.z, wb.w)};
-                const uint32_t xw[4] = {xb[cur][c].x, xb[cur][c].y, xb[cur][c].z, xb[cur][c].w};
-                const uint32_t kw[4] = {kb[cur][c].x, kb[cur][c].y, kb[cur][c].z, kb[cur][c].w};
+                const uint32_t xw[4] = {xq[c].x, xq[c].y, xq[c].z, xq[c].w};
+                const uint32_t kw[4] = {kq[c].x, kq[c].y, kq[c].z, kq[c].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 x2 = bf2(xw[e]);
@@ -112,6 +120,16 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_kernel(const GateFwdParams p)
                     // x*k is exact in fp32 (two 8-bit significands)
                     cacc_prod_x2(hi, lo, mul2(x2, k2), w2[e]);
                 }
+            }
+        };
+        load(0, xa, ka);
+#pragma unroll
+        for (int g = 0; g < ng; g += 2) {
+            if (g + 1 < ng) load(g + 1, xb, kb);
+            accum(g, xa, ka);
+            if (g + 1 < ng) {
+                if (g + 2 < ng) load(g + 2, xa, ka);
+                accum(g + 1, xb, kb);
             }
         }
         float sx = __fadd_rn(ssx.x, ssx.y);
@@ -126,25 +144,36 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_kernel(const GateFwdParams p)
         const float rstd_x = rsqrtf(fmaf(sx, inv_d, p.eps));
         const float rstd_k = rsqrtf(fmaf(sk, inv_d, p.eps));
         const float dot = __fadd_rn(h, l) * rstd_x * rstd_k;
-        const float ad = fmaxf(fabsf(dot), 1e-6f);
+        const float ad = fmaxf(fabsf(dot), p.clamp);
         const float sqm = ad * rsqrtf(ad);
         const float sq = dot > 0.f ? sqm : (dot < 0.f ? -sqm : 0.f);
         const float gate = on ? __frcp_rn(1.0f + __expf(-sq)) : 0.f;
-        if (lane == 0 && p.saved != nullptr) stg_f4(p.saved + row * 4, gate, dot, rstd_x, rstd_k);
+        if (lane == 0) {
+            if (kDFix) {
+                if (p.saved != nullptr) stg_f4(p.saved + row * 4, gate, dot, rstd_x, rstd_k);
+            } else if (p.sv_gate != nullptr) {
+                p.sv_gate[row] = gate;
+                p.sv_dot[row] = dot;
+                p.sv_rx[row] = rstd_x;
+                p.sv_rk[row] = rstd_k;
+            }
+        }
 
         // ---- pass 2: out = x + gate * v, one rounding; a false mask copies X
-        uint4* o = reinterpret_cast<uint4*>(p.out + (n * kS + s) * kD) + lane;
+        uint4* o = reinterpret_cast<uint4*>(p.out + (n * kS + s) * d) + lane;
         const float2 g2 = splat2(gate);
 #pragma unroll
-        for (int g = 0; g < kChunks / kGroup; ++g) {
+        for (int g = 0; g < ng; ++g) {
             uint4 xq[kGroup], vq[kGroup];
 #pragma unroll
             for (int c = 0; c < kGroup; ++c) {
-                xq[c] = ldg16(xr + 32 * (g * kGroup + c));
-                vq[c] = on ? ldg16(vr + 32 * (g * kGroup + c)) : make_uint4(0, 0, 0, 0);
+                const int m = g * kGroup + c;
+                xq[c] = has(m) ? ldg16(xr + 32 * m) : make_uint4(0, 0, 0, 0);
+                vq[c] = (on && has(m)) ? ldg16(vr + 32 * m) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int c = 0; c < kGroup; ++c) {
+                const int m = g * kGroup + c;
                 uint4 ov = xq[c];
                 if (on) {
                     ov.x = pack2(fma2(g2, bf2(vq[c].x), bf2(xq[c].x)));
@@ -152,7 +181,7 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_kernel(const GateFwdParams p)
                     ov.z = pack2(fma2(g2, bf2(vq[c].z), bf2(xq[c].z)));
                     ov.w = pack2(fma2(g2, bf2(vq[c].w), bf2(xq[c].w)));
                 }
-                stg_cs(o + 32 * (g * kGroup + c), ov);
+                if (has(m)) stg_cs(o + 32 * m, ov);
             }
         }
     }
@@ -161,13 +190,16 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_kernel(const GateFwdParams p)
 }  // namespace
 
 cudaError_t gate_fwd_prepare(int) {
-    return cudaFuncSetAttribute(gate_fwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
+    cudaError_t e = cudaFuncSetAttribute(gate_fwd_kernel<kGateHidden>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout, 0);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gate_fwd_kernel<0>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
 }
 
 // Co-resident CTAs of the forward on this device (threads per CTA given).
 cudaError_t gate_fwd_max_clusters(int, int threads, int, int* out) {
     int per_sm = 0, dev = 0, sms = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_fwd_kernel, threads, 0);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_fwd_kernel<kGateHidden>, threads, 0);
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     *out = per_sm * sms;
@@ -175,7 +207,11 @@ cudaError_t gate_fwd_max_clusters(int, int threads, int, int* out) {
 }
 
 cudaError_t gate_fwd_launch(const GateFwdParams& p, const LaunchCfg& c, cudaStream_t s) {
-    gate_fwd_kernel<<<c.clusters, c.threads, 0, s>>>(p);
+    // the compile-time specialisation serves the packed layout (d = 5120)
+    if (p.packed)
+        gate_fwd_kernel<kGateHidden><<<c.clusters, c.threads, 0, s>>>(p);
+    else
+        gate_fwd_kernel<0><<<c.clusters, c.threads, 0, s>>>(p);
     return cudaPeekAtLastError();
 }
 

@@ -73,6 +73,8 @@ const char* engram_status_string(engram_status_t s);
 #define ENGRAM_GATE_MAX_TOKENS 4194240   /* forward: 1 <= N <= 65535*64     */
 #define ENGRAM_GATE_BWD_MAX_TOKENS 8192  /* backward: N % 64 == 0, N <= 8192 */
 #define ENGRAM_GATECONV_MAX_D 8192       /* GateConv: 8 <= d <= 8192, d % 8 == 0 */
+#define ENGRAM_GATE_CLAMP 1e-6f          /* clamp of the signed square root         */
+#define ENGRAM_GATE_SEP_MAX_HIDDEN 65536 /* separate-tensor gate: H % 8 == 0        */
 
 /*
  * Saved-state gate, forward (cuDNN "Engram saved-state gate", semantics and
@@ -128,6 +130,54 @@ engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weig
                                 const float* saved, const void* grad_out, void* grad_x,
                                 void* grad_kv, float* grad_weight, void* workspace,
                                 size_t workspace_bytes, int64_t N, cudaStream_t stream);
+
+/*
+ * Saved-state gate with separate key and value tensors and any hidden size
+ * (tile-kernels 1.0.0 engram tests: engram_gate_fwd / engram_gate_bwd take x,
+ * k (N, hc, H), v (N, H) and the fused weight, have no mask, return the saved
+ * dot, gate score and both rstd only when asked, and return grad_w as
+ * per-block partials that the caller sums).  Same arithmetic as
+ * engram_gate_fwd / engram_gate_bwd, with hc = 4 streams.
+ *   x, k       bf16 (N, 4, H)      streams and their keys
+ *   v          bf16 (N, H)         shared value
+ *   weight     fp32 (4, H)         fused weight
+ *   out        bf16 (N, 4, H)      out: bf16(x + gate * v)
+ *   dot, gate, rstd_x, rstd_k  fp32 (N, 4)  out, saved state: all four, or all
+ *              four NULL to skip them (out is bit-identical either way)
+ *   N: 1 <= N <= ENGRAM_GATE_MAX_TOKENS; H: 8 <= H <= ENGRAM_GATE_SEP_MAX_HIDDEN,
+ *   H % 8 == 0; eps inside the root (1e-20 in the pages' tests); clamp of the
+ *   signed square root (1e-6).  All pointers 16-byte aligned; outputs must
+ *   not overlap anything.  Asynchronous on `stream`, no allocation.
+ */
+engram_status_t engram_gate_sep_fwd(const void* x, const void* k, const void* v,
+                                    const float* weight, void* out, float* dot, float* gate,
+                                    float* rstd_x, float* rstd_k, int64_t N, int64_t H, float eps,
+                                    float clamp, cudaStream_t stream);
+
+/* Bytes of workspace engram_gate_sep_bwd needs: 64 N (per-token scalars);
+ * 0 if N is out of range. */
+size_t engram_gate_sep_bwd_workspace_size(int64_t N);
+
+/*
+ * Backward of engram_gate_sep_fwd.
+ *   grad_out   bf16 (N, 4, H)
+ *   x, k, v, weight            as in the forward
+ *   dot, gate, rstd_x, rstd_k  fp32 (N, 4), the forward's saved state
+ *   grad_x, grad_k   bf16 (N, 4, H)   out
+ *   grad_v           bf16 (N, H)      out: sum over the 4 streams of
+ *                                     gate * grad_out before its BF16 cast
+ *   grad_w_partial   fp32 (ceil(N/64), 4, H)  out: block b holds the grad_weight
+ *                                     contribution of tokens 64b .. 64b+63
+ *                                     (the caller sums over blocks)
+ *   workspace  >= engram_gate_sep_bwd_workspace_size(N) bytes, 16-B aligned
+ * Limits and errors as the forward.
+ */
+engram_status_t engram_gate_sep_bwd(const void* grad_out, const void* x, const void* k,
+                                    const void* v, const float* weight, const float* dot,
+                                    const float* gate, const float* rstd_x, const float* rstd_k,
+                                    void* grad_x, void* grad_k, void* grad_v, float* grad_w_partial,
+                                    void* workspace, size_t workspace_bytes, int64_t N, int64_t H,
+                                    float clamp, cudaStream_t stream);
 
 /*
  * GateConv, forward (TileOPs "Engram Operators", EngramGateConvFwdOp).

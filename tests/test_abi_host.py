@@ -145,3 +145,39 @@ def test_binding_has_no_cpu_fallback():
     for name in os.listdir(src_dir):
         if name.endswith(".py"):
             assert not pat.search(open(os.path.join(src_dir, name)).read()), name
+
+
+def test_gate_sep_validation_and_workspace():
+    lib = eg.load()
+    assert eg.engram_gate_sep_bwd_workspace_size(1) == 64
+    assert eg.engram_gate_sep_bwd_workspace_size(8192) == 64 * 8192
+    assert eg.engram_gate_sep_bwd_workspace_size(0) == 0
+
+    def fwd(ptrs, N=4, H=64):
+        return lib.engram_gate_sep_fwd(*(p(v) if v else None for v in ptrs), N, H, 1e-20, 1e-6, None)
+
+    base = [A * i for i in range(1, 10)]       # x, k, v, weight, out, dot, gate, rstd_x, rstd_k
+    assert fwd([0] + base[1:]) == ENULL
+    partial = list(base)
+    partial[6] = 0                             # three of the four saved arrays
+    assert fwd(partial) == ENULL
+    assert fwd(base, H=12) == ESHAPE
+    assert fwd(base, H=0) == ESHAPE
+    assert fwd(base, N=0) == ESHAPE
+    bad = list(base)
+    bad[2] = base[2] + 8
+    assert fwd(bad) == EALIGN
+    ov = list(base)
+    ov[4] = base[1]                            # out aliases k
+    assert fwd(ov) == EOVERLAP
+
+    def bwd(ptrs, ws_bytes=1 << 20, N=4, H=64):
+        return lib.engram_gate_sep_bwd(*(p(v) if v else None for v in ptrs), ws_bytes, N, H, 1e-6, None)
+
+    b14 = [A * i for i in range(1, 15)]
+    assert bwd([0] + b14[1:]) == ENULL
+    assert bwd(b14, H=7) == ESHAPE
+    assert bwd(b14, ws_bytes=64 * 4 - 16) == EWS
+    ov = list(b14)
+    ov[12] = b14[0]                            # grad_w_partial aliases grad_out
+    assert bwd(ov) == EOVERLAP

@@ -1,0 +1,141 @@
+"""GPU parity of the separate-tensor gate (engram_gate_sep_fwd / _bwd) against
+the fp64 oracle: the same gate as the packed entry points (cuDNN Frontend
+"Engram saved-state gate", semantics paragraph) with the tile-kernels layout
+(tile-kernels 1.0.0 engram tests: x, k (N, hc, H), v (N, H), no mask, optional
+saved state as separate tensors, grad_w returned as per-block partials).
+
+The oracle takes packed KV, so the test packs k and v for it and unpacks its
+grad_kv; per-block grad_w partials are checked against the oracle run on each
+64-token block, and their sum against the oracle on the whole batch.
+"""
+import numpy as np
+import pytest
+import torch
+
+import engram_memory_gating_gb300 as eg
+import oracle
+from engram_memory_gating_gb300.inputs import bf16_bits, gate_inputs
+from tolerance import bf16_bits_to_f64, check_bf16, check_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def no_device_error():
+    yield
+    assert eg.engram_device_error() == 0
+
+
+def f64(t):
+    if t.dtype == torch.bfloat16:
+        return bf16_bits_to_f64(bf16_bits(t)).reshape(tuple(t.shape))
+    return t.detach().double().cpu().numpy()
+
+
+def split_inputs(N, H, seed, sigma=None):
+    inp = gate_inputs(N, seed, d=H, sigma=sigma)
+    kv = inp["kv"]
+    k = kv[:, :4 * H].reshape(N, 4, H).contiguous()
+    v = kv[:, 4 * H:].contiguous()
+    return inp, k, v
+
+
+def run(N, H, seed, eps=oracle.GATE_EPS, clamp=oracle.GATE_CLAMP, w_scale=None, sigma=None):
+    inp, k, v = split_inputs(N, H, seed, sigma)
+    w = inp["weight"] if w_scale is None else inp["weight"] * w_scale
+    x, g = inp["x"], inp["grad_out"]
+    dev = {n: t.cuda() for n, t in (("x", x), ("k", k), ("v", v), ("w", w), ("g", g))}
+    out, dot, gate, rx, rk = eg.gate_sep_forward(dev["x"], dev["k"], dev["v"], dev["w"], eps=eps, clamp=clamp)
+    gx, gk, gv, gwp = eg.gate_sep_backward(dev["g"], dev["x"], dev["k"], dev["v"], dev["w"], dot, gate,
+                                           rx, rk, clamp=clamp)
+    torch.cuda.synchronize()
+    # oracle: packed KV, the GPU forward's saved state fed to its backward
+    kv64 = f64(inp["kv"])
+    eo, es = oracle.gate_fwd(f64(x), kv64, f64(w), None, eps=eps, clamp=clamp)
+    check_bf16("out", bf16_bits(out), eo)
+    for i, (name, t) in enumerate((("gate", gate), ("dot", dot), ("rstd_x", rx), ("rstd_k", rk))):
+        check_f32(name, t.cpu().numpy(), es[..., i])
+    saved = np.stack([f64(t) for t in (gate, dot, rx, rk)], axis=-1)
+    ex, ekv, ew = oracle.gate_bwd(f64(x), kv64, f64(w), saved, f64(g), clamp=clamp)
+    check_bf16("grad_x", bf16_bits(gx), ex)
+    check_bf16("grad_k", bf16_bits(gk), ekv[:, :4 * H].reshape(N, 4, H))
+    check_bf16("grad_v", bf16_bits(gv), ekv[:, 4 * H:])
+    part = gwp.cpu().double().numpy()
+    assert part.shape == ((N + 63) // 64, 4, H)
+    for b in range(part.shape[0]):
+        sl = slice(64 * b, min(N, 64 * b + 64))
+        _, _, ewb = oracle.gate_bwd(f64(x)[sl], kv64[sl], f64(w), saved[sl], f64(g)[sl], clamp=clamp)
+        check_f32(f"grad_w_partial[{b}]", part[b], ewb)
+    check_f32("sum of grad_w_partial", part.sum(axis=0), ew)
+    return out
+
+
+@pytest.mark.parametrize("N,H,seed", [(1, 8, 0), (37, 64, 1), (64, 1000, 2), (130, 1024, 3),
+                                      (70, 5120, 4), (65, 7168, 5), (3, 3000, 6)])
+def test_sep_parity(N, H, seed):
+    run(N, H, seed)
+
+
+def test_sep_scales_eps_and_clamp():
+    run(96, 512, 7, sigma="loguniform")
+    run(64, 256, 8, eps=1e-6)
+    # tiny weights put every dot under a 1e-2 clamp: sq = +-0.1, zero derivative
+    run(64, 128, 9, clamp=1e-2, w_scale=1e-6)
+
+
+def test_sep_save_off_is_bit_identical():
+    inp, k, v = split_inputs(50, 2048, 10)
+    x, w = inp["x"].cuda(), inp["weight"].cuda()
+    k, v = k.cuda(), v.cuda()
+    a = eg.gate_sep_forward(x, k, v, w, save=True)[0]
+    b = eg.gate_sep_forward(x, k, v, w, save=False)[0]
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_sep_matches_packed_entry_points_at_5120():
+    """At H = 5120 the separate layout gives bit-identical results to the
+    packed one (same arithmetic, same order)."""
+    N = 128
+    inp, k, v = split_inputs(N, 5120, 11)
+    d = {n: t.cuda() for n, t in (("x", inp["x"]), ("kv", inp["kv"]), ("w", inp["weight"]),
+                                  ("g", inp["grad_out"]), ("k", k), ("v", v))}
+    out, saved = eg.gate_forward(d["x"], d["kv"], d["w"])
+    gx, gkv, gw = eg.gate_backward(d["x"], d["kv"], d["w"], saved, d["g"])
+    out2, dot, gate, rx, rk = eg.gate_sep_forward(d["x"], d["k"], d["v"], d["w"])
+    gx2, gk2, gv2, gwp = eg.gate_sep_backward(d["g"], d["x"], d["k"], d["v"], d["w"], dot, gate, rx, rk)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(saved[..., 0], gate) and torch.equal(saved[..., 1], dot)
+    assert torch.equal(gx.view(torch.int16), gx2.view(torch.int16))
+    assert torch.equal(gkv[:, :4 * 5120].view(torch.int16), gk2.reshape(N, -1).view(torch.int16))
+    assert torch.equal(gkv[:, 4 * 5120:].view(torch.int16), gv2.view(torch.int16))
+    # grad_w: 64-token partials summed in fp32 here vs the compensated merge of
+    # 128-token pairs there; equal to fp32 rounding of sums of that magnitude
+    assert torch.allclose(gwp.sum(0), gw, rtol=1e-5, atol=1e-6 * float(gw.abs().max()))
+
+
+def test_sep_graph_capture():
+    inp, k, v = split_inputs(64, 1536, 12)
+    x, w, g = inp["x"].cuda(), inp["weight"].cuda(), inp["grad_out"].cuda()
+    k, v = k.cuda(), v.cuda()
+    out = torch.empty_like(x)
+    sv = [torch.empty((64, 4), device="cuda") for _ in range(4)]
+    gx, gk, gv = torch.empty_like(x), torch.empty_like(k), torch.empty_like(v)
+    gwp = torch.empty((1, 4, 1536), device="cuda")
+    ws = torch.empty(eg.engram_gate_sep_bwd_workspace_size(64), device="cuda", dtype=torch.uint8)
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        eg.engram_gate_sep_fwd(x, k, v, w, out, *sv, stream=s)
+        eg.engram_gate_sep_bwd(g, x, k, v, w, *sv, gx, gk, gv, gwp, ws, stream=s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=s):
+            eg.engram_gate_sep_fwd(x, k, v, w, out, *sv, stream=s)
+            eg.engram_gate_sep_bwd(g, x, k, v, w, *sv, gx, gk, gv, gwp, ws, stream=s)
+    ref = [t.clone() for t in (out, gx, gk, gv, gwp)]
+    for t in (out, gx, gk, gv, gwp):
+        t.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip((out, gx, gk, gv, gwp), ref):
+        assert torch.equal(a, b)
