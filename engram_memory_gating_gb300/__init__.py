@@ -31,7 +31,8 @@ __all__ = [
     "engram_device_error", "engram_launch_info", "engram_gate_bwd_noalloc",
     "engram_gate_sep_fwd", "engram_gate_sep_bwd", "engram_gate_sep_bwd_workspace_size",
     "gate_forward", "gate_backward", "gateconv_forward", "gateconv_backward",
-    "gate_sep_forward", "gate_sep_backward",
+    "gate_sep_forward", "gate_sep_backward", "engram_fused_weight", "engram_fused_weight_bwd",
+    "fused_weight", "fused_weight_backward",
     "GATE_EPS", "GATE_CLAMP", "GATECONV_EPS", "EXPORTED_SYMBOLS",
 ]
 
@@ -46,7 +47,7 @@ EXPORTED_SYMBOLS = (
     "engram_gate_bwd", "engram_gateconv_fwd", "engram_gateconv_bwd_workspace_size",
     "engram_gateconv_bwd", "engram_device_error", "engram_launch_info",
     "engram_gate_bwd_noalloc", "engram_gate_sep_fwd", "engram_gate_sep_bwd_workspace_size",
-    "engram_gate_sep_bwd",
+    "engram_gate_sep_bwd", "engram_fused_weight", "engram_fused_weight_bwd",
 )
 
 _STATUS = {0: "ok", 1: "null pointer", 2: "misaligned pointer", 3: "size out of range",
@@ -99,6 +100,8 @@ def load(path: str | None = None):
         lib.engram_gate_sep_bwd_workspace_size.argtypes = [I64]
         lib.engram_gate_sep_bwd_workspace_size.restype = SZ
         lib.engram_gate_sep_bwd.argtypes = [P] * 14 + [SZ, I64, I64, F, P]
+        lib.engram_fused_weight.argtypes = [P, P, P, I64, P]
+        lib.engram_fused_weight_bwd.argtypes = [P, I64, P, P, P, P, P, I64, P]
         lib.engram_gateconv_fwd.argtypes = [P] * 12 + [I64, I64, I64, F, P]
         lib.engram_gateconv_bwd_workspace_size.argtypes = [I64, I64, I64]
         lib.engram_gateconv_bwd_workspace_size.restype = SZ
@@ -107,7 +110,8 @@ def load(path: str | None = None):
         lib.engram_launch_info.argtypes = [ctypes.c_int, I64, I64, I64,
                                            ctypes.POINTER(_LaunchInfo)]
         for name in ("engram_gate_fwd", "engram_gate_bwd", "engram_gate_bwd_noalloc",
-                     "engram_gate_sep_fwd", "engram_gate_sep_bwd", "engram_gateconv_fwd",
+                     "engram_gate_sep_fwd", "engram_gate_sep_bwd", "engram_fused_weight",
+                     "engram_fused_weight_bwd", "engram_gateconv_fwd",
                      "engram_gateconv_bwd", "engram_device_error", "engram_launch_info"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -229,6 +233,27 @@ def engram_gate_sep_bwd(grad_out, x, k, v, weight, dot, gate, rstd_x, rstd_k, gr
         _ptr(workspace), nbytes, N, H, float(clamp), _stream(stream)))
 
 
+def engram_fused_weight(wh, we, weight, stream=None):
+    n = wh.numel()
+    _need(wh, torch.bfloat16, tuple(wh.shape), "wh")
+    _need(we, torch.bfloat16, tuple(wh.shape), "we")
+    _need(weight, torch.float32, tuple(wh.shape), "weight")
+    _check("engram_fused_weight", load().engram_fused_weight(_ptr(wh), _ptr(we), _ptr(weight), n,
+                                                             _stream(stream)))
+
+
+def engram_fused_weight_bwd(grad_w_partial, wh, we, grad_w, grad_wh, grad_we, stream=None):
+    """grad_w_partial (nblocks, *wh.shape); grad_w may be None."""
+    n = wh.numel()
+    nblocks = grad_w_partial.numel() // n
+    _need(grad_w_partial, torch.float32, (nblocks,) + tuple(wh.shape), "grad_w_partial")
+    for t, nm in ((grad_wh, "grad_wh"), (grad_we, "grad_we")) + (((grad_w, "grad_w"),) if grad_w is not None else ()):
+        _need(t, torch.float32, tuple(wh.shape), nm)
+    _check("engram_fused_weight_bwd", load().engram_fused_weight_bwd(
+        _ptr(grad_w_partial), nblocks, _ptr(wh), _ptr(we), _ptr(grad_w), _ptr(grad_wh), _ptr(grad_we),
+        n, _stream(stream)))
+
+
 def engram_gateconv_fwd(H, k, v, rms_w_h, rms_w_v, conv_w, Y, vhat, alpha, rrms_h, rrms_k,
                         rrms_v, eps: float = GATECONV_EPS, stream=None):
     M, T, d = H.shape
@@ -320,6 +345,20 @@ def gate_sep_backward(grad_out, x, k, v, weight, dot, gate, rstd_x, rstd_k,
     engram_gate_sep_bwd(grad_out, x, k, v, weight, dot, gate, rstd_x, rstd_k, gx, gk, gv, gwp, ws,
                         clamp=clamp)
     return gx, gk, gv, gwp
+
+
+def fused_weight(wh, we):
+    """fp32 (4, H) fused weight wh * we from bf16 (4, H) weights."""
+    w = torch.empty(wh.shape, device=wh.device, dtype=torch.float32)
+    engram_fused_weight(wh, we, w)
+    return w
+
+
+def fused_weight_backward(grad_w_partial, wh, we):
+    """Returns (grad_w, grad_wh, grad_we) from per-block grad_w partials."""
+    out = [torch.empty(wh.shape, device=wh.device, dtype=torch.float32) for _ in range(3)]
+    engram_fused_weight_bwd(grad_w_partial, wh, we, *out)
+    return tuple(out)
 
 
 def gateconv_forward(H, k, v, rms_w_h, rms_w_v, conv_w, eps: float = GATECONV_EPS):

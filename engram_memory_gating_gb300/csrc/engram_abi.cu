@@ -594,6 +594,52 @@ engram_status_t engram_gate_sep_bwd(const void* grad_out, const void* x, const v
     return launch_status(gate_bwd_launch(p, c, stream));
 }
 
+engram_status_t engram_fused_weight(const void* wh, const void* we, float* weight, int64_t n,
+                                    cudaStream_t stream) {
+    if (!wh || !we || !weight) return ENGRAM_ERR_NULL;
+    if (n < 1 || n > (int64_t(1) << 40)) return ENGRAM_ERR_SHAPE;
+    if (!aligned16(wh) || !aligned16(we) || !aligned16(weight)) return ENGRAM_ERR_ALIGN;
+    const size_t m = static_cast<size_t>(n);
+    const Range ins[] = {{wh, m * 2}, {we, m * 2}};
+    const Range outs[] = {{weight, m * 4}};
+    if (any_overlap(outs, 1, ins, 2)) return ENGRAM_ERR_OVERLAP;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!device_state()) return ENGRAM_ERR_DEVICE;
+    FusedWeightParams p = {};
+    p.wh = static_cast<const uint16_t*>(wh);
+    p.we = static_cast<const uint16_t*>(we);
+    p.weight = weight;
+    p.n = n;
+    return launch_status(fused_weight_launch(p, stream));
+}
+
+engram_status_t engram_fused_weight_bwd(const float* grad_w_partial, int64_t nblocks,
+                                        const void* wh, const void* we, float* grad_w,
+                                        float* grad_wh, float* grad_we, int64_t n,
+                                        cudaStream_t stream) {
+    if (!grad_w_partial || !wh || !we || !grad_wh || !grad_we) return ENGRAM_ERR_NULL;
+    if (n < 1 || nblocks < 1 || n > (int64_t(1) << 40) / nblocks) return ENGRAM_ERR_SHAPE;
+    if (!aligned16(grad_w_partial) || !aligned16(wh) || !aligned16(we) || !aligned16(grad_wh) ||
+        !aligned16(grad_we) || (grad_w && !aligned16(grad_w)))
+        return ENGRAM_ERR_ALIGN;
+    const size_t m = static_cast<size_t>(n);
+    const Range ins[] = {{grad_w_partial, m * static_cast<size_t>(nblocks) * 4}, {wh, m * 2}, {we, m * 2}};
+    const Range outs[] = {{grad_w, grad_w ? m * 4 : 0}, {grad_wh, m * 4}, {grad_we, m * 4}};
+    if (any_overlap(outs, 3, ins, 3)) return ENGRAM_ERR_OVERLAP;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!device_state()) return ENGRAM_ERR_DEVICE;
+    FusedWeightParams p = {};
+    p.wh = static_cast<const uint16_t*>(wh);
+    p.we = static_cast<const uint16_t*>(we);
+    p.partial = grad_w_partial;
+    p.grad_w = grad_w;
+    p.grad_wh = grad_wh;
+    p.grad_we = grad_we;
+    p.n = n;
+    p.nblocks = nblocks;
+    return launch_status(fused_weight_bwd_launch(p, stream));
+}
+
 size_t engram_gateconv_bwd_workspace_size(int64_t M, int64_t T, int64_t d) {
     if (!gc_shape_ok(M, T, d)) return 0;
     return static_cast<size_t>(gc_bwd_slots(M, T)) * 6 * static_cast<size_t>(d) * 4;

@@ -124,6 +124,20 @@ struct GateConvBwdParams {
     float inv_sqrt_d;
 };
 
+// Fused weight of the gate (forward: weight = wh * we) and its backward
+// (grad_w = sum over nblocks partials of n values each; grad_wh, grad_we).
+struct FusedWeightParams {
+    const uint16_t* wh;
+    const uint16_t* we;
+    float* weight;
+    const float* partial;
+    float* grad_w;
+    float* grad_wh;
+    float* grad_we;
+    long long n;
+    long long nblocks;
+};
+
 struct LaunchCfg {
     int cluster;
     int threads;
@@ -144,6 +158,9 @@ cudaError_t gate_bwd_prepare(int smem_bytes);
 cudaError_t gate_bwd_max_clusters(int cluster, int threads, int smem, int* out);
 cudaError_t gate_bwd_launch(const GateBwdParams& p, const LaunchCfg& c, cudaStream_t s);
 cudaError_t gate_wreduce_launch(const GateWReduceParams& p, cudaStream_t s);
+
+cudaError_t fused_weight_launch(const FusedWeightParams& p, cudaStream_t s);
+cudaError_t fused_weight_bwd_launch(const FusedWeightParams& p, cudaStream_t s);
 
 cudaError_t gateconv_fwd_prepare(int smem_bytes);
 cudaError_t gateconv_fwd_max_clusters(int cluster, int threads, int smem, int* out);

@@ -180,6 +180,28 @@ engram_status_t engram_gate_sep_bwd(const void* grad_out, const void* x, const v
                                     float clamp, cudaStream_t stream);
 
 /*
+ * Fused weight of the gate and its gradients (cuDNN "Engram saved-state
+ * gate", semantics paragraph: the weight is the FP32 product of the query-
+ * and key-side normalisation weights; tile-kernels engram tests).
+ * engram_fused_weight: weight[i] = wh[i] * we[i] (exact in fp32).
+ * engram_fused_weight_bwd: grad_w[i] = sum over b < nblocks of
+ *   grad_w_partial[b * n + i] (fixed order, error-free additions), then
+ *   grad_wh[i] = grad_w[i] * we[i] and grad_we[i] = grad_w[i] * wh[i].
+ *   grad_w may be NULL.  grad_w_partial is the output of engram_gate_sep_bwd
+ *   (nblocks = ceil(N/64), n = 4 H), or a single block (nblocks = 1) holding
+ *   engram_gate_bwd's grad_weight.
+ *   wh, we  bf16 (n); weight, grad_w, grad_wh, grad_we fp32 (n); all 16-byte
+ *   aligned; 1 <= n, 1 <= nblocks, nblocks * n < 2^40; outputs must not
+ *   overlap anything.  Asynchronous on `stream`, no allocation.
+ */
+engram_status_t engram_fused_weight(const void* wh, const void* we, float* weight, int64_t n,
+                                    cudaStream_t stream);
+engram_status_t engram_fused_weight_bwd(const float* grad_w_partial, int64_t nblocks,
+                                        const void* wh, const void* we, float* grad_w,
+                                        float* grad_wh, float* grad_we, int64_t n,
+                                        cudaStream_t stream);
+
+/*
  * GateConv, forward (TileOPs "Engram Operators", EngramGateConvFwdOp).
  *   H, k, v   bf16 (M, T, d)   hidden states, key and value projections
  *   rms_w_h   fp32 (d)         RMSNorm weight shared by H and k

@@ -73,8 +73,10 @@ def _load():
                                                 P, P, P, P, P, P]
             lib.oracle_gateconv_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P,
                                                 I64, I64, I64, P, P, P, P, P, P]
-            for f in (lib.oracle_gate_fwd, lib.oracle_gate_bwd,
-                      lib.oracle_gateconv_fwd, lib.oracle_gateconv_bwd):
+            lib.oracle_fused_weight.argtypes = [P, P, I64, P]
+            lib.oracle_fused_weight_bwd.argtypes = [P, I64, P, P, I64, P, P, P]
+            for f in (lib.oracle_gate_fwd, lib.oracle_gate_bwd, lib.oracle_fused_weight,
+                      lib.oracle_fused_weight_bwd, lib.oracle_gateconv_fwd, lib.oracle_gateconv_bwd):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -151,6 +153,29 @@ def gate_bwd(x, kv, w, saved, grad_out, clamp: float = GATE_CLAMP):
     if rc != 0:
         raise ValueError("oracle_gate_bwd: bad shape")
     return gx, gkv, gw
+
+
+def fused_weight(wh, we):
+    """The gate's fused weight wh * we (fp64; exact for bf16 inputs)."""
+    wh = _f64(wh)
+    we = _f64(we).reshape(wh.shape)
+    out = np.empty_like(wh)
+    if _load().oracle_fused_weight(_p(wh), _p(we), wh.size, _p(out)) != 0:
+        raise ValueError("oracle_fused_weight: bad shape")
+    return out
+
+
+def fused_weight_bwd(partial, wh, we):
+    """partial (B, ...) per-block grad_weight; returns (grad_w, grad_wh, grad_we)
+    with grad_w = sum over blocks and the product rule for wh, we."""
+    wh = _f64(wh)
+    we = _f64(we).reshape(wh.shape)
+    pa = _f64(partial).reshape((-1,) + wh.shape)
+    gw, gwh, gwe = np.empty_like(wh), np.empty_like(wh), np.empty_like(wh)
+    if _load().oracle_fused_weight_bwd(_p(pa), pa.shape[0], _p(wh), _p(we), wh.size, _p(gw),
+                                       _p(gwh), _p(gwe)) != 0:
+        raise ValueError("oracle_fused_weight_bwd: bad shape")
+    return gw, gwh, gwe
 
 
 def gateconv_fwd(H, k, v, rms_w_h, rms_w_v, conv_w, eps: float = GATECONV_EPS):

@@ -268,6 +268,33 @@ int oracle_gate_bwd(const double* x, const double* kv, const double* w,
 // the conv has dilation 1 and no bias; tap 3 multiplies the current token.
 // Outputs are exact fp64; Y and vhat are rounded to bf16 by the caller.
 // ---------------------------------------------------------------------------
+// Fused weight of the gate: the product of the two bf16 normalisation weights
+// of the query and key sides (cuDNN Frontend "Engram saved-state gate",
+// semantics paragraph: the fused weight is their FP32 product; tile-kernels
+// engram fused-weight test).  weight[i] = wh[i] * we[i].
+int oracle_fused_weight(const double* wh, const double* we, int64_t n, double* weight) {
+    if (n < 0) return 1;
+    for (int64_t i = 0; i < n; ++i) weight[i] = wh[i] * we[i];
+    return 0;
+}
+
+// Gradients of the two weights from per-block grad_weight partials (tile-kernels
+// engram backward test): grad_w = sum over blocks, then the product rule
+// grad_wh = grad_w * we, grad_we = grad_w * wh.
+int oracle_fused_weight_bwd(const double* partial, int64_t nblocks, const double* wh,
+                            const double* we, int64_t n, double* grad_w, double* grad_wh,
+                            double* grad_we) {
+    if (n < 0 || nblocks < 0) return 1;
+    for (int64_t i = 0; i < n; ++i) {
+        double g = 0.0;
+        for (int64_t b = 0; b < nblocks; ++b) g += partial[b * n + i];
+        grad_w[i] = g;
+        grad_wh[i] = g * we[i];
+        grad_we[i] = g * wh[i];
+    }
+    return 0;
+}
+
 int oracle_gateconv_fwd(const double* H, const double* k, const double* v,
                         const double* wh, const double* wv, const double* cw,
                         int64_t M, int64_t T, int64_t d, double eps, double* Y,

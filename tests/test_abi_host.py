@@ -181,3 +181,15 @@ def test_gate_sep_validation_and_workspace():
     ov = list(b14)
     ov[12] = b14[0]                            # grad_w_partial aliases grad_out
     assert bwd(ov) == EOVERLAP
+
+
+def test_fused_weight_validation():
+    lib = eg.load()
+    assert lib.engram_fused_weight(None, p(A), p(2 * A), 64, None) == ENULL
+    assert lib.engram_fused_weight(p(A), p(2 * A), p(3 * A), 0, None) == ESHAPE
+    assert lib.engram_fused_weight(p(A + 2), p(2 * A), p(3 * A), 64, None) == EALIGN
+    assert lib.engram_fused_weight(p(A), p(2 * A), p(A + 16), 64, None) == EOVERLAP
+    bwd = lib.engram_fused_weight_bwd
+    assert bwd(p(A), 1, p(2 * A), p(3 * A), None, None, p(5 * A), 64, None) == ENULL
+    assert bwd(p(A), 0, p(2 * A), p(3 * A), None, p(4 * A), p(5 * A), 64, None) == ESHAPE
+    assert bwd(p(A), 2, p(2 * A), p(3 * A), None, p(A + 256), p(5 * A), 64, None) == EOVERLAP

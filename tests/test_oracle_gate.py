@@ -296,3 +296,32 @@ def test_saturated_gate_keeps_its_derivative_through_fp32_saved_state():
              (r64[1][:, 4 * d:], r32[1][:, 4 * d:]), (r64[2], r32[2])]
     for a, b in pairs:
         assert np.max(np.abs(a - b)) <= 2e-6 * np.max(np.abs(a))
+
+
+def test_fused_weight_is_the_exact_product():
+    # products of bf16 values are exact in fp64; compare with rational arithmetic
+    from fractions import Fraction
+    rng = np.random.default_rng(31)
+    wh = oracle.bf16_to_f64(oracle.round_bf16(rng.standard_normal(64)))
+    we = oracle.bf16_to_f64(oracle.round_bf16(3.0 * rng.standard_normal(64)))
+    got = oracle.fused_weight(wh, we)
+    for a, b, c in zip(wh, we, got):
+        assert Fraction(c) == Fraction(a) * Fraction(b)
+
+
+def test_fused_weight_bwd_sums_blocks_and_applies_the_product_rule():
+    # per-block partials of the gate's grad_w, summed and pushed through
+    # w = wh * we, give the derivatives of the loss in wh and we (differences)
+    rng, x, kv, _ = _safe_case(6, 6, 4, 16)
+    wh = 1.0 + 0.3 * rng.standard_normal((4, 16))
+    we = 1.0 + 0.3 * rng.standard_normal((4, 16))
+    g = rng.standard_normal((6, 4, 16))
+    w = oracle.fused_weight(wh, we)
+    _, saved = oracle.gate_fwd(x, kv, w)
+    parts = np.stack([oracle.gate_bwd(x[b:b + 2], kv[b:b + 2], w, saved[b:b + 2], g[b:b + 2])[2]
+                      for b in range(0, 6, 2)])
+    gw, gwh, gwe = oracle.fused_weight_bwd(parts, wh, we)
+    _, _, gw_all = oracle.gate_bwd(x, kv, w, saved, g)
+    assert np.allclose(gw, gw_all, rtol=1e-13, atol=1e-15)
+    _fd_check(lambda: _loss(x, kv, oracle.fused_weight(wh, we), g), wh, gwh)
+    _fd_check(lambda: _loss(x, kv, oracle.fused_weight(wh, we), g), we, gwe)
