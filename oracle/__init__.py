@@ -74,8 +74,10 @@ def _load():
             lib.oracle_gateconv_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P,
                                                 I64, I64, I64, P, P, P, P, P, P]
             lib.oracle_fused_weight.argtypes = [P, P, I64, P]
+            lib.oracle_decode_fwd.argtypes = [P, P, P, I64, P, P, P, P, P, I64, I64, I64, I64, I64,
+                                              I64, D, P, P]
             lib.oracle_fused_weight_bwd.argtypes = [P, I64, P, P, I64, P, P, P]
-            for f in (lib.oracle_gate_fwd, lib.oracle_gate_bwd, lib.oracle_fused_weight,
+            for f in (lib.oracle_gate_fwd, lib.oracle_gate_bwd, lib.oracle_fused_weight, lib.oracle_decode_fwd,
                       lib.oracle_fused_weight_bwd, lib.oracle_gateconv_fwd, lib.oracle_gateconv_bwd):
                 f.restype = ctypes.c_int
             _lib = lib
@@ -229,3 +231,32 @@ def gateconv_bwd(dY, H, k, v, rms_w_h, rms_w_v, conv_w, vhat, alpha, rrms_h, rrm
     if rc != 0:
         raise ValueError("oracle_gateconv_bwd: bad shape")
     return dH, dk, dv, dwh, dwv, dcw
+
+
+def decode_fwd(e, h, conv_state, W_K, W_V, rms_w_h, rms_w_v, conv_w, max_len: int, dilation: int,
+               eps: float = GATECONV_EPS):
+    """GateConv decode step in fp64.
+
+    e (B,d_mem), h (B,d), conv_state (B,L,d) with L <= max_len, W_K, W_V (d_mem,d),
+    rms_w_h, rms_w_v (d,), conv_w (w,d).  Returns y (B,d) and new_state
+    (B,max_len,d), exact (the last state row is this token's exact u).
+    """
+    e = _f64(e)
+    B, dmem = e.shape
+    h = _f64(h).reshape(B, -1)
+    d = h.shape[1]
+    st = _f64(conv_state).reshape(B, -1, d)
+    L = st.shape[1]
+    WK = _f64(W_K).reshape(dmem, d)
+    WV = _f64(W_V).reshape(dmem, d)
+    wh = _f64(rms_w_h).reshape(d)
+    wv = _f64(rms_w_v).reshape(d)
+    cw = _f64(conv_w).reshape(-1, d)
+    y = np.empty((B, d))
+    ns = np.empty((B, max_len, d))
+    rc = _load().oracle_decode_fwd(_p(e), _p(h), _p(st), L, _p(WK), _p(WV), _p(wh), _p(wv), _p(cw),
+                                   B, dmem, d, int(max_len), cw.shape[0], int(dilation), float(eps),
+                                   _p(y), _p(ns))
+    if rc != 0:
+        raise ValueError("oracle_decode_fwd: bad shape")
+    return y, ns

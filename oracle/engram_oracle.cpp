@@ -469,4 +469,85 @@ int oracle_gateconv_bwd(const double* dY, const double* H, const double* k,
     return 0;
 }
 
+// GateConv decode, one token (TileOPs "Engram Operators", Decode section,
+// EngramDecodeFwdOp: GEMV projection + gating + dilated conv + SiLU with a
+// conv_state cache).  The page gives the interface only; this follows the
+// readings of the GateConv forward above:
+//   k = e W_K, v = e W_V                       (d_mem -> d, no bias)
+//   alpha = sigmoid(sum (h rrms_h w_h)(k rrms_k w_h) / sqrt(d)),  vhat = alpha v
+//   u = vhat rrms_v w_v,  rrms_v = 1/sqrt(mean(vhat^2) + eps)
+//   c = sum_{j<w} conv_w[j] u_{t - (w-1-j) dil}   (u_t this token's u; older u
+//       from conv_state, oldest first, most recent last; 0 beyond its L rows)
+//   y = SiLU(c) + vhat
+//   new_state = the last max_len rows of [0 (max_len - L rows), conv_state, u_t]
+// e (B,d_mem), h (B,d), state (B,L,d), W_K, W_V (d_mem,d), w_h, w_v (d),
+// conv_w (w,d); outputs y (B,d) and new_state (B,max_len,d) exact (the caller
+// rounds; the stored u_t of a real cache is its bf16 rounding).
+int oracle_decode_fwd(const double* e, const double* h, const double* state, int64_t L,
+                      const double* WK, const double* WV, const double* wh, const double* wv,
+                      const double* cw, int64_t B, int64_t dmem, int64_t d, int64_t max_len,
+                      int64_t w, int64_t dil, double eps, double* y, double* new_state) {
+    if (B < 0 || dmem < 1 || d < 1 || L < 0 || max_len < 1 || L > max_len || w < 1 || dil < 1) return 1;
+    const double sqrt_d = std::sqrt(static_cast<double>(d));
+    std::vector<double> k(static_cast<size_t>(d)), v(static_cast<size_t>(d)), u(static_cast<size_t>(d));
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t i = 0; i < d; ++i) {
+            double sk = 0.0, sv = 0.0;
+            for (int64_t m = 0; m < dmem; ++m) {
+                sk += e[b * dmem + m] * WK[m * d + i];
+                sv += e[b * dmem + m] * WV[m * d + i];
+            }
+            k[static_cast<size_t>(i)] = sk;
+            v[static_cast<size_t>(i)] = sv;
+        }
+        double mh = 0.0, mk = 0.0;
+        for (int64_t i = 0; i < d; ++i) {
+            mh += h[b * d + i] * h[b * d + i];
+            mk += k[static_cast<size_t>(i)] * k[static_cast<size_t>(i)];
+        }
+        const double rh = 1.0 / std::sqrt(mh / static_cast<double>(d) + eps);
+        const double rk = 1.0 / std::sqrt(mk / static_cast<double>(d) + eps);
+        double z = 0.0;
+        for (int64_t i = 0; i < d; ++i)
+            z += (h[b * d + i] * rh * wh[i]) * (k[static_cast<size_t>(i)] * rk * wh[i]);
+        z /= sqrt_d;
+        const double alpha = sigmoid(z);
+        double mv = 0.0;
+        for (int64_t i = 0; i < d; ++i) {
+            const double vh = alpha * v[static_cast<size_t>(i)];
+            mv += vh * vh;
+        }
+        const double rv = 1.0 / std::sqrt(mv / static_cast<double>(d) + eps);
+        for (int64_t i = 0; i < d; ++i) {
+            const double vh = alpha * v[static_cast<size_t>(i)];
+            u[static_cast<size_t>(i)] = vh * rv * wv[i];
+            double c = 0.0;
+            for (int64_t j = 0; j < w; ++j) {
+                const int64_t lag = (w - 1 - j) * dil;   // 0: this token
+                double uj = 0.0;
+                if (lag == 0)
+                    uj = u[static_cast<size_t>(i)];
+                else if (lag <= L)
+                    uj = state[(b * L + (L - lag)) * d + i];
+                c += cw[j * d + i] * uj;
+            }
+            y[b * d + i] = c * sigmoid(c) + vh;
+        }
+        // shift by one token: row r of the new state is row r + 1 of the old
+        // state left-padded to max_len rows; the last row is u_t
+        for (int64_t r = 0; r < max_len; ++r) {
+            const int64_t src = r + 1 - (max_len - L);   // row of the old state
+            for (int64_t i = 0; i < d; ++i) {
+                double val = 0.0;
+                if (r == max_len - 1)
+                    val = u[static_cast<size_t>(i)];
+                else if (src >= 0 && src < L)
+                    val = state[(b * L + src) * d + i];
+                new_state[(b * max_len + r) * d + i] = val;
+            }
+        }
+    }
+    return 0;
+}
+
 }  // extern "C"
