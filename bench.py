@@ -209,6 +209,34 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
                                                N * (44 * H + 64) + 16 * H + (N // 64) * 16 * H, peak)
     del inp, k, v, out, sv, gx, gk, gv, gwp, ws, gf, gb
     torch.cuda.empty_cache()
+    # GateConv decode step, B = 8, d_mem = 1024, d = 4096, full cache of 16, w = 4, dilation 3;
+    # L2 flushed before every timed replay (the weights would otherwise stay resident)
+    B, dm, d, L, w, dil = 8, 1024, 4096, 16, 4, 3
+    di = inputs_mod.decode_inputs(B, dm, d, L, w, seed=107, device="cuda")
+    y = torch.empty_like(di["h"])
+    ns = torch.empty((B, L, d), device="cuda", dtype=torch.bfloat16)
+    ws = torch.empty(eg.engram_decode_workspace_size(B, dm, d), device="cuda", dtype=torch.uint8)
+    f = lambda: eg.engram_decode_fwd(di["e"], di["h"], di["conv_state"], di["W_K"], di["W_V"],
+                                     di["rms_w_h"], di["rms_w_v"], di["conv_w"], y, ns, ws, dil, stream=s)
+    gd = graph_of(torch, f, s)
+    flush = torch.ones(64 << 20, device="cuda", dtype=torch.float32)
+    total = 0.0
+    reps = 20
+    with torch.cuda.stream(s):
+        for r in range(reps + 3):
+            flush.sum()  # reads 256 MB: L2 holds clean flush lines, not the weights
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            gd.replay()
+            e1.record(s)
+            e1.synchronize()
+            if r >= 3:
+                total += e0.elapsed_time(e1)
+    nbytes = 2 * dm * d * 2 + B * dm * 2 + B * d * 2 + B * L * d * 2 + d * 4 * (2 + w) + B * d * 2 + B * L * d * 2
+    ops["decode_B8_dmem1024_d4096"] = op_entry(total / reps, nbytes, peak)
+    ops["decode_B8_dmem1024_d4096"]["us"] = round(1000 * total / reps, 2)
+    del di, y, ns, ws, gd, flush
+    torch.cuda.empty_cache()
     # GateConv, two configurations
     for (M, T, d, hs, vs, name) in ((4, 4096, 4096, 1.0, 1.0, "gateconv_M4_T4096_d4096"),
                                     (8, 8192, 7168, 10.0, 0.1 ** 0.5, "gateconv_M8_T8192_d7168")):

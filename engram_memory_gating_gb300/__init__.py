@@ -32,7 +32,8 @@ __all__ = [
     "engram_gate_sep_fwd", "engram_gate_sep_bwd", "engram_gate_sep_bwd_workspace_size",
     "gate_forward", "gate_backward", "gateconv_forward", "gateconv_backward",
     "gate_sep_forward", "gate_sep_backward", "engram_fused_weight", "engram_fused_weight_bwd",
-    "fused_weight", "fused_weight_backward",
+    "fused_weight", "fused_weight_backward", "engram_decode_fwd", "engram_decode_workspace_size",
+    "decode_forward",
     "GATE_EPS", "GATE_CLAMP", "GATECONV_EPS", "EXPORTED_SYMBOLS",
 ]
 
@@ -48,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "engram_gateconv_bwd", "engram_device_error", "engram_launch_info",
     "engram_gate_bwd_noalloc", "engram_gate_sep_fwd", "engram_gate_sep_bwd_workspace_size",
     "engram_gate_sep_bwd", "engram_fused_weight", "engram_fused_weight_bwd",
+    "engram_decode_workspace_size", "engram_decode_fwd",
 )
 
 _STATUS = {0: "ok", 1: "null pointer", 2: "misaligned pointer", 3: "size out of range",
@@ -101,6 +103,9 @@ def load(path: str | None = None):
         lib.engram_gate_sep_bwd_workspace_size.restype = SZ
         lib.engram_gate_sep_bwd.argtypes = [P] * 14 + [SZ, I64, I64, F, P]
         lib.engram_fused_weight.argtypes = [P, P, P, I64, P]
+        lib.engram_decode_workspace_size.argtypes = [I64, I64, I64]
+        lib.engram_decode_workspace_size.restype = SZ
+        lib.engram_decode_fwd.argtypes = [P, P, P, I64] + [P] * 8 + [SZ, I64, I64, I64, I64, I64, I64, F, P]
         lib.engram_fused_weight_bwd.argtypes = [P, I64, P, P, P, P, P, I64, P]
         lib.engram_gateconv_fwd.argtypes = [P] * 12 + [I64, I64, I64, F, P]
         lib.engram_gateconv_bwd_workspace_size.argtypes = [I64, I64, I64]
@@ -111,7 +116,7 @@ def load(path: str | None = None):
                                            ctypes.POINTER(_LaunchInfo)]
         for name in ("engram_gate_fwd", "engram_gate_bwd", "engram_gate_bwd_noalloc",
                      "engram_gate_sep_fwd", "engram_gate_sep_bwd", "engram_fused_weight",
-                     "engram_fused_weight_bwd", "engram_gateconv_fwd",
+                     "engram_fused_weight_bwd", "engram_decode_fwd", "engram_gateconv_fwd",
                      "engram_gateconv_bwd", "engram_device_error", "engram_launch_info"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -254,6 +259,38 @@ def engram_fused_weight_bwd(grad_w_partial, wh, we, grad_w, grad_wh, grad_we, st
         n, _stream(stream)))
 
 
+def engram_decode_workspace_size(B: int, d_mem: int, d: int) -> int:
+    return int(load().engram_decode_workspace_size(int(B), int(d_mem), int(d)))
+
+
+def engram_decode_fwd(e, h, conv_state, W_K, W_V, rms_w_h, rms_w_v, conv_w, y, new_state,
+                      workspace, dilation: int, eps: float = GATECONV_EPS, stream=None):
+    """conv_state (B, L, d) with L <= new_state.shape[1] (None or L = 0 for an
+    empty cache)."""
+    B, d_mem = e.shape
+    d = h.shape[1]
+    max_len = new_state.shape[1]
+    w = conv_w.shape[0]
+    L = 0 if conv_state is None else conv_state.shape[1]
+    _need(e, torch.bfloat16, (B, d_mem), "e")
+    _need(h, torch.bfloat16, (B, d), "h")
+    if conv_state is not None:
+        _need(conv_state, torch.bfloat16, (B, L, d), "conv_state")
+    for t, n in ((W_K, "W_K"), (W_V, "W_V")):
+        _need(t, torch.bfloat16, (d_mem, d), n)
+    _need(rms_w_h, torch.float32, (d,), "rms_w_h")
+    _need(rms_w_v, torch.float32, (d,), "rms_w_v")
+    _need(conv_w, torch.float32, (w, d), "conv_w")
+    _need(y, torch.bfloat16, (B, d), "y")
+    _need(new_state, torch.bfloat16, (B, max_len, d), "new_state")
+    st = conv_state if (conv_state is not None and L > 0) else None
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("engram_decode_fwd", load().engram_decode_fwd(
+        _ptr(e), _ptr(h), _ptr(st), L, _ptr(W_K), _ptr(W_V), _ptr(rms_w_h), _ptr(rms_w_v),
+        _ptr(conv_w), _ptr(y), _ptr(new_state), _ptr(workspace), nbytes, B, d_mem, d, max_len, w,
+        int(dilation), float(eps), _stream(stream)))
+
+
 def engram_gateconv_fwd(H, k, v, rms_w_h, rms_w_v, conv_w, Y, vhat, alpha, rrms_h, rrms_k,
                         rrms_v, eps: float = GATECONV_EPS, stream=None):
     M, T, d = H.shape
@@ -359,6 +396,17 @@ def fused_weight_backward(grad_w_partial, wh, we):
     out = [torch.empty(wh.shape, device=wh.device, dtype=torch.float32) for _ in range(3)]
     engram_fused_weight_bwd(grad_w_partial, wh, we, *out)
     return tuple(out)
+
+
+def decode_forward(e, h, conv_state, W_K, W_V, rms_w_h, rms_w_v, conv_w, max_len: int,
+                   dilation: int, eps: float = GATECONV_EPS):
+    """One decode step: returns y (B, d) and the new cache (B, max_len, d)."""
+    B, d = h.shape
+    y = torch.empty_like(h)
+    ns = torch.empty((B, max_len, d), device=h.device, dtype=torch.bfloat16)
+    ws = torch.empty(engram_decode_workspace_size(B, e.shape[1], d), device=h.device, dtype=torch.uint8)
+    engram_decode_fwd(e, h, conv_state, W_K, W_V, rms_w_h, rms_w_v, conv_w, y, ns, ws, dilation, eps)
+    return y, ns
 
 
 def gateconv_forward(H, k, v, rms_w_h, rms_w_v, conv_w, eps: float = GATECONV_EPS):

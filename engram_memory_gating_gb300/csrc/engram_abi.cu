@@ -59,6 +59,7 @@ struct DeviceState {
     int vals[kCache];
     int n = 0;
     GcCacheEntry gc_last[2];  // forward, backward
+    bool decode_ready = false;
 };
 
 std::mutex g_mu;
@@ -301,6 +302,31 @@ const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
     e.d = d;
     e.g = g;
     return &e.g;
+}
+
+// Decode: d_mem rows per projection split (a multiple of 32, at most 2048)
+// and the number of splits, chosen from the shape alone (the workspace size
+// depends on it): enough CTAs for about two per SM of a 152-SM part.
+void decode_split(int64_t B, int64_t dmem, int64_t d, int& splits, int& rows) {
+    const int64_t tiles = ((d + 127) / 128) * ((B + 7) / 8);
+    int64_t s = (304 + tiles - 1) / tiles;
+    // at least 32 rows per split, and partial sums of at most a quarter of
+    // the weight bytes (splits * B * d * 8 <= 2 * d_mem * d * 2 / 4)
+    int64_t max_s = dmem / 32;
+    const int64_t cap = dmem / (8 * B);
+    if (cap < max_s) max_s = cap;
+    if (s > max_s) s = max_s;
+    if (s < 1) s = 1;
+    int64_t r = (dmem + s - 1) / s;
+    r = (r + 31) / 32 * 32;
+    if (r > 2048) r = 2048;
+    rows = static_cast<int>(r);
+    splits = static_cast<int>((dmem + r - 1) / r);
+}
+
+bool decode_shape_ok(int64_t B, int64_t dmem, int64_t d) {
+    return B >= 1 && B <= 1048560 && dmem >= 8 && dmem <= 65536 && dmem % 8 == 0 && d >= 64 &&
+           d <= 65536 && d % 64 == 0;
 }
 
 }  // namespace
@@ -638,6 +664,74 @@ engram_status_t engram_fused_weight_bwd(const float* grad_w_partial, int64_t nbl
     p.n = n;
     p.nblocks = nblocks;
     return launch_status(fused_weight_bwd_launch(p, stream));
+}
+
+size_t engram_decode_workspace_size(int64_t B, int64_t d_mem, int64_t d) {
+    if (!decode_shape_ok(B, d_mem, d)) return 0;
+    int splits, rows;
+    decode_split(B, d_mem, d, splits, rows);
+    return static_cast<size_t>(2) * splits * static_cast<size_t>(B) * static_cast<size_t>(d) * 4;
+}
+
+engram_status_t engram_decode_fwd(const void* e, const void* h, const void* state, int64_t L,
+                                  const void* W_K, const void* W_V, const float* rms_w_h,
+                                  const float* rms_w_v, const float* conv_w, void* y,
+                                  void* new_state, void* workspace, size_t workspace_bytes,
+                                  int64_t B, int64_t d_mem, int64_t d, int64_t max_len, int64_t w,
+                                  int64_t dilation, float eps, cudaStream_t stream) {
+    if (!e || !h || !W_K || !W_V || !rms_w_h || !rms_w_v || !conv_w || !y || !new_state || !workspace ||
+        (L > 0 && !state))
+        return ENGRAM_ERR_NULL;
+    if (!decode_shape_ok(B, d_mem, d) || w < 1 || w > 64 || dilation < 1 || dilation > (1 << 20) ||
+        max_len < 1 || max_len > 65536 || L < 0 || L > max_len)
+        return ENGRAM_ERR_SHAPE;
+    const void* all[] = {e, h, W_K, W_V, rms_w_h, rms_w_v, conv_w, y, new_state, workspace};
+    for (const void* ptr : all)
+        if (!aligned16(ptr)) return ENGRAM_ERR_ALIGN;
+    if (L > 0 && !aligned16(state)) return ENGRAM_ERR_ALIGN;
+    const size_t need = engram_decode_workspace_size(B, d_mem, d);
+    if (workspace_bytes < need) return ENGRAM_ERR_WORKSPACE;
+    const size_t b = static_cast<size_t>(B), dm = static_cast<size_t>(d_mem), dd = static_cast<size_t>(d);
+    const Range ins[] = {{e, b * dm * 2}, {h, b * dd * 2}, {state, L > 0 ? b * L * dd * 2 : 0},
+                         {W_K, dm * dd * 2}, {W_V, dm * dd * 2}, {rms_w_h, dd * 4}, {rms_w_v, dd * 4},
+                         {conv_w, static_cast<size_t>(w) * dd * 4}};
+    const Range outs[] = {{y, b * dd * 2}, {new_state, b * static_cast<size_t>(max_len) * dd * 2},
+                          {workspace, need}};
+    if (any_overlap(outs, 3, ins, 8)) return ENGRAM_ERR_OVERLAP;
+
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st = device_state();
+    if (!st) return ENGRAM_ERR_DEVICE;
+    if (!st->decode_ready) {
+        if (decode_prepare() != cudaSuccess) {
+            (void)cudaGetLastError();
+            return ENGRAM_ERR_DEVICE;
+        }
+        st->decode_ready = true;
+    }
+    DecodeParams p = {};
+    p.e = static_cast<const uint16_t*>(e);
+    p.h = static_cast<const uint16_t*>(h);
+    p.state = static_cast<const uint16_t*>(state);
+    p.WK = static_cast<const uint16_t*>(W_K);
+    p.WV = static_cast<const uint16_t*>(W_V);
+    p.wh = rms_w_h;
+    p.wv = rms_w_v;
+    p.cw = conv_w;
+    p.y = static_cast<uint16_t*>(y);
+    p.new_state = static_cast<uint16_t*>(new_state);
+    p.part = static_cast<float*>(workspace);
+    p.B = static_cast<int>(B);
+    p.dmem = static_cast<int>(d_mem);
+    p.d = static_cast<int>(d);
+    p.L = static_cast<int>(L);
+    p.max_len = static_cast<int>(max_len);
+    p.w = static_cast<int>(w);
+    p.dil = static_cast<int>(dilation);
+    decode_split(B, d_mem, d, p.splits, p.rows_per_split);
+    p.eps = eps;
+    p.inv_sqrt_d = static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
+    return launch_status(decode_launch(p, stream));
 }
 
 size_t engram_gateconv_bwd_workspace_size(int64_t M, int64_t T, int64_t d) {

@@ -138,6 +138,24 @@ struct FusedWeightParams {
     long long nblocks;
 };
 
+// GateConv decode step (one token per batch row).
+struct DecodeParams {
+    const uint16_t* e;        // (B, dmem) bf16
+    const uint16_t* h;        // (B, d) bf16
+    const uint16_t* state;    // (B, L, d) bf16, may be null when L == 0
+    const uint16_t* WK;       // (dmem, d) bf16
+    const uint16_t* WV;
+    const float* wh;          // (d)
+    const float* wv;          // (d)
+    const float* cw;          // (w, d)
+    uint16_t* y;              // (B, d) bf16
+    uint16_t* new_state;      // (B, max_len, d) bf16
+    float* part;              // workspace: (2, splits, B, d) fp32 partial k, v
+    int B, dmem, d, L, max_len, w, dil;
+    int splits, rows_per_split;
+    float eps, inv_sqrt_d;
+};
+
 struct LaunchCfg {
     int cluster;
     int threads;
@@ -161,6 +179,10 @@ cudaError_t gate_wreduce_launch(const GateWReduceParams& p, cudaStream_t s);
 
 cudaError_t fused_weight_launch(const FusedWeightParams& p, cudaStream_t s);
 cudaError_t fused_weight_bwd_launch(const FusedWeightParams& p, cudaStream_t s);
+
+int decode_proj_smem(int rows_per_split);
+cudaError_t decode_prepare();
+cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);
 
 cudaError_t gateconv_fwd_prepare(int smem_bytes);
 cudaError_t gateconv_fwd_max_clusters(int cluster, int threads, int smem, int* out);

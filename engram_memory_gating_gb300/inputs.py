@@ -131,3 +131,22 @@ def gateconv_inputs_formula(M: int = 2, T: int = 7, d: int = 16) -> dict:
     dY = _formula((M, T, d), 0.41, 0.5, 0.7).to(torch.bfloat16)
     return {"H": H, "k": k, "v": v, "rms_w_h": wh.contiguous(), "rms_w_v": wv.contiguous(),
             "conv_w": cw.contiguous(), "dY": dY}
+
+
+def decode_inputs(B: int, d_mem: int, d: int, L: int, w: int = 4, seed: int = 0, *,
+                  device="cpu") -> dict:
+    """Inputs of one GateConv decode step: e (B,d_mem), h (B,d), conv_state
+    (B,L,d) bf16 ~N(0,1); W_K, W_V (d_mem,d) bf16 ~N(0, 1/d_mem) (so k, v are
+    of unit scale); rms_w_h, rms_w_v = 1 + 0.1 N(0,1); conv_w (w,d) ~N(0, 0.25)."""
+    dev = torch.device(device)
+    g = _gen(dev, seed)
+    e = _randn_bf16((B, d_mem), g, dev)
+    h = _randn_bf16((B, d), g, dev)
+    st = _randn_bf16((B, L, d), g, dev)
+    WK = _randn_bf16((d_mem, d), g, dev, 1.0 / math.sqrt(d_mem))
+    WV = _randn_bf16((d_mem, d), g, dev, 1.0 / math.sqrt(d_mem))
+    wh = (1.0 + 0.1 * torch.randn(d, generator=g, device=dev)).contiguous()
+    wv = (1.0 + 0.1 * torch.randn(d, generator=g, device=dev)).contiguous()
+    cw = (0.5 * torch.randn((w, d), generator=g, device=dev)).contiguous()
+    return {"e": e, "h": h, "conv_state": st, "W_K": WK, "W_V": WV, "rms_w_h": wh, "rms_w_v": wv,
+            "conv_w": cw}

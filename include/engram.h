@@ -257,6 +257,40 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
                                     int64_t T, int64_t d, float eps, cudaStream_t stream);
 
 /*
+ * GateConv decode, one token per batch row (TileOPs "Engram Operators",
+ * Decode section, EngramDecodeFwdOp: GEMV projection + gating + dilated conv
+ * + SiLU with a conv cache).
+ *   e        bf16 (B, d_mem)    gathered N-gram embedding of the token
+ *   h        bf16 (B, d)        hidden state of the token
+ *   state    bf16 (B, L, d)     conv cache: conv inputs u of earlier tokens,
+ *                               oldest first, most recent last; L <= max_len
+ *                               (NULL allowed when L == 0)
+ *   W_K, W_V bf16 (d_mem, d)    key and value projections (k = e W_K, v = e W_V)
+ *   rms_w_h  fp32 (d)           RMSNorm weight of h and k
+ *   rms_w_v  fp32 (d)           RMSNorm weight of the gated value
+ *   conv_w   fp32 (w, d)        depthwise taps; tap j multiplies u at
+ *                               (w-1-j)*dilation tokens back (tap w-1: this token)
+ *   y        bf16 (B, d)        out: SiLU(c) + vhat (the residual to add to h)
+ *   new_state bf16 (B, max_len, d)  out: the cache shifted by one token, this
+ *                               token's u (rounded to bf16) in the last row
+ * with alpha = sigmoid(sum (h rrms_h w_h)(k rrms_k w_h) / sqrt(d)), vhat =
+ * alpha v, u = vhat rrms_v w_v, as in engram_gateconv_fwd; cache rows beyond L
+ * read as zero.  workspace >= engram_decode_workspace_size(B, d_mem, d) bytes.
+ *   1 <= B <= 1048560, 8 <= d_mem <= 65536 with d_mem % 8 == 0,
+ *   64 <= d <= 65536 with d % 64 == 0, 1 <= w <= 64, dilation >= 1,
+ *   1 <= max_len <= 65536, 0 <= L <= max_len.  All pointers 16-byte aligned;
+ *   outputs and workspace must not overlap anything (the new cache is a
+ *   separate buffer).  Asynchronous on `stream`, no allocation.
+ */
+size_t engram_decode_workspace_size(int64_t B, int64_t d_mem, int64_t d);
+engram_status_t engram_decode_fwd(const void* e, const void* h, const void* state, int64_t L,
+                                  const void* W_K, const void* W_V, const float* rms_w_h,
+                                  const float* rms_w_v, const float* conv_w, void* y,
+                                  void* new_state, void* workspace, size_t workspace_bytes,
+                                  int64_t B, int64_t d_mem, int64_t d, int64_t max_len, int64_t w,
+                                  int64_t dilation, float eps, cudaStream_t stream);
+
+/*
  * Saved-state gate, backward, for callers that cannot allocate.  The pages
  * have no counterpart to this entry point.
  *

@@ -193,3 +193,29 @@ def test_fused_weight_validation():
     assert bwd(p(A), 1, p(2 * A), p(3 * A), None, None, p(5 * A), 64, None) == ENULL
     assert bwd(p(A), 0, p(2 * A), p(3 * A), None, p(4 * A), p(5 * A), 64, None) == ESHAPE
     assert bwd(p(A), 2, p(2 * A), p(3 * A), None, p(A + 256), p(5 * A), 64, None) == EOVERLAP
+
+
+def test_decode_validation_and_workspace():
+    lib = eg.load()
+    assert eg.engram_decode_workspace_size(8, 1024, 4096) > 0
+    for shape in ((0, 64, 64), (1, 12, 64), (1, 64, 100), (1, 64, 32)):
+        assert eg.engram_decode_workspace_size(*shape) == 0
+    ws = eg.engram_decode_workspace_size(2, 64, 64)
+    ptrs = [A * i for i in range(1, 13)]   # e, h, state, W_K, W_V, wh, wv, cw, y, new_state, workspace
+
+    def call(pt=ptrs, L=2, B=2, dmem=64, d=64, max_len=4, w=4, dil=1, wsb=ws):
+        return lib.engram_decode_fwd(p(pt[0]), p(pt[1]), p(pt[2]) if pt[2] else None, L,
+                                     *(p(v) if v else None for v in pt[3:11]), wsb, B, dmem, d,
+                                     max_len, w, dil, 1e-6, None)
+
+    assert call(pt=[0] + ptrs[1:]) == ENULL
+    no_state = list(ptrs)
+    no_state[2] = 0
+    assert call(pt=no_state, L=1) == ENULL          # a non-empty cache needs its pointer
+    assert call(L=5) == ESHAPE                      # L > max_len
+    assert call(w=0) == ESHAPE
+    assert call(dil=0) == ESHAPE
+    assert call(wsb=ws - 16) == EWS
+    ov = list(ptrs)
+    ov[9] = ptrs[2]                                 # the new cache aliases the old one
+    assert call(pt=ov) == EOVERLAP
