@@ -56,7 +56,8 @@ def source_hash(files):
 
 def profile_traffic(profile_md, sources):
     """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
-    the current sources; else None."""
+    the current kernel sources (the kernel's file and the headers it
+    includes); else None."""
     path = os.path.join(ROOT, "profiles", profile_md)
     if not os.path.exists(path):
         return None
@@ -262,7 +263,7 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
                                       tok * (16 * d + 16) + 48 * d, peak)
         if M == 4:  # DRAM bytes per launch from the committed ncu summaries
             csrc = "engram_memory_gating_gb300/csrc/"
-            common = [csrc + "gateconv_xch.cuh", csrc + "common.cuh", csrc + "engram_abi.cu"]
+            common = [csrc + "gateconv_xch.cuh", csrc + "common.cuh", csrc + "engram_internal.h"]
             ops[name + "_fwd"]["traffic"] = profile_traffic(
                 "gateconv_fwd_m4_t4096_d4096.md", [csrc + "gateconv_fwd.cu"] + common)
             ops[name + "_bwd"]["traffic"] = profile_traffic(
@@ -468,10 +469,9 @@ def main():
     bwd_gbs = bwd_bytes / (bwd_ms * 1e-3) / 1e9
     fwd_gbs = fwd_bytes / (fwd_ms * 1e-3) / 1e9
     csrc = "engram_memory_gating_gb300/csrc/"
-    traffic = profile_traffic("gate_bwd_n8192.md",
-                              [csrc + "gate_bwd.cu", csrc + "common.cuh", csrc + "engram_abi.cu"])
-    traffic_fwd = profile_traffic("gate_fwd_n8192.md",
-                                  [csrc + "gate_fwd.cu", csrc + "common.cuh", csrc + "engram_abi.cu"])
+    hdrs = [csrc + "common.cuh", csrc + "engram_internal.h"]
+    traffic = profile_traffic("gate_bwd_n8192.md", [csrc + "gate_bwd.cu"] + hdrs)
+    traffic_fwd = profile_traffic("gate_fwd_n8192.md", [csrc + "gate_fwd.cu"] + hdrs)
 
     # ---- end to end through the public API with host buffers (pinned)
     h = {k: v.cpu().pin_memory() for k, v in inp.items()}
