@@ -473,7 +473,11 @@ def main():
     traffic = profile_traffic("gate_bwd_n8192.md", [csrc + "gate_bwd.cu"] + hdrs)
     traffic_fwd = profile_traffic("gate_fwd_n8192.md", [csrc + "gate_fwd.cu"] + hdrs)
 
-    # ---- end to end through the public API with host buffers (pinned)
+    # ---- end to end through the public API with host buffers (pinned).  Every
+    # step copies all of its inputs host -> device and all of its outputs
+    # device -> host.  Three streams and two device buffer sets pipeline the
+    # steps: step i + 1's inputs go in and step i - 1's outputs come out while
+    # step i computes (the link carries both directions at once).
     h = {k: v.cpu().pin_memory() for k, v in inp.items()}
     ho = {"out": torch.empty_like(h["x"]).pin_memory(),
           "saved": torch.empty((N_TOK, S, 4), dtype=torch.float32).pin_memory(),
@@ -481,24 +485,55 @@ def main():
           "gw": torch.empty_like(h["weight"]).pin_memory()}
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = sum(t.numel() * t.element_size() for t in ho.values())
+    sets = []
+    for _ in range(2):
+        di = {k: torch.empty_like(v, device="cuda") for k, v in h.items()}
+        do = {"out": torch.empty_like(di["x"]), "saved": torch.empty((N_TOK, S, 4), device="cuda"),
+              "gx": torch.empty_like(di["x"]), "gkv": torch.empty_like(di["kv"]),
+              "gw": torch.empty_like(di["weight"])}
+        sets.append((di, do))
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "done", "out")}
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
+    def e2e_step(i):
+        b = i & 1
+        di, do = sets[b]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev["done"][b])          # step i - 2 has consumed these inputs
             for k in ("x", "kv", "weight", "mask", "grad_out"):
-                inp[k].copy_(h[k], non_blocking=True)
-        fwd()
-        bwd()
-        with torch.cuda.stream(stream):
-            ho["out"].copy_(out, non_blocking=True)
-            ho["saved"].copy_(saved, non_blocking=True)
-            ho["gx"].copy_(gx, non_blocking=True)
-            ho["gkv"].copy_(gkv, non_blocking=True)
-            ho["gw"].copy_(gw, non_blocking=True)
+                di[k].copy_(h[k], non_blocking=True)
+            ev["in"][b].record(s_in)
+        stream.wait_event(ev["in"][b])
+        if i >= 2:
+            stream.wait_event(ev["out"][b])             # step i - 2's outputs have left
+        eg.engram_gate_fwd(di["x"], di["kv"], di["weight"], di["mask"], do["out"], do["saved"],
+                           stream=stream)
+        eg.engram_gate_bwd(di["x"], di["kv"], di["weight"], do["saved"], di["grad_out"], do["gx"],
+                           do["gkv"], do["gw"], ws, stream=stream)
+        ev["done"][b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["done"][b])
+            for k in ("out", "saved", "gx", "gkv", "gw"):
+                ho[k].copy_(do[k], non_blocking=True)
+            ev["out"][b].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
-    Ke = max(5, min(50, K // 20))
-    e2e_ms = max_over_ranks(time_region(torch, e2e_step, Ke, stream), dist, "cuda")
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    Ke = max(6, min(50, K // 20))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(s_in)
+    for i in range(Ke):
+        e2e_step(i)
+    s_in.wait_stream(s_out)
+    t1.record(s_in)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / Ke, dist, "cuda")
+    del sets
 
     launch = {"fwd": eg.engram_launch_info(0, N_TOK), "bwd": eg.engram_launch_info(1, N_TOK)}
     ops = None
