@@ -188,6 +188,23 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
     ops["gate_fwd_N262144"] = op_entry(ms, N * FWD_BYTES_PER_TOKEN + FWD_FIXED, peak)
     del inp, out, saved, g
     torch.cuda.empty_cache()
+    # backward past the 8192-token cap: N = 65536, mask Bernoulli(0.9)
+    N = 65536
+    inp = inputs_mod.gate_inputs(N, 104, device="cuda", mask="bern0.9")
+    out = torch.empty_like(inp["x"])
+    saved = torch.empty((N, 4, 4), device="cuda", dtype=torch.float32)
+    eg.engram_gate_fwd(inp["x"], inp["kv"], inp["weight"], inp["mask"], out, saved, stream=s)
+    del out
+    gx, gkv, gw = torch.empty_like(inp["x"]), torch.empty_like(inp["kv"]), torch.empty_like(inp["weight"])
+    ws = torch.empty(eg.engram_gate_bwd_workspace_size(N), device="cuda", dtype=torch.uint8)
+    fn = lambda: eg.engram_gate_bwd(inp["x"], inp["kv"], inp["weight"], saved, inp["grad_out"], gx, gkv,
+                                    gw, ws, stream=s)
+    g = graph_of(torch, fn, s)
+    time_region(torch, g.replay, 3, s)
+    ms = time_region(torch, g.replay, 10, s)
+    ops["gate_bwd_N65536"] = op_entry(ms, N * BWD_BYTES_PER_TOKEN + BWD_FIXED, peak)
+    del inp, saved, gx, gkv, gw, ws, g
+    torch.cuda.empty_cache()
     # separate-tensor gate (tile-kernels layout), N = 8192, H = 4096
     N, H = 8192, 4096
     inp = inputs_mod.gate_inputs(N, 105, device="cuda", d=H)

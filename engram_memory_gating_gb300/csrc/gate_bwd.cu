@@ -33,7 +33,7 @@
 //     memory and the last one to leave it issues its refill;
 //  3. the pairs are merged in ascending group order (bitwise reproducible).
 // The per-token scalars are evaluated in fp64 because a relative error of a
-// few fp32 ulps in A, summed over 8192 tokens, would exceed the 1e-6
+// few fp32 ulps in A, summed over thousands of tokens, would exceed the 1e-6
 // absolute accuracy asked of grad_w near zero.
 #include "common.cuh"
 #include "engram_internal.h"

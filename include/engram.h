@@ -71,7 +71,7 @@ const char* engram_status_string(engram_status_t s);
 #define ENGRAM_GATE_HIDDEN 5120
 #define ENGRAM_GATE_KV_COLS 25600
 #define ENGRAM_GATE_MAX_TOKENS 4194240   /* forward: 1 <= N <= 65535*64     */
-#define ENGRAM_GATE_BWD_MAX_TOKENS 8192  /* backward: N % 64 == 0, N <= 8192 */
+#define ENGRAM_GATE_BWD_MAX_TOKENS 4194240 /* backward: N % 64 == 0, N <= 65535*64 */
 #define ENGRAM_GATECONV_MAX_D 8192       /* GateConv: 8 <= d <= 8192, d % 8 == 0 */
 #define ENGRAM_GATE_CLAMP 1e-6f          /* clamp of the signed square root         */
 #define ENGRAM_GATE_SEP_MAX_HIDDEN 65536 /* separate-tensor gate: H % 8 == 0        */
@@ -123,8 +123,12 @@ size_t engram_gate_bwd_workspace_size(int64_t N);
  *                               reproducible run to run)
  *   workspace  >= engram_gate_bwd_workspace_size(N) bytes, 16-B aligned,
  *              contents need no initialisation and are left undefined
- *   N        64 <= N <= 8192, N % 64 == 0
- * Two kernels on `stream`, no host synchronisation between them.
+ *   N        64 <= N <= ENGRAM_GATE_BWD_MAX_TOKENS, N % 64 == 0.  The cuDNN
+ *            page caps N at 8192 (a limit of its workspace design); here the
+ *            workspace grows by 1,344 bytes per token and the grad_weight
+ *            merge reads N/64 slots per column, so any multiple of 64 up to
+ *            the forward's maximum is accepted.
+ * Three kernels on `stream`, no host synchronisation between them.
  */
 engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weight,
                                 const float* saved, const void* grad_out, void* grad_x,

@@ -43,10 +43,10 @@ def test_status_strings():
 
 def test_gate_bwd_workspace_size_formula():
     # 4 * (16 N + 4 * 5120 * (N // 64)) bytes
-    for N in (64, 128, 4096, 8192):
+    for N in (64, 128, 4096, 8192, 8256, 65536, 4194240):
         assert eg.engram_gate_bwd_workspace_size(N) == 4 * (16 * N + 4 * 5120 * (N // 64))
     assert eg.engram_gate_bwd_workspace_size(8192) == 11010048
-    for N in (0, 1, 63, 100, 8256, -64):
+    for N in (0, 1, 63, 100, 8200, -64, 4194304):
         assert eg.engram_gate_bwd_workspace_size(N) == 0
 
 
@@ -102,7 +102,8 @@ def gate_bwd(N=64, ws_bytes=None, **kw):
 def test_gate_bwd_validation():
     assert gate_bwd(ws=0) == ENULL
     assert gate_bwd(N=100, ws_bytes=1 << 30) == ESHAPE
-    assert gate_bwd(N=8256, ws_bytes=1 << 30) == ESHAPE
+    assert gate_bwd(N=4194304, ws_bytes=1 << 40) == ESHAPE    # 65536 * 64: past the limit
+    assert gate_bwd(N=8200, ws_bytes=1 << 30) == ESHAPE       # not a multiple of 64
     assert gate_bwd(N=0, ws_bytes=1 << 30) == ESHAPE
     assert gate_bwd(gx=A * 500 + 2) == EALIGN
     assert gate_bwd(ws_bytes=eg.engram_gate_bwd_workspace_size(64) - 16) == EWS

@@ -197,7 +197,7 @@ def test_bwd_parity_from_oracle_saved(N, mask, seed):
 
 @pytest.mark.parametrize("seed", [1, 2, 3])
 def test_fwd_bwd_full_batch_8192(seed):
-    """N = 8192 (the backward maximum), mask Bernoulli(0.9): the GPU forward's
+    """N = 8192 (the cuDNN page's backward maximum), mask Bernoulli(0.9): the GPU forward's
     saved state feeds the GPU backward; every element is compared."""
     N = 8192
     inp = gate_inputs(N, seed, device=DEV, mask="bern0.9")
@@ -213,6 +213,41 @@ def test_fwd_bwd_full_batch_8192(seed):
     m = ~host["mask"]
     assert torch.equal(gx.cpu()[m].view(torch.int16), host["grad_out"][m].view(torch.int16))
     assert torch.all(gkv.cpu()[m][:, :4 * D].float() == 0)
+
+
+def test_bwd_long_batch():
+    """N = 65,728 (1,027 blocks of 64: an odd count, so three-block token
+    groups and a one-block last group), past the cuDNN page's 8192 cap.  The
+    GPU forward's saved state feeds the backward; grad_x and grad_kv are
+    compared element by element on a sample of tokens (the first and last
+    block and 256 random tokens) against the oracle run on those tokens, and
+    grad_weight against the oracle's sum over every token, formed as the fp64
+    sum of the oracle's grad_weight over 4096-token chunks (grad_weight is a
+    plain sum over tokens)."""
+    N = 65728
+    inp = gate_inputs(N, 5, device=DEV, mask="bern0.9")
+    _, saved = eg.gate_forward(inp["x"], inp["kv"], inp["weight"], inp["mask"])
+    gx, gkv, gw = eg.gate_backward(inp["x"], inp["kv"], inp["weight"], saved, inp["grad_out"])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    pick = np.unique(np.concatenate([np.arange(64), np.arange(N - 64, N),
+                                     rng.choice(N, 256, replace=False)]))
+    idx = torch.from_numpy(pick).to(DEV)
+    w64 = f64(inp["weight"])
+    sub = {k: inp[k].index_select(0, idx).cpu() for k in ("x", "kv", "grad_out")}
+    sv = saved.index_select(0, idx).double().cpu().numpy()
+    ex, ekv, _ = oracle.gate_bwd(f64(sub["x"]), f64(sub["kv"]), w64, sv, f64(sub["grad_out"]))
+    check_bf16("grad_x", bf16_bits(gx.index_select(0, idx)), ex)
+    gkv_bits = bf16_bits(gkv.index_select(0, idx)).reshape(len(pick), 5, D)
+    check_bf16("grad_key", gkv_bits[:, :4], ekv.reshape(len(pick), 5, D)[:, :4])
+    check_bf16("grad_v", gkv_bits[:, 4], ekv.reshape(len(pick), 5, D)[:, 4])
+    ew = np.zeros((4, D))
+    for c0 in range(0, N, 4096):
+        sl = slice(c0, min(N, c0 + 4096))
+        _, _, ewc = oracle.gate_bwd(f64(inp["x"][sl]), f64(inp["kv"][sl]), w64,
+                                    saved[sl].double().cpu().numpy(), f64(inp["grad_out"][sl]))
+        ew += ewc
+    check_f32("grad_weight", gw.cpu().numpy(), ew)
 
 
 def test_bwd_is_deterministic():
