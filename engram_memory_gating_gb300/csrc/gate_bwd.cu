@@ -64,6 +64,9 @@ EG_DEV void warp_sum_pair(float& hi, float& lo) {
 // kDFix = 0: any hidden size (a multiple of 8), separate saved arrays.
 template <int kDFix>
 __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdParams p) {
+    // the elementwise kernel may start its input copies while this one runs;
+    // it waits for this grid before it reads the scalars
+    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const long long gwarp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -226,7 +229,9 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     __syncthreads();
 
     const uint32_t gate_bytes = 16u * static_cast<uint32_t>(gstride);
-    auto issue = [&](int j, int st) {
+    // a stage: the token's input rows and saved gates, then its scalars (the
+    // coefficient kernel's output, copied only after that grid has completed)
+    auto issue_inputs = [&](int j, int st) {
         const long long n = t0 + j;
         unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
         mbar_arrive_expect_tx(&full[st], kRows * copy_bytes + 64u + gate_bytes);
@@ -237,14 +242,25 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
                      copy_bytes, &full[st]);
             bulk_g2s(b + (2 * kS + r) * row_bytes, p.gout + (n * kS + r) * d + col0, copy_bytes, &full[st]);
         }
-        bulk_g2s(b + kRows * row_bytes, p.coef + n * kS * 4, 64u, &full[st]);
         const float* gsrc = p.saved != nullptr ? p.saved + n * kS * 4 : p.sv_gate + n * kS;
         bulk_g2s(b + kRows * row_bytes + 64, gsrc, gate_bytes, &full[st]);
     };
-    if (tid == 0) {
-        const int pro = ntok < stages ? static_cast<int>(ntok) : stages;
-        for (int j = 0; j < pro; ++j) issue(j, j);
-    }
+    auto issue_scalars = [&](int j, int st) {
+        unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
+        bulk_g2s(b + kRows * row_bytes, p.coef + (t0 + j) * kS * 4, 64u, &full[st]);
+    };
+    auto issue = [&](int j, int st) {
+        issue_inputs(j, st);
+        issue_scalars(j, st);
+    };
+    const int pro = ntok < stages ? static_cast<int>(ntok) : stages;
+    if (tid == 0)
+        for (int j = 0; j < pro; ++j) issue_inputs(j, j);
+    // the inputs above were written before the coefficient kernel started;
+    // the scalars are that kernel's output
+    grid_dep_wait();
+    if (tid == 0)
+        for (int j = 0; j < pro; ++j) issue_scalars(j, j);
 
     float2 phi[4], plo[4];  // grad_w of this thread's columns, hi + lo
 #pragma unroll
@@ -445,11 +461,20 @@ cudaError_t gate_bwd_launch(const GateBwdParams& p, const LaunchCfg& c, cudaStre
         gate_bwd_coef_kernel<0><<<c.aux_blocks, 256, 0, s>>>(p);
     cudaError_t e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
-    if (p.packed)
-        gate_bwd_main_kernel<true><<<dim3(c.clusters, c.grid_y, 1), c.threads, c.smem, s>>>(p);
-    else
-        gate_bwd_main_kernel<false><<<dim3(c.clusters, c.grid_y, 1), c.threads, c.smem, s>>>(p);
-    return cudaPeekAtLastError();
+    // programmatic stream serialisation: kernel 2 may be scheduled while
+    // kernel 1 finishes (it waits for kernel 1's grid before reading the scalars)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(c.clusters, c.grid_y, 1);
+    cfg.blockDim = dim3(c.threads, 1, 1);
+    cfg.dynamicSmemBytes = c.smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return p.packed ? cudaLaunchKernelEx(&cfg, gate_bwd_main_kernel<true>, p)
+                    : cudaLaunchKernelEx(&cfg, gate_bwd_main_kernel<false>, p);
 }
 
 cudaError_t gate_wreduce_launch(const GateWReduceParams& p, cudaStream_t s) {
