@@ -132,13 +132,6 @@ EG_DEV void st_async_f2(uint32_t remote_addr, float a, float b, uint32_t remote_
         : "memory");
 }
 
-// Programmatic dependent launch.  grid_dep_launch: this CTA lets the next
-// kernel of the stream (launched with programmatic stream serialisation) be
-// scheduled; grid_dep_wait: waits until the preceding kernel has completed
-// and its memory operations are visible (a no-op without such a predecessor).
-EG_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-EG_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 EG_DEV void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -53,6 +53,13 @@ EG_DEV uint4 ldg16_na(const uint4* p) {
     return v;
 }
 
+// Programmatic dependent launch.  grid_dep_launch: this CTA lets the next
+// kernel of the stream (launched with programmatic stream serialisation) be
+// scheduled; grid_dep_wait: waits until the preceding kernel has completed
+// and its memory operations are visible (a no-op without such a predecessor).
+EG_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+EG_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 EG_DEV void warp_sum_pair(float& hi, float& lo) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
