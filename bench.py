@@ -370,7 +370,8 @@ def run_single_op(args):
     profiler captures: the gate at the step's N = 8192 inputs, GateConv at
     --gc-workload (m4: M=4, T=4096, d=4096; m8: M=8, T=8192, d=7168).  Prints
     the mean event-timed call.  Launches per call: gate_fwd 1, gate_bwd 3,
-    gateconv_fwd 1, gateconv_bwd 4."""
+    gateconv_fwd 1, gateconv_bwd 4, decode 2 (B = 8, d_mem = 1024, d = 4096,
+    a full cache of 16, w = 4, dilation 3; back to back, weights L2-warm)."""
     import torch
     import engram_memory_gating_gb300 as eg
     from engram_memory_gating_gb300 import inputs as inputs_mod
@@ -387,6 +388,14 @@ def run_single_op(args):
         else:
             fn = lambda: eg.engram_gate_bwd(inp["x"], inp["kv"], inp["weight"], saved,
                                             inp["grad_out"], gx, gkv, gw, ws, stream=s)
+    elif args.op == "decode":
+        B, dm, d, L, w, dil = 8, 1024, 4096, 16, 4, 3
+        di = inputs_mod.decode_inputs(B, dm, d, L, w, seed=107, device="cuda")
+        y = torch.empty_like(di["h"])
+        ns = torch.empty((B, L, d), device="cuda", dtype=torch.bfloat16)
+        ws = torch.empty(eg.engram_decode_workspace_size(B, dm, d), device="cuda", dtype=torch.uint8)
+        fn = lambda: eg.engram_decode_fwd(di["e"], di["h"], di["conv_state"], di["W_K"], di["W_V"],
+                                          di["rms_w_h"], di["rms_w_v"], di["conv_w"], y, ns, ws, dil, stream=s)
     else:
         M, T, d, hs, vs = GC_WORKLOADS[args.gc_workload]
         ci = inputs_mod.gateconv_inputs(M, T, d, 31, device="cuda", h_scale=hs, v_std=vs)
@@ -417,7 +426,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-op sweep")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
-    ap.add_argument("--op", choices=["step", "gate_fwd", "gate_bwd", "gateconv_fwd", "gateconv_bwd"],
+    ap.add_argument("--op", choices=["step", "gate_fwd", "gate_bwd", "gateconv_fwd", "gateconv_bwd", "decode"],
                     default="step", help="time one entry point alone (profiler captures)")
     ap.add_argument("--gc-workload", choices=sorted(GC_WORKLOADS), default="m4")
     args = ap.parse_args()

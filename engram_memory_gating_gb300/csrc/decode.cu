@@ -26,6 +26,12 @@
 namespace eg {
 namespace {
 
+// Programmatic dependent launch: the row kernel is scheduled while the
+// projection runs and waits for the projection grid only where it reads the
+// partial sums.
+EG_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+EG_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 constexpr int kCols = 128;   // columns per projection CTA (32 lanes x 4 columns)
 constexpr int kWarps1 = 8;   // warps of a projection CTA (interleaved 4-row groups)
 constexpr int kBc = 8;       // batch rows per projection CTA
@@ -46,6 +52,7 @@ __global__ void __launch_bounds__(32 * kWarps1, 2) decode_proj_kernel(const Deco
     const int m1 = min(p.dmem, m0 + rows);
     const int b0 = blockIdx.z * kBc;
     const int nb = min(kBc, p.B - b0);
+    grid_dep_launch();
     // the cache shift (independent of the projection), spread over all CTAs:
     // row r < max_len - 1 of the new cache is row r + 1 of the left-padded old one
     {
@@ -182,18 +189,35 @@ __global__ void __launch_bounds__(kThreads2) decode_row_kernel(const DecodeParam
     auto bf = [](const uint16_t* q, long long i) { return __uint_as_float(static_cast<uint32_t>(__ldg(q + i)) << 16); };
 
     // ---- this CTA's share of the row statistics (v of the first kCache
-    // columns of each thread kept for the second pass)
-    float vc[kCache];
+    // columns of each thread kept for the second pass).  h and w_h of those
+    // columns are inputs, read before waiting for the projection grid.
+    float vc[kCache], hc[kCache], wc[kCache];
+#pragma unroll
+    for (int q = 0; q < kCache; ++q) {
+        const int i = c0 + threadIdx.x + q * static_cast<int>(blockDim.x);
+        const bool ok = i < c0 + ncol;
+        hc[q] = ok ? bf(p.h, static_cast<long long>(b) * d + i) : 0.f;
+        wc[q] = ok ? __ldg(p.wh + i) : 0.f;
+    }
+    grid_dep_wait();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // sum h^2, k^2, h k w_h^2, v^2
     int it = 0;
     for (int i = c0 + threadIdx.x; i < c0 + ncol; i += blockDim.x, ++it) {
         float kk, vv;
         kv_at(i, kk, vv);
+        float hh = 0.f, w = 0.f;
+        if (it < kCache) {
 #pragma unroll
-        for (int q = 0; q < kCache; ++q)
-            if (q == it) vc[q] = vv;
-        const float hh = bf(p.h, static_cast<long long>(b) * d + i);
-        const float w = __ldg(p.wh + i);
+            for (int q = 0; q < kCache; ++q)
+                if (q == it) {
+                    vc[q] = vv;
+                    hh = hc[q];
+                    w = wc[q];
+                }
+        } else {
+            hh = bf(p.h, static_cast<long long>(b) * d + i);
+            w = __ldg(p.wh + i);
+        }
         acc.x = fmaf(hh, hh, acc.x);
         acc.y = fmaf(kk, kk, acc.y);
         acc.z = fmaf(hh * kk, w * w, acc.z);
@@ -288,17 +312,19 @@ cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s) {
     cudaError_t e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kCluster2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(p.B) * kCluster2, 1, 1);
     cfg.blockDim = dim3(kThreads2, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, decode_row_kernel, p);
 }
 
