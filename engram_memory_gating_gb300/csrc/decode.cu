@@ -32,6 +32,21 @@ namespace {
 EG_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 EG_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// The two halves of a cluster barrier (every thread of every CTA; release on
+// arrive, acquire on wait), so that work can run between them.
+EG_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+EG_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Asynchronous 16-byte store into the shared memory of a CTA of this cluster,
+// completing 16 bytes on that CTA's mbarrier.
+EG_DEV void st_async_f4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+            remote_addr),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+        : "memory");
+}
+
 constexpr int kCols = 128;   // columns per projection CTA (32 lanes x 4 columns)
 constexpr int kWarps1 = 8;   // warps of a projection CTA (interleaved 4-row groups)
 constexpr int kBc = 8;       // batch rows per projection CTA
@@ -152,13 +167,25 @@ constexpr int kCluster2 = 8;   // CTAs per batch row in kernel 2
 constexpr int kCache = 4;      // columns per thread whose v is kept between the passes
 
 // Kernel 2: a cluster of kCluster2 CTAs per batch row, CTA `rank` owning
-// d / kCluster2 columns.  Each CTA sums its columns' row statistics, the
-// cluster exchanges the four partial sums through distributed shared memory
-// (read in rank order, so every CTA forms identical scalars), and each CTA
-// then writes y and the new cache for its columns.
+// d / kCluster2 columns.  Each CTA sums its columns' row statistics and stores
+// the four partial sums into slot `rank` of every CTA of the cluster
+// (asynchronous remote stores completing on that CTA's mbarrier); each CTA
+// adds the eight slots in rank order, so all form identical scalars, then
+// writes y and the new cache for its columns.  Every CTA waits for all eight
+// slots before it goes on, so none leaves while a store to it is in flight.
 __global__ void __launch_bounds__(kThreads2) decode_row_kernel(const DecodeParams p) {
     __shared__ float4 sh[kThreads2 / 32];
     __shared__ float4 cta_sum;
+    __shared__ float4 slots[kCluster2];
+    __shared__ uint64_t xbar;
+    if (threadIdx.x == 0) {
+        mbar_init(&xbar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&xbar, kCluster2 * 16u);
+    }
+    // the barrier is initialised before any peer stores into this CTA (the
+    // matching wait comes just before the stores)
+    cluster_arrive();
     const uint32_t rank = cluster_rank();
     const int b = static_cast<int>(cluster_index());
     const int d = p.d;
@@ -242,19 +269,21 @@ __global__ void __launch_bounds__(kThreads2) decode_row_kernel(const DecodeParam
         }
         cta_sum = t;
     }
-    cluster_sync();
-    // lane r < 8 fetches rank r's sums (one vector load each, all in flight),
-    // then every lane adds them in rank order
-    const int lane = threadIdx.x & 31;
-    float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane < kCluster2) mine = ld_cluster_f4(map_to_rank(smem_addr(&cta_sum), static_cast<uint32_t>(lane)));
+    __syncthreads();
+    cluster_wait();
+    if (threadIdx.x < kCluster2) {
+        const uint32_t dst = static_cast<uint32_t>(threadIdx.x);
+        st_async_f4(map_to_rank(smem_addr(&slots[rank]), dst), cta_sum, map_to_rank(smem_addr(&xbar), dst));
+    }
+    if (!mbar_wait_cluster(&xbar, 0u) && threadIdx.x == 0) atomicOr(p.err, kErrTimeout);
     float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < kCluster2; ++r) {
-        t.x += __shfl_sync(kFullMask, mine.x, r);
-        t.y += __shfl_sync(kFullMask, mine.y, r);
-        t.z += __shfl_sync(kFullMask, mine.z, r);
-        t.w += __shfl_sync(kFullMask, mine.w, r);
+        const float4 q = slots[r];
+        t.x += q.x;
+        t.y += q.y;
+        t.z += q.z;
+        t.w += q.w;
     }
     const float inv_d = 1.0f / static_cast<float>(d);
     const float rh = rsqrtf(fmaf(t.x, inv_d, p.eps));
@@ -289,8 +318,6 @@ __global__ void __launch_bounds__(kThreads2) decode_row_kernel(const DecodeParam
         p.y[static_cast<long long>(b) * d + i] = static_cast<uint16_t>(pack_bf16x2(y, 0.f) & 0xffffu);
         ns[static_cast<long long>(p.max_len - 1) * d + i] = static_cast<uint16_t>(pack_bf16x2(u, 0.f) & 0xffffu);
     }
-    // no CTA leaves while another may still read its partial sums
-    cluster_sync();
 }
 
 }  // namespace

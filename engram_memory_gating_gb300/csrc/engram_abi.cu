@@ -730,6 +730,7 @@ engram_status_t engram_decode_fwd(const void* e, const void* h, const void* stat
     p.y = static_cast<uint16_t*>(y);
     p.new_state = static_cast<uint16_t*>(new_state);
     p.part = static_cast<float*>(workspace);
+    p.err = st->err;
     p.B = static_cast<int>(B);
     p.dmem = static_cast<int>(d_mem);
     p.d = static_cast<int>(d);

@@ -151,6 +151,7 @@ struct DecodeParams {
     uint16_t* y;              // (B, d) bf16
     uint16_t* new_state;      // (B, max_len, d) bf16
     float* part;              // workspace: (2, splits, B, d) fp32 partial k, v
+    unsigned int* err;        // sticky device error word
     int B, dmem, d, L, max_len, w, dil;
     int splits, rows_per_split;
     float eps, inv_sqrt_d;
