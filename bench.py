@@ -253,6 +253,9 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
     nbytes = 2 * dm * d * 2 + B * dm * 2 + B * d * 2 + B * L * d * 2 + d * 4 * (2 + w) + B * d * 2 + B * L * d * 2
     ops["decode_B8_dmem1024_d4096"] = op_entry(total / reps, nbytes, peak)
     ops["decode_B8_dmem1024_d4096"]["us"] = round(1000 * total / reps, 2)
+    csrc = "engram_memory_gating_gb300/csrc/"
+    ops["decode_B8_dmem1024_d4096"]["traffic"] = profile_traffic(
+        "decode_b8_dmem1024_d4096.md", [csrc + "decode.cu", csrc + "common.cuh", csrc + "engram_internal.h"])
     del di, y, ns, ws, gd, flush
     torch.cuda.empty_cache()
     # GateConv, two configurations
