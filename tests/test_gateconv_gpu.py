@@ -63,7 +63,7 @@ def check_bwd(res, exact, sums=True):
 # than the conv (T = 1, 2) and rows cut into several token ranges with halos
 SMALL = [(1, 1, 8, 0), (2, 37, 64, 1), (3, 129, 512, 2), (1, 1000, 64, 3), (2, 300, 4096, 4),
          (1, 70, 7168, 5), (1, 5, 5120, 6), (2, 45, 1032, 7), (1, 40, 8192, 8), (3, 2, 264, 9),
-         (1, 2500, 64, 10)]
+         (1, 2500, 64, 10), (1, 40, 4200, 11), (2, 33, 6144, 12)]
 
 
 @pytest.mark.parametrize("M,T,d,seed", SMALL)
