@@ -227,7 +227,7 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
     }
     c.clusters = C;
     c.grid_y = static_cast<int>((N + group_tokens - 1) / group_tokens);
-    const int64_t need1 = (N + 7) / 8;
+    const int64_t need1 = (N + 3) / 4;  // coefficient kernel: a warp pair per token
     c.aux_blocks = static_cast<int>(need1 < mc1 ? need1 : mc1);
     return true;
 }

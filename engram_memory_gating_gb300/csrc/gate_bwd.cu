@@ -66,25 +66,47 @@ EG_DEV void warp_sum_pair(float& hi, float& lo) {
         cacc_merge(hi, lo, __shfl_xor_sync(kFullMask, hi, off), __shfl_xor_sync(kFullMask, lo, off));
 }
 
+// Named barrier of the two warps of pair `pair` (ids 1..4, 64 threads; the
+// ids must be immediates).
+EG_DEV void pair_sync(int pair) {
+    switch (pair) {
+        case 0: asm volatile("bar.sync 1, 64;" ::: "memory"); break;
+        case 1: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
+        case 2: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
+        default: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
+    }
+}
+
 // ---------------------------------------------------------------- kernel 1
 // kDFix = 5120: hidden size known at compile time, packed saved records;
 // kDFix = 0: any hidden size (a multiple of 8), separate saved arrays.
+// Two warps of a CTA share a token: warp 2q + h reduces column half h of its
+// grad_out rows and v; the second hands its four (hi, lo) sums to the first
+// through shared memory (two slots, by token parity, one pair barrier per
+// token), which merges them after its own and evaluates the scalars.
 template <int kDFix>
 __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdParams p) {
     // the elementwise kernel may start its input copies while this one runs;
     // it waits for this grid before it reads the scalars
     grid_dep_launch();
+    __shared__ float2 xfer[4][2][kS];   // [pair][token parity][stream]
     const int lane = threadIdx.x & 31;
-    const long long gwarp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int pair = warp >> 1, half = warp & 1;
+    const long long gpair = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 6;
+    const long long npairs = (static_cast<long long>(gridDim.x) * blockDim.x) >> 6;
     const int d = kDFix ? kDFix : p.d;
     const int nch = d >> 3;                                   // 16-byte chunks per row
-    const int ng = (((nch + 31) / 32 + kCG - 1) / kCG + 1) & ~1;  // even number of load groups
-    auto has = [&](int m) { return (kDFix != 0 && (kDFix / 8) % (32 * 2 * kCG) == 0) || lane + 32 * m < nch; };
+    // this warp's chunks [ch0, ch0 + nhalf) of each row
+    const int nfirst = kDFix ? kDFix / 16 : (nch + 1) / 2;
+    const int ch0 = half ? nfirst : 0;
+    const int nhalf = kDFix ? kDFix / 16 : (half ? nch - nfirst : nfirst);
+    const int ng = (((nhalf + 31) / 32 + kCG - 1) / kCG + 1) & ~1;  // even number of load groups
+    auto has = [&](int m) { return (kDFix != 0 && (kDFix / 16) % 32 == 0) ? (32 * m < kDFix / 16) : lane + 32 * m < nhalf; };
     uint4 v0[kCG], g0[kS][kCG], v1[kCG], g1[kS][kCG];
     auto load_group = [&](long long n, int grp, uint4 (&vb)[kCG], uint4 (&gb)[kS][kCG]) {
-        const uint4* vr = reinterpret_cast<const uint4*>(p.v + n * (kDFix ? 5LL * kDFix : p.v_ts)) + lane;
-        const uint4* gr = reinterpret_cast<const uint4*>(p.gout + n * kS * d) + lane;
+        const uint4* vr = reinterpret_cast<const uint4*>(p.v + n * (kDFix ? 5LL * kDFix : p.v_ts)) + ch0 + lane;
+        const uint4* gr = reinterpret_cast<const uint4*>(p.gout + n * kS * d) + ch0 + lane;
 #pragma unroll
         for (int c = 0; c < kCG; ++c) {
             const int m = grp * kCG + c;
@@ -95,9 +117,10 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
         }
     };
     float2 hi[kS], lo[kS];
-    auto accumulate = [&](const uint4 (&vb)[kCG], const uint4 (&gb)[kS][kCG]) {
+    auto accumulate = [&](int grp, const uint4 (&vb)[kCG], const uint4 (&gb)[kS][kCG]) {
 #pragma unroll
         for (int c = 0; c < kCG; ++c) {
+            if (kDFix != 0 && !has(grp * kCG + c)) continue;   // compile-time empty group
             const float2 v2[4] = {bf2(vb[c].x), bf2(vb[c].y), bf2(vb[c].z), bf2(vb[c].w)};
 #pragma unroll
             for (int s = 0; s < kS; ++s) {
@@ -110,8 +133,9 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
             }
         }
     };
-    if (gwarp < p.N) load_group(gwarp, 0, v0, g0);
-    for (long long n = gwarp; n < p.N; n += nwarps) {
+    if (gpair < p.N) load_group(gpair, 0, v0, g0);
+    int par = 0;
+    for (long long n = gpair; n < p.N; n += npairs, par ^= 1) {
 #pragma unroll
         for (int s = 0; s < kS; ++s) hi[s] = lo[s] = make_float2(0.f, 0.f);
 #pragma unroll
@@ -120,12 +144,12 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
             // buffer 0 takes group grp + 2 or the first group of the next
             // token (whose loads then overlap this token's reduction and fp64 work)
             load_group(n, grp + 1, v1, g1);
-            accumulate(v0, g0);
+            accumulate(grp, v0, g0);
             if (grp + 2 < ng)
                 load_group(n, grp + 2, v0, g0);
-            else if (n + nwarps < p.N)
-                load_group(n + nwarps, 0, v0, g0);
-            accumulate(v1, g1);
+            else if (n + npairs < p.N)
+                load_group(n + npairs, 0, v0, g0);
+            accumulate(grp + 1, v1, g1);
         }
         float h[kS], l[kS];
 #pragma unroll
@@ -135,11 +159,19 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
             cacc_merge(h[s], l[s], hi[s].y, lo[s].y);
             warp_sum_pair(h[s], l[s]);
         }
+        // the second half's sums to the first warp of the pair
+        if (half == 1 && lane < kS)
+            xfer[pair][par][lane] = lane == 0 ? make_float2(h[0], l[0]) : lane == 1 ? make_float2(h[1], l[1])
+                                  : lane == 2 ? make_float2(h[2], l[2]) : make_float2(h[3], l[3]);
+        pair_sync(pair);
+        if (half == 1) continue;
         if (lane < kS) {
             // stream s = lane: fp64 scalars; rsqrt and the reciprocal start from
             // fp32 estimates refined by one Newton step, exp is the fp64 routine
-            const float hs = lane == 0 ? h[0] : lane == 1 ? h[1] : lane == 2 ? h[2] : h[3];
-            const float ls = lane == 0 ? l[0] : lane == 1 ? l[1] : lane == 2 ? l[2] : l[3];
+            float hs = lane == 0 ? h[0] : lane == 1 ? h[1] : lane == 2 ? h[2] : h[3];
+            float ls = lane == 0 ? l[0] : lane == 1 ? l[1] : lane == 2 ? l[2] : l[3];
+            const float2 other = xfer[pair][par][lane];
+            cacc_merge(hs, ls, other.x, other.y);
             const long long rs = n * kS + lane;
             float4 sv;
             if (kDFix)
