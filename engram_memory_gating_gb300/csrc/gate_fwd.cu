@@ -13,8 +13,8 @@
 // l+32, ...; two groups of chunks in flight), forms the three sums with
 // packed fp32x2 arithmetic, reduces them with a butterfly of shuffles (every
 // lane ends with the same totals), computes the gate, then streams X again
-// (an L2 hit: the row was read a few microseconds earlier) and v, and writes
-// `out` with streaming stores.  The four rows of a token go to four warps of
+// (an L2 hit: the row was read a few microseconds earlier) and v, two groups
+// in flight, and writes `out` with streaming stores.  The four rows of a token go to four warps of
 // the same CTA, so v is read from HBM once and from L1/L2 after.  The fused
 // weight (80 KB) stays resident in L1.  Warps loop over rows persistently.
 //
@@ -159,18 +159,19 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_kernel(const GateFwdParams p)
             }
         }
 
-        // ---- pass 2: out = x + gate * v, one rounding; a false mask copies X
+        // ---- pass 2: out = x + gate * v, one rounding; a false mask copies X.
+        // Two load groups in flight (the pass-1 buffers are free by now).
         uint4* o = reinterpret_cast<uint4*>(p.out + (n * kS + s) * d) + lane;
         const float2 g2 = splat2(gate);
-#pragma unroll
-        for (int g = 0; g < ng; ++g) {
-            uint4 xq[kGroup], vq[kGroup];
+        auto load2 = [&](int g, uint4 (&xq)[kGroup], uint4 (&vq)[kGroup]) {
 #pragma unroll
             for (int c = 0; c < kGroup; ++c) {
                 const int m = g * kGroup + c;
                 xq[c] = has(m) ? ldg16(xr + 32 * m) : make_uint4(0, 0, 0, 0);
                 vq[c] = (on && has(m)) ? ldg16(vr + 32 * m) : make_uint4(0, 0, 0, 0);
             }
+        };
+        auto store2 = [&](int g, const uint4 (&xq)[kGroup], const uint4 (&vq)[kGroup]) {
 #pragma unroll
             for (int c = 0; c < kGroup; ++c) {
                 const int m = g * kGroup + c;
@@ -182,6 +183,16 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_kernel(const GateFwdParams p)
                     ov.w = pack2(fma2(g2, bf2(vq[c].w), bf2(xq[c].w)));
                 }
                 if (has(m)) stg_cs(o + 32 * m, ov);
+            }
+        };
+        load2(0, xa, ka);
+#pragma unroll
+        for (int g = 0; g < ng; g += 2) {
+            if (g + 1 < ng) load2(g + 1, xb, kb);
+            store2(g, xa, ka);
+            if (g + 1 < ng) {
+                if (g + 2 < ng) load2(g + 2, xa, ka);
+                store2(g + 1, xb, kb);
             }
         }
     }
