@@ -592,7 +592,7 @@ def main():
                    "l2": "inputs larger than L2 (1.85 GB read+written per step); no flush",
                    "parallelism": f"replicas x{world}", "launch": launch},
         "hbm_GB_s": round(step_bytes / (ms * 1e-3) / 1e9, 1),
-        "roofline": {"kernel": "engram_gate_bwd (gate_bwd_kernel + wreduce_kernel), N=8192",
+        "roofline": {"kernel": "engram_gate_bwd (gate_bwd_coef_kernel + gate_bwd_main_kernel + wreduce_kernel), N=8192",
                      "bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(bwd_gbs / peak, 4),
                      "traffic": traffic},
