@@ -227,7 +227,9 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
     }
     c.clusters = C;
     c.grid_y = static_cast<int>((N + group_tokens - 1) / group_tokens);
-    const int64_t need1 = (N + 3) / 4;  // coefficient kernel: a warp pair per token
+    // coefficient kernel: a warp pair per token (packed, d = 5120) or a warp per
+    // token (runtime d, the separate-tensor layout)
+    const int64_t need1 = blocks ? (N + 7) / 8 : (N + 3) / 4;
     c.aux_blocks = static_cast<int>(need1 < mc1 ? need1 : mc1);
     return true;
 }

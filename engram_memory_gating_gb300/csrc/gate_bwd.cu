@@ -80,27 +80,31 @@ EG_DEV void pair_sync(int pair) {
 // ---------------------------------------------------------------- kernel 1
 // kDFix = 5120: hidden size known at compile time, packed saved records;
 // kDFix = 0: any hidden size (a multiple of 8), separate saved arrays.
-// Two warps of a CTA share a token: warp 2q + h reduces column half h of its
-// grad_out rows and v; the second hands its four (hi, lo) sums to the first
-// through shared memory (two slots, by token parity, one pair barrier per
-// token), which merges them after its own and evaluates the scalars.
+// With kDFix = 5120 two warps of a CTA share a token: warp 2q + h reduces
+// column half h of its grad_out rows and v; the second hands its four (hi, lo)
+// sums to the first through shared memory (two slots, by token parity, one
+// pair barrier per token), which merges them after its own and evaluates the
+// scalars.  The runtime-d instantiation keeps one warp per token (the pair
+// version spilled there and ran slower).
 template <int kDFix>
 __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdParams p) {
     // the elementwise kernel may start its input copies while this one runs;
     // it waits for this grid before it reads the scalars
     grid_dep_launch();
+    constexpr bool kPair = kDFix != 0;
     __shared__ float2 xfer[4][2][kS];   // [pair][token parity][stream]
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int pair = warp >> 1, half = warp & 1;
-    const long long gpair = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 6;
-    const long long npairs = (static_cast<long long>(gridDim.x) * blockDim.x) >> 6;
+    const int pair = warp >> 1, half = kPair ? (warp & 1) : 0;
+    constexpr int kUnitShift = kPair ? 6 : 5;  // threads per token: 64 or 32
+    const long long gpair = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> kUnitShift;
+    const long long npairs = (static_cast<long long>(gridDim.x) * blockDim.x) >> kUnitShift;
     const int d = kDFix ? kDFix : p.d;
     const int nch = d >> 3;                                   // 16-byte chunks per row
     // this warp's chunks [ch0, ch0 + nhalf) of each row
-    const int nfirst = kDFix ? kDFix / 16 : (nch + 1) / 2;
+    const int nfirst = kDFix ? kDFix / 16 : nch;
     const int ch0 = half ? nfirst : 0;
-    const int nhalf = kDFix ? kDFix / 16 : (half ? nch - nfirst : nfirst);
+    const int nhalf = kDFix ? kDFix / 16 : nch;
     const int ng = (((nhalf + 31) / 32 + kCG - 1) / kCG + 1) & ~1;  // even number of load groups
     auto has = [&](int m) { return (kDFix != 0 && (kDFix / 16) % 32 == 0) ? (32 * m < kDFix / 16) : lane + 32 * m < nhalf; };
     uint4 v0[kCG], g0[kS][kCG], v1[kCG], g1[kS][kCG];
@@ -159,19 +163,23 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
             cacc_merge(h[s], l[s], hi[s].y, lo[s].y);
             warp_sum_pair(h[s], l[s]);
         }
-        // the second half's sums to the first warp of the pair
-        if (half == 1 && lane < kS)
-            xfer[pair][par][lane] = lane == 0 ? make_float2(h[0], l[0]) : lane == 1 ? make_float2(h[1], l[1])
-                                  : lane == 2 ? make_float2(h[2], l[2]) : make_float2(h[3], l[3]);
-        pair_sync(pair);
-        if (half == 1) continue;
+        if (kPair) {
+            // the second half's sums to the first warp of the pair
+            if (half == 1 && lane < kS)
+                xfer[pair][par][lane] = lane == 0 ? make_float2(h[0], l[0]) : lane == 1 ? make_float2(h[1], l[1])
+                                      : lane == 2 ? make_float2(h[2], l[2]) : make_float2(h[3], l[3]);
+            pair_sync(pair);
+            if (half == 1) continue;
+        }
         if (lane < kS) {
             // stream s = lane: fp64 scalars; rsqrt and the reciprocal start from
             // fp32 estimates refined by one Newton step, exp is the fp64 routine
             float hs = lane == 0 ? h[0] : lane == 1 ? h[1] : lane == 2 ? h[2] : h[3];
             float ls = lane == 0 ? l[0] : lane == 1 ? l[1] : lane == 2 ? l[2] : l[3];
-            const float2 other = xfer[pair][par][lane];
-            cacc_merge(hs, ls, other.x, other.y);
+            if (kPair) {
+                const float2 other = xfer[pair][par][lane];
+                cacc_merge(hs, ls, other.x, other.y);
+            }
             const long long rs = n * kS + lane;
             float4 sv;
             if (kDFix)
