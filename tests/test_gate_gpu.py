@@ -133,11 +133,13 @@ def test_fwd_graph_capture_matches_eager():
     assert torch.equal(saved, saved_e)
 
 
-@pytest.mark.parametrize("N", [4096, 65536, 262144])
+@pytest.mark.parametrize("N", [4096, 32768, 32769, 65536, 262144])
 def test_fwd_full_size_sweep_graph(N):
     """Full-size forward sweep: per-token sigma ~ LogUniform(1e-2, 1e2), mask
     Bernoulli(0.5), CUDA-graph captured execute.  Sampled tokens are checked
-    against the oracle; the masked identity is checked on every token."""
+    against the oracle; the masked identity is checked on every token.  32768
+    and 32769 sit on either side of the switch from four warps per row to one
+    warp per row."""
     inp = gate_inputs(N, 100 + N % 97, device=DEV, mask="bern0.5", sigma="loguniform",
                       with_grad=False)
     out = torch.empty_like(inp["x"])
