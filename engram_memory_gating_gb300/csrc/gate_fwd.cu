@@ -18,7 +18,7 @@
 //    and v, two groups in flight, and writes `out` with streaming stores.  The
 //    four rows of a token go to four warps of the same CTA, so v is read from
 //    HBM once and from L1/L2 after.
-//  * gate_fwd_quad_kernel (packed layout, batches up to kGateQuadMaxTokens):
+//  * gate_fwd_quad_kernel (batches up to kGateQuadMaxTokens, d <= 5120):
 //    the four warps of a quad share a row, each owning a quarter of the
 //    columns (five chunks per lane).  A warp keeps its X chunks in registers
 //    from the reduction to the output pass, issues its v loads before the
@@ -222,19 +222,24 @@ EG_DEV void quad_sync(int q) {
         asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
-// Packed layout (d = 5120): the four warps of a quad share a row, warp 4q + j
-// owning chunks 160j .. 160j + 159 (five per lane).  Each keeps its X chunks in
+// The four warps of a quad share a row, warp 4q + j owning the j-th quarter of
+// its 16-byte chunks (at most five per lane: d <= 5120; for the packed layout,
+// d = 5120, exactly chunks 160j .. 160j + 159).  Each keeps its X chunks in
 // registers from the reduction to the output pass, so that pass loads only v.
 // The quad exchanges its partial sums through shared memory (two slots by row
 // parity, one quad barrier per row) and every warp merges them in part order,
-// so all four form the same gate.
+// so all four form the same gate.  kPacked: packed KV and saved records with
+// d = 5120 at compile time; otherwise runtime d and strides, saved arrays.
 constexpr int kParts = 4;
-constexpr int kPartChunks = kGateHidden / 8 / kParts;  // 160 chunks per part
-constexpr int kPerLane = kPartChunks / 32;             // 5
+constexpr int kPerLane = kGateHidden / 8 / kParts / 32;  // 5
+constexpr int kQuadMaxHidden = kParts * kPerLane * 32 * 8;  // 5120
 
+template <bool kPacked>
 __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdParams p) {
     __shared__ float4 xch[2][2][kParts];   // [quad][row parity][part]: sum x^2, sum k^2, hi, lo
-    constexpr int d = kGateHidden;
+    const int d = kPacked ? kGateHidden : p.d;
+    const long long key_ts = kPacked ? 5LL * kGateHidden : p.key_ts;
+    const long long v_ts = kPacked ? 5LL * kGateHidden : p.v_ts;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int quad = warp >> 2, part = warp & 3;
@@ -242,31 +247,33 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
     const long long nq = (static_cast<long long>(gridDim.x) * blockDim.x) >> 7;
     const long long rows = p.N * kS;
     const float inv_d = 1.0f / static_cast<float>(d);
-    const int ch0 = part * kPartChunks + lane;
-    auto load_xk = [&](long long row, uint4 (&xq)[kPerLane], uint4 (&kq)[kPerLane]) {
-        const uint4* xr = reinterpret_cast<const uint4*>(p.x + row * d) + ch0;
-        const uint4* kr = reinterpret_cast<const uint4*>(p.key + (row >> 2) * (5LL * d) +
-                                                         static_cast<long long>(row & 3) * d) + ch0;
-#pragma unroll
-        for (int m = 0; m < kPerLane; ++m) {
-            xq[m] = ldg16(xr + 32 * m);
-            kq[m] = ldg16_na(kr + 32 * m);
-        }
-    };
+    const int nch = d >> 3;
+    const int per = kPacked ? kGateHidden / 8 / kParts : (nch + kParts - 1) / kParts;  // chunks per part
+    const int cbeg = part * per;
+    const int cnt = kPacked ? per : max(0, min(per, nch - cbeg));       // this part's chunks
+    const int ch0 = cbeg + lane;
+    auto has = [&](int m) { return kPacked || lane + 32 * m < cnt; };
     int par = 0;
     for (long long row = gq; row < rows; row += nq, par ^= 1) {
         const long long n = row >> 2;
         const int s = static_cast<int>(row & 3);
-        uint4 xq[kPerLane], kq[kPerLane];
-        load_xk(row, xq, kq);
-        const uint4* vr = reinterpret_cast<const uint4*>(p.v + n * (5LL * d)) + ch0;
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x + row * d) + ch0;
+        const uint4* kr = reinterpret_cast<const uint4*>(p.key + n * key_ts + static_cast<long long>(s) * d) + ch0;
+        const uint4* vr = reinterpret_cast<const uint4*>(p.v + n * v_ts) + ch0;
         const float4* wr = reinterpret_cast<const float4*>(p.w + static_cast<long long>(s) * d) + 2 * ch0;
         const bool on = (p.mask == nullptr) || (__ldg(p.mask + n) != 0);
+        uint4 xq[kPerLane], kq[kPerLane];
+#pragma unroll
+        for (int m = 0; m < kPerLane; ++m) {
+            xq[m] = has(m) ? ldg16(xr + 32 * m) : make_uint4(0, 0, 0, 0);
+            kq[m] = has(m) ? ldg16_na(kr + 32 * m) : make_uint4(0, 0, 0, 0);
+        }
 
         // ---- pass 1 over this part: sum x^2, sum k^2, sum x w k (compensated)
         float2 ssx = make_float2(0.f, 0.f), ssk = ssx, hi = ssx, lo = ssx;
 #pragma unroll
         for (int m = 0; m < kPerLane; ++m) {
+            if (!has(m)) continue;
             const float4 wa = __ldg(wr + 64 * m);
             const float4 wb = __ldg(wr + 64 * m + 1);
             const float2 w2[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w),
@@ -283,11 +290,10 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
                 cacc_prod_x2(hi, lo, mul2(x2, k2), w2[e]);
             }
         }
-        // v for the output pass, and the next row's X and key, in flight
-        // during the exchange
+        // v for the output pass, in flight during the exchange
         uint4 vq[kPerLane];
 #pragma unroll
-        for (int m = 0; m < kPerLane; ++m) vq[m] = on ? ldg16(vr + 32 * m) : make_uint4(0, 0, 0, 0);
+        for (int m = 0; m < kPerLane; ++m) vq[m] = (on && has(m)) ? ldg16(vr + 32 * m) : make_uint4(0, 0, 0, 0);
         float sx = __fadd_rn(ssx.x, ssx.y);
         float sk = __fadd_rn(ssk.x, ssk.y);
         float h = hi.x, l = lo.x;
@@ -320,7 +326,16 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
         const float sqm = ad * rsqrtf(ad);
         const float sq = dot > 0.f ? sqm : (dot < 0.f ? -sqm : 0.f);
         const float gate = on ? __frcp_rn(1.0f + __expf(-sq)) : 0.f;
-        if (lane == 0 && part == 0 && p.saved != nullptr) stg_f4(p.saved + row * 4, gate, dot, rstd_x, rstd_k);
+        if (lane == 0 && part == 0) {
+            if (kPacked) {
+                if (p.saved != nullptr) stg_f4(p.saved + row * 4, gate, dot, rstd_x, rstd_k);
+            } else if (p.sv_gate != nullptr) {
+                p.sv_gate[row] = gate;
+                p.sv_dot[row] = dot;
+                p.sv_rx[row] = rstd_x;
+                p.sv_rk[row] = rstd_k;
+            }
+        }
 
         // ---- pass 2: out = x + gate * v, one rounding; a false mask copies X
         uint4* o = reinterpret_cast<uint4*>(p.out + row * d) + ch0;
@@ -334,7 +349,7 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
                 ov.z = pack2(fma2(g2, bf2(vq[m].z), bf2(xq[m].z)));
                 ov.w = pack2(fma2(g2, bf2(vq[m].w), bf2(xq[m].w)));
             }
-            stg_cs(o + 32 * m, ov);
+            if (has(m)) stg_cs(o + 32 * m, ov);
         }
     }
 }
@@ -342,7 +357,9 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
 }  // namespace
 
 cudaError_t gate_fwd_prepare(int) {
-    cudaError_t e = cudaFuncSetAttribute(gate_fwd_quad_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
+    cudaError_t e = cudaFuncSetAttribute(gate_fwd_quad_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gate_fwd_quad_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gate_fwd_kernel<kGateHidden>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
     if (e != cudaSuccess) return e;
@@ -352,25 +369,35 @@ cudaError_t gate_fwd_prepare(int) {
 // Co-resident CTAs of the forward on this device (threads per CTA given): the
 // smallest count of its kernels, so the grid suits each.
 cudaError_t gate_fwd_max_clusters(int, int threads, int, int* out) {
-    int a = 0, b = 0, c = 0, dev = 0, sms = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, gate_fwd_quad_kernel, threads, 0);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, gate_fwd_kernel<kGateHidden>, threads, 0);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, gate_fwd_kernel<0>, threads, 0);
+    int m = 1 << 30, v = 0, dev = 0, sms = 0;
+    cudaError_t e = cudaSuccess;
+    const void* kernels[] = {reinterpret_cast<const void*>(gate_fwd_quad_kernel<true>),
+                             reinterpret_cast<const void*>(gate_fwd_quad_kernel<false>),
+                             reinterpret_cast<const void*>(gate_fwd_kernel<kGateHidden>),
+                             reinterpret_cast<const void*>(gate_fwd_kernel<0>)};
+    for (const void* k : kernels) {
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k, threads, 0);
+        if (e == cudaSuccess && v < m) m = v;
+    }
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int m = a < b ? (a < c ? a : c) : (b < c ? b : c);
     *out = m * sms;
     return e;
 }
 
-// Packed layout: the four-warps-per-row kernel up to kGateQuadMaxTokens
-// tokens; above, the warp-per-row kernel, whose output pass gets cheap on
-// masked rows and streams a little faster on long, heavily masked batches.
+// Four warps per row up to kGateQuadMaxTokens tokens for 4096 <= d <= 5120
+// (narrower rows leave most lanes of a quarter idle; at d = 4096 the two
+// kernels time the same); otherwise one warp per row, whose output pass gets
+// cheap on masked rows and streams a little faster on long, heavily masked
+// batches.
 cudaError_t gate_fwd_launch(const GateFwdParams& p, const LaunchCfg& c, cudaStream_t s) {
-    if (p.packed && p.N <= kGateQuadMaxTokens)
-        gate_fwd_quad_kernel<<<c.clusters, c.threads, 0, s>>>(p);
+    const bool quad = p.N <= kGateQuadMaxTokens && p.d >= 4096 && p.d <= kQuadMaxHidden;
+    if (p.packed && quad)
+        gate_fwd_quad_kernel<true><<<c.clusters, c.threads, 0, s>>>(p);
     else if (p.packed)
         gate_fwd_kernel<kGateHidden><<<c.clusters, c.threads, 0, s>>>(p);
+    else if (quad)
+        gate_fwd_quad_kernel<false><<<c.clusters, c.threads, 0, s>>>(p);
     else
         gate_fwd_kernel<0><<<c.clusters, c.threads, 0, s>>>(p);
     return cudaPeekAtLastError();

@@ -71,7 +71,8 @@ def run(N, H, seed, eps=oracle.GATE_EPS, clamp=oracle.GATE_CLAMP, w_scale=None, 
 
 
 @pytest.mark.parametrize("N,H,seed", [(1, 8, 0), (37, 64, 1), (64, 1000, 2), (130, 1024, 3),
-                                      (70, 5120, 4), (65, 7168, 5), (3, 3000, 6)])
+                                      (70, 5120, 4), (65, 7168, 5), (3, 3000, 6), (40, 4096, 13),
+                                      (33, 4104, 14), (64, 4600, 15)])
 def test_sep_parity(N, H, seed):
     run(N, H, seed)
 
@@ -103,12 +104,11 @@ def within_two_tolerances(a, b):
 
 
 def test_sep_matches_packed_entry_points_at_5120():
-    """At H = 5120 the two layouts agree to rounding: the packed forward splits
-    each row over four warps and adds their partial sums in part order, the
-    separate-tensor forward (any H) reduces a row in one warp, so the fp32
-    row sums may differ in their last bits.  Both paths are pinned to the
-    oracle elsewhere; here they agree within twice the oracle tolerance and
-    the saved fp32 values to a few ulps."""
+    """At H = 5120 both layouts run the same forward kernel (four warps per
+    row), so the forward is bit-identical; the backward's coefficient kernels
+    differ (a warp pair per token for the packed layout, one warp for the
+    runtime-d one), so the backward agrees to rounding: within twice the oracle
+    tolerance (both paths are pinned to the oracle elsewhere)."""
     N = 128
     inp, k, v = split_inputs(N, 5120, 11)
     d = {n: t.cuda() for n, t in (("x", inp["x"]), ("kv", inp["kv"]), ("w", inp["weight"]),
@@ -118,9 +118,9 @@ def test_sep_matches_packed_entry_points_at_5120():
     out2, dot, gate, rx, rk = eg.gate_sep_forward(d["x"], d["k"], d["v"], d["w"])
     gx2, gk2, gv2, gwp = eg.gate_sep_backward(d["g"], d["x"], d["k"], d["v"], d["w"], dot, gate, rx, rk)
     torch.cuda.synchronize()
-    assert within_two_tolerances(out, out2)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     for i, t in enumerate((gate, dot, rx, rk)):
-        assert torch.allclose(saved[..., i], t, rtol=1e-5, atol=1e-6)
+        assert torch.equal(saved[..., i], t)
     assert within_two_tolerances(gx, gx2)
     assert within_two_tolerances(gkv[:, :4 * 5120].reshape(N, 4, 5120), gk2)
     assert within_two_tolerances(gkv[:, 4 * 5120:], gv2)
