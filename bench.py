@@ -596,7 +596,7 @@ def main():
                      "bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(bwd_gbs / peak, 4),
                      "traffic": traffic},
-        "roofline_fwd": {"kernel": "engram_gate_fwd (gate_fwd_quad_kernel), N=8192", "bound": "hbm",
+        "roofline_fwd": {"kernel": "engram_gate_fwd (gate_fwd_quad_kernel<true>), N=8192", "bound": "hbm",
                          "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(fwd_gbs / peak, 4), "traffic": traffic_fwd},
         "cpu_baseline": cpu,
