@@ -137,6 +137,58 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
             }
         }
     };
+    // The (hi, lo) dgate sums of a unit's tokens wait in shared memory until
+    // kBatch of them are ready; one full-warp pass then evaluates their
+    // scalars in fp64, lane = kS * token + stream.  An fp64 warp instruction
+    // occupies the (narrow) fp64 pipe as long with 4 active lanes as with
+    // 32, so this takes 8x fewer of them than a pass per token.
+    constexpr int kBatch = 32 / kS;
+    constexpr int kUnits = kPair ? 4 : 8;
+    __shared__ float2 pend[kUnits][kBatch][kS];
+    __shared__ long long pend_n[kUnits][kBatch];
+    const int unit = kPair ? pair : warp;
+    int npend = 0;
+    auto flush = [&]() {
+        __syncwarp();
+        const int t = lane / kS, sl = lane % kS;
+        if (t < npend) {
+            // rsqrt and the reciprocal start from fp32 estimates refined by one
+            // Newton step, exp is the fp64 routine
+            const float2 hl = pend[unit][t][sl];
+            const long long rs = pend_n[unit][t] * kS + sl;
+            float4 sv;
+            if (kDFix)
+                sv = __ldg(reinterpret_cast<const float4*>(p.saved + rs * 4));
+            else
+                sv = make_float4(__ldg(p.sv_gate + rs), __ldg(p.sv_dot + rs), __ldg(p.sv_rx + rs), __ldg(p.sv_rk + rs));
+            const float gate = sv.x;
+            const double dot = sv.y, rx = sv.z, rk = sv.w;
+            const double ad = fabs(dot);
+            double ddot = 0.0;
+            if (ad >= static_cast<double>(p.clamp) && gate != 0.f) {
+                double y = rsqrtf(fabsf(sv.y));
+                y = y * (1.5 - 0.5 * ad * y * y);           // 1/sqrt(|dot|)
+                const double sqm = ad * y;                  // |sq| = sqrt(|dot|)
+                const double ex = exp(-sqm);
+                const double den = 1.0 + ex;
+                double rc = __frcp_rn(static_cast<float>(den));
+                rc = rc * (2.0 - den * rc);                 // 1/(1 + e^-|sq|)
+                const double dsig = ex * rc * rc;           // sigmoid(sq) sigmoid(-sq)
+                const double dgate = static_cast<double>(hl.x) + static_cast<double>(hl.y);
+                ddot = dgate * dsig * (0.5 * y);            // d sq/d dot = 0.5/sqrt(|dot|)
+            }
+            const double dd = dot / static_cast<double>(d);
+            const double av = ddot * rx * rk;
+            // A = a8 + arest: a8 keeps 8 significant bits, so a8 * (x*k) is exact
+            // in fp32 (8 + 16 bits); arest carries the next 24 bits
+            const float a8 = __uint_as_float(__float_as_uint(static_cast<float>(av)) & 0xffff0000u);
+            const float arest = static_cast<float>(av - static_cast<double>(a8));
+            stg_f4(p.coef + rs * 4, a8, arest, static_cast<float>(-(ddot * rx * rx * dd)),
+                   static_cast<float>(-(ddot * rk * rk * dd)));
+        }
+        __syncwarp();
+        npend = 0;
+    };
     if (gpair < p.N) load_group(gpair, 0, v0, g0);
     int par = 0;
     for (long long n = gpair; n < p.N; n += npairs, par ^= 1) {
@@ -172,46 +224,18 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
             if (half == 1) continue;
         }
         if (lane < kS) {
-            // stream s = lane: fp64 scalars; rsqrt and the reciprocal start from
-            // fp32 estimates refined by one Newton step, exp is the fp64 routine
             float hs = lane == 0 ? h[0] : lane == 1 ? h[1] : lane == 2 ? h[2] : h[3];
             float ls = lane == 0 ? l[0] : lane == 1 ? l[1] : lane == 2 ? l[2] : l[3];
             if (kPair) {
                 const float2 other = xfer[pair][par][lane];
                 cacc_merge(hs, ls, other.x, other.y);
             }
-            const long long rs = n * kS + lane;
-            float4 sv;
-            if (kDFix)
-                sv = __ldg(reinterpret_cast<const float4*>(p.saved + rs * 4));
-            else
-                sv = make_float4(__ldg(p.sv_gate + rs), __ldg(p.sv_dot + rs), __ldg(p.sv_rx + rs), __ldg(p.sv_rk + rs));
-            const float gate = sv.x;
-            const double dot = sv.y, rx = sv.z, rk = sv.w;
-            const double ad = fabs(dot);
-            double ddot = 0.0;
-            if (ad >= static_cast<double>(p.clamp) && gate != 0.f) {
-                double y = rsqrtf(fabsf(sv.y));
-                y = y * (1.5 - 0.5 * ad * y * y);           // 1/sqrt(|dot|)
-                const double sqm = ad * y;                  // |sq| = sqrt(|dot|)
-                const double ex = exp(-sqm);
-                const double den = 1.0 + ex;
-                double rc = __frcp_rn(static_cast<float>(den));
-                rc = rc * (2.0 - den * rc);                 // 1/(1 + e^-|sq|)
-                const double dsig = ex * rc * rc;           // sigmoid(sq) sigmoid(-sq)
-                const double dgate = static_cast<double>(hs) + static_cast<double>(ls);
-                ddot = dgate * dsig * (0.5 * y);            // d sq/d dot = 0.5/sqrt(|dot|)
-            }
-            const double dd = dot / static_cast<double>(d);
-            const double av = ddot * rx * rk;
-            // A = a8 + arest: a8 keeps 8 significant bits, so a8 * (x*k) is exact
-            // in fp32 (8 + 16 bits); arest carries the next 24 bits
-            const float a8 = __uint_as_float(__float_as_uint(static_cast<float>(av)) & 0xffff0000u);
-            const float arest = static_cast<float>(av - static_cast<double>(a8));
-            stg_f4(p.coef + rs * 4, a8, arest, static_cast<float>(-(ddot * rx * rx * dd)),
-                   static_cast<float>(-(ddot * rk * rk * dd)));
+            pend[unit][npend][lane] = make_float2(hs, ls);
+            if (lane == 0) pend_n[unit][npend] = n;
         }
+        if (++npend == kBatch) flush();
     }
+    if (npend > 0) flush();
 }
 
 // ---------------------------------------------------------------- kernel 2
