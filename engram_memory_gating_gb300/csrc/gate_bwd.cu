@@ -42,7 +42,10 @@ namespace eg {
 namespace {
 
 constexpr int kS = 4;
-constexpr int kCG = 2;              // chunk indices per load group (kernel 1)
+// chunk indices per load group (kernel 1): two for d = 5120, one for the
+// runtime-d instantiation, whose two-chunk groups spilled registers
+template <int kDFix>
+constexpr int kCGOf = kDFix != 0 ? 2 : 1;
 constexpr int kRows = 3 * kS;       // X rows, key rows, grad_out rows (kernel 2)
 
 EG_DEV uint4 ldg16_na(const uint4* p) {
@@ -84,8 +87,9 @@ EG_DEV void pair_sync(int pair) {
 // column half h of its grad_out rows and v; the second hands its four (hi, lo)
 // sums to the first through shared memory (two slots, by token parity, one
 // pair barrier per token), which merges them after its own and evaluates the
-// scalars.  The runtime-d instantiation keeps one warp per token (the pair
-// version spilled there and ran slower).
+// scalars.  The runtime-d instantiation keeps one warp per token and loads
+// one chunk index per group (with two it spilled; a warp pair there gained
+// nothing further).
 template <int kDFix>
 __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdParams p) {
     // the elementwise kernel may start its input copies while this one runs;
@@ -105,6 +109,7 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
     const int nfirst = kDFix ? kDFix / 16 : nch;
     const int ch0 = half ? nfirst : 0;
     const int nhalf = kDFix ? kDFix / 16 : nch;
+    constexpr int kCG = kCGOf<kDFix>;
     const int ng = (((nhalf + 31) / 32 + kCG - 1) / kCG + 1) & ~1;  // even number of load groups
     auto has = [&](int m) { return (kDFix != 0 && (kDFix / 16) % 32 == 0) ? (32 * m < kDFix / 16) : lane + 32 * m < nhalf; };
     uint4 v0[kCG], g0[kS][kCG], v1[kCG], g1[kS][kCG];
