@@ -253,6 +253,9 @@ constexpr int kRing2Off = 256;  // after the stage mbarriers and release counter
 // known at compile time; otherwise runtime d and strides.
 template <bool kPacked>
 __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdParams p) {
+    // the merge kernel may be scheduled as this grid's CTAs leave; it waits
+    // for the whole grid before it reads the partials
+    grid_dep_launch();
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);                            // [stages]
     unsigned int* released = reinterpret_cast<unsigned int*>(smem + kMaxStages * 8);  // [stages]
@@ -453,6 +456,9 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
 constexpr int kRedGroups = 8;
 
 __global__ void __launch_bounds__(32 * kRedGroups) wreduce_kernel(const GateWReduceParams p) {
+    // launched behind the elementwise kernel with programmatic stream
+    // serialisation: the partials are complete and visible after this wait
+    grid_dep_wait();
     __shared__ float shi[kRedGroups][32], slo[kRedGroups][32];
     const int lane = threadIdx.x & 31;
     const int g = threadIdx.x >> 5;
@@ -554,8 +560,16 @@ cudaError_t gate_bwd_launch(const GateBwdParams& p, const LaunchCfg& c, cudaStre
 }
 
 cudaError_t gate_wreduce_launch(const GateWReduceParams& p, cudaStream_t s) {
-    wreduce_kernel<<<(p.n + 31) / 32, 32 * kRedGroups, 0, s>>>(p);
-    return cudaPeekAtLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>((p.n + 31) / 32), 1, 1);
+    cfg.blockDim = dim3(32 * kRedGroups, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, wreduce_kernel, p);
 }
 
 }  // namespace eg
