@@ -475,25 +475,33 @@ def main():
         fwd()
         bwd()
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    # the timed steps, back to back: no event between two kernels, which
+    # would end the overlap of one kernel's tail with the next one's launch
     with Clocks(local) as clk:
         t_start.record(stream)
         for i in range(K):
-            evs[i][0].record(stream)
             fwd()
-            evs[i][1].record(stream)
             bwd()
-            evs[i][2].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
     ms = t_start.elapsed_time(t_end) / K
+    # forward / backward split (for the per-kernel rooflines): the same steps
+    # again with an event around each entry point
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for i in range(K):
+        evs[i][0].record(stream)
+        fwd()
+        evs[i][1].record(stream)
+        bwd()
+        evs[i][2].record(stream)
+    torch.cuda.synchronize()
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     ms = max_over_ranks(ms, dist, "cuda")

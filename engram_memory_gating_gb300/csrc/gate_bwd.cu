@@ -92,8 +92,11 @@ EG_DEV void pair_sync(int pair) {
 // nothing further).
 template <int kDFix>
 __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdParams p) {
-    // the elementwise kernel may start its input copies while this one runs;
-    // it waits for this grid before it reads the scalars
+    // launched with programmatic stream serialisation: first wait for the
+    // preceding kernel (e.g. the forward that wrote the saved state), then let
+    // the elementwise kernel be scheduled; it may copy its input rows while
+    // this one runs and waits for this grid before it reads the scalars
+    grid_dep_wait();
     grid_dep_launch();
     constexpr bool kPair = kDFix != 0;
     __shared__ float2 xfer[4][2][kS];   // [pair][token parity][stream]
@@ -308,8 +311,9 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     __syncthreads();
 
     const uint32_t gate_bytes = 16u * static_cast<uint32_t>(gstride);
-    // a stage: the token's input rows and saved gates, then its scalars (the
-    // coefficient kernel's output, copied only after that grid has completed)
+    // a stage: the token's input rows, then its scalars and saved gates (the
+    // coefficient kernel's output and the state it read, copied only after
+    // that grid has completed)
     auto issue_inputs = [&](int j, int st) {
         const long long n = t0 + j;
         unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
@@ -321,12 +325,13 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
                      copy_bytes, &full[st]);
             bulk_g2s(b + (2 * kS + r) * row_bytes, p.gout + (n * kS + r) * d + col0, copy_bytes, &full[st]);
         }
-        const float* gsrc = p.saved != nullptr ? p.saved + n * kS * 4 : p.sv_gate + n * kS;
-        bulk_g2s(b + kRows * row_bytes + 64, gsrc, gate_bytes, &full[st]);
     };
     auto issue_scalars = [&](int j, int st) {
+        const long long n = t0 + j;
         unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
-        bulk_g2s(b + kRows * row_bytes, p.coef + (t0 + j) * kS * 4, 64u, &full[st]);
+        bulk_g2s(b + kRows * row_bytes, p.coef + n * kS * 4, 64u, &full[st]);
+        const float* gsrc = p.saved != nullptr ? p.saved + n * kS * 4 : p.sv_gate + n * kS;
+        bulk_g2s(b + kRows * row_bytes + 64, gsrc, gate_bytes, &full[st]);
     };
     auto issue = [&](int j, int st) {
         issue_inputs(j, st);
@@ -457,8 +462,10 @@ constexpr int kRedGroups = 8;
 
 __global__ void __launch_bounds__(32 * kRedGroups) wreduce_kernel(const GateWReduceParams p) {
     // launched behind the elementwise kernel with programmatic stream
-    // serialisation: the partials are complete and visible after this wait
+    // serialisation: the partials are complete and visible after this wait;
+    // then the next kernel of the stream may be scheduled
     grid_dep_wait();
+    grid_dep_launch();
     __shared__ float shi[kRedGroups][32], slo[kRedGroups][32];
     const int lane = threadIdx.x & 31;
     const int g = threadIdx.x >> 5;
@@ -536,19 +543,22 @@ cudaError_t gate_bwd_max_clusters(int, int threads, int smem, int* out) {
 
 // kernel 1 then kernel 2 on the stream (kernel 3 is gate_wreduce_launch)
 cudaError_t gate_bwd_launch(const GateBwdParams& p, const LaunchCfg& c, cudaStream_t s) {
-    // the compile-time specialisations serve the packed layout (d = 5120)
-    if (p.packed)
-        gate_bwd_coef_kernel<kGateHidden><<<c.aux_blocks, 256, 0, s>>>(p);
-    else
-        gate_bwd_coef_kernel<0><<<c.aux_blocks, 256, 0, s>>>(p);
-    cudaError_t e = cudaPeekAtLastError();
-    if (e != cudaSuccess) return e;
-    // programmatic stream serialisation: kernel 2 may be scheduled while
-    // kernel 1 finishes (it waits for kernel 1's grid before reading the scalars)
+    // programmatic stream serialisation for both: kernel 1 waits for its
+    // predecessor first; kernel 2 may be scheduled while kernel 1 finishes
+    // (it waits for kernel 1's grid before reading the scalars)
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(c.aux_blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // the compile-time specialisations serve the packed layout (d = 5120)
+    cudaError_t e = p.packed ? cudaLaunchKernelEx(&cfg, gate_bwd_coef_kernel<kGateHidden>, p)
+                             : cudaLaunchKernelEx(&cfg, gate_bwd_coef_kernel<0>, p);
+    if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(c.clusters, c.grid_y, 1);
     cfg.blockDim = dim3(c.threads, 1, 1);
     cfg.dynamicSmemBytes = c.smem;

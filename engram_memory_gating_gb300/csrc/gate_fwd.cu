@@ -38,6 +38,16 @@ namespace eg {
 namespace {
 
 constexpr int kS = 4;       // streams
+
+// Programmatic dependent launch.  Launched with programmatic stream
+// serialisation, a forward kernel first waits for the preceding kernel of the
+// stream to complete (griddepcontrol.wait: its writes are then visible) and
+// only then lets the next kernel be scheduled, so that early scheduling never
+// runs ahead of a producer; only the launch latency overlaps.
+EG_DEV void grid_dep_start() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 // Largest batch (tokens) the packed forward runs with four warps per row.
 // Measured on GB300 with 10% and 50% of the tokens masked: the quad kernel is
 // faster up to 32,768 tokens (by 5-8% at 4,096-16,384), the row kernel on
@@ -78,6 +88,7 @@ EG_DEV void warp_sum_pair(float& hi, float& lo) {
 // state as four (N, 4) arrays.
 template <int kDFix>
 __global__ void __launch_bounds__(256, 2) gate_fwd_kernel(const GateFwdParams p) {
+    grid_dep_start();
     const int lane = threadIdx.x & 31;
     const long long gwarp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -236,6 +247,7 @@ constexpr int kQuadMaxHidden = kParts * kPerLane * 32 * 8;  // 5120
 
 template <bool kPacked>
 __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdParams p) {
+    grid_dep_start();
     __shared__ float4 xch[2][2][kParts];   // [quad][row parity][part]: sum x^2, sum k^2, hi, lo
     const int d = kPacked ? kGateHidden : p.d;
     const long long key_ts = kPacked ? 5LL * kGateHidden : p.key_ts;
@@ -392,15 +404,20 @@ cudaError_t gate_fwd_max_clusters(int, int threads, int, int* out) {
 // batches.
 cudaError_t gate_fwd_launch(const GateFwdParams& p, const LaunchCfg& c, cudaStream_t s) {
     const bool quad = p.N <= kGateQuadMaxTokens && p.d >= 4096 && p.d <= kQuadMaxHidden;
-    if (p.packed && quad)
-        gate_fwd_quad_kernel<true><<<c.clusters, c.threads, 0, s>>>(p);
-    else if (p.packed)
-        gate_fwd_kernel<kGateHidden><<<c.clusters, c.threads, 0, s>>>(p);
-    else if (quad)
-        gate_fwd_quad_kernel<false><<<c.clusters, c.threads, 0, s>>>(p);
-    else
-        gate_fwd_kernel<0><<<c.clusters, c.threads, 0, s>>>(p);
-    return cudaPeekAtLastError();
+    // programmatic stream serialisation (each kernel waits for its predecessor first)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(c.clusters), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(c.threads), 1, 1);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.packed && quad) return cudaLaunchKernelEx(&cfg, gate_fwd_quad_kernel<true>, p);
+    if (p.packed) return cudaLaunchKernelEx(&cfg, gate_fwd_kernel<kGateHidden>, p);
+    if (quad) return cudaLaunchKernelEx(&cfg, gate_fwd_quad_kernel<false>, p);
+    return cudaLaunchKernelEx(&cfg, gate_fwd_kernel<0>, p);
 }
 
 }  // namespace eg
