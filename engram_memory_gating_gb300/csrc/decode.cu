@@ -28,7 +28,10 @@ namespace {
 
 // Programmatic dependent launch: the row kernel is scheduled while the
 // projection runs and waits for the projection grid only where it reads the
-// partial sums.
+// partial sums.  The projection is itself launched that way: it waits for the
+// preceding kernel (e.g. the previous decode step, which wrote the cache it
+// shifts) before reading anything, so only its launch overlaps that kernel's
+// tail.  Each kernel lets its successor be scheduled only after its own wait.
 EG_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 EG_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -67,6 +70,7 @@ __global__ void __launch_bounds__(32 * kWarps1, 2) decode_proj_kernel(const Deco
     const int m1 = min(p.dmem, m0 + rows);
     const int b0 = blockIdx.z * kBc;
     const int nb = min(kBc, p.B - b0);
+    grid_dep_wait();
     grid_dep_launch();
     // the cache shift (independent of the projection), spread over all CTAs:
     // row r < max_len - 1 of the new cache is row r + 1 of the left-padded old one
@@ -227,6 +231,7 @@ __global__ void __launch_bounds__(kThreads2) decode_row_kernel(const DecodeParam
         wc[q] = ok ? __ldg(p.wh + i) : 0.f;
     }
     grid_dep_wait();
+    grid_dep_launch();   // the next decode step's projection may be scheduled (it waits for this grid)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // sum h^2, k^2, h k w_h^2, v^2
     int it = 0;
     for (int i = c0 + threadIdx.x; i < c0 + ncol; i += blockDim.x, ++it) {
@@ -335,8 +340,17 @@ cudaError_t decode_prepare() {
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s) {
     const dim3 g1(static_cast<unsigned>((p.d + kCols - 1) / kCols), static_cast<unsigned>(p.splits),
                   static_cast<unsigned>((p.B + kBc - 1) / kBc));
-    decode_proj_kernel<<<g1, 32 * kWarps1, decode_proj_smem(p.rows_per_split), s>>>(p);
-    cudaError_t e = cudaPeekAtLastError();
+    cudaLaunchConfig_t cfg1 = {};
+    cudaLaunchAttribute attr1[1];
+    attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr1[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg1.gridDim = g1;
+    cfg1.blockDim = dim3(32 * kWarps1, 1, 1);
+    cfg1.dynamicSmemBytes = static_cast<size_t>(decode_proj_smem(p.rows_per_split));
+    cfg1.stream = s;
+    cfg1.attrs = attr1;
+    cfg1.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg1, decode_proj_kernel, p);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
