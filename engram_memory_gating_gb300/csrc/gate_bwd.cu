@@ -256,9 +256,6 @@ constexpr int kRing2Off = 256;  // after the stage mbarriers and release counter
 // known at compile time; otherwise runtime d and strides.
 template <bool kPacked>
 __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdParams p) {
-    // the merge kernel may be scheduled as this grid's CTAs leave; it waits
-    // for the whole grid before it reads the partials
-    grid_dep_launch();
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);                            // [stages]
     unsigned int* released = reinterpret_cast<unsigned int*>(smem + kMaxStages * 8);  // [stages]
@@ -341,8 +338,11 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     if (tid == 0)
         for (int j = 0; j < pro; ++j) issue_inputs(j, j);
     // the inputs above were written before the coefficient kernel started;
-    // the scalars are that kernel's output
+    // the scalars are that kernel's output.  After the wait the merge kernel
+    // may be scheduled (as this grid's CTAs leave; it waits for the whole grid
+    // before it reads the partials)
     grid_dep_wait();
+    grid_dep_launch();
     if (tid == 0)
         for (int j = 0; j < pro; ++j) issue_scalars(j, j);
 

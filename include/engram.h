@@ -32,6 +32,13 @@
  *    so it may be captured in a CUDA graph.  The first call on a device also
  *    performs one-time, per-device set-up (kernel attributes and occupancy
  *    queries); make that first call before any stream capture.
+ *  - Ordering is plain stream order.  Most kernels are launched with
+ *    programmatic stream serialisation, so a kernel may be scheduled while
+ *    the one before it on the stream finishes. Each waits for that kernel to
+ *    complete (griddepcontrol.wait) before it reads anything the kernel may
+ *    have written, and lets the next kernel be scheduled only after that
+ *    wait.  A caller's kernel launched the same way after one of ours must
+ *    likewise wait before it reads our outputs, as that launch mode requires.
  *  - A non-OK status means nothing was enqueued, except ENGRAM_ERR_LAUNCH
  *    (the launch itself failed; the stream state is then the CUDA runtime's).
  *    The library never prints, traps or aborts.
