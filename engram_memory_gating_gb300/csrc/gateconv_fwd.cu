@@ -208,8 +208,9 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
                     const float2 cc =
                         fma2(cw[0][i], U[(w + 1) & 3][i],
                              fma2(cw[1][i], U[(w + 2) & 3][i], fma2(cw[2][i], U[(w + 3) & 3][i], mul2(cw[3][i], u))));
-                    const float2 den = make_float2(1.0f + __expf(-cc.x), 1.0f + __expf(-cc.y));
-                    y[i] = add2(make_float2(__fdividef(cc.x, den.x), __fdividef(cc.y, den.y)), vh[i]);
+                    // SiLU(c) = c / (1 + e^-c)
+                    const float2 rden = make_float2(rcp_ftz(1.0f + exp_neg_ftz(cc.x)), rcp_ftz(1.0f + exp_neg_ftz(cc.y)));
+                    y[i] = fma2(cc, rden, vh[i]);
                     U[w][i] = u;
                 }
                 if (active && j0 + w < ntok && t_first + j0 + w >= t_out) {
