@@ -142,24 +142,6 @@ EG_DEV void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* 
         : "memory");
 }
 
-// e^-x and 1/x on the special-function unit with the .ftz forms of the PTX
-// approximate instructions (subnormal inputs and results flushed to zero,
-// which spares the extra handling of the plain forms): e^-x = 2^(-x log2 e)
-// by ex2.approx.ftz.f32, 1/x by rcp.approx.ftz.f32 (each about 2^-22
-// relative error, PTX ISA).  Used only where a subnormal cannot matter: in
-// 1 / (1 + e^-x) the denominator is at least 1, and an exponential that
-// underflows only saturates the sigmoid.
-EG_DEV float exp_neg_ftz(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * -1.44269504f));
-    return y;
-}
-EG_DEV float rcp_ftz(float x) {
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 EG_DEV uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -77,7 +77,7 @@ EG_DEV void consume(Windows& W, float2 (&gcw)[4][2], const Weights& P, const uns
         const float2 cc = fma2(P.cw[0][i], W.U[(S + 1) & 3][i],
                                fma2(P.cw[1][i], W.U[(S + 2) & 3][i],
                                     fma2(P.cw[2][i], W.U[(S + 3) & 3][i], mul2(P.cw[3][i], u))));
-        const float2 sg = make_float2(rcp_ftz(1.0f + exp_neg_ftz(cc.x)), rcp_ftz(1.0f + exp_neg_ftz(cc.y)));
+        const float2 sg = make_float2(gc::rcp_ftz(1.0f + gc::exp_neg_ftz(cc.x)), gc::rcp_ftz(1.0f + gc::exp_neg_ftz(cc.y)));
         // SiLU'(c) = s (1 + c (1 - s))
         const float2 one = splat2(1.0f);
         float2 d = mul2(mul2(dy, sg), fma2(cc, sub2(one, sg), one));

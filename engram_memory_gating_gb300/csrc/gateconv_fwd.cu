@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
                         fma2(cw[0][i], U[(w + 1) & 3][i],
                              fma2(cw[1][i], U[(w + 2) & 3][i], fma2(cw[2][i], U[(w + 3) & 3][i], mul2(cw[3][i], u))));
                     // SiLU(c) = c / (1 + e^-c)
-                    const float2 rden = make_float2(rcp_ftz(1.0f + exp_neg_ftz(cc.x)), rcp_ftz(1.0f + exp_neg_ftz(cc.y)));
+                    const float2 rden = make_float2(gc::rcp_ftz(1.0f + gc::exp_neg_ftz(cc.x)), gc::rcp_ftz(1.0f + gc::exp_neg_ftz(cc.y)));
                     y[i] = fma2(cc, rden, vh[i]);
                     U[w][i] = u;
                 }
