@@ -88,3 +88,41 @@ def test_decode_is_deterministic_and_graph_capturable():
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), ref[0].view(torch.int16))
     assert torch.equal(ns.view(torch.int16), ref[1].view(torch.int16))
+
+
+def test_decode_chain_on_device_without_host_sync():
+    """Eight decode steps on one stream, each reading the cache the previous
+    step wrote (two buffers used in turn) and sharing one workspace, enqueued
+    back to back.  Each step's projection is launched with programmatic stream
+    serialisation behind the previous step's row kernel, so it may be scheduled
+    early; this checks that it waits for that kernel before it reads the cache
+    or overwrites the workspace, against the same chain synchronised after
+    every step (bit-exact: the kernels are deterministic)."""
+    B, dmem, d, max_len, w, dil = 4, 512, 1024, 8, 4, 3
+    inp = {k: v.cuda() for k, v in decode_inputs(B, dmem, d, max_len, w, seed=11).items()}
+    g = torch.Generator().manual_seed(12)
+    es = [torch.randn((B, dmem), generator=g).to(torch.bfloat16).cuda() for _ in range(8)]
+    hs = [torch.randn((B, d), generator=g).to(torch.bfloat16).cuda() for _ in range(8)]
+    ws = torch.empty(eg.engram_decode_workspace_size(B, dmem, d), device="cuda", dtype=torch.uint8)
+
+    def run(sync):
+        caches = [inp["conv_state"].clone(), torch.empty((B, max_len, d), device="cuda", dtype=torch.bfloat16)]
+        ys = []
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for t in range(8):
+                y = torch.empty((B, d), device="cuda", dtype=torch.bfloat16)
+                eg.engram_decode_fwd(es[t], hs[t], caches[t & 1], inp["W_K"], inp["W_V"], inp["rms_w_h"],
+                                     inp["rms_w_v"], inp["conv_w"], y, caches[(t + 1) & 1], ws, dil, stream=s)
+                if sync:
+                    torch.cuda.synchronize()
+                ys.append(y)
+        torch.cuda.synchronize()
+        return ys, caches[0]
+
+    want_y, want_cache = run(True)
+    got_y, got_cache = run(False)
+    for a, b in zip(want_y, got_y):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(want_cache.view(torch.int16), got_cache.view(torch.int16))

@@ -300,3 +300,48 @@ def test_launch_geometry():
     bwd = eg.engram_launch_info(1, 8192)
     assert bwd["cluster"] >= 2 and 5120 % (8 * bwd["cluster"]) == 0
     assert bwd["clusters"] <= 8192 // 128
+
+
+def test_chained_steps_without_host_sync_match_synchronised_ones():
+    """Three forward + backward steps in which each step's grad_x is the next
+    step's X and its out the next step's grad_out, enqueued back to back on one
+    stream with nothing between the calls.  The gate kernels are launched with
+    programmatic stream serialisation, so each may be scheduled while its
+    predecessor finishes; this checks that every kernel still reads only
+    completed data, against the same chain with a device synchronisation after
+    every call (no overlap at all).  The kernels are deterministic, so the two
+    chains must agree bit for bit."""
+    N = 256
+    inp = to_dev(gate_inputs(N, 21, mask="bern0.9"))
+    ws = torch.empty(eg.engram_gate_bwd_workspace_size(N), device=DEV, dtype=torch.uint8)
+
+    def run(sync):
+        x, gout = inp["x"].clone(), inp["grad_out"].clone()
+        results = []
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                out = torch.empty_like(x)
+                saved = torch.empty((N, 4, 4), device=DEV)
+                gx, gkv = torch.empty_like(x), torch.empty_like(inp["kv"])
+                gw = torch.empty_like(inp["weight"])
+                eg.engram_gate_fwd(x, inp["kv"], inp["weight"], inp["mask"], out, saved, stream=s)
+                if sync:
+                    torch.cuda.synchronize()
+                eg.engram_gate_bwd(x, inp["kv"], inp["weight"], saved, gout, gx, gkv, gw, ws, stream=s)
+                if sync:
+                    torch.cuda.synchronize()
+                results.append((out, saved, gx, gkv, gw))
+                x, gout = gx, out
+        torch.cuda.synchronize()
+        return results
+
+    want = run(True)
+    got = run(False)
+    for step_w, step_g in zip(want, got):
+        for a, b in zip(step_w, step_g):
+            if a.dtype == torch.bfloat16:
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+            else:
+                assert torch.equal(a, b)
