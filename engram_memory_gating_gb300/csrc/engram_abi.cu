@@ -205,7 +205,9 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
     c.cluster = 1;
     c.threads = 256;
     c.stages = kGateBwdStages;
-    c.smem = 256 + c.stages * (12 * ncols * 2 + 128);
+    // barriers, (packed layout, blocks == false) the token group's scalars
+    // (64 B a token) and zero flags, the ring
+    c.smem = 256 + (blocks ? 0 : kGateBwdTableTokens * (64 + 1)) + c.stages * (12 * ncols * 2 + 128);
     if (max_clusters(st, 1, 1, c.threads, c.smem) <= 0) return false;
     const int mc1 = max_clusters(st, 1, 1, 256, 0);
     if (mc1 <= 0) return false;
@@ -222,7 +224,11 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
         const int resident = max_clusters(st, 1, 1, c.threads, c.smem);
         const int64_t wave = resident / C > 0 ? resident / C : 1;
         const int64_t most = nb >= 2 ? nb / 2 : 1;
-        const int64_t groups = most <= wave ? most : wave * (most / wave);
+        int64_t groups = most <= wave ? most : wave * (most / wave);
+        // at most kGateBwdTableTokens tokens a group (its scalars are staged in
+        // shared memory); ceil(N / 256) groups still fit the slots (<= nb / 2)
+        const int64_t least = (N + kGateBwdTableTokens - 1) / kGateBwdTableTokens;
+        if (groups < least) groups = least;
         group_tokens = static_cast<int>((N + groups - 1) / groups);
     }
     c.clusters = C;

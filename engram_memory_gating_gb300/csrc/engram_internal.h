@@ -13,6 +13,10 @@ constexpr int kGateHidden = 5120;
 // Largest number of ring stages any kernel uses (mbarrier area sizing).
 constexpr int kMaxStages = 16;
 
+// Largest token group of the backward's elementwise kernel: its per-token
+// scalars (64 bytes a token) and zero flags are staged in shared memory.
+constexpr int kGateBwdTableTokens = 256;
+
 // Saved-state gate.  Row (n, s) of X is x + (n*4 + s)*d; the key row is
 // key + n*key_ts + s*d and the shared value row v + n*v_ts (packed KV:
 // key = kv, key_ts = 5d, v = kv + 4d, v_ts = 5d).  Saved state: packed

@@ -197,24 +197,41 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
         __syncwarp();
         npend = 0;
     };
-    if (gpair < p.N) load_group(gpair, 0, v0, g0);
+    // A masked token (its four saved gates 0) has ddot = 0 whatever dgate is,
+    // so its grad_out and v rows are not read (its sums stay 0).  Lane s < 4
+    // loads the saved gate of stream s one token ahead of its use.
+    auto load_gate = [&](long long n) -> float {
+        if (n >= p.N || lane >= kS) return 0.f;
+        return kDFix ? __ldg(p.saved + (n * kS + lane) * 4) : __ldg(p.sv_gate + n * kS + lane);
+    };
+    bool skip = __all_sync(kFullMask, load_gate(gpair) == 0.f);
+    if (gpair < p.N && !skip) load_group(gpair, 0, v0, g0);
+    float gnext = load_gate(gpair + npairs);
     int par = 0;
     for (long long n = gpair; n < p.N; n += npairs, par ^= 1) {
+        const bool has_next = n + npairs < p.N;
+        const bool skip_next = __all_sync(kFullMask, gnext == 0.f);   // loaded one token ago
+        gnext = load_gate(n + 2 * npairs);                            // in flight during this token
 #pragma unroll
         for (int s = 0; s < kS; ++s) hi[s] = lo[s] = make_float2(0.f, 0.f);
+        if (!skip) {
 #pragma unroll
-        for (int grp = 0; grp < ng; grp += 2) {
-            // buffer 0 holds group grp; its successor goes to buffer 1, then
-            // buffer 0 takes group grp + 2 or the first group of the next
-            // token (whose loads then overlap this token's reduction and fp64 work)
-            load_group(n, grp + 1, v1, g1);
-            accumulate(grp, v0, g0);
-            if (grp + 2 < ng)
-                load_group(n, grp + 2, v0, g0);
-            else if (n + npairs < p.N)
-                load_group(n + npairs, 0, v0, g0);
-            accumulate(grp + 1, v1, g1);
+            for (int grp = 0; grp < ng; grp += 2) {
+                // buffer 0 holds group grp; its successor goes to buffer 1, then
+                // buffer 0 takes group grp + 2 or the first group of the next
+                // token (whose loads then overlap this token's reduction and fp64 work)
+                load_group(n, grp + 1, v1, g1);
+                accumulate(grp, v0, g0);
+                if (grp + 2 < ng)
+                    load_group(n, grp + 2, v0, g0);
+                else if (has_next && !skip_next)
+                    load_group(n + npairs, 0, v0, g0);
+                accumulate(grp + 1, v1, g1);
+            }
+        } else if (has_next && !skip_next) {
+            load_group(n + npairs, 0, v0, g0);
         }
+        skip = skip_next;
         float h[kS], l[kS];
 #pragma unroll
         for (int s = 0; s < kS; ++s) {
@@ -247,7 +264,14 @@ __global__ void __launch_bounds__(256, 2) gate_bwd_coef_kernel(const GateBwdPara
 }
 
 // ---------------------------------------------------------------- kernel 2
-constexpr int kRing2Off = 256;  // after the stage mbarriers and release counters
+// Shared memory: stage mbarriers and release counters, the table's mbarrier,
+// (packed layout) the token group's scalars and zero flags, then the ring.
+constexpr int kTableBarOff = 192;
+constexpr int kTableOff = 256;
+constexpr int kZeroOff = kTableOff + kGateBwdTableTokens * 64;
+template <bool kPacked>
+constexpr int kRing2Off = kPacked ? kZeroOff + kGateBwdTableTokens : 256;
+static_assert(kRing2Off<true> % 128 == 0, "ring alignment");
 
 // Thread mapping: lane = 8 * stream + g, warp w; the thread owns the 8 columns
 // col0 + 8 * (8w + g) of one stream.  The four streams of a column group sit
@@ -259,7 +283,8 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);                            // [stages]
     unsigned int* released = reinterpret_cast<unsigned int*>(smem + kMaxStages * 8);  // [stages]
-    unsigned char* ring = smem + kRing2Off;
+    uint64_t* tbar = reinterpret_cast<uint64_t*>(smem + kTableBarOff);
+    unsigned char* ring = smem + kRing2Off<kPacked>;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -284,6 +309,13 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     const long long t0 = grp * p.group_tokens;
     const long long t1 = (t0 + p.group_tokens < p.N) ? t0 + p.group_tokens : p.N;
     const long long ntok = t1 > t0 ? t1 - t0 : 0;
+    // Packed layout: the group's per-token scalars (16 floats a token), and a
+    // flag per token whose scalars are all zero (a masked token: grad_x =
+    // grad_out, grad_key = 0, no grad_w term, so its X and key rows are not
+    // needed).  The separate-tensor gate has no mask; its stages carry their
+    // token's scalars instead.
+    float* table = reinterpret_cast<float*>(smem + kTableOff);
+    unsigned char* zero_tok = smem + kZeroOff;
 
     float2 w2[4];
     if (active) {
@@ -303,69 +335,104 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
             mbar_init(&full[st], 1);
             released[st] = 0u;
         }
+        mbar_init(tbar, 1);
         fence_mbar_init();
     }
     __syncthreads();
 
     const uint32_t gate_bytes = 16u * static_cast<uint32_t>(gstride);
-    // a stage: the token's input rows, then its scalars and saved gates (the
-    // coefficient kernel's output and the state it read, copied only after
-    // that grid has completed)
-    auto issue_inputs = [&](int j, int st) {
+    const uint32_t scalar_bytes = kPacked ? 0u : 64u;   // per-stage scalars (separate layout)
+    // a stage: the token's input rows (grad_out only for a token whose scalars
+    // are all zero), then (separate layout) its scalars and its saved gates
+    // (the coefficient kernel's output and the state it read, copied only
+    // after that grid has completed)
+    auto issue_inputs = [&](int j, int st, bool rows_xk) {
         const long long n = t0 + j;
         unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
-        mbar_arrive_expect_tx(&full[st], kRows * copy_bytes + 64u + gate_bytes);
+        mbar_arrive_expect_tx(&full[st], (rows_xk ? kRows : kS) * copy_bytes + scalar_bytes + gate_bytes);
 #pragma unroll
         for (int r = 0; r < kS; ++r) {
-            bulk_g2s(b + r * row_bytes, p.x + (n * kS + r) * d + col0, copy_bytes, &full[st]);
-            bulk_g2s(b + (kS + r) * row_bytes, p.key + n * key_ts + static_cast<long long>(r) * d + col0,
-                     copy_bytes, &full[st]);
+            if (rows_xk) {
+                bulk_g2s(b + r * row_bytes, p.x + (n * kS + r) * d + col0, copy_bytes, &full[st]);
+                bulk_g2s(b + (kS + r) * row_bytes, p.key + n * key_ts + static_cast<long long>(r) * d + col0,
+                         copy_bytes, &full[st]);
+            }
             bulk_g2s(b + (2 * kS + r) * row_bytes, p.gout + (n * kS + r) * d + col0, copy_bytes, &full[st]);
         }
     };
-    auto issue_scalars = [&](int j, int st) {
+    auto issue_gates = [&](int j, int st) {
         const long long n = t0 + j;
         unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
-        bulk_g2s(b + kRows * row_bytes, p.coef + n * kS * 4, 64u, &full[st]);
+        if (!kPacked) bulk_g2s(b + kRows * row_bytes, p.coef + n * kS * 4, 64u, &full[st]);
         const float* gsrc = p.saved != nullptr ? p.saved + n * kS * 4 : p.sv_gate + n * kS;
         bulk_g2s(b + kRows * row_bytes + 64, gsrc, gate_bytes, &full[st]);
     };
-    auto issue = [&](int j, int st) {
-        issue_inputs(j, st);
-        issue_scalars(j, st);
-    };
     const int pro = ntok < stages ? static_cast<int>(ntok) : stages;
     if (tid == 0)
-        for (int j = 0; j < pro; ++j) issue_inputs(j, j);
+        for (int j = 0; j < pro; ++j) issue_inputs(j, j, true);
     // the inputs above were written before the coefficient kernel started;
     // the scalars are that kernel's output.  After the wait the merge kernel
     // may be scheduled (as this grid's CTAs leave; it waits for the whole grid
     // before it reads the partials)
     grid_dep_wait();
     grid_dep_launch();
-    if (tid == 0)
-        for (int j = 0; j < pro; ++j) issue_scalars(j, j);
+    if (tid == 0) {
+        if (kPacked) {
+            // the group's scalars in one copy (ntok <= kGateBwdTableTokens)
+            const uint32_t tb = static_cast<uint32_t>(ntok) * kS * 16u;
+            mbar_arrive_expect_tx(tbar, tb);
+            if (tb > 0) bulk_g2s(table, p.coef + t0 * kS * 4, tb, tbar);
+        }
+        for (int j = 0; j < pro; ++j) issue_gates(j, j);
+    }
+    bool failed = false;
+    if (kPacked) {
+        failed = !mbar_wait(tbar, 0u);
+        for (int j = tid; j < ntok; j += blockDim.x) {
+            const float4* c = reinterpret_cast<const float4*>(table + j * kS * 4);
+            bool z = true;
+#pragma unroll
+            for (int q = 0; q < kS; ++q) {
+                const float4 v = c[q];
+                z = z && v.x == 0.f && v.y == 0.f && v.z == 0.f && v.w == 0.f;
+            }
+            zero_tok[j] = z ? 1 : 0;
+        }
+        __syncthreads();
+    }
 
     float2 phi[4], plo[4];  // grad_w of this thread's columns, hi + lo
 #pragma unroll
     for (int e = 0; e < 4; ++e) phi[e] = plo[e] = make_float2(0.f, 0.f);
 
-    bool failed = false;
     int st = 0;
     uint32_t phase = 0;
     for (int j = 0; j < ntok; ++j) {
         const long long n = t0 + j;
         if (!failed && !mbar_wait(&full[st], phase)) failed = true;
         const unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
-        const float* cf = reinterpret_cast<const float*>(b + kRows * row_bytes);  // [s][4]
-        const float4 c4 = *reinterpret_cast<const float4*>(cf + 4 * s);
+        const float* cf = kPacked ? table + j * kS * 4 : reinterpret_cast<const float*>(b + kRows * row_bytes);
+        const float4 c4 = *reinterpret_cast<const float4*>(cf + 4 * s);   // [s][4]
         const float2 A82 = splat2(c4.x), Ar2 = splat2(c4.y);
         const float2 A2 = splat2(__fadd_rn(c4.x, c4.y));
         const float2 nB2 = splat2(c4.z), nC2 = splat2(c4.w);
-        const float2 G2 = splat2(cf[16 + gstride * s]);  // saved gate of stream s
+        // saved gate of stream s
+        const float2 G2 = splat2(reinterpret_cast<const float*>(b + kRows * row_bytes + 64)[gstride * s]);
+        const bool zt = kPacked && zero_tok[j] != 0;   // the same for the whole CTA
         float2 gv[4];
         uint32_t ox[4], ok[4];
-        if (active) {
+        if (active && zt) {
+            // all scalars zero: grad_x = grad_out bit for bit, grad_key = 0,
+            // no grad_w term (X and key were not copied for this token)
+            const uint4 gq = lds128(b + (2 * kS + s) * row_bytes + 16 * cg);
+            const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                ox[e] = gw[e];
+                ok[e] = 0u;
+                gv[e] = mul2(G2, bf2(gw[e]));
+            }
+        } else if (active) {
             const uint4 xq = lds128(b + s * row_bytes + 16 * cg);
             const uint4 kq = lds128(b + (kS + s) * row_bytes + 16 * cg);
             const uint4 gq = lds128(b + (2 * kS + s) * row_bytes + 16 * cg);
@@ -398,7 +465,8 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
                 released[st] = 0u;
                 if (j + stages < ntok) {
                     fence_proxy_async();
-                    issue(j + stages, st);
+                    issue_inputs(j + stages, st, !kPacked || zero_tok[j + stages] == 0);
+                    issue_gates(j + stages, st);
                 }
             }
         }
@@ -447,9 +515,11 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     if (failed) {
         atomicOr(p.err, kErrTimeout);
         // let the copies this CTA issued land before it leaves (bounded)
-        if (tid == 0)
+        if (tid == 0) {
+            if (kPacked) (void)mbar_wait(tbar, 0u);
             for (int t = ntok > stages ? static_cast<int>(ntok) - stages : 0; t < ntok; ++t)
                 (void)mbar_wait(&full[t % stages], static_cast<uint32_t>((t / stages) & 1));
+        }
     }
 }
 
