@@ -300,6 +300,12 @@ def test_launch_geometry():
     bwd = eg.engram_launch_info(1, 8192)
     assert bwd["cluster"] >= 2 and 5120 % (8 * bwd["cluster"]) == 0
     assert bwd["clusters"] <= 8192 // 128
+    # token groups of at most 256 tokens (their scalars are staged in shared
+    # memory), and their (hi, lo) grad_weight pairs fit the workspace's slots
+    for N in (64, 128, 192, 4096, 8192, 11520, 65536, 65728, 1 << 20):
+        groups = eg.engram_launch_info(1, N)["clusters"]
+        assert -(-N // groups) <= 256
+        assert N // 64 < 2 or 2 * groups <= N // 64
 
 
 def test_chained_steps_without_host_sync_match_synchronised_ones():
