@@ -26,3 +26,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    try:
+        from tolerance import WORST
+    except Exception:  # pragma: no cover
+        return
+    if not WORST:
+        return
+    tr = terminalreporter
+    tr.section("parity: worst |gpu - exact| / tol per output (1.0 = at the bound)")
+    tr.write_line(f"{'output':<40} {'worst':>9} {'near-zero only':>15} {'elements':>12}")
+    for name in sorted(WORST):
+        worst, floor_hits, n = WORST[name]
+        tr.write_line(f"{name:<40} {worst:9.4f} {floor_hits:15d} {n:12d}")
