@@ -16,10 +16,11 @@ Each function follows the page and section cited in the C++ source:
 Parity status: gate_fwd, gate_bwd and the bf16 helpers are pinned by the
 tests in ``tests/test_oracle_*.py`` (closed forms, invariants, brute-force
 finite differences, library rounding).  gateconv_fwd / gateconv_bwd are
-pinned by closed forms, causality and finite differences, but the gate
-formula inside them (a plain sigmoid of the normalised dot scaled by
-1/sqrt(d)) and the conv tap order are readings the page does not print:
-for those two choices parity is unpinned.
+pinned by closed forms, causality and finite differences, and their conv
+(tap order, causal padding; with a dilation in decode_fwd) against the
+standard causal depthwise conv1d of torch.  The gate formula inside them (a
+plain sigmoid of the normalised dot scaled by 1/sqrt(d)) is a reading the
+page does not print: for that choice parity is unpinned.
 """
 from __future__ import annotations
 

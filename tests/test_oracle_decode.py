@@ -7,7 +7,10 @@ are the GateConv ones.  Pinned here without re-typing the formula:
     delta positions (zeros between);
   * a single nonzero tap reads exactly the cached token at its lag (or the
     current token, or zero beyond the cache);
-  * the cache update is a one-token shift of the left-padded cache.
+  * the cache update is a one-token shift of the left-padded cache;
+  * the dilated taps against the standard causal conv1d (torch's grouped
+    Conv1d with dilation and left padding, written independently of the
+    oracle), which fixes the tap order at every dilation.
 """
 import numpy as np
 import pytest
@@ -91,3 +94,39 @@ def test_cache_update_is_a_one_token_shift(L, max_len):
     # the new last row is this token's conv input: rms 1 after w_v is divided out
     u = s[:, -1] / wv
     assert np.allclose(np.sqrt(np.mean(u * u, axis=1)), 1.0, rtol=1e-5)
+
+
+@pytest.mark.parametrize("w,dil,L,max_len,seed", [(4, 1, 6, 8, 41), (4, 3, 12, 16, 42),
+                                                  (3, 2, 2, 8, 43), (5, 4, 16, 16, 44)])
+def test_dilated_tap_order_is_the_standard_causal_conv1d(w, dil, L, max_len, seed):
+    """The page's decode step is a dilated depthwise conv over the cached conv
+    inputs.  The standard causal form is PyTorch's grouped Conv1d with
+    dilation delta and (w - 1) delta zeros of left padding: at the last
+    position, tap j multiplies the input (w - 1 - j) delta steps back.  torch's
+    fp64 conv1d, applied to the sequence [cache rows oldest first, this
+    token's u], recomputes y = SiLU(c) + vhat from the oracle's own u (read
+    back from the last row of the new cache), which pins the tap order, the
+    dilation and the zero reads beyond the cache to that convention."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(seed)
+    B, dmem, d = 2, 8, 16
+    e = rng.standard_normal((B, dmem))
+    h = rng.standard_normal((B, d))
+    state = rng.standard_normal((B, L, d))
+    WK = rng.standard_normal((dmem, d)) / np.sqrt(dmem)
+    WV = rng.standard_normal((dmem, d)) / np.sqrt(dmem)
+    wh, wv, cw = weights(rng, d, w)
+    y, ns = oracle.decode_fwd(e, h, state, WK, WV, wh, wv, cw, max_len, dil)
+    u = ns[:, -1]                                                   # this token's u
+    k = e @ WK
+    v = e @ WV
+    rh = 1.0 / np.sqrt(np.mean(h * h, axis=1) + oracle.GATECONV_EPS)
+    rk = 1.0 / np.sqrt(np.mean(k * k, axis=1) + oracle.GATECONV_EPS)
+    alpha = sig(np.sum((h * rh[:, None] * wh) * (k * rk[:, None] * wh), axis=1) / np.sqrt(d))
+    vhat = alpha[:, None] * v
+    seq = np.concatenate([state, u[:, None]], axis=1)               # (B, L + 1, d)
+    x = torch.from_numpy(seq).permute(0, 2, 1)                       # (B, d, L + 1)
+    x = torch.nn.functional.pad(x, ((w - 1) * dil, 0))
+    wt = torch.from_numpy(cw.T.copy()).unsqueeze(1)                 # (d, 1, w)
+    c = torch.nn.functional.conv1d(x, wt, groups=d, dilation=dil)[..., -1].numpy()
+    assert np.allclose(y, c / (1.0 + np.exp(-c)) + vhat, rtol=1e-12, atol=1e-13)

@@ -8,9 +8,13 @@ formula.  Checked here:
     (Y = 0 and no gradient into H or k), H = k (alpha = sigmoid(sqrt(d)));
   * invariants: causality along the sequence, independence of batch rows;
   * brute force: fourth-order central finite differences of the fp64
-    forward against the analytic backward for every input and weight.
-The gate formula's 1/sqrt(d) scale and the tap order are readings of the
-page, not printed by it: for those, parity is unpinned.
+    forward against the analytic backward for every input and weight;
+  * the conv against the standard causal depthwise conv1d (torch's grouped
+    Conv1d with left padding, written independently of the oracle), which
+    fixes the tap order and the causal zero padding.
+The gate formula (a plain sigmoid of the normalised dot scaled by 1/sqrt(d),
+one weight shared by H and k) is a reading of the page, not printed by it:
+for that choice parity is unpinned.
 """
 import math
 
@@ -165,3 +169,27 @@ def test_backward_matches_finite_differences(M, T, d):
                                                     rh, rk, rv)
     for theta, an in ((H, dH), (k, dk), (v, dv), (wh, dwh), (wv, dwv), (cw, dcw)):
         _fd_check(loss, theta, an)
+
+
+@pytest.mark.parametrize("M,T,d,seed", [(2, 11, 16, 31), (1, 3, 8, 32), (3, 40, 24, 33)])
+def test_conv_is_the_standard_causal_depthwise_conv1d(M, T, d, seed):
+    """The page names the op's middle stage a causal depthwise conv1d with
+    (4, d) weights.  The standard form of that layer is PyTorch's grouped
+    Conv1d (groups = d, one 4-tap filter per channel, no bias) applied with
+    3 zeros of left padding and the output cut to the first T positions, i.e.
+    a cross-correlation in which tap j multiplies the input 3 - j steps back
+    (tap 3 the current token).  Here torch's fp64 conv1d, an implementation
+    written independently of the oracle, recomputes Y = SiLU(conv(u)) + vhat
+    from the oracle's own u = vhat rrms_v w_v, so the tap order, the causal
+    padding and the per-row reset are pinned to that convention."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(seed)
+    H, k, v, wh, wv, cw = rand_case(rng, M, T, d)
+    Y, vhat, alpha, rh, rk, rv = oracle.gateconv_fwd(H, k, v, wh, wv, cw)
+    u = torch.from_numpy(vhat * rv[..., None] * wv)                 # (M, T, d)
+    x = u.permute(0, 2, 1)                                           # (M, d, T)
+    x = torch.nn.functional.pad(x, (3, 0))                           # causal left padding
+    w = torch.from_numpy(cw.T.copy()).unsqueeze(1)                  # (d, 1, 4): tap j at index j
+    c = torch.nn.functional.conv1d(x, w, groups=d)[..., :T]          # (M, d, T)
+    c = c.permute(0, 2, 1).numpy()
+    assert np.allclose(Y, silu(c) + vhat, rtol=1e-13, atol=1e-14)
