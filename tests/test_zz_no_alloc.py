@@ -4,26 +4,22 @@ engram_gate_bwd_noalloc runs the same backward as engram_gate_bwd, with its
 workspace taken from a fixed array inside the library instead of a buffer the
 caller allocates (for callers inside a graph capture, inside a framework that
 owns all device memory, or on a fixed memory budget).  Checked through the C
-ABI: two calls in a row agree with the workspace entry point within the
-tests' tolerances, they change the device's free memory by nothing, and a
-size beyond the array's limit is refused before any work is enqueued.
+ABI: two calls in a row give the same bits as the workspace entry point (the
+same deterministic kernels run, only the workspace's address differs, so any
+difference would mean a misplaced workspace slot), they change the device's
+free memory by nothing, and a size beyond the array's limit is refused before
+any work is enqueued.
 This file is collected last on purpose.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 import engram_memory_gating_gb300 as eg
-from engram_memory_gating_gb300.inputs import bf16_bits, gate_inputs
-from tolerance import bf16_bits_to_f64, check_bf16, check_f32
+from engram_memory_gating_gb300.inputs import gate_inputs
 
 MAX_N = 2048
-
-
-def as_exact(t):
-    return bf16_bits_to_f64(bf16_bits(t)).reshape(tuple(t.shape))
 
 
 @pytest.mark.gpu
@@ -51,10 +47,9 @@ def test_gate_bwd_noalloc_matches_workspace_entry_point_twice():
             torch.cuda.synchronize()
             if call == 1:
                 assert torch.cuda.mem_get_info()[0] == free_before
-            check_bf16("grad_x", bf16_bits(gx), as_exact(ref[0]))
-            check_bf16("grad_kv", bf16_bits(gkv).reshape(N, 5, 5120),
-                       as_exact(ref[1]).reshape(N, 5, 5120))
-            check_f32("grad_weight", gw.cpu().numpy(), ref[2].double().cpu().numpy())
+            assert torch.equal(gx.view(torch.int16), ref[0].view(torch.int16))
+            assert torch.equal(gkv.view(torch.int16), ref[1].view(torch.int16))
+            assert torch.equal(gw.view(torch.int32), ref[2].view(torch.int32))
     assert eg.engram_device_error() == 0
 
 
