@@ -32,6 +32,7 @@ BWD_BYTES_PER_TOKEN = 4 * D * 2 + 5 * D * 2 + 64 + 4 * D * 2 + 4 * D * 2 + 5 * D
 FWD_FIXED = 4 * D * 4                 # weight
 BWD_FIXED = 2 * 4 * D * 4             # weight + grad_weight
 METRIC = "Engram gate fwd+bwd tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+NOMINAL_GBS = 8000.0  # GB300's nominal HBM3e bandwidth (~8 TB/s), the second denominator
 WORKLOAD = ("saved-state gate fwd+bwd, N=8192, S=4, d=5120, bf16 X/KV ~N(0,1), "
             "weight 1+0.1N(0,1), mask~Bernoulli(0.9), grad_out ~N(0,1), eps 1e-20, seed 1")
 
@@ -166,7 +167,8 @@ def graph_of(torch, fn, stream):
 def op_entry(ms, nbytes, peak):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"ms": round(ms, 5), "algorithmic_bytes": int(nbytes), "GB_s": round(gbs, 1),
-            "frac_of_measured_peak": round(gbs / peak, 4)}
+            "frac_of_measured_peak": round(gbs / peak, 4),
+            "frac_of_nominal_peak": round(gbs / NOMINAL_GBS, 4)}
 
 
 def extra_ops(torch, eg, inputs_mod, stream, peak):
@@ -603,10 +605,12 @@ def main():
         "roofline": {"kernel": "engram_gate_bwd (gate_bwd_coef_kernel + gate_bwd_main_kernel + wreduce_kernel), N=8192",
                      "bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(bwd_gbs / peak, 4),
+                     "peak_nominal": NOMINAL_GBS, "frac_nominal": round(bwd_gbs / NOMINAL_GBS, 4),
                      "traffic": traffic},
         "roofline_fwd": {"kernel": "engram_gate_fwd (gate_fwd_quad_kernel<true>), N=8192", "bound": "hbm",
                          "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(fwd_gbs / peak, 4), "traffic": traffic_fwd},
+                         "frac": round(fwd_gbs / peak, 4), "peak_nominal": NOMINAL_GBS,
+                         "frac_nominal": round(fwd_gbs / NOMINAL_GBS, 4), "traffic": traffic_fwd},
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_throughput(N_TOK, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
