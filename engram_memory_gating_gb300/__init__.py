@@ -30,6 +30,7 @@ __all__ = [
     "engram_gateconv_fwd", "engram_gateconv_bwd", "engram_gateconv_bwd_workspace_size",
     "engram_device_error", "engram_launch_info", "engram_gate_bwd_noalloc",
     "engram_gate_sep_fwd", "engram_gate_sep_bwd", "engram_gate_sep_bwd_workspace_size",
+    "engram_gate_bwd_fused_weight", "gate_backward_fused_weight",
     "gate_forward", "gate_backward", "gateconv_forward", "gateconv_backward",
     "gate_sep_forward", "gate_sep_backward", "engram_fused_weight", "engram_fused_weight_bwd",
     "fused_weight", "fused_weight_backward", "engram_decode_fwd", "engram_decode_workspace_size",
@@ -49,7 +50,7 @@ EXPORTED_SYMBOLS = (
     "engram_gateconv_bwd", "engram_device_error", "engram_launch_info",
     "engram_gate_bwd_noalloc", "engram_gate_sep_fwd", "engram_gate_sep_bwd_workspace_size",
     "engram_gate_sep_bwd", "engram_fused_weight", "engram_fused_weight_bwd",
-    "engram_decode_workspace_size", "engram_decode_fwd",
+    "engram_decode_workspace_size", "engram_decode_fwd", "engram_gate_bwd_fused_weight",
 )
 
 _STATUS = {0: "ok", 1: "null pointer", 2: "misaligned pointer", 3: "size out of range",
@@ -98,6 +99,7 @@ def load(path: str | None = None):
         lib.engram_gate_bwd_workspace_size.restype = SZ
         lib.engram_gate_bwd.argtypes = [P, P, P, P, P, P, P, P, P, SZ, I64, P]
         lib.engram_gate_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I64, P]
+        lib.engram_gate_bwd_fused_weight.argtypes = [P] * 13 + [SZ, I64, P]
         lib.engram_gate_sep_fwd.argtypes = [P] * 9 + [I64, I64, F, F, P]
         lib.engram_gate_sep_bwd_workspace_size.argtypes = [I64]
         lib.engram_gate_sep_bwd_workspace_size.restype = SZ
@@ -115,6 +117,7 @@ def load(path: str | None = None):
         lib.engram_launch_info.argtypes = [ctypes.c_int, I64, I64, I64,
                                            ctypes.POINTER(_LaunchInfo)]
         for name in ("engram_gate_fwd", "engram_gate_bwd", "engram_gate_bwd_noalloc",
+                     "engram_gate_bwd_fused_weight",
                      "engram_gate_sep_fwd", "engram_gate_sep_bwd", "engram_fused_weight",
                      "engram_fused_weight_bwd", "engram_decode_fwd", "engram_gateconv_fwd",
                      "engram_gateconv_bwd", "engram_device_error", "engram_launch_info"):
@@ -184,6 +187,28 @@ def engram_gate_bwd(x, kv, weight, saved, grad_out, grad_x, grad_kv, grad_weight
     _check("engram_gate_bwd", load().engram_gate_bwd(
         _ptr(x), _ptr(kv), _ptr(weight), _ptr(saved), _ptr(grad_out), _ptr(grad_x),
         _ptr(grad_kv), _ptr(grad_weight), _ptr(workspace), nbytes, N, _stream(stream)))
+
+
+def engram_gate_bwd_fused_weight(x, kv, weight, saved, grad_out, wh, we, grad_x, grad_kv,
+                                 grad_weight, grad_wh, grad_we, workspace, stream=None):
+    """engram_gate_bwd for weight = wh * we (bf16 (4, 5120) factors): the
+    grad_weight merge also writes grad_wh = grad_weight * we and grad_we =
+    grad_weight * wh.  grad_weight may be None."""
+    N = x.shape[0]
+    _need(saved, torch.float32, (N, S_GATE, 4), "saved")
+    _need(grad_out, torch.bfloat16, (N, S_GATE, D_GATE), "grad_out")
+    _need(grad_x, torch.bfloat16, (N, S_GATE, D_GATE), "grad_x")
+    _need(grad_kv, torch.bfloat16, (N, (S_GATE + 1) * D_GATE), "grad_kv")
+    for t, n in ((wh, "wh"), (we, "we")):
+        _need(t, torch.bfloat16, (S_GATE, D_GATE), n)
+    for t, n in ((grad_wh, "grad_wh"), (grad_we, "grad_we")) + (
+            ((grad_weight, "grad_weight"),) if grad_weight is not None else ()):
+        _need(t, torch.float32, (S_GATE, D_GATE), n)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("engram_gate_bwd_fused_weight", load().engram_gate_bwd_fused_weight(
+        _ptr(x), _ptr(kv), _ptr(weight), _ptr(saved), _ptr(grad_out), _ptr(wh), _ptr(we),
+        _ptr(grad_x), _ptr(grad_kv), _ptr(grad_weight), _ptr(grad_wh), _ptr(grad_we),
+        _ptr(workspace), nbytes, N, _stream(stream)))
 
 
 def engram_gate_bwd_noalloc(x, kv, weight, saved, grad_out, grad_x, grad_kv, grad_weight,
@@ -360,6 +385,16 @@ def gate_backward(x, kv, weight, saved, grad_out):
     ws = torch.empty(engram_gate_bwd_workspace_size(N), device=x.device, dtype=torch.uint8)
     engram_gate_bwd(x, kv, weight, saved, grad_out, gx, gkv, gw, ws)
     return gx, gkv, gw
+
+
+def gate_backward_fused_weight(x, kv, weight, saved, grad_out, wh, we):
+    """Returns grad_x, grad_kv, grad_weight, grad_wh, grad_we for weight = wh * we."""
+    N = x.shape[0]
+    gx, gkv = torch.empty_like(x), torch.empty_like(kv)
+    gw, gwh, gwe = (torch.empty(weight.shape, device=x.device, dtype=torch.float32) for _ in range(3))
+    ws = torch.empty(engram_gate_bwd_workspace_size(N), device=x.device, dtype=torch.uint8)
+    engram_gate_bwd_fused_weight(x, kv, weight, saved, grad_out, wh, we, gx, gkv, gw, gwh, gwe, ws)
+    return gx, gkv, gw, gwh, gwe
 
 
 def gate_sep_forward(x, k, v, weight, eps: float = GATE_EPS, clamp: float = GATE_CLAMP,

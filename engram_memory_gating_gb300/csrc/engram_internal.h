@@ -68,11 +68,17 @@ struct GateBwdParams {
 
 struct GateWReduceParams {
     const float* partial;  // partial[b * stride + i], b < nblocks, i < n (fp32)
-    float* out;            // (n)
+    float* out;            // (n), may be null when grad_wh / grad_we are written
     int nblocks;
     int n;
     int stride;
     int pairs;  // slots come as (hi, lo) pairs
+    // product rule of a fused weight w = wh * we (null: not written):
+    // grad_wh = grad_w * we, grad_we = grad_w * wh, wh and we bf16 (n)
+    const uint16_t* wh;
+    const uint16_t* we;
+    float* grad_wh;
+    float* grad_we;
 };
 
 // GateConv: one cluster per token range (consecutive tokens of one batch

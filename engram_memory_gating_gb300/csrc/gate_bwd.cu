@@ -16,11 +16,15 @@
 // (sum_i xh_i w_i kh_i): d dot/d x_i = rstd_X (w_i kh_i - xh_i dot/d).
 //
 // Three kernels, none of which communicates across CTAs:
-//  1. coefficients: one warp per token reads the token's grad_out rows and v
-//     (16-byte loads), reduces the four dgate sums with error-free
-//     accumulation and shuffles, and lanes 0..3 turn them into the per-stream
-//     scalars in fp64 (A split as an 8-significant-bit head plus a float
-//     tail, -B, -Ck), written to the workspace's 16 floats per token;
+//  1. coefficients: a pair of warps per token (the packed layout; one warp
+//     per token for a runtime hidden size) reads the token's grad_out rows
+//     and v (16-byte loads), each warp one column half, and reduces the four
+//     dgate sums with error-free accumulation and shuffles; the second warp
+//     hands its sums to the first through shared memory.  Once eight tokens'
+//     sums are waiting, one full-warp fp64 pass (lane = 4 token + stream)
+//     turns them into the per-stream scalars (A split as an 8-significant-bit
+//     head plus a float tail, -B, -Ck), written to the workspace's 16 floats
+//     per token;
 //  2. elementwise: a CTA owns a 512-column slice of every stream over a
 //     group of consecutive tokens; the slice rows of X, the keys and grad_out
 //     plus the token's scalars and saved record stream through a ring of
@@ -31,7 +35,9 @@
 //     workspace's block slots (group g: slots 2g and 2g+1).  The warps never
 //     wait for one another: each counts itself out of a stage in shared
 //     memory and the last one to leave it issues its refill;
-//  3. the pairs are merged in ascending group order (bitwise reproducible).
+//  3. the pairs are merged in ascending group order (bitwise reproducible);
+//     for a fused weight w = wh * we the same pass also writes the product-rule
+//     gradients grad_wh = grad_w * we and grad_we = grad_w * wh.
 // The per-token scalars are evaluated in fp64 because a relative error of a
 // few fp32 ulps in A, summed over thousands of tokens, would exceed the 1e-6
 // absolute accuracy asked of grad_w near zero.
@@ -572,7 +578,13 @@ __global__ void __launch_bounds__(32 * kRedGroups) wreduce_kernel(const GateWRed
         float h = shi[0][lane], l = slo[0][lane];
 #pragma unroll
         for (int k = 1; k < kRedGroups; ++k) cacc_merge(h, l, shi[k][lane], slo[k][lane]);
-        p.out[i] = __fadd_rn(h, l);
+        const float gw = __fadd_rn(h, l);
+        if (p.out != nullptr) p.out[i] = gw;
+        if (p.grad_wh != nullptr) {
+            // product rule of w = wh * we, in the same pass (one fp32 rounding each)
+            p.grad_wh[i] = __fmul_rn(gw, __uint_as_float(static_cast<uint32_t>(p.we[i]) << 16));
+            p.grad_we[i] = __fmul_rn(gw, __uint_as_float(static_cast<uint32_t>(p.wh[i]) << 16));
+        }
     }
 }
 

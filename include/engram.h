@@ -143,6 +143,31 @@ engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weig
                                 size_t workspace_bytes, int64_t N, cudaStream_t stream);
 
 /*
+ * Saved-state gate, backward, when the weight is a fused weight w = wh * we
+ * (cuDNN "Engram saved-state gate", semantics paragraph: the weight is the
+ * FP32 product of the query- and key-side normalisation weights and the
+ * caller forms their product-rule gradients from grad_weight; tile-kernels
+ * test_engram_gate_bwd.py checks grad_wh and grad_we formed that way).
+ * engram_gate_bwd, plus the product rule in the same pass that merges
+ * grad_weight (no further launch and no re-read of grad_weight):
+ *   grad_wh[i] = grad_weight[i] * we[i],  grad_we[i] = grad_weight[i] * wh[i]
+ * each one FP32 rounding of the FP32 grad_weight times the factor.
+ *   wh, we      bf16 (4, 5120)  the factors of `weight` (weight[i] = wh[i] we[i],
+ *                               as engram_fused_weight computes it), 16-B aligned
+ *   grad_weight fp32 (4, 5120)  out, or NULL to skip it
+ *   grad_wh, grad_we fp32 (4, 5120)  out
+ * Every other argument, limit and error as engram_gate_bwd; outputs must not
+ * overlap anything.  Three kernels on `stream`.
+ */
+engram_status_t engram_gate_bwd_fused_weight(const void* x, const void* kv, const float* weight,
+                                             const float* saved, const void* grad_out,
+                                             const void* wh, const void* we, void* grad_x,
+                                             void* grad_kv, float* grad_weight, float* grad_wh,
+                                             float* grad_we, void* workspace,
+                                             size_t workspace_bytes, int64_t N,
+                                             cudaStream_t stream);
+
+/*
  * Saved-state gate with separate key and value tensors and any hidden size
  * (tile-kernels 1.0.0 engram tests: engram_gate_fwd / engram_gate_bwd take x,
  * k (N, hc, H), v (N, H) and the fused weight, have no mask, return the saved

@@ -67,3 +67,38 @@ def test_chain_through_the_separate_tensor_gate():
     check_f32("grad_w", gw.cpu().numpy(), egw)
     check_f32("grad_wh", gwh.cpu().numpy(), egw * f64(we))
     check_f32("grad_we", gwe.cpu().numpy(), egw * f64(wh))
+
+
+@pytest.mark.parametrize("N,mask", [(64, "all"), (320, "bern0.9"), (8192, "bern0.9")])
+def test_packed_backward_applies_the_product_rule_in_its_merge(N, mask):
+    """engram_gate_bwd_fused_weight: w = wh * we -> packed gate forward ->
+    backward whose grad_weight merge also writes grad_wh = grad_w * we and
+    grad_we = grad_w * wh.  Against the oracle's gate backward and product
+    rule, and bitwise against engram_gate_bwd followed by the separate product
+    rule call (one block holding grad_weight), which it replaces."""
+    inp = gate_inputs(N, 50 + N % 11, device="cuda", mask=mask)
+    g = torch.Generator(device="cuda").manual_seed(N)
+    wh = (1 + 0.3 * torch.randn((4, 5120), generator=g, device="cuda")).to(torch.bfloat16)
+    we = (1 + 0.3 * torch.randn((4, 5120), generator=g, device="cuda")).to(torch.bfloat16)
+    w = eg.fused_weight(wh, we)
+    out, saved = eg.gate_forward(inp["x"], inp["kv"], w, inp["mask"])
+    gx, gkv, gw, gwh, gwe = eg.gate_backward_fused_weight(inp["x"], inp["kv"], w, saved,
+                                                          inp["grad_out"], wh, we)
+    rx, rkv, rw = eg.gate_backward(inp["x"], inp["kv"], w, saved, inp["grad_out"])
+    _, rwh, rwe = eg.fused_weight_backward(rw.unsqueeze(0), wh, we)
+    # grad_weight may be skipped: the product-rule outputs are unchanged
+    gwh2, gwe2 = torch.empty_like(gwh), torch.empty_like(gwe)
+    ws = torch.empty(eg.engram_gate_bwd_workspace_size(N), device="cuda", dtype=torch.uint8)
+    eg.engram_gate_bwd_fused_weight(inp["x"], inp["kv"], w, saved, inp["grad_out"], wh, we,
+                                    torch.empty_like(gx), torch.empty_like(gkv), None, gwh2, gwe2, ws)
+    torch.cuda.synchronize()
+    for a, b in ((gx, rx), (gkv, rkv)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in ((gw, rw), (gwh, rwh), (gwe, rwe), (gwh2, gwh), (gwe2, gwe)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    _, _, egw = oracle.gate_bwd(f64(inp["x"]), f64(inp["kv"]), f64(w), f64(saved),
+                                f64(inp["grad_out"]))
+    _, egwh, egwe = oracle.fused_weight_bwd(egw[None], f64(wh), f64(we))
+    check_f32("grad_weight (fused-weight bwd)", gw.cpu().numpy(), egw)
+    check_f32("grad_wh (fused-weight bwd)", gwh.cpu().numpy(), egwh)
+    check_f32("grad_we (fused-weight bwd)", gwe.cpu().numpy(), egwe)
