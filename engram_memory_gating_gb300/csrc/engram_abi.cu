@@ -2,6 +2,9 @@
 // set-up and kernel launches.  No allocation, copy or synchronisation happens
 // on the execute path (cuDNN Frontend "Engram saved-state gate": plan/execute
 // paragraph -- execute does no allocation, conversion, compilation or sync).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <mutex>
 
@@ -51,6 +54,7 @@ struct GcCacheEntry {
 struct DeviceState {
     bool init = false;
     bool ok = false;
+    unsigned long long ctx = 0;  // unique ID of the context the set-up was done in
     int sm_count = 0;
     int smem_optin = 0;  // largest dynamic shared memory a CTA may opt in to
     unsigned int* err = nullptr;
@@ -113,7 +117,48 @@ int max_clusters(DeviceState& st, int op, int cluster, int threads, int smem) {
     return v;
 }
 
-// Returns the calling thread's current-device state, initialising it once.
+// Unique ID of the calling thread's current CUDA context (0 if none is
+// current or the driver does not offer the query).  A device reset
+// (cudaDeviceReset) replaces the primary context, and everything set up in the
+// old one -- kernel attributes, device addresses of the library's __device__
+// variables -- is void in the new one; comparing IDs tells the two apart (a
+// context handle alone may be reused).  The driver functions are looked up
+// through the runtime, so the library has no link-time dependence on libcuda.
+unsigned long long current_ctx_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        looked_up = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+        (void)cudaGetLastError();
+    }
+    if (!get_current || !get_id) return 0;
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr || get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Per-device, per-context state (callers hold g_mu).  The context is
+// identified by its ID; a call made after the device's context was replaced
+// redoes the set-up instead of using the old context's addresses.
+struct NoallocScratch {
+    unsigned long long ctx = 0;
+    void* ptr = nullptr;
+};
+
+// Returns the calling thread's current-device state, initialising it once per
+// context of the device.
 DeviceState* device_state() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -121,7 +166,19 @@ DeviceState* device_state() {
         return nullptr;
     }
     DeviceState& st = g_dev[dev];
+    unsigned long long ctx = current_ctx_id();
+    if (ctx == 0) {
+        // no context current on this thread yet: make the device's primary
+        // context current (cudaSetDevice initialises it) and ask again
+        if (cudaSetDevice(dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        ctx = current_ctx_id();
+    }
+    if (st.init && ctx != st.ctx) st = DeviceState();  // a new context: set up again
     if (!st.init) {
+        st.ctx = ctx;
         st.init = true;
         st.ok = false;
         int major = 0, minor = 0;
@@ -431,26 +488,39 @@ engram_status_t engram_gate_fwd(const void* x, const void* kv, const float* weig
     return launch_status(gate_fwd_launch(p, c, stream));
 }
 
-engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weight,
-                                const float* saved, const void* grad_out, void* grad_x,
-                                void* grad_kv, float* grad_weight, void* workspace,
-                                size_t workspace_bytes, int64_t N, cudaStream_t stream) {
-    if (!x || !kv || !weight || !saved || !grad_out || !grad_x || !grad_kv || !grad_weight ||
-        !workspace)
+}  // extern "C"
+
+namespace {
+
+// The packed gate backward; with wh / we set (a fused weight w = wh * we) the
+// grad_weight merge also writes grad_wh and grad_we, and grad_weight may be
+// null.  Arguments are validated by the callers' shared checks below.
+engram_status_t gate_bwd_impl(const void* x, const void* kv, const float* weight,
+                              const float* saved, const void* grad_out, const void* wh,
+                              const void* we, void* grad_x, void* grad_kv, float* grad_weight,
+                              float* grad_wh, float* grad_we, void* workspace,
+                              size_t workspace_bytes, int64_t N, cudaStream_t stream) {
+    const bool prod = wh != nullptr;
+    if (!x || !kv || !weight || !saved || !grad_out || !grad_x || !grad_kv || !workspace ||
+        (!prod && !grad_weight) || (prod && (!we || !grad_wh || !grad_we)))
         return ENGRAM_ERR_NULL;
     if (N < 64 || N > ENGRAM_GATE_BWD_MAX_TOKENS || N % 64 != 0) return ENGRAM_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(kv) || !aligned16(weight) || !aligned16(saved) ||
         !aligned16(grad_out) || !aligned16(grad_x) || !aligned16(grad_kv) ||
-        !aligned16(grad_weight) || !aligned16(workspace))
+        (grad_weight && !aligned16(grad_weight)) || !aligned16(workspace) ||
+        (prod && (!aligned16(wh) || !aligned16(we) || !aligned16(grad_wh) || !aligned16(grad_we))))
         return ENGRAM_ERR_ALIGN;
     const size_t need = engram_gate_bwd_workspace_size(N);
     if (workspace_bytes < need) return ENGRAM_ERR_WORKSPACE;
     const size_t n = static_cast<size_t>(N);
+    const size_t wn = 4 * kGateD;
     const Range ins[] = {{x, n * 4 * kGateD * 2}, {kv, n * 5 * kGateD * 2},
-                         {weight, 4 * kGateD * 4}, {saved, n * 64}, {grad_out, n * 4 * kGateD * 2}};
+                         {weight, wn * 4}, {saved, n * 64}, {grad_out, n * 4 * kGateD * 2},
+                         {wh, prod ? wn * 2 : 0}, {we, prod ? wn * 2 : 0}};
     const Range outs[] = {{grad_x, n * 4 * kGateD * 2}, {grad_kv, n * 5 * kGateD * 2},
-                          {grad_weight, 4 * kGateD * 4}, {workspace, need}};
-    if (any_overlap(outs, 4, ins, 5)) return ENGRAM_ERR_OVERLAP;
+                          {grad_weight, grad_weight ? wn * 4 : 0}, {workspace, need},
+                          {grad_wh, prod ? wn * 4 : 0}, {grad_we, prod ? wn * 4 : 0}};
+    if (any_overlap(outs, 6, ins, 7)) return ENGRAM_ERR_OVERLAP;
 
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState* st = device_state();
@@ -487,14 +557,44 @@ engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weig
     p.clamp = ENGRAM_GATE_CLAMP;
     engram_status_t s = launch_status(gate_bwd_launch(p, c, stream));
     if (s != ENGRAM_OK) return s;
-    GateWReduceParams r;
+    GateWReduceParams r = {};
     r.partial = partial;
     r.out = grad_weight;
     r.nblocks = p.pair_slots ? 2 * c.grid_y : c.grid_y;
     r.n = 4 * kGateD;
     r.stride = 4 * kGateD;
     r.pairs = p.pair_slots;
+    if (prod) {
+        r.wh = static_cast<const uint16_t*>(wh);
+        r.we = static_cast<const uint16_t*>(we);
+        r.grad_wh = grad_wh;
+        r.grad_we = grad_we;
+    }
     return launch_status(gate_wreduce_launch(r, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weight,
+                                const float* saved, const void* grad_out, void* grad_x,
+                                void* grad_kv, float* grad_weight, void* workspace,
+                                size_t workspace_bytes, int64_t N, cudaStream_t stream) {
+    return gate_bwd_impl(x, kv, weight, saved, grad_out, nullptr, nullptr, grad_x, grad_kv,
+                         grad_weight, nullptr, nullptr, workspace, workspace_bytes, N, stream);
+}
+
+engram_status_t engram_gate_bwd_fused_weight(const void* x, const void* kv, const float* weight,
+                                             const float* saved, const void* grad_out,
+                                             const void* wh, const void* we, void* grad_x,
+                                             void* grad_kv, float* grad_weight, float* grad_wh,
+                                             float* grad_we, void* workspace,
+                                             size_t workspace_bytes, int64_t N,
+                                             cudaStream_t stream) {
+    if (!wh) return ENGRAM_ERR_NULL;
+    return gate_bwd_impl(x, kv, weight, saved, grad_out, wh, we, grad_x, grad_kv, grad_weight,
+                         grad_wh, grad_we, workspace, workspace_bytes, N, stream);
 }
 
 engram_status_t engram_gateconv_fwd(const void* H, const void* k, const void* v,
@@ -849,7 +949,7 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
     const int offs[3] = {0, 1, 2};
     const int lens[3] = {1, 1, 4};
     for (int i = 0; i < 3; ++i) {
-        GateWReduceParams r;
+        GateWReduceParams r = {};
         r.partial = partial + static_cast<size_t>(offs[i]) * dd;
         r.out = outs3[i];
         r.nblocks = R;
@@ -871,8 +971,9 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
 static __device__ __align__(256) unsigned char g_gate_bwd_scratch[ENGRAM_GATE_BWD_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-bool g_scratch_ready[eg::kMaxDevices] = {};
-void* g_scratch_addr[eg::kMaxDevices] = {};
+// the array's device address per device, with the ID of the context it was
+// looked up in (a reset device gets a new context and a new address)
+eg::NoallocScratch g_scratch[eg::kMaxDevices];
 }  // namespace
 
 extern "C" {
@@ -886,20 +987,24 @@ engram_status_t engram_gate_bwd_noalloc(const void* x, const void* kv, const flo
     {
         std::lock_guard<std::mutex> lk(g_mu);
         int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= eg::kMaxDevices) {
+        // device_state() makes the device's context current and identifies it
+        if (!eg::device_state() || cudaGetDevice(&dev) != cudaSuccess || dev < 0 ||
+            dev >= eg::kMaxDevices) {
             (void)cudaGetLastError();
             return ENGRAM_ERR_DEVICE;
         }
-        if (!g_scratch_ready[dev]) {
+        eg::NoallocScratch& sc = g_scratch[dev];
+        const unsigned long long ctx = eg::g_dev[dev].ctx;
+        if (sc.ptr == nullptr || sc.ctx != ctx) {
             void* ptr = nullptr;
             if (cudaGetSymbolAddress(&ptr, g_gate_bwd_scratch) != cudaSuccess || ptr == nullptr) {
                 (void)cudaGetLastError();
                 return ENGRAM_ERR_DEVICE;
             }
-            g_scratch_addr[dev] = ptr;
-            g_scratch_ready[dev] = true;
+            sc.ptr = ptr;
+            sc.ctx = ctx;
         }
-        scratch = g_scratch_addr[dev];
+        scratch = sc.ptr;
     }
     // the regular backward, with the library's array as its workspace
     return engram_gate_bwd(x, kv, weight, saved, grad_out, grad_x, grad_kv, grad_weight, scratch,
