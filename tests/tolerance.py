@@ -8,6 +8,17 @@ bf16 tensors (out, grad_x, grad_kv, Y, vhat, dH, dk, dv):
   about 2^-23 of those terms; 2^-16 of the row's RMS leaves a 100x margin and
   is still far below one ulp of any typical element.  A row whose exact
   values are all zero must match exactly.
+GateConv's dH and dk take the near-zero allowance from the rms over the whole
+compared slice instead of the token's row.  Both are the token's scalar dz
+times per-element terms, and dz = dalpha alpha (1 - alpha) with dalpha =
+sum_i dvhat_i v_i, which the kernel forms in fp32 as a difference of row sums
+(the RMSNorm of vhat makes them cancel).  The rounding error of dz therefore
+scales with those sums, i.e. with the dz of a typical token, not with the
+token's own dz: a token whose dalpha happens to cancel to 1e-4 of its terms
+has a row 1e4 times below the others with a relative error of a few percent
+and an absolute error of a few 2^-23 of the typical row.  2^-16 of the slice's
+rms bounds that with a wide margin and stays 2^-8 below one ulp of any typical
+element.
 fp32 tensors (saved gate/dot/rstd, grad_weight, alpha, rrms_*):
     |gpu - exact| <= 1e-4 |exact| + 1e-6
 fp32 weight gradients of GateConv, summed over up to 65536 tokens:
@@ -64,9 +75,15 @@ def _report(name, got, exact, tol, bad):
     return "\n".join(lines)
 
 
-def check_bf16(name, got_bits, exact, row_axis=-1):
+def check_bf16(name, got_bits, exact, row_axis=-1, floor="row"):
+    """floor="row": near-zero allowance from the rms of each row (token);
+    floor="all": from the rms of the whole compared array (see the module
+    docstring: GateConv's dH and dk)."""
     got = bf16_bits_to_f64(got_bits).reshape(exact.shape)
-    rms = np.sqrt(np.mean(exact * exact, axis=row_axis, keepdims=True))
+    if floor == "all":
+        rms = np.sqrt(np.mean(exact * exact)) if exact.size else 0.0
+    else:
+        rms = np.sqrt(np.mean(exact * exact, axis=row_axis, keepdims=True))
     rel_tol = BF16_REL * np.abs(exact)
     tol = rel_tol + ROW_FLOOR * rms
     diff = np.abs(got - exact)
