@@ -8,17 +8,19 @@ bf16 tensors (out, grad_x, grad_kv, Y, vhat, dH, dk, dv):
   about 2^-23 of those terms; 2^-16 of the row's RMS leaves a 100x margin and
   is still far below one ulp of any typical element.  A row whose exact
   values are all zero must match exactly.
-GateConv's dH and dk take the near-zero allowance from the rms over the whole
-compared slice instead of the token's row.  Both are the token's scalar dz
-times per-element terms, and dz = dalpha alpha (1 - alpha) with dalpha =
-sum_i dvhat_i v_i, which the kernel forms in fp32 as a difference of row sums
-(the RMSNorm of vhat makes them cancel).  The rounding error of dz therefore
-scales with those sums, i.e. with the dz of a typical token, not with the
-token's own dz: a token whose dalpha happens to cancel to 1e-4 of its terms
-has a row 1e4 times below the others with a relative error of a few percent
-and an absolute error of a few 2^-23 of the typical row.  2^-16 of the slice's
-rms bounds that with a wide margin and stays 2^-8 below one ulp of any typical
-element.
+GateConv's dH and dk:
+    |gpu - exact| <= 2^-7 |exact| + 2^-12 rms(compared slice of exact)
+  Both are the token's scalar dz times per-element terms, and dz = dalpha
+  alpha (1 - alpha) with dalpha = sum_i dvhat_i v_i.  In one pass the kernel
+  can only form dalpha as S1 - rrms_v^3 S4 S3 / d from fp32 row sums, where S1
+  = sum (dY + rrms_v w_v du) v and the subtracted term share a part rrms_v
+  sum w_v du v that the RMSNorm of vhat cancels.  For a token with a small
+  gate, rrms_v is large and both terms exceed dalpha by up to 1e3, so the
+  fp32 rounding of the sums, not dalpha, sets the error: the token's whole dH
+  row is off by a common factor of up to a few percent.  An fp32 emulation of
+  the kernel's sums at the M8 T8192 d7168 distributions puts that error at
+  most 2^-14 of the slice's rms over 20,000 tokens (2^-15.8 seen on the GPU);
+  2^-12 leaves a 4x margin and stays 2^-5 below one ulp of a typical element.
 fp32 tensors (saved gate/dot/rstd, grad_weight, alpha, rrms_*):
     |gpu - exact| <= 1e-4 |exact| + 1e-6
 fp32 weight gradients of GateConv, summed over up to 65536 tokens:
@@ -57,6 +59,7 @@ def _record(name, diff, tol, floor_only=None):
 
 BF16_REL = 2.0 ** -7
 ROW_FLOOR = 2.0 ** -16
+SLICE_FLOOR = 2.0 ** -12   # GateConv dH, dk (see above)
 F32_REL = 1e-4
 F32_ABS = 1e-6
 
@@ -76,16 +79,18 @@ def _report(name, got, exact, tol, bad):
 
 
 def check_bf16(name, got_bits, exact, row_axis=-1, floor="row"):
-    """floor="row": near-zero allowance from the rms of each row (token);
-    floor="all": from the rms of the whole compared array (see the module
-    docstring: GateConv's dH and dk)."""
+    """floor="row": near-zero allowance 2^-16 of the rms of each row (token);
+    floor="all": 2^-12 of the rms of the whole compared array (GateConv's dH
+    and dk; see the module docstring)."""
     got = bf16_bits_to_f64(got_bits).reshape(exact.shape)
     if floor == "all":
         rms = np.sqrt(np.mean(exact * exact)) if exact.size else 0.0
+        floor_factor = SLICE_FLOOR
     else:
         rms = np.sqrt(np.mean(exact * exact, axis=row_axis, keepdims=True))
+        floor_factor = ROW_FLOOR
     rel_tol = BF16_REL * np.abs(exact)
-    tol = rel_tol + ROW_FLOOR * rms
+    tol = rel_tol + floor_factor * rms
     diff = np.abs(got - exact)
     bad = ~(diff <= tol)
     assert not bad.any(), _report(name, got, exact, tol, bad)
