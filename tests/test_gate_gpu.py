@@ -252,8 +252,8 @@ def test_bwd_long_batch():
     check_f32("grad_weight", gw.cpu().numpy(), ew)
 
 
-def test_bwd_is_deterministic():
-    N = 1024
+@pytest.mark.parametrize("N", [1024, 8192])
+def test_bwd_is_deterministic(N):
     inp = gate_inputs(N, 4, device=DEV, mask="bern0.9")
     _, saved = eg.gate_forward(inp["x"], inp["kv"], inp["weight"], inp["mask"])
     r1 = eg.gate_backward(inp["x"], inp["kv"], inp["weight"], saved, inp["grad_out"])
@@ -263,8 +263,10 @@ def test_bwd_is_deterministic():
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
 
 
-def test_bwd_graph_capture_matches_eager():
-    N = 256
+@pytest.mark.parametrize("N", [256, 8192])
+def test_bwd_graph_capture_matches_eager(N):
+    """The backward captured in a CUDA graph and replayed twice (outputs
+    cleared in between) gives the eager call's bits."""
     inp = to_dev(gate_inputs(N, 11, mask="bern0.5"))
     _, saved = eg.gate_forward(inp["x"], inp["kv"], inp["weight"], inp["mask"])
     ref = eg.gate_backward(inp["x"], inp["kv"], inp["weight"], saved, inp["grad_out"])
@@ -278,11 +280,13 @@ def test_bwd_graph_capture_matches_eager():
             eg.engram_gate_bwd(inp["x"], inp["kv"], inp["weight"], saved, inp["grad_out"], gx,
                                gkv, gw, ws, stream=s)
     torch.cuda.current_stream().wait_stream(s)
-    g.replay()
-    torch.cuda.synchronize()
-    assert torch.equal(gx.view(torch.int16), ref[0].view(torch.int16))
-    assert torch.equal(gkv.view(torch.int16), ref[1].view(torch.int16))
-    assert torch.equal(gw, ref[2])
+    for _ in range(2):
+        gx.zero_(), gkv.zero_(), gw.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(gx.view(torch.int16), ref[0].view(torch.int16))
+        assert torch.equal(gkv.view(torch.int16), ref[1].view(torch.int16))
+        assert torch.equal(gw, ref[2])
 
 
 def test_launch_geometry():
@@ -316,8 +320,13 @@ def test_chained_steps_without_host_sync_match_synchronised_ones():
     predecessor finishes; this checks that every kernel still reads only
     completed data, against the same chain with a device synchronisation after
     every call (no overlap at all).  The kernels are deterministic, so the two
-    chains must agree bit for bit."""
-    N = 256
+    chains must agree bit for bit.  N = 4096 also spans a full wave of the
+    elementwise kernel's token groups."""
+    for N in (256, 4096):
+        _chain_check(N)
+
+
+def _chain_check(N):
     inp = to_dev(gate_inputs(N, 21, mask="bern0.9"))
     ws = torch.empty(eg.engram_gate_bwd_workspace_size(N), device=DEV, dtype=torch.uint8)
 
