@@ -220,6 +220,15 @@ EG_DEV void stg_cs8(void* p, const uint2& v) {
     asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
+// Streaming 8-byte global store done only where `pred` holds, as one
+// predicated instruction (no branch), so that it can sit in straight-line code.
+// No memory clobber: it only writes outputs that the kernel never reads.
+EG_DEV void stg_cs8_if(void* p, const uint2& v, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t@q st.global.cs.v2.b32 [%0], {%1, %2};\n\t}" ::"l"(p),
+        "r"(v.x), "r"(v.y), "r"(static_cast<uint32_t>(pred)));
+}
+
 // Asynchronous 4-byte store into the shared memory of a CTA of this cluster,
 // completing 4 bytes on that CTA's mbarrier.
 EG_DEV void st_async_f32(uint32_t remote_addr, float a, uint32_t remote_bar) {

@@ -367,6 +367,7 @@ const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
     auto shape = [&](int C, GcGeom& g) {
         g = {};
         gc_split(d, rows, C, g);
+        if (op == 0) g.c.smem = gateconv_fwd_smem();   // fixed layout (2048-byte row slots)
         if (op == 1) {
             g.sc_off = g.c.smem;  // saved scalars of up to kGcBwdMaxRange + 7 streamed tokens
             g.c.smem += 16 * (kGcBwdMaxRange + 8);

@@ -195,6 +195,7 @@ int decode_proj_smem(int rows_per_split);
 cudaError_t decode_prepare();
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);
 
+int gateconv_fwd_smem();  // dynamic shared memory of the forward kernel (fixed layout)
 cudaError_t gateconv_fwd_prepare(int smem_bytes);
 cudaError_t gateconv_fwd_max_clusters(int cluster, int threads, int smem, int* out);
 cudaError_t gateconv_fwd_launch(const GateConvFwdParams& p, const LaunchCfg& c, cudaStream_t s);

@@ -22,6 +22,8 @@
 // A range that does not start at t = 0 first runs the 4 tokens before it
 // (the halo) through A and B without writing them, to fill the window.
 // Arithmetic on pairs of columns uses the packed fp32x2 instructions.
+#include <type_traits>
+
 #include "common.cuh"
 #include "engram_internal.h"
 #include "gateconv_xch.cuh"
@@ -31,13 +33,34 @@ namespace {
 
 using gc::kChunk;
 
+// Shared memory: a fixed layout, so that every ring address of a token is a
+// chunk base plus an immediate.  Each row slot is 2048 bytes (the widest
+// column slice, 1024 columns); a narrower slice leaves the slot's tail zero,
+// which the threads without columns read.
+constexpr int kRows = 3;                         // H, k, v
+constexpr int kPitch = 2048;                     // bytes per row slot
+constexpr int kStageBytes = kRows * kPitch;
+constexpr int kStages = gc::kStages;             // 16 one-token stages
+constexpr int kOffFull = 0;                      // [kStages] stage mbarriers
+constexpr int kOffXbar = 128;                    // [2] cluster-exchange mbarriers
+constexpr int kOffRel = 160;                     // [kStages] stage release counters
+constexpr int kOffArr = 224;                     // [2] per-chunk arrival counters
+constexpr int kOffLocal = 256;                   // [2][8 warps][16] warp totals
+constexpr int kOffTot = kOffLocal + 2 * 8 * gc::kVals * 4;   // [2][8 ranks][16] CTA totals
+constexpr int kRingOff = kOffTot + 2 * 8 * gc::kVals * 4;
+constexpr int kSmem = kRingOff + kStages * kStageBytes;
+static_assert(kRingOff % 128 == 0, "ring alignment");
+static_assert(kStages % kChunk == 0, "a chunk must not wrap around the ring");
+
 __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const GateConvFwdParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + gc::kOffFull);
-    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + gc::kOffXbar);
-    unsigned int* released = reinterpret_cast<unsigned int*>(smem + gc::kOffRel);
-    float* xch = reinterpret_cast<float*>(smem + gc::kOffXch);
-    unsigned char* ring = smem + p.ring_off;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffFull);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + kOffXbar);
+    unsigned int* released = reinterpret_cast<unsigned int*>(smem + kOffRel);
+    unsigned int* arrived = reinterpret_cast<unsigned int*>(smem + kOffArr);
+    float* local = reinterpret_cast<float*>(smem + kOffLocal);
+    float* tot = reinterpret_cast<float*>(smem + kOffTot);
+    unsigned char* ring = smem + kRingOff;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -45,8 +68,6 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
     const int nw = blockDim.x >> 5;
     const uint32_t C = cluster_size();
     const uint32_t rank = cluster_rank();
-    const int parts = static_cast<int>(C) * nw;
-    const int part = static_cast<int>(rank) * nw + warp;
     const int q = static_cast<int>(cluster_index());
     const int d = p.d;
     const int col0 = static_cast<int>(rank) * p.ncols;
@@ -54,10 +75,6 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
     const bool active = 4 * tid < cols;
     const int c0 = col0 + 4 * tid;
     const uint32_t row_bytes = 2u * static_cast<uint32_t>(cols);
-    const uint32_t pitch = 2u * static_cast<uint32_t>(p.ncols);
-    const uint32_t stage_bytes = 3u * pitch;
-    constexpr int stages = gc::kStages;
-    static_assert(stages % kChunk == 0, "a chunk must not wrap around the ring");
 
     // ranges start at multiples of kChunk, and so does the streamed halo, so
     // token t of the stream sits in window slot t % 4 = w for chunk position w
@@ -66,9 +83,10 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
     const int t_end = min(p.T, t_out + p.range_len);
     const int t_first = t_out >= kChunk ? t_out - kChunk : 0;
     const int ntok = t_end - t_first;
+    const int j_out = t_out - t_first;               // first streamed token that is written
     const int nchunks = (ntok + kChunk - 1) / kChunk;
     const long long row0 = static_cast<long long>(m) * p.T;
-    const uint32_t xbytes = static_cast<uint32_t>(parts) * gc::kVals * 4u;
+    const uint32_t xbytes = C * gc::kVals * 4u;      // one 16-value total from each CTA
 
     float2 wh2[2], wv[2], cw[4][2];
     if (active) {
@@ -93,31 +111,45 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
         }
     }
 
+    const uint16_t* srcH = p.H + (row0 + t_first) * d + col0;
+    const uint16_t* srcK = p.k + (row0 + t_first) * d + col0;
+    const uint16_t* srcV = p.v + (row0 + t_first) * d + col0;
     auto issue = [&](int j) {
-        const int st = j % stages;
-        const long long off = (row0 + t_first + j) * d + col0;
-        unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
+        const int st = j & (kStages - 1);
+        const long long off = static_cast<long long>(j) * d;
+        unsigned char* b = ring + st * kStageBytes;
         mbar_arrive_expect_tx(&full[st], 3u * row_bytes);
-        bulk_g2s(b, p.H + off, row_bytes, &full[st]);
-        bulk_g2s(b + pitch, p.k + off, row_bytes, &full[st]);
-        bulk_g2s(b + 2 * pitch, p.v + off, row_bytes, &full[st]);
+        bulk_g2s(b, srcH + off, row_bytes, &full[st]);
+        bulk_g2s(b + kPitch, srcK + off, row_bytes, &full[st]);
+        bulk_g2s(b + 2 * kPitch, srcV + off, row_bytes, &full[st]);
     };
 
     if (tid == 0) {
-        for (int s = 0; s < stages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             released[s] = 0u;
         }
         mbar_init(&xbar[0], 1);
         mbar_init(&xbar[1], 1);
+        arrived[0] = arrived[1] = 0u;
         fence_mbar_init();
         // arm the exchange of chunks 0 and 1 (peers' bytes may land before or after)
         mbar_arrive_expect_tx(&xbar[0], xbytes);
         if (nchunks > 1) mbar_arrive_expect_tx(&xbar[1], xbytes);
-        const int pro = ntok < stages ? ntok : stages;
+        const int pro = ntok < kStages ? ntok : kStages;
         for (int j = 0; j < pro; ++j) issue(j);
     }
-    // every CTA's barriers exist before any peer stores into its slots
+    // the tails of the row slots past this slice's columns, which no copy
+    // writes, are zero (threads without columns read them)
+    if (row_bytes < kPitch) {
+        const int words = (kPitch - static_cast<int>(row_bytes)) / 4;
+        for (int i = tid; i < kStages * kRows * words; i += blockDim.x) {
+            const int slot = i / words;
+            reinterpret_cast<uint32_t*>(ring + slot * kPitch + row_bytes)[i - slot * words] = 0u;
+        }
+    }
+    // every CTA's barriers exist (and the tails are zero) before any peer
+    // stores into its slots
     cluster_sync();
 
     float2 U[kChunk][2];  // u of the last four tokens, slot t % 4 (zero before the row start)
@@ -126,79 +158,94 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
 
     const float inv_d = 1.0f / static_cast<float>(d);
     bool failed = false;
-    float alpha_l = 0.f, rv_l = 0.f;  // scalars of token (lane & 3) of chunk c - 1
+    const unsigned char* bthread = ring + 8 * tid;
+    uint16_t* outY = p.Y + (row0 + t_first) * d + c0;
+    uint16_t* outV = p.vhat + (row0 + t_first) * d + c0;
 
-    for (int c = 0; c <= nchunks; ++c) {
-        // ---- A: partial sums of chunk c over this warp's columns (all waits
-        // first, then branch-free arithmetic so the four tokens interleave)
-        float val = 0.f;
-        if (c < nchunks) {
-            float sums[gc::kVals];
-            const int j0 = c * kChunk;
-            const unsigned char* b0 = ring + static_cast<size_t>(j0 % stages) * stage_bytes + 8 * tid;
-            const uint32_t par = static_cast<uint32_t>((j0 / stages) & 1);
+    // One iteration per chunk c = 0 .. nchunks: A(c) forms the chunk's partial
+    // sums, B(c - 1) turns the previous chunk's cluster totals into its
+    // scalars and writes its outputs.  All waits of an iteration come first,
+    // then one straight-line block with both halves (the scheduler overlaps
+    // their latency chains), then the hand-in of chunk c and the release of
+    // chunk c - 1's stages.  The first iteration has no B, the last no A.
+    auto iteration = [&](auto has_a, auto has_b, int c) {
+        constexpr bool kA = decltype(has_a)::value;
+        constexpr bool kB = decltype(has_b)::value;
+        const int buf = c & 1;
+        const int ja = c * kChunk;             // first token of chunk c
+        const int jb = ja - kChunk;            // first token of chunk c - 1
+        const int sta = ja & (kStages - 1);
+        const int stb = jb & (kStages - 1);
+        if (kA) {
+            const uint32_t par = static_cast<uint32_t>((ja / kStages) & 1);
 #pragma unroll
             for (int w = 0; w < kChunk; ++w)
-                if (j0 + w < ntok && !failed && !mbar_wait(&full[j0 % stages + w], par)) failed = true;
+                if (ja + w < ntok && !failed && !mbar_wait(&full[sta + w], par)) failed = true;
+        }
+        if (kB) {
+            // every warp reads chunk c - 1's totals before it hands in chunk c
+            if (!failed && !mbar_wait_cluster(&xbar[buf ^ 1], static_cast<uint32_t>(((c - 1) >> 1) & 1)))
+                failed = true;
+            if (tid == 0 && c + 1 < nchunks) mbar_arrive_expect_tx(&xbar[buf ^ 1], xbytes);
+        }
+        // ---------------- straight-line block
+        float alpha_l = 0.f, ar_l = 0.f;       // scalars of token (lane & 3) of chunk c - 1
+        if (kB) {
+            const float* tp = tot + (buf ^ 1) * 8 * gc::kVals + (lane & 15);
+            float tv = 0.f;
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                if (r < static_cast<int>(C)) tv += tp[r * gc::kVals];
+            const int tw = 4 * (lane & 3);
+            const float sh = __shfl_sync(kFullMask, tv, tw + 0);
+            const float sk = __shfl_sync(kFullMask, tv, tw + 1);
+            const float shk = __shfl_sync(kFullMask, tv, tw + 2);
+            const float sv = __shfl_sync(kFullMask, tv, tw + 3);
+            const float rh = rsqrtf(fmaf(sh, inv_d, p.eps));
+            const float rk = rsqrtf(fmaf(sk, inv_d, p.eps));
+            const float z = rh * rk * shk * p.inv_sqrt_d;
+            alpha_l = __fdividef(1.0f, 1.0f + __expf(-z));
+            const float rv = rsqrtf(fmaf(alpha_l * alpha_l * sv, inv_d, p.eps));
+            ar_l = alpha_l * rv;
+            const int j = jb + lane;
+            if (rank == 0 && warp == 0 && lane < kChunk && j < ntok && j >= j_out) {
+                const long long r = row0 + t_first + j;
+                p.alpha[r] = alpha_l;
+                p.rh[r] = rh;
+                p.rk[r] = rk;
+                p.rv[r] = rv;
+            }
+        }
+        float val = 0.f;
+        if (kA) {
+            // a token past the range reads a stale stage; its sums are never used
+            const unsigned char* b0 = bthread + sta * kStageBytes;
+            float sums[gc::kVals];
 #pragma unroll
             for (int w = 0; w < kChunk; ++w) {
-                const unsigned char* b = b0 + static_cast<size_t>(w) * stage_bytes;
-                const uint2 hq = lds64(b), kq = lds64(b + pitch), vq = lds64(b + 2 * pitch);
+                const unsigned char* b = b0 + w * kStageBytes;
+                const uint2 hq = lds64(b), kq = lds64(b + kPitch), vq = lds64(b + 2 * kPitch);
                 const float2 h0 = bf2(hq.x), h1 = bf2(hq.y), k0 = bf2(kq.x), k1 = bf2(kq.y);
                 const float2 v0 = bf2(vq.x), v1 = bf2(vq.y);
                 const float2 hh = fma2(h1, h1, mul2(h0, h0));
                 const float2 kk = fma2(k1, k1, mul2(k0, k0));
                 const float2 hk = fma2(mul2(h1, k1), wh2[1], mul2(mul2(h0, k0), wh2[0]));
                 const float2 vv = fma2(v1, v1, mul2(v0, v0));
-                const bool ok = active && j0 + w < ntok;
-                sums[4 * w + 0] = ok ? hh.x + hh.y : 0.f;
-                sums[4 * w + 1] = ok ? kk.x + kk.y : 0.f;
-                sums[4 * w + 2] = ok ? hk.x + hk.y : 0.f;
-                sums[4 * w + 3] = ok ? vv.x + vv.y : 0.f;
+                sums[4 * w + 0] = hh.x + hh.y;
+                sums[4 * w + 1] = kk.x + kk.y;
+                sums[4 * w + 2] = hk.x + hk.y;
+                sums[4 * w + 3] = vv.x + vv.y;
             }
             val = gc::warp_reduce16(sums, lane);
         }
-        // ---- totals of chunk c - 1 -> per-token scalars
-        if (c >= 1) {
-            const int buf = (c - 1) & 1;
-            if (!failed && !mbar_wait_cluster(&xbar[buf], static_cast<uint32_t>(((c - 1) >> 1) & 1)))
-                failed = true;
-            if (tid == 0 && c + 1 < nchunks) mbar_arrive_expect_tx(&xbar[buf], xbytes);
-            const float tot = gc::xch_total(xch, buf, parts, lane);
-            const int tw = 4 * (lane & 3);
-            const float sh = __shfl_sync(kFullMask, tot, tw + 0);
-            const float sk = __shfl_sync(kFullMask, tot, tw + 1);
-            const float shk = __shfl_sync(kFullMask, tot, tw + 2);
-            const float sv = __shfl_sync(kFullMask, tot, tw + 3);
-            const float rh = rsqrtf(fmaf(sh, inv_d, p.eps));
-            const float rk = rsqrtf(fmaf(sk, inv_d, p.eps));
-            const float z = rh * rk * shk * p.inv_sqrt_d;
-            alpha_l = __fdividef(1.0f, 1.0f + __expf(-z));
-            rv_l = rsqrtf(fmaf(alpha_l * alpha_l * sv, inv_d, p.eps));
-            const int j = (c - 1) * kChunk + lane;
-            if (rank == 0 && warp == 0 && lane < kChunk && j < ntok && t_first + j >= t_out) {
-                const long long r = row0 + t_first + j;
-                p.alpha[r] = alpha_l;
-                p.rh[r] = rh;
-                p.rk[r] = rk;
-                p.rv[r] = rv_l;
-            }
-        }
-        // ---- send chunk c (after this warp has read chunk c - 1)
-        if (c < nchunks) gc::xch_send(xch, xbar, c & 1, parts, part, val, lane, C);
-        // ---- B: conv, SiLU and outputs of chunk c - 1 (branch-free; stores
-        // predicated)
-        if (c >= 1) {
-            const int j0 = (c - 1) * kChunk;
-            const unsigned char* b0 =
-                ring + static_cast<size_t>(j0 % stages) * stage_bytes + 2 * pitch + 8 * tid;
-            const long long off0 = (row0 + t_first + j0) * d + c0;
+        if (kB) {
+            const unsigned char* b0 = bthread + stb * kStageBytes + 2 * kPitch;
 #pragma unroll
             for (int w = 0; w < kChunk; ++w) {
                 const float alpha = __shfl_sync(kFullMask, alpha_l, w);
-                const float rv = __shfl_sync(kFullMask, rv_l, w);
-                const uint2 vq = lds64(b0 + static_cast<size_t>(w) * stage_bytes);
-                const float2 a2 = splat2(alpha), ar2 = splat2(alpha * rv);
+                const float ar = __shfl_sync(kFullMask, ar_l, w);
+                const uint2 vq = lds64(b0 + w * kStageBytes);
+                const float2 a2 = splat2(alpha), ar2 = splat2(ar);
                 float2 vh[2], y[2];
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
@@ -209,41 +256,76 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
                         fma2(cw[0][i], U[(w + 1) & 3][i],
                              fma2(cw[1][i], U[(w + 2) & 3][i], fma2(cw[2][i], U[(w + 3) & 3][i], mul2(cw[3][i], u))));
                     // SiLU(c) = c / (1 + e^-c)
-                    const float2 rden = make_float2(gc::rcp_ftz(1.0f + gc::exp_neg_ftz(cc.x)), gc::rcp_ftz(1.0f + gc::exp_neg_ftz(cc.y)));
+                    const float2 rden = make_float2(gc::rcp_ftz(1.0f + gc::exp_neg_ftz(cc.x)),
+                                                    gc::rcp_ftz(1.0f + gc::exp_neg_ftz(cc.y)));
                     y[i] = fma2(cc, rden, vh[i]);
                     U[w][i] = u;
                 }
-                if (active && j0 + w < ntok && t_first + j0 + w >= t_out) {
-                    const long long off = off0 + static_cast<long long>(w) * d;
-                    stg_cs8(p.Y + off, make_uint2(pack2(y[0]), pack2(y[1])));
-                    stg_cs8(p.vhat + off, make_uint2(pack2(vh[0]), pack2(vh[1])));
+                const int j = jb + w;
+                const bool st_ok = active && j >= j_out && j < ntok;
+                const long long off = static_cast<long long>(j) * d;
+                stg_cs8_if(outY + off, make_uint2(pack2(y[0]), pack2(y[1])), st_ok);
+                stg_cs8_if(outV + off, make_uint2(pack2(vh[0]), pack2(vh[1])), st_ok);
+            }
+        }
+        // ---------------- hand in chunk c: the warp's 16 totals go to shared
+        // memory; the last warp of the CTA to do so adds the warps' totals in
+        // warp order and sends the CTA's total into slot `rank` of every CTA of
+        // the cluster (st.async, completing on that CTA's exchange barrier)
+        if (kA) {
+            local[(buf * 8 + warp) * gc::kVals + (lane >> 1)] = val;
+            __syncwarp();
+            unsigned int last = 0u;
+            if (lane == 0) {
+                __threadfence_block();
+                if (atomicAdd(&arrived[buf], 1u) == static_cast<unsigned int>(nw - 1)) {
+                    arrived[buf] = 0u;
+                    __threadfence_block();
+                    last = 1u;
                 }
             }
-            // this warp is done with the chunk's stages; the last warp refills them
+            last = __shfl_sync(kFullMask, last, 0);
+            if (last) {
+                __syncwarp();   // the other warps' totals, seen by lane 0, to every lane
+                const float* lp = local + buf * 8 * gc::kVals + (lane & 15);
+                float cta = 0.f;
+                for (int w = 0; w < nw; ++w) cta += lp[w * gc::kVals];
+                const uint32_t dst = smem_addr(tot + (buf * 8 + static_cast<int>(rank)) * gc::kVals + (lane & 15));
+                const uint32_t bar = smem_addr(xbar + buf);
+                for (uint32_t r = static_cast<uint32_t>(lane >> 4); r < C; r += 2)
+                    st_async_f32(map_to_rank(dst, r), cta, map_to_rank(bar, r));
+            }
+        }
+        // ---------------- chunk c - 1's stages are done; the last warp refills them
+        if (kB) {
             __syncwarp();
             if (lane == 0) {
                 __threadfence_block();
-                const int st0 = j0 % stages;
-                if (atomicAdd(&released[st0], 1u) == static_cast<unsigned int>(nw - 1)) {
-                    released[st0] = 0u;
+                if (atomicAdd(&released[stb], 1u) == static_cast<unsigned int>(nw - 1)) {
+                    released[stb] = 0u;
                     fence_proxy_async();
-                    for (int w = 0; w < kChunk && j0 + stages + w < ntok; ++w) issue(j0 + stages + w);
+                    for (int w = 0; w < kChunk && jb + kStages + w < ntok; ++w) issue(jb + kStages + w);
                 }
             }
         }
-    }
+    };
+    iteration(std::true_type(), std::false_type(), 0);
+    for (int c = 1; c < nchunks; ++c) iteration(std::true_type(), std::true_type(), c);
+    iteration(std::false_type(), std::true_type(), nchunks);
     if (failed) {
         atomicOr(p.err, kErrTimeout);
         // let copies issued by this CTA land before it leaves (bounded)
         if (tid == 0)
-            for (int j = ntok > stages ? ntok - stages : 0; j < ntok; ++j)
-                (void)mbar_wait(&full[j % stages], static_cast<uint32_t>((j / stages) & 1));
+            for (int j = ntok > kStages ? ntok - kStages : 0; j < ntok; ++j)
+                (void)mbar_wait(&full[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
     }
     // no CTA leaves while a peer may still store into its slots
     cluster_sync();
 }
 
 }  // namespace
+
+int gateconv_fwd_smem() { return kSmem; }
 
 cudaError_t gateconv_fwd_prepare(int smem_bytes) {
     if (smem_bytes <= 0) return cudaSuccess;
