@@ -30,7 +30,6 @@ constexpr int kGcStages = 16;
 constexpr int kGcMinRange = 16;    // tokens; bounds the 3-token halo overhead
 constexpr int kGcRangeCost = 8;    // per-range set-up, in token-steps, for the range split
 constexpr int64_t kGcBwdSlots = 256;  // backward weight-gradient slots (one per range)
-constexpr int kGcBwdMaxRange = 1024;  // backward range cap (its saved scalars sit in shared memory)
 
 struct OccKey {
     int op, cluster, threads, smem;
@@ -367,11 +366,9 @@ const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
     auto shape = [&](int C, GcGeom& g) {
         g = {};
         gc_split(d, rows, C, g);
-        if (op == 0) g.c.smem = gateconv_fwd_smem();   // fixed layout (2048-byte row slots)
-        if (op == 1) {
-            g.sc_off = g.c.smem;  // saved scalars of up to kGcBwdMaxRange + 7 streamed tokens
-            g.c.smem += 16 * (kGcBwdMaxRange + 8);
-        }
+        // fixed layouts (2048-byte row slots; the backward's with the staged
+        // saved scalars of up to kGcBwdMaxRange + 7 streamed tokens)
+        g.c.smem = op == 0 ? gateconv_fwd_smem() : gateconv_bwd_smem();
     };
     GcGeom g;
     const int C0 = static_cast<int>((d + 1023) / 1024);

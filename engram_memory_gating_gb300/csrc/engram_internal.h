@@ -13,6 +13,10 @@ constexpr int kGateHidden = 5120;
 // Largest number of ring stages any kernel uses (mbarrier area sizing).
 constexpr int kMaxStages = 16;
 
+// GateConv backward: longest token range (its saved scalars are staged in
+// shared memory, 16 bytes a token, with up to 8 halo tokens).
+constexpr int kGcBwdMaxRange = 1024;
+
 // Largest token group of the backward's elementwise kernel: its per-token
 // scalars (64 bytes a token) and zero flags are staged in shared memory.
 constexpr int kGateBwdTableTokens = 256;
@@ -196,6 +200,7 @@ cudaError_t decode_prepare();
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);
 
 int gateconv_fwd_smem();  // dynamic shared memory of the forward kernel (fixed layout)
+int gateconv_bwd_smem();  // dynamic shared memory of the backward kernel (fixed layout)
 cudaError_t gateconv_fwd_prepare(int smem_bytes);
 cudaError_t gateconv_fwd_max_clusters(int cluster, int threads, int smem, int* out);
 cudaError_t gateconv_fwd_launch(const GateConvFwdParams& p, const LaunchCfg& c, cudaStream_t s);

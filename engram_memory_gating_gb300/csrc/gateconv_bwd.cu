@@ -102,14 +102,32 @@ EG_DEV void conv_t(const Windows& W, const Weights& P, float2 (&du)[2]) {
                           fma2(P.cw[1][i], W.D[(S + 2) & 3][i], mul2(P.cw[0][i], W.D[(S + 3) & 3][i]))));
 }
 
+// Shared memory: a fixed layout, so that every ring address of a token is a
+// chunk base plus an immediate.  Each row slot is 2048 bytes (the widest
+// column slice, 1024 columns); a narrower slice leaves the slot's tail zero.
+constexpr int kPitch = 2048;
+constexpr int kStageBytes = kRows * kPitch;
+constexpr int kOffFull = 0;                      // [kStages] stage mbarriers
+constexpr int kOffXbar = 128;                    // [2] cluster-exchange mbarriers
+constexpr int kOffRel = 160;                     // [kStages] stage release counters
+constexpr int kOffArr = 224;                     // [2] per-chunk arrival counters
+constexpr int kOffLocal = 256;                   // [2][8 warps][16] warp totals
+constexpr int kOffTot = kOffLocal + 2 * 8 * gc::kVals * 4;   // [2][8 ranks][16] CTA totals
+constexpr int kRingOff = kOffTot + 2 * 8 * gc::kVals * 4;
+constexpr int kScOff = kRingOff + kStages * kStageBytes;     // saved scalars of the streamed tokens
+constexpr int kSmem = kScOff + 16 * (kGcBwdMaxRange + 8);
+static_assert(kRingOff % 128 == 0 && kScOff % 16 == 0, "alignment");
+
 __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const GateConvBwdParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + gc::kOffFull);
-    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + gc::kOffXbar);
-    unsigned int* released = reinterpret_cast<unsigned int*>(smem + gc::kOffRel);
-    float* xch = reinterpret_cast<float*>(smem + gc::kOffXch);
-    unsigned char* ring = smem + p.ring_off;
-    float4* sc = reinterpret_cast<float4*>(smem + p.sc_off);  // (rrms_v, alpha, rrms_h, rrms_k)
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffFull);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + kOffXbar);
+    unsigned int* released = reinterpret_cast<unsigned int*>(smem + kOffRel);
+    unsigned int* arrived = reinterpret_cast<unsigned int*>(smem + kOffArr);
+    float* local = reinterpret_cast<float*>(smem + kOffLocal);
+    float* tot = reinterpret_cast<float*>(smem + kOffTot);
+    unsigned char* ring = smem + kRingOff;
+    float4* sc = reinterpret_cast<float4*>(smem + kScOff);  // (rrms_v, alpha, rrms_h, rrms_k)
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -117,8 +135,6 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
     const int nw = blockDim.x >> 5;
     const uint32_t C = cluster_size();
     const uint32_t rank = cluster_rank();
-    const int parts = static_cast<int>(C) * nw;
-    const int part = static_cast<int>(rank) * nw + warp;
     const int q = static_cast<int>(cluster_index());
     const int d = p.d;
     const int col0 = static_cast<int>(rank) * p.ncols;
@@ -126,8 +142,6 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
     const bool active = 4 * tid < cols;
     const int c0 = col0 + 4 * tid;
     const uint32_t row_bytes = 2u * static_cast<uint32_t>(cols);
-    const uint32_t pitch = 2u * static_cast<uint32_t>(p.ncols);
-    const uint32_t stage_bytes = kRows * pitch;
 
     // ranges start at multiples of kChunk, and so does the streamed halo, so
     // token t sits in window slot t % 4 (known at compile time below)
@@ -139,14 +153,17 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
     const int ntok = t_last - t_first;             // streamed tokens (halo included)
     const int nchunks = (t_end - t_out + kChunk - 1) / kChunk;
     const long long row0 = static_cast<long long>(m) * p.T;
-    const uint32_t xbytes = static_cast<uint32_t>(parts) * gc::kVals * 4u;
+    const uint32_t xbytes = C * gc::kVals * 4u;     // one 16-value total from each CTA
 
     Weights P;
+    float2 wh[2];  // w_h itself, for drms_w_h
     if (active) {
         const float4 a = __ldg(reinterpret_cast<const float4*>(p.wh + c0));
         const float4 b = __ldg(reinterpret_cast<const float4*>(p.wv + c0));
         P.wh2[0] = make_float2(a.x * a.x, a.y * a.y);
         P.wh2[1] = make_float2(a.z * a.z, a.w * a.w);
+        wh[0] = make_float2(a.x, a.y);
+        wh[1] = make_float2(a.z, a.w);
         P.wv[0] = make_float2(b.x, b.y);
         P.wv[1] = make_float2(b.z, b.w);
 #pragma unroll
@@ -158,39 +175,34 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
     } else {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            P.wh2[i] = P.wv[i] = make_float2(0.f, 0.f);
+            P.wh2[i] = P.wv[i] = wh[i] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < 4; ++j) P.cw[j][i] = make_float2(0.f, 0.f);
         }
     }
-    float2 wh[2];  // w_h itself, for drms_w_h
-    if (active) {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(p.wh + c0));
-        wh[0] = make_float2(a.x, a.y);
-        wh[1] = make_float2(a.z, a.w);
-    } else {
-        wh[0] = wh[1] = make_float2(0.f, 0.f);
-    }
 
+    const long long base = (row0 + t_first) * d + col0;
     auto issue = [&](int j) {
-        const int st = j % kStages;
-        const long long off = (row0 + t_first + j) * d + col0;
-        unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
+        const int st = j & (kStages - 1);
+        const long long off = base + static_cast<long long>(j) * d;
+        unsigned char* b = ring + st * kStageBytes;
         mbar_arrive_expect_tx(&full[st], kRows * row_bytes);
         bulk_g2s(b, p.dY + off, row_bytes, &full[st]);
-        bulk_g2s(b + pitch, p.vhat + off, row_bytes, &full[st]);
-        bulk_g2s(b + 2 * pitch, p.v + off, row_bytes, &full[st]);
-        bulk_g2s(b + 3 * pitch, p.H + off, row_bytes, &full[st]);
-        bulk_g2s(b + 4 * pitch, p.k + off, row_bytes, &full[st]);
+        bulk_g2s(b + kPitch, p.vhat + off, row_bytes, &full[st]);
+        bulk_g2s(b + 2 * kPitch, p.v + off, row_bytes, &full[st]);
+        bulk_g2s(b + 3 * kPitch, p.H + off, row_bytes, &full[st]);
+        bulk_g2s(b + 4 * kPitch, p.k + off, row_bytes, &full[st]);
     };
+    const unsigned char* bthread = ring + 8 * tid;
+    // this thread's 8 bytes of row r of streamed token t (t_first <= t < t_last)
     auto row_of = [&](int t) -> const unsigned char* {
-        return ring + static_cast<size_t>((t - t_first) % kStages) * stage_bytes + 8 * tid;
+        return bthread + ((t - t_first) & (kStages - 1)) * kStageBytes;
     };
     // this warp is done with the stages of tokens t .. t+n-1 (one counter per
     // group, at its first stage); the last warp refills them
     auto release = [&](int t, int n) {
         const int j = t - t_first;
-        const int st = j % kStages;
+        const int st = j & (kStages - 1);
         __syncwarp();
         if (lane == 0) {
             __threadfence_block();
@@ -201,11 +213,10 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
             }
         }
     };
-    // waits for token tau's stage (a real token: t_first <= tau < t_last)
     bool failed = false;
     auto wait_tok = [&](int tau) {
         const int j = tau - t_first;
-        if (!failed && !mbar_wait(&full[j % kStages], static_cast<uint32_t>((j / kStages) & 1)))
+        if (!failed && !mbar_wait(&full[j & (kStages - 1)], static_cast<uint32_t>((j / kStages) & 1)))
             failed = true;
     };
 
@@ -216,6 +227,7 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
         }
         mbar_init(&xbar[0], 1);
         mbar_init(&xbar[1], 1);
+        arrived[0] = arrived[1] = 0u;
         fence_mbar_init();
         mbar_arrive_expect_tx(&xbar[0], xbytes);
         if (nchunks > 1) mbar_arrive_expect_tx(&xbar[1], xbytes);
@@ -226,6 +238,15 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
     for (int i = tid; i < ntok; i += blockDim.x) {
         const long long r = row0 + t_first + i;
         sc[i] = make_float4(__ldg(p.rv + r), __ldg(p.alpha + r), __ldg(p.rh + r), __ldg(p.rk + r));
+    }
+    // the tails of the row slots past this slice's columns, which no copy
+    // writes, are zero (threads without columns read them)
+    if (row_bytes < kPitch) {
+        const int words = (kPitch - static_cast<int>(row_bytes)) / 4;
+        for (int i = tid; i < kStages * kRows * words; i += blockDim.x) {
+            const int slot = i / words;
+            reinterpret_cast<uint32_t*>(ring + slot * kPitch + row_bytes)[i - slot * words] = 0u;
+        }
     }
     cluster_sync();
 
@@ -250,9 +271,7 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
         }
         wait_tok(tau);
         const float rv = sc[tau - t_first].x;
-        consume<S>(W, gcw, P, row_of(tau), pitch, rv, true, tau >= t_out, active && tau >= t_out && tau < t_end);
-        // the halo before the range is not needed again (the halo after it
-        // sits at the end of the stream, its stages are never refilled)
+        consume<S>(W, gcw, P, row_of(tau), kPitch, rv, true, tau >= t_out, active && tau >= t_out && tau < t_end);
         if (tau < t_out) release(tau, 1);
     };
 
@@ -266,118 +285,47 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
     step(std::integral_constant<int, 2>(), t_out + 2);
 
     const float inv_d = 1.0f / static_cast<float>(d);
-    float2 duA[kChunk][2], duB[kChunk][2];  // du of chunk c and of chunk c - 1
-    float P_l = 0.f, Q_l = 0.f, a_l = 0.f, Ah_l = 0.f, Bh_l = 0.f, Bk_l = 0.f;
-
-    // one output token t = tc + S of chunk c: consume t + 3, then du_t, the
-    // partial sums and drms_w_v (branch-free: tokens past the range select 0)
-    auto out1 = [&](auto slot, int tc, const float (&rvt)[kChunk], const float (&rvc)[kChunk],
-                    float (&sums)[gc::kVals]) {
-        constexpr int S = decltype(slot)::value;
-        const int t = tc + S;
-        const bool vt = active && t < t_end;
-        consume<(S + 3) & 3>(W, gcw, P, row_of(t + 3), pitch, rvc[S], t + 3 < t_last, true,
-                             active && t + 3 < t_end);
-        float2 du[2];
-        conv_t<S>(W, P, du);
-        const unsigned char* b = row_of(t);
-        const uint2 yq = lds64(b), hq = lds64(b + pitch), vq = lds64(b + 2 * pitch);
-        const uint2 Hq = lds64(b + 3 * pitch), kq = lds64(b + 4 * pitch);
-        const float2 rv2 = splat2(rvt[S]);
-        const float2 zero = make_float2(0.f, 0.f);
-        float2 s1 = zero, s3 = zero, s4 = zero, s5 = zero;
+    float2 du[kChunk][2];  // du of the chunk handed in last (read by its phase 2)
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float2 dy = bf2(i == 0 ? yq.x : yq.y), vh = bf2(i == 0 ? hq.x : hq.y);
-            const float2 vv = bf2(i == 0 ? vq.x : vq.y);
-            const float2 h = bf2(i == 0 ? Hq.x : Hq.y), kk = bf2(i == 0 ? kq.x : kq.y);
-            const float2 wdu = mul2(P.wv[i], du[i]);
-            s1 = fma2(fma2(rv2, wdu, dy), vv, s1);
-            s3 = fma2(vh, vv, s3);
-            s4 = fma2(wdu, vh, s4);
-            s5 = fma2(mul2(h, kk), P.wh2[i], s5);
-            const float2 g = mul2(du[i], mul2(vh, rv2));
-            gwv[i] = add2(gwv[i], vt ? g : zero);
-            duA[S][i] = du[i];
-        }
-        sums[4 * S + 0] = vt ? s1.x + s1.y : 0.f;
-        sums[4 * S + 1] = vt ? s3.x + s3.y : 0.f;
-        sums[4 * S + 2] = vt ? s4.x + s4.y : 0.f;
-        sums[4 * S + 3] = vt ? s5.x + s5.y : 0.f;
-    };
+    for (int w = 0; w < kChunk; ++w) du[w][0] = du[w][1] = make_float2(0.f, 0.f);
 
-    // one output token t of chunk c - 1 in slot S: dv, dH, dk, drms_w_h
-    auto out2 = [&](auto slot, int t) {
-        constexpr int S = decltype(slot)::value;
-        const float Pv = __shfl_sync(kFullMask, P_l, S);
-        const float Q = __shfl_sync(kFullMask, Q_l, S);
-        const float a = __shfl_sync(kFullMask, a_l, S);
-        const float Ah = __shfl_sync(kFullMask, Ah_l, S);
-        const float Bh = __shfl_sync(kFullMask, Bh_l, S);
-        const float Bk = __shfl_sync(kFullMask, Bk_l, S);
-        const bool vt = active && t < t_end;
-        const unsigned char* b = row_of(t);
-        const uint2 yq = lds64(b), hq = lds64(b + pitch);
-        const uint2 Hq = lds64(b + 3 * pitch), kq = lds64(b + 4 * pitch);
-        const float2 P2 = splat2(Pv), nQ2 = splat2(-Q), a2 = splat2(a);
-        const float2 Ah2 = splat2(Ah), nBh2 = splat2(-Bh), nBk2 = splat2(-Bk), Ah22 = splat2(2.0f * Ah);
-        const float2 zero = make_float2(0.f, 0.f);
-        uint32_t oh[2], ok[2], ov[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float2 dy = bf2(i == 0 ? yq.x : yq.y), vh = bf2(i == 0 ? hq.x : hq.y);
-            const float2 h = bf2(i == 0 ? Hq.x : Hq.y), kk = bf2(i == 0 ? kq.x : kq.y);
-            const float2 dvh = fma2(nQ2, vh, fma2(mul2(P2, P.wv[i]), duB[S][i], dy));
-            ov[i] = pack2(mul2(a2, dvh));
-            const float2 aw = mul2(Ah2, P.wh2[i]);
-            oh[i] = pack2(fma2(aw, kk, mul2(nBh2, h)));
-            ok[i] = pack2(fma2(aw, h, mul2(nBk2, kk)));
-            const float2 g = mul2(mul2(Ah22, wh[i]), mul2(h, kk));
-            gwh[i] = add2(gwh[i], vt ? g : zero);
-        }
-        if (vt) {
-            const long long off = (row0 + t) * d + c0;
-            stg_cs8(p.dH + off, make_uint2(oh[0], oh[1]));
-            stg_cs8(p.dk + off, make_uint2(ok[0], ok[1]));
-            stg_cs8(p.dv + off, make_uint2(ov[0], ov[1]));
-        }
-    };
-
-    for (int c = 0; c <= nchunks; ++c) {
-        const int tc = t_out + c * kChunk;          // first token of chunk c
-        // ---- 1: du and partial sums of chunk c
-        float val = 0.f;
-        if (c < nchunks) {
-            // all waits first, then branch-free arithmetic over the chunk
+    // One iteration per chunk c = 0 .. nchunks: phase 2 of chunk c - 1 (its
+    // totals -> coefficients; dv, dH, dk, drms_w_h from the rows still in the
+    // ring) and phase 1 of chunk c (consume tokens t + 3, du, the partial
+    // sums).  All waits come first, then one straight-line block with both
+    // phases (the scheduler overlaps their latency chains), then the hand-in
+    // of chunk c and the release of chunk c - 1's stages.
+    auto iteration = [&](auto has1, auto has2, int c) {
+        constexpr bool k1 = decltype(has1)::value;
+        constexpr bool k2 = decltype(has2)::value;
+        const int buf = c & 1;
+        const int tc = t_out + c * kChunk;      // first token of chunk c
+        const int tp = tc - kChunk;             // first token of chunk c - 1
+        if (k1) {
 #pragma unroll
             for (int w = 0; w < kChunk; ++w)
                 if (tc + w < t_end && tc + w + 3 < t_last) wait_tok(tc + w + 3);
-            float rvt[kChunk], rvc[kChunk];
-#pragma unroll
-            for (int w = 0; w < kChunk; ++w) {
-                rvt[w] = sc[min(tc + w, t_end - 1) - t_first].x;
-                rvc[w] = sc[min(tc + w + 3, t_last - 1) - t_first].x;
-            }
-            float sums[gc::kVals];
-            out1(std::integral_constant<int, 0>(), tc, rvt, rvc, sums);
-            out1(std::integral_constant<int, 1>(), tc, rvt, rvc, sums);
-            out1(std::integral_constant<int, 2>(), tc, rvt, rvc, sums);
-            out1(std::integral_constant<int, 3>(), tc, rvt, rvc, sums);
-            val = gc::warp_reduce16(sums, lane);
         }
-        // ---- totals of chunk c - 1 -> coefficients of token (lane & 3)
-        if (c >= 1) {
-            const int buf = (c - 1) & 1;
-            if (!failed && !mbar_wait_cluster(&xbar[buf], static_cast<uint32_t>(((c - 1) >> 1) & 1)))
+        if (k2) {
+            // every warp reads chunk c - 1's totals before it hands in chunk c
+            if (!failed && !mbar_wait_cluster(&xbar[buf ^ 1], static_cast<uint32_t>(((c - 1) >> 1) & 1)))
                 failed = true;
-            if (tid == 0 && c + 1 < nchunks) mbar_arrive_expect_tx(&xbar[buf], xbytes);
-            const float tot = gc::xch_total(xch, buf, parts, lane);
+            if (tid == 0 && c + 1 < nchunks) mbar_arrive_expect_tx(&xbar[buf ^ 1], xbytes);
+        }
+        // ---------------- straight-line block
+        float P_l = 0.f, Q_l = 0.f, a_l = 0.f, Ah_l = 0.f, Bh_l = 0.f, Bk_l = 0.f;
+        if (k2) {
+            const float* tq = tot + (buf ^ 1) * 8 * gc::kVals + (lane & 15);
+            float tv = 0.f;
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                if (r < static_cast<int>(C)) tv += tq[r * gc::kVals];
             const int tw = 4 * (lane & 3);
-            const float S1 = __shfl_sync(kFullMask, tot, tw + 0);
-            const float S3 = __shfl_sync(kFullMask, tot, tw + 1);
-            const float S4 = __shfl_sync(kFullMask, tot, tw + 2);
-            const float S5 = __shfl_sync(kFullMask, tot, tw + 3);
-            const int t = min(tc - kChunk + (lane & 3), t_end - 1);
+            const float S1 = __shfl_sync(kFullMask, tv, tw + 0);
+            const float S3 = __shfl_sync(kFullMask, tv, tw + 1);
+            const float S4 = __shfl_sync(kFullMask, tv, tw + 2);
+            const float S5 = __shfl_sync(kFullMask, tv, tw + 3);
+            const int t = min(tp + (lane & 3), t_end - 1);
             const float4 s4 = sc[t - t_first];
             const float rv = s4.x, a = s4.y, rh = s4.z, rk = s4.w;
             const float mu = rv * S4 * inv_d;
@@ -393,20 +341,128 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
             Bh_l = Ah * rh * rh * e5;
             Bk_l = Ah * rk * rk * e5;
         }
-        // ---- send chunk c
-        if (c < nchunks) gc::xch_send(xch, xbar, c & 1, parts, part, val, lane, C);
-        // ---- 2: dv, dH, dk of chunk c - 1
-        if (c >= 1) {
-            const int tp = tc - kChunk;
-            out2(std::integral_constant<int, 0>(), tp);
-            out2(std::integral_constant<int, 1>(), tp + 1);
-            out2(std::integral_constant<int, 2>(), tp + 2);
-            out2(std::integral_constant<int, 3>(), tp + 3);
-            release(tp, min(kChunk, t_end - tp));
-        }
+        if (k2) {
+            // one output token t = tp + S of chunk c - 1: dv, dH, dk, drms_w_h
+            auto out2 = [&](auto slot) {
+                constexpr int S = decltype(slot)::value;
+                const int t = tp + S;
+                const float Pv = __shfl_sync(kFullMask, P_l, S);
+                const float Qv = __shfl_sync(kFullMask, Q_l, S);
+                const float av = __shfl_sync(kFullMask, a_l, S);
+                const float Ah = __shfl_sync(kFullMask, Ah_l, S);
+                const float Bh = __shfl_sync(kFullMask, Bh_l, S);
+                const float Bk = __shfl_sync(kFullMask, Bk_l, S);
+                const bool vt = active && t < t_end;
+                const unsigned char* b = row_of(t);
+                const uint2 yq = lds64(b), hq = lds64(b + kPitch);
+                const uint2 Hq = lds64(b + 3 * kPitch), kq = lds64(b + 4 * kPitch);
+                const float2 P2 = splat2(Pv), nQ2 = splat2(-Qv), a2 = splat2(av);
+                const float2 Ah2 = splat2(Ah), nBh2 = splat2(-Bh), nBk2 = splat2(-Bk), Ah22 = splat2(2.0f * Ah);
+                const float2 zero = make_float2(0.f, 0.f);
+                uint32_t oh[2], ok[2], ov[2];
 #pragma unroll
-        for (int w = 0; w < kChunk; ++w) duB[w][0] = duA[w][0], duB[w][1] = duA[w][1];
-    }
+                for (int i = 0; i < 2; ++i) {
+                    const float2 dy = bf2(i == 0 ? yq.x : yq.y), vh = bf2(i == 0 ? hq.x : hq.y);
+                    const float2 h = bf2(i == 0 ? Hq.x : Hq.y), kk = bf2(i == 0 ? kq.x : kq.y);
+                    const float2 dvh = fma2(nQ2, vh, fma2(mul2(P2, P.wv[i]), du[S][i], dy));
+                    ov[i] = pack2(mul2(a2, dvh));
+                    const float2 aw = mul2(Ah2, P.wh2[i]);
+                    oh[i] = pack2(fma2(aw, kk, mul2(nBh2, h)));
+                    ok[i] = pack2(fma2(aw, h, mul2(nBk2, kk)));
+                    const float2 g = mul2(mul2(Ah22, wh[i]), mul2(h, kk));
+                    gwh[i] = add2(gwh[i], vt ? g : zero);
+                }
+                const long long off = (row0 + t) * d + c0;
+                stg_cs8_if(p.dH + off, make_uint2(oh[0], oh[1]), vt);
+                stg_cs8_if(p.dk + off, make_uint2(ok[0], ok[1]), vt);
+                stg_cs8_if(p.dv + off, make_uint2(ov[0], ov[1]), vt);
+            };
+            out2(std::integral_constant<int, 0>());
+            out2(std::integral_constant<int, 1>());
+            out2(std::integral_constant<int, 2>());
+            out2(std::integral_constant<int, 3>());
+        }
+        float val = 0.f;
+        if (k1) {
+            float rvt[kChunk], rvc[kChunk];
+#pragma unroll
+            for (int w = 0; w < kChunk; ++w) {
+                rvt[w] = sc[min(tc + w, t_end - 1) - t_first].x;
+                rvc[w] = sc[min(tc + w + 3, t_last - 1) - t_first].x;
+            }
+            float sums[gc::kVals];
+            // one output token t = tc + S of chunk c: consume t + 3, then du_t,
+            // the partial sums and drms_w_v (tokens past the range select 0)
+            auto out1 = [&](auto slot) {
+                constexpr int S = decltype(slot)::value;
+                const int t = tc + S;
+                const bool vt = active && t < t_end;
+                consume<(S + 3) & 3>(W, gcw, P, row_of(t + 3), kPitch, rvc[S], t + 3 < t_last, true,
+                                     active && t + 3 < t_end);
+                float2 d2[2];
+                conv_t<S>(W, P, d2);
+                const unsigned char* b = row_of(t);
+                const uint2 yq = lds64(b), hq = lds64(b + kPitch), vq = lds64(b + 2 * kPitch);
+                const uint2 Hq = lds64(b + 3 * kPitch), kq = lds64(b + 4 * kPitch);
+                const float2 rv2 = splat2(rvt[S]);
+                const float2 zero = make_float2(0.f, 0.f);
+                float2 s1 = zero, s3 = zero, s4 = zero, s5 = zero;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const float2 dy = bf2(i == 0 ? yq.x : yq.y), vh = bf2(i == 0 ? hq.x : hq.y);
+                    const float2 vv = bf2(i == 0 ? vq.x : vq.y);
+                    const float2 h = bf2(i == 0 ? Hq.x : Hq.y), kk = bf2(i == 0 ? kq.x : kq.y);
+                    const float2 wdu = mul2(P.wv[i], d2[i]);
+                    s1 = fma2(fma2(rv2, wdu, dy), vv, s1);
+                    s3 = fma2(vh, vv, s3);
+                    s4 = fma2(wdu, vh, s4);
+                    s5 = fma2(mul2(h, kk), P.wh2[i], s5);
+                    const float2 g = mul2(d2[i], mul2(vh, rv2));
+                    gwv[i] = add2(gwv[i], vt ? g : zero);
+                    du[S][i] = d2[i];
+                }
+                sums[4 * S + 0] = s1.x + s1.y;
+                sums[4 * S + 1] = s3.x + s3.y;
+                sums[4 * S + 2] = s4.x + s4.y;
+                sums[4 * S + 3] = s5.x + s5.y;
+            };
+            out1(std::integral_constant<int, 0>());
+            out1(std::integral_constant<int, 1>());
+            out1(std::integral_constant<int, 2>());
+            out1(std::integral_constant<int, 3>());
+            val = gc::warp_reduce16(sums, lane);
+        }
+        // ---------------- hand in chunk c (as in the forward: warp totals to
+        // shared memory, the last warp sends the CTA's total to every CTA)
+        if (k1) {
+            local[(buf * 8 + warp) * gc::kVals + (lane >> 1)] = val;
+            __syncwarp();
+            unsigned int last = 0u;
+            if (lane == 0) {
+                __threadfence_block();
+                if (atomicAdd(&arrived[buf], 1u) == static_cast<unsigned int>(nw - 1)) {
+                    arrived[buf] = 0u;
+                    __threadfence_block();
+                    last = 1u;
+                }
+            }
+            last = __shfl_sync(kFullMask, last, 0);
+            if (last) {
+                __syncwarp();
+                const float* lp = local + buf * 8 * gc::kVals + (lane & 15);
+                float cta = 0.f;
+                for (int w = 0; w < nw; ++w) cta += lp[w * gc::kVals];
+                const uint32_t dst = smem_addr(tot + (buf * 8 + static_cast<int>(rank)) * gc::kVals + (lane & 15));
+                const uint32_t bar = smem_addr(xbar + buf);
+                for (uint32_t r = static_cast<uint32_t>(lane >> 4); r < C; r += 2)
+                    st_async_f32(map_to_rank(dst, r), cta, map_to_rank(bar, r));
+            }
+        }
+        if (k2) release(tp, min(kChunk, t_end - tp));
+    };
+    iteration(std::true_type(), std::false_type(), 0);
+    for (int c = 1; c < nchunks; ++c) iteration(std::true_type(), std::true_type(), c);
+    iteration(std::false_type(), std::true_type(), nchunks);
 
     // per-range weight-gradient partial: [dwh | dwv | dcw0..3], each d wide
     if (active) {
@@ -445,6 +501,8 @@ __global__ void __launch_bounds__(256) gc_wreduce_kernel(const GateWReduceParams
 }
 
 }  // namespace
+
+int gateconv_bwd_smem() { return kSmem; }
 
 cudaError_t gateconv_bwd_prepare(int smem_bytes) {
     if (smem_bytes <= 0) return cudaSuccess;

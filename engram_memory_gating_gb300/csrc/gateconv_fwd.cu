@@ -41,7 +41,8 @@ constexpr int kRows = 3;                         // H, k, v
 constexpr int kPitch = 2048;                     // bytes per row slot
 constexpr int kStageBytes = kRows * kPitch;
 constexpr int kStages = gc::kStages;             // 16 one-token stages
-constexpr int kOffFull = 0;                      // [kStages] stage mbarriers
+constexpr int kSlots = kStages / kChunk;         // 4 chunk slots of the ring
+constexpr int kOffFull = 0;                      // [kSlots] chunk-slot mbarriers
 constexpr int kOffXbar = 128;                    // [2] cluster-exchange mbarriers
 constexpr int kOffRel = 160;                     // [kStages] stage release counters
 constexpr int kOffArr = 224;                     // [2] per-chunk arrival counters
@@ -114,18 +115,25 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
     const uint16_t* srcH = p.H + (row0 + t_first) * d + col0;
     const uint16_t* srcK = p.k + (row0 + t_first) * d + col0;
     const uint16_t* srcV = p.v + (row0 + t_first) * d + col0;
-    auto issue = [&](int j) {
-        const int st = j & (kStages - 1);
-        const long long off = static_cast<long long>(j) * d;
-        unsigned char* b = ring + st * kStageBytes;
-        mbar_arrive_expect_tx(&full[st], 3u * row_bytes);
-        bulk_g2s(b, srcH + off, row_bytes, &full[st]);
-        bulk_g2s(b + kPitch, srcK + off, row_bytes, &full[st]);
-        bulk_g2s(b + 2 * kPitch, srcV + off, row_bytes, &full[st]);
+    // the tokens of chunk c (those of the stream) into chunk slot c % 4, all
+    // completing on that slot's barrier
+    auto issue = [&](int c) {
+        const int slot = c & (kSlots - 1);
+        const int j0 = c * kChunk;
+        const int n = min(kChunk, ntok - j0);
+        uint64_t* bar = &full[slot];
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * 3u * row_bytes);
+        for (int w = 0; w < n; ++w) {
+            const long long off = static_cast<long long>(j0 + w) * d;
+            unsigned char* b = ring + (slot * kChunk + w) * kStageBytes;
+            bulk_g2s(b, srcH + off, row_bytes, bar);
+            bulk_g2s(b + kPitch, srcK + off, row_bytes, bar);
+            bulk_g2s(b + 2 * kPitch, srcV + off, row_bytes, bar);
+        }
     };
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kSlots; ++s) {
             mbar_init(&full[s], 1);
             released[s] = 0u;
         }
@@ -136,8 +144,7 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
         // arm the exchange of chunks 0 and 1 (peers' bytes may land before or after)
         mbar_arrive_expect_tx(&xbar[0], xbytes);
         if (nchunks > 1) mbar_arrive_expect_tx(&xbar[1], xbytes);
-        const int pro = ntok < kStages ? ntok : kStages;
-        for (int j = 0; j < pro; ++j) issue(j);
+        for (int c = 0; c < kSlots && c < nchunks; ++c) issue(c);
     }
     // the tails of the row slots past this slice's columns, which no copy
     // writes, are zero (threads without columns read them)
@@ -177,10 +184,8 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
         const int sta = ja & (kStages - 1);
         const int stb = jb & (kStages - 1);
         if (kA) {
-            const uint32_t par = static_cast<uint32_t>((ja / kStages) & 1);
-#pragma unroll
-            for (int w = 0; w < kChunk; ++w)
-                if (ja + w < ntok && !failed && !mbar_wait(&full[sta + w], par)) failed = true;
+            if (!failed && !mbar_wait(&full[c & (kSlots - 1)], static_cast<uint32_t>((c / kSlots) & 1)))
+                failed = true;
         }
         if (kB) {
             // every warp reads chunk c - 1's totals before it hands in chunk c
@@ -301,10 +306,11 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
             __syncwarp();
             if (lane == 0) {
                 __threadfence_block();
-                if (atomicAdd(&released[stb], 1u) == static_cast<unsigned int>(nw - 1)) {
-                    released[stb] = 0u;
+                const int slot = (c - 1) & (kSlots - 1);
+                if (atomicAdd(&released[slot], 1u) == static_cast<unsigned int>(nw - 1)) {
+                    released[slot] = 0u;
                     fence_proxy_async();
-                    for (int w = 0; w < kChunk && jb + kStages + w < ntok; ++w) issue(jb + kStages + w);
+                    if (c - 1 + kSlots < nchunks) issue(c - 1 + kSlots);
                 }
             }
         }
@@ -316,8 +322,8 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
         atomicOr(p.err, kErrTimeout);
         // let copies issued by this CTA land before it leaves (bounded)
         if (tid == 0)
-            for (int j = ntok > kStages ? ntok - kStages : 0; j < ntok; ++j)
-                (void)mbar_wait(&full[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
+            for (int c = nchunks > kSlots ? nchunks - kSlots : 0; c < nchunks; ++c)
+                (void)mbar_wait(&full[c & (kSlots - 1)], static_cast<uint32_t>((c / kSlots) & 1));
     }
     // no CTA leaves while a peer may still store into its slots
     cluster_sync();
