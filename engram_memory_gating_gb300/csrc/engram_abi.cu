@@ -367,8 +367,10 @@ const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
         g = {};
         gc_split(d, rows, C, g);
         // fixed layouts (2048-byte row slots; the backward's with the staged
-        // saved scalars of up to kGcBwdMaxRange + 7 streamed tokens)
+        // saved scalars of up to kGcBwdMaxRange + 7 streamed tokens); a
+        // backward CTA has two warp groups over its column slice
         g.c.smem = op == 0 ? gateconv_fwd_smem() : gateconv_bwd_smem();
+        if (op == 1) g.c.threads = gateconv_bwd_threads();
     };
     GcGeom g;
     const int C0 = static_cast<int>((d + 1023) / 1024);

@@ -201,6 +201,7 @@ cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);
 
 int gateconv_fwd_smem();  // dynamic shared memory of the forward kernel (fixed layout)
 int gateconv_bwd_smem();  // dynamic shared memory of the backward kernel (fixed layout)
+int gateconv_bwd_threads();  // threads of a backward CTA (two warp groups over one column slice)
 cudaError_t gateconv_fwd_prepare(int smem_bytes);
 cudaError_t gateconv_fwd_max_clusters(int cluster, int threads, int smem, int* out);
 cudaError_t gateconv_fwd_launch(const GateConvFwdParams& p, const LaunchCfg& c, cudaStream_t s);

@@ -102,137 +102,157 @@ EG_DEV void conv_t(const Windows& W, const Weights& P, float2 (&du)[2]) {
                           fma2(P.cw[1][i], W.D[(S + 2) & 3][i], mul2(P.cw[0][i], W.D[(S + 3) & 3][i]))));
 }
 
-// Shared memory: a fixed layout, so that every ring address of a token is a
-// chunk base plus an immediate.  Each row slot is 2048 bytes (the widest
-// column slice, 1024 columns); a narrower slice leaves the slot's tail zero.
+// Warp-specialised kernel.  A CTA has two groups of eight warps over the same
+// column slice, thread i of each group owning columns 4i .. 4i+3:
+//  * phase-1 warps (warps 0-7) step through the tokens with the conv windows
+//    (u, c, dc, du), form the partial sums S1, S3, S4, S5 of each chunk of
+//    four output tokens and hand them to the cluster exchange, accumulate
+//    dconv_w and drms_w_v, and leave t1 = dY + rrms_v w_v du of every column in
+//    shared memory (three chunk slots);
+//  * phase-2 warps (warps 8-15) take a chunk's cluster totals, form its
+//    per-token coefficients and write dv = alpha (t1 - Q vhat), dH and dk from
+//    t1 and the vhat, H and k rows still in the ring, accumulating drms_w_h.
+// Splitting the two phases over different warps halves the state a thread
+// holds, so a CTA of sixteen warps fits the register file (phase-1 warps take
+// kP1Regs registers a thread, phase-2 warps kP2Regs, by setmaxnreg) where one
+// warp doing both phases needed 236.
+// Ordering: phase-1 warps hand in chunk c only after this CTA's phase-2 warps
+// have read the totals of chunk c - 1 (barrier `tread`), so a peer's exchange
+// buffer for chunk c (shared with chunk c - 2) has been read everywhere before
+// it is written, and phase 1 never runs more than two chunks ahead, so three
+// t1 slots suffice.  The ring completes per chunk of four streamed tokens
+// (one mbarrier per chunk slot); phase-2 warps release a chunk's stages once
+// they have written its outputs (phase-1 warps are done with them by then),
+// and phase-1 warps release the halo chunk before the range.
 constexpr int kPitch = 2048;
 constexpr int kStageBytes = kRows * kPitch;
-constexpr int kOffFull = 0;                      // [kStages] stage mbarriers
-constexpr int kOffXbar = 128;                    // [2] cluster-exchange mbarriers
-constexpr int kOffRel = 160;                     // [kStages] stage release counters
-constexpr int kOffArr = 224;                     // [2] per-chunk arrival counters
+constexpr int kSlots = kStages / kChunk;         // 4 chunk slots of the ring
+constexpr int kT1Slots = 3;
+constexpr int kGroupWarps = 8;
+constexpr int kWsThreads = 2 * 32 * kGroupWarps;  // 512
+constexpr int kP1Regs = 152, kP2Regs = 104;
+static_assert(kGroupWarps * 32 * (kP1Regs + kP2Regs) == 65536, "register split of a 512-thread CTA");
+constexpr int kOffFull = 0;                      // [kSlots] chunk-slot mbarriers
+constexpr int kOffXbar = 32;                     // [2] cluster-exchange mbarriers
+constexpr int kOffTread = 48;                    // [2] phase-2 warps have read a chunk's totals
+constexpr int kOffTready = 64;                   // [kT1Slots] phase-1 warps have written a chunk's t1
+constexpr int kOffRel = 96;                      // [kSlots] release counters
+constexpr int kOffArr = 112;                     // [2] hand-in counters
 constexpr int kOffLocal = 256;                   // [2][8 warps][16] warp totals
 constexpr int kOffTot = kOffLocal + 2 * 8 * gc::kVals * 4;   // [2][8 ranks][16] CTA totals
 constexpr int kRingOff = kOffTot + 2 * 8 * gc::kVals * 4;
-constexpr int kScOff = kRingOff + kStages * kStageBytes;     // saved scalars of the streamed tokens
+constexpr int kT1Off = kRingOff + kStages * kStageBytes;     // [kT1Slots][4 tokens][256 threads] float4
+constexpr int kScOff = kT1Off + kT1Slots * kChunk * 256 * 16;   // saved scalars of the streamed tokens
 constexpr int kSmem = kScOff + 16 * (kGcBwdMaxRange + 8);
-static_assert(kRingOff % 128 == 0 && kScOff % 16 == 0, "alignment");
+static_assert(kRingOff % 128 == 0 && kT1Off % 16 == 0 && kScOff % 16 == 0, "alignment");
+static_assert(kSmem <= 232448, "shared memory");
 
-__global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const GateConvBwdParams p) {
+EG_DEV void reg_alloc_p1() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kP1Regs)); }
+EG_DEV void reg_dealloc_p2() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kP2Regs)); }
+
+__global__ void __launch_bounds__(kWsThreads, 1) gateconv_bwd_kernel(const GateConvBwdParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffFull);
     uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + kOffXbar);
+    uint64_t* tread = reinterpret_cast<uint64_t*>(smem + kOffTread);
+    uint64_t* tready = reinterpret_cast<uint64_t*>(smem + kOffTready);
     unsigned int* released = reinterpret_cast<unsigned int*>(smem + kOffRel);
     unsigned int* arrived = reinterpret_cast<unsigned int*>(smem + kOffArr);
     float* local = reinterpret_cast<float*>(smem + kOffLocal);
     float* tot = reinterpret_cast<float*>(smem + kOffTot);
     unsigned char* ring = smem + kRingOff;
+    float4* t1buf = reinterpret_cast<float4*>(smem + kT1Off);
     float4* sc = reinterpret_cast<float4*>(smem + kScOff);  // (rrms_v, alpha, rrms_h, rrms_k)
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int nw = blockDim.x >> 5;
+    const bool phase1 = warp < kGroupWarps;
+    const int gt = tid & 255;                   // thread index within the group
+    const int gw = warp & (kGroupWarps - 1);    // warp index within the group
     const uint32_t C = cluster_size();
     const uint32_t rank = cluster_rank();
     const int q = static_cast<int>(cluster_index());
     const int d = p.d;
     const int col0 = static_cast<int>(rank) * p.ncols;
     const int cols = min(p.ncols, d - col0);
-    const bool active = 4 * tid < cols;
-    const int c0 = col0 + 4 * tid;
+    const bool active = 4 * gt < cols;
+    const int c0 = col0 + 4 * gt;
     const uint32_t row_bytes = 2u * static_cast<uint32_t>(cols);
 
     // ranges start at multiples of kChunk, and so does the streamed halo, so
-    // token t sits in window slot t % 4 (known at compile time below)
+    // token t sits in window slot t % 4 and the streamed chunks hold whole
+    // output chunks
     const int m = q / p.ranges_per_row;
     const int t_out = (q - m * p.ranges_per_row) * p.range_len;
     const int t_end = min(p.T, t_out + p.range_len);
     const int t_first = t_out >= kChunk ? t_out - kChunk : 0;
+    const int hc = (t_out - t_first) / kChunk;   // 1 if a halo chunk precedes the range
     const int t_last = min(p.T, t_end + 3);
     const int ntok = t_last - t_first;             // streamed tokens (halo included)
+    const int nstream = (ntok + kChunk - 1) / kChunk;
     const int nchunks = (t_end - t_out + kChunk - 1) / kChunk;
     const long long row0 = static_cast<long long>(m) * p.T;
     const uint32_t xbytes = C * gc::kVals * 4u;     // one 16-value total from each CTA
 
-    Weights P;
-    float2 wh[2];  // w_h itself, for drms_w_h
-    if (active) {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(p.wh + c0));
-        const float4 b = __ldg(reinterpret_cast<const float4*>(p.wv + c0));
-        P.wh2[0] = make_float2(a.x * a.x, a.y * a.y);
-        P.wh2[1] = make_float2(a.z * a.z, a.w * a.w);
-        wh[0] = make_float2(a.x, a.y);
-        wh[1] = make_float2(a.z, a.w);
-        P.wv[0] = make_float2(b.x, b.y);
-        P.wv[1] = make_float2(b.z, b.w);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float4 c = __ldg(reinterpret_cast<const float4*>(p.cw + static_cast<long long>(j) * d + c0));
-            P.cw[j][0] = make_float2(c.x, c.y);
-            P.cw[j][1] = make_float2(c.z, c.w);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            P.wh2[i] = P.wv[i] = wh[i] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) P.cw[j][i] = make_float2(0.f, 0.f);
-        }
-    }
-
     const long long base = (row0 + t_first) * d + col0;
-    auto issue = [&](int j) {
-        const int st = j & (kStages - 1);
-        const long long off = base + static_cast<long long>(j) * d;
-        unsigned char* b = ring + st * kStageBytes;
-        mbar_arrive_expect_tx(&full[st], kRows * row_bytes);
-        bulk_g2s(b, p.dY + off, row_bytes, &full[st]);
-        bulk_g2s(b + kPitch, p.vhat + off, row_bytes, &full[st]);
-        bulk_g2s(b + 2 * kPitch, p.v + off, row_bytes, &full[st]);
-        bulk_g2s(b + 3 * kPitch, p.H + off, row_bytes, &full[st]);
-        bulk_g2s(b + 4 * kPitch, p.k + off, row_bytes, &full[st]);
-    };
-    const unsigned char* bthread = ring + 8 * tid;
-    // this thread's 8 bytes of row r of streamed token t (t_first <= t < t_last)
-    auto row_of = [&](int t) -> const unsigned char* {
-        return bthread + ((t - t_first) & (kStages - 1)) * kStageBytes;
-    };
-    // this warp is done with the stages of tokens t .. t+n-1 (one counter per
-    // group, at its first stage); the last warp refills them
-    auto release = [&](int t, int n) {
-        const int j = t - t_first;
-        const int st = j & (kStages - 1);
-        __syncwarp();
-        if (lane == 0) {
-            __threadfence_block();
-            if (atomicAdd(&released[st], 1u) == static_cast<unsigned int>(nw - 1)) {
-                released[st] = 0u;
-                fence_proxy_async();
-                for (int i = 0; i < n && j + kStages + i < ntok; ++i) issue(j + kStages + i);
-            }
+    // streamed chunk k (tokens 4k .. 4k+3 of the stream) into ring slot k % 4
+    auto issue = [&](int k) {
+        const int slot = k & (kSlots - 1);
+        const int j0 = k * kChunk;
+        const int n = min(kChunk, ntok - j0);
+        uint64_t* bar = &full[slot];
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * kRows * row_bytes);
+        for (int w = 0; w < n; ++w) {
+            const long long off = base + static_cast<long long>(j0 + w) * d;
+            unsigned char* b = ring + (slot * kChunk + w) * kStageBytes;
+            bulk_g2s(b, p.dY + off, row_bytes, bar);
+            bulk_g2s(b + kPitch, p.vhat + off, row_bytes, bar);
+            bulk_g2s(b + 2 * kPitch, p.v + off, row_bytes, bar);
+            bulk_g2s(b + 3 * kPitch, p.H + off, row_bytes, bar);
+            bulk_g2s(b + 4 * kPitch, p.k + off, row_bytes, bar);
         }
     };
     bool failed = false;
-    auto wait_tok = [&](int tau) {
-        const int j = tau - t_first;
-        if (!failed && !mbar_wait(&full[j & (kStages - 1)], static_cast<uint32_t>((j / kStages) & 1)))
+    auto wait_chunk = [&](int k) {   // streamed chunk k has landed
+        if (!failed && !mbar_wait(&full[k & (kSlots - 1)], static_cast<uint32_t>((k / kSlots) & 1)))
             failed = true;
+    };
+    // this warp is done with streamed chunk k; the last of the group's eight
+    // warps to say so refills its slot with chunk k + 4
+    auto release = [&](int k) {
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            const int slot = k & (kSlots - 1);
+            if (atomicAdd(&released[slot], 1u) == static_cast<unsigned int>(kGroupWarps - 1)) {
+                released[slot] = 0u;
+                fence_proxy_async();
+                if (k + kSlots < nstream) issue(k + kSlots);
+            }
+        }
+    };
+    const unsigned char* bthread = ring + 8 * gt;
+    // this thread's 8 bytes of row 0 of streamed token t (t_first <= t < t_last)
+    auto row_of = [&](int t) -> const unsigned char* {
+        return bthread + ((t - t_first) & (kStages - 1)) * kStageBytes;
     };
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kSlots; ++s) {
             mbar_init(&full[s], 1);
             released[s] = 0u;
         }
         mbar_init(&xbar[0], 1);
         mbar_init(&xbar[1], 1);
+        mbar_init(&tread[0], kGroupWarps);
+        mbar_init(&tread[1], kGroupWarps);
+        for (int s = 0; s < kT1Slots; ++s) mbar_init(&tready[s], kGroupWarps);
         arrived[0] = arrived[1] = 0u;
         fence_mbar_init();
         mbar_arrive_expect_tx(&xbar[0], xbytes);
         if (nchunks > 1) mbar_arrive_expect_tx(&xbar[1], xbytes);
-        const int pro = ntok < kStages ? ntok : kStages;
-        for (int j = 0; j < pro; ++j) issue(j);
+        for (int k = 0; k < kSlots && k < nstream; ++k) issue(k);
     }
     // the saved per-token scalars of the streamed tokens, staged once
     for (int i = tid; i < ntok; i += blockDim.x) {
@@ -250,83 +270,192 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
     }
     cluster_sync();
 
-    Windows W;
-    float2 gcw[4][2], gwh[2], gwv[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-#pragma unroll
-        for (int s = 0; s < 4; ++s) W.U[s][i] = W.D[s][i] = gcw[s][i] = make_float2(0.f, 0.f);
-        gwh[i] = gwv[i] = make_float2(0.f, 0.f);
-    }
-
-    // Steps to token tau in slot S: real tokens are consumed (the halo before
-    // the range for u only, and released at once), tokens past the row end
-    // give dc = 0.
-    auto step = [&](auto slot, int tau) {
-        constexpr int S = decltype(slot)::value;
-        if (tau < 0) return;
-        if (tau >= t_last) {
-            W.D[S][0] = W.D[S][1] = make_float2(0.f, 0.f);
-            return;
-        }
-        wait_tok(tau);
-        const float rv = sc[tau - t_first].x;
-        consume<S>(W, gcw, P, row_of(tau), kPitch, rv, true, tau >= t_out, active && tau >= t_out && tau < t_end);
-        if (tau < t_out) release(tau, 1);
-    };
-
-    // fill the windows: the 4 tokens before the range, and dc of its first 3
-    step(std::integral_constant<int, 0>(), t_out - 4);
-    step(std::integral_constant<int, 1>(), t_out - 3);
-    step(std::integral_constant<int, 2>(), t_out - 2);
-    step(std::integral_constant<int, 3>(), t_out - 1);
-    step(std::integral_constant<int, 0>(), t_out);
-    step(std::integral_constant<int, 1>(), t_out + 1);
-    step(std::integral_constant<int, 2>(), t_out + 2);
-
     const float inv_d = 1.0f / static_cast<float>(d);
-    float2 du[kChunk][2];  // du of the chunk handed in last (read by its phase 2)
+    if (phase1) {
+        reg_alloc_p1();
+        Weights P;
+        if (active) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(p.wh + c0));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(p.wv + c0));
+            P.wh2[0] = make_float2(a.x * a.x, a.y * a.y);
+            P.wh2[1] = make_float2(a.z * a.z, a.w * a.w);
+            P.wv[0] = make_float2(b.x, b.y);
+            P.wv[1] = make_float2(b.z, b.w);
 #pragma unroll
-    for (int w = 0; w < kChunk; ++w) du[w][0] = du[w][1] = make_float2(0.f, 0.f);
+            for (int j = 0; j < 4; ++j) {
+                const float4 c = __ldg(reinterpret_cast<const float4*>(p.cw + static_cast<long long>(j) * d + c0));
+                P.cw[j][0] = make_float2(c.x, c.y);
+                P.cw[j][1] = make_float2(c.z, c.w);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                P.wh2[i] = P.wv[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) P.cw[j][i] = make_float2(0.f, 0.f);
+            }
+        }
+        Windows W;
+        float2 gcw[4][2], gwv[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s) W.U[s][i] = W.D[s][i] = gcw[s][i] = make_float2(0.f, 0.f);
+            gwv[i] = make_float2(0.f, 0.f);
+        }
+        // Steps to token tau in slot S: real tokens are consumed (the halo
+        // before the range for u only), tokens past the row end give dc = 0.
+        auto step = [&](auto slot, int tau) {
+            constexpr int S = decltype(slot)::value;
+            if (tau < 0) return;
+            if (tau >= t_last) {
+                W.D[S][0] = W.D[S][1] = make_float2(0.f, 0.f);
+                return;
+            }
+            wait_chunk((tau - t_first) / kChunk);
+            const float rv = sc[tau - t_first].x;
+            consume<S>(W, gcw, P, row_of(tau), kPitch, rv, true, tau >= t_out, active && tau >= t_out && tau < t_end);
+        };
+        // fill the windows: the 4 tokens before the range, and dc of its first 3
+        step(std::integral_constant<int, 0>(), t_out - 4);
+        step(std::integral_constant<int, 1>(), t_out - 3);
+        step(std::integral_constant<int, 2>(), t_out - 2);
+        step(std::integral_constant<int, 3>(), t_out - 1);
+        step(std::integral_constant<int, 0>(), t_out);
+        step(std::integral_constant<int, 1>(), t_out + 1);
+        step(std::integral_constant<int, 2>(), t_out + 2);
+        if (hc) release(0);   // the halo chunk before the range is not needed again
 
-    // One iteration per chunk c = 0 .. nchunks: phase 2 of chunk c - 1 (its
-    // totals -> coefficients; dv, dH, dk, drms_w_h from the rows still in the
-    // ring) and phase 1 of chunk c (consume tokens t + 3, du, the partial
-    // sums).  All waits come first, then one straight-line block with both
-    // phases (the scheduler overlaps their latency chains), then the hand-in
-    // of chunk c and the release of chunk c - 1's stages.
-    auto iteration = [&](auto has1, auto has2, int c) {
-        constexpr bool k1 = decltype(has1)::value;
-        constexpr bool k2 = decltype(has2)::value;
-        const int buf = c & 1;
-        const int tc = t_out + c * kChunk;      // first token of chunk c
-        const int tp = tc - kChunk;             // first token of chunk c - 1
-        if (k1) {
+        for (int c = 0; c < nchunks; ++c) {
+            const int tc = t_out + c * kChunk;      // first token of output chunk c
+            const int buf = c & 1;
+            // the streamed chunk of tokens tc .. tc + 3 (output chunk c; it also
+            // holds token tc + 3) and the next one, which holds tokens tc + 4 ..
+            // tc + 6, consumed while tc + 1 is in the range and tc + 4 streamed
+            wait_chunk(c + hc);
+            if (tc + 1 < t_end && tc + 4 < t_last) wait_chunk(c + hc + 1);
+            float rvt[kChunk], rvc[kChunk];
 #pragma unroll
-            for (int w = 0; w < kChunk; ++w)
-                if (tc + w < t_end && tc + w + 3 < t_last) wait_tok(tc + w + 3);
-        }
-        if (k2) {
-            // every warp reads chunk c - 1's totals before it hands in chunk c
-            if (!failed && !mbar_wait_cluster(&xbar[buf ^ 1], static_cast<uint32_t>(((c - 1) >> 1) & 1)))
+            for (int w = 0; w < kChunk; ++w) {
+                rvt[w] = sc[min(tc + w, t_end - 1) - t_first].x;
+                rvc[w] = sc[min(tc + w + 3, t_last - 1) - t_first].x;
+            }
+            float4* t1w = t1buf + ((c % kT1Slots) * kChunk) * 256 + gt;
+            float sums[gc::kVals];
+            // output token t = tc + S: consume t + 3, then du_t, the partial
+            // sums, drms_w_v and t1 (tokens past the range select 0)
+            auto out1 = [&](auto slot) {
+                constexpr int S = decltype(slot)::value;
+                const int t = tc + S;
+                const bool vt = active && t < t_end;
+                consume<(S + 3) & 3>(W, gcw, P, row_of(t + 3), kPitch, rvc[S], t + 3 < t_last, true,
+                                     active && t + 3 < t_end);
+                float2 d2[2];
+                conv_t<S>(W, P, d2);
+                const unsigned char* b = row_of(t);
+                const uint2 yq = lds64(b), hq = lds64(b + kPitch), vq = lds64(b + 2 * kPitch);
+                const uint2 Hq = lds64(b + 3 * kPitch), kq = lds64(b + 4 * kPitch);
+                const float2 rv2 = splat2(rvt[S]);
+                const float2 zero = make_float2(0.f, 0.f);
+                float2 s1 = zero, s3 = zero, s4 = zero, s5 = zero, t1[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const float2 dy = bf2(i == 0 ? yq.x : yq.y), vh = bf2(i == 0 ? hq.x : hq.y);
+                    const float2 vv = bf2(i == 0 ? vq.x : vq.y);
+                    const float2 h = bf2(i == 0 ? Hq.x : Hq.y), kk = bf2(i == 0 ? kq.x : kq.y);
+                    const float2 wdu = mul2(P.wv[i], d2[i]);
+                    t1[i] = fma2(rv2, wdu, dy);             // dY + rrms_v w_v du
+                    s1 = fma2(t1[i], vv, s1);
+                    s3 = fma2(vh, vv, s3);
+                    s4 = fma2(wdu, vh, s4);
+                    s5 = fma2(mul2(h, kk), P.wh2[i], s5);
+                    const float2 g = mul2(d2[i], mul2(vh, rv2));
+                    gwv[i] = add2(gwv[i], vt ? g : zero);
+                }
+                t1w[S * 256] = make_float4(t1[0].x, t1[0].y, t1[1].x, t1[1].y);
+                sums[4 * S + 0] = s1.x + s1.y;
+                sums[4 * S + 1] = s3.x + s3.y;
+                sums[4 * S + 2] = s4.x + s4.y;
+                sums[4 * S + 3] = s5.x + s5.y;
+            };
+            out1(std::integral_constant<int, 0>());
+            out1(std::integral_constant<int, 1>());
+            out1(std::integral_constant<int, 2>());
+            out1(std::integral_constant<int, 3>());
+            const float val = gc::warp_reduce16(sums, lane);
+            // this chunk's t1 is in shared memory (for the phase-2 warps)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tready[c % kT1Slots]);
+            // hand in chunk c once the phase-2 warps have read chunk c - 1's totals
+            if (c >= 1 && lane == 0 && !failed &&
+                !mbar_wait(&tread[buf ^ 1], static_cast<uint32_t>(((c - 1) >> 1) & 1)))
                 failed = true;
-            if (tid == 0 && c + 1 < nchunks) mbar_arrive_expect_tx(&xbar[buf ^ 1], xbytes);
+            __syncwarp();
+            local[(buf * 8 + gw) * gc::kVals + (lane >> 1)] = val;
+            __syncwarp();
+            unsigned int last = 0u;
+            if (lane == 0) {
+                __threadfence_block();
+                if (atomicAdd(&arrived[buf], 1u) == static_cast<unsigned int>(kGroupWarps - 1)) {
+                    arrived[buf] = 0u;
+                    __threadfence_block();
+                    last = 1u;
+                }
+            }
+            last = __shfl_sync(kFullMask, last, 0);
+            if (last) {
+                __syncwarp();
+                const float* lp = local + buf * 8 * gc::kVals + (lane & 15);
+                float cta = 0.f;
+#pragma unroll
+                for (int w = 0; w < kGroupWarps; ++w) cta += lp[w * gc::kVals];
+                const uint32_t dst = smem_addr(tot + (buf * 8 + static_cast<int>(rank)) * gc::kVals + (lane & 15));
+                const uint32_t bar = smem_addr(xbar + buf);
+                for (uint32_t r = static_cast<uint32_t>(lane >> 4); r < C; r += 2)
+                    st_async_f32(map_to_rank(dst, r), cta, map_to_rank(bar, r));
+            }
         }
-        // ---------------- straight-line block
-        float P_l = 0.f, Q_l = 0.f, a_l = 0.f, Ah_l = 0.f, Bh_l = 0.f, Bk_l = 0.f;
-        if (k2) {
-            const float* tq = tot + (buf ^ 1) * 8 * gc::kVals + (lane & 15);
+        // per-range weight-gradient partial: [dwh | dwv | dcw0..3], each d wide
+        if (active) {
+            float* o = p.partial + static_cast<long long>(q) * 6 * d + c0;
+            stg_f4(o + d, gwv[0].x, gwv[0].y, gwv[1].x, gwv[1].y);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                stg_f4(o + (2 + j) * d, gcw[j][0].x, gcw[j][0].y, gcw[j][1].x, gcw[j][1].y);
+        }
+    } else {
+        reg_dealloc_p2();
+        float2 wh2[2], wh[2], gwh[2];
+        if (active) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(p.wh + c0));
+            wh2[0] = make_float2(a.x * a.x, a.y * a.y);
+            wh2[1] = make_float2(a.z * a.z, a.w * a.w);
+            wh[0] = make_float2(a.x, a.y);
+            wh[1] = make_float2(a.z, a.w);
+        } else {
+            wh2[0] = wh2[1] = wh[0] = wh[1] = make_float2(0.f, 0.f);
+        }
+        gwh[0] = gwh[1] = make_float2(0.f, 0.f);
+        for (int c = 0; c < nchunks; ++c) {
+            const int tp = t_out + c * kChunk;      // first token of output chunk c
+            const int buf = c & 1;
+            if (!failed && !mbar_wait_cluster(&xbar[buf], static_cast<uint32_t>((c >> 1) & 1))) failed = true;
+            if (gt == 0 && c + 2 < nchunks) mbar_arrive_expect_tx(&xbar[buf], xbytes);
+            const float* tq = tot + buf * 8 * gc::kVals + (lane & 15);
             float tv = 0.f;
 #pragma unroll
             for (int r = 0; r < 8; ++r)
                 if (r < static_cast<int>(C)) tv += tq[r * gc::kVals];
+            // the totals are read: phase-1 warps may hand in chunk c + 1
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tread[buf]);
             const int tw = 4 * (lane & 3);
             const float S1 = __shfl_sync(kFullMask, tv, tw + 0);
             const float S3 = __shfl_sync(kFullMask, tv, tw + 1);
             const float S4 = __shfl_sync(kFullMask, tv, tw + 2);
             const float S5 = __shfl_sync(kFullMask, tv, tw + 3);
-            const int t = min(tp + (lane & 3), t_end - 1);
-            const float4 s4 = sc[t - t_first];
+            const int tt = min(tp + (lane & 3), t_end - 1);
+            const float4 s4 = sc[tt - t_first];
             const float rv = s4.x, a = s4.y, rh = s4.z, rk = s4.w;
             const float mu = rv * S4 * inv_d;
             const float q2 = rv * rv * mu;
@@ -334,19 +463,15 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
             const float dz = dalpha * a * (1.0f - a);
             const float Ah = dz * rh * rk * p.inv_sqrt_d;
             const float e5 = S5 * inv_d;
-            P_l = rv;
-            Q_l = q2;
-            a_l = a;
-            Ah_l = Ah;
-            Bh_l = Ah * rh * rh * e5;
-            Bk_l = Ah * rk * rk * e5;
-        }
-        if (k2) {
-            // one output token t = tp + S of chunk c - 1: dv, dH, dk, drms_w_h
+            const float Q_l = q2, a_l = a, Ah_l = Ah;
+            const float Bh_l = Ah * rh * rh * e5, Bk_l = Ah * rk * rk * e5;
+            // t1 of the chunk, and its rows in the ring
+            if (!failed && !mbar_wait(&tready[c % kT1Slots], static_cast<uint32_t>((c / kT1Slots) & 1))) failed = true;
+            wait_chunk(c + hc);
+            const float4* t1r = t1buf + ((c % kT1Slots) * kChunk) * 256 + gt;
             auto out2 = [&](auto slot) {
                 constexpr int S = decltype(slot)::value;
                 const int t = tp + S;
-                const float Pv = __shfl_sync(kFullMask, P_l, S);
                 const float Qv = __shfl_sync(kFullMask, Q_l, S);
                 const float av = __shfl_sync(kFullMask, a_l, S);
                 const float Ah = __shfl_sync(kFullMask, Ah_l, S);
@@ -354,19 +479,21 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
                 const float Bk = __shfl_sync(kFullMask, Bk_l, S);
                 const bool vt = active && t < t_end;
                 const unsigned char* b = row_of(t);
-                const uint2 yq = lds64(b), hq = lds64(b + kPitch);
+                const float4 t1 = t1r[S * 256];
+                const uint2 hq = lds64(b + kPitch);
                 const uint2 Hq = lds64(b + 3 * kPitch), kq = lds64(b + 4 * kPitch);
-                const float2 P2 = splat2(Pv), nQ2 = splat2(-Qv), a2 = splat2(av);
+                const float2 nQ2 = splat2(-Qv), a2 = splat2(av);
                 const float2 Ah2 = splat2(Ah), nBh2 = splat2(-Bh), nBk2 = splat2(-Bk), Ah22 = splat2(2.0f * Ah);
                 const float2 zero = make_float2(0.f, 0.f);
                 uint32_t oh[2], ok[2], ov[2];
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    const float2 dy = bf2(i == 0 ? yq.x : yq.y), vh = bf2(i == 0 ? hq.x : hq.y);
+                    const float2 vh = bf2(i == 0 ? hq.x : hq.y);
                     const float2 h = bf2(i == 0 ? Hq.x : Hq.y), kk = bf2(i == 0 ? kq.x : kq.y);
-                    const float2 dvh = fma2(nQ2, vh, fma2(mul2(P2, P.wv[i]), du[S][i], dy));
+                    const float2 t12 = i == 0 ? make_float2(t1.x, t1.y) : make_float2(t1.z, t1.w);
+                    const float2 dvh = fma2(nQ2, vh, t12);
                     ov[i] = pack2(mul2(a2, dvh));
-                    const float2 aw = mul2(Ah2, P.wh2[i]);
+                    const float2 aw = mul2(Ah2, wh2[i]);
                     oh[i] = pack2(fma2(aw, kk, mul2(nBh2, h)));
                     ok[i] = pack2(fma2(aw, h, mul2(nBk2, kk)));
                     const float2 g = mul2(mul2(Ah22, wh[i]), mul2(h, kk));
@@ -381,103 +508,18 @@ __global__ void __launch_bounds__(gc::kThreads, 1) gateconv_bwd_kernel(const Gat
             out2(std::integral_constant<int, 1>());
             out2(std::integral_constant<int, 2>());
             out2(std::integral_constant<int, 3>());
+            release(c + hc);
         }
-        float val = 0.f;
-        if (k1) {
-            float rvt[kChunk], rvc[kChunk];
-#pragma unroll
-            for (int w = 0; w < kChunk; ++w) {
-                rvt[w] = sc[min(tc + w, t_end - 1) - t_first].x;
-                rvc[w] = sc[min(tc + w + 3, t_last - 1) - t_first].x;
-            }
-            float sums[gc::kVals];
-            // one output token t = tc + S of chunk c: consume t + 3, then du_t,
-            // the partial sums and drms_w_v (tokens past the range select 0)
-            auto out1 = [&](auto slot) {
-                constexpr int S = decltype(slot)::value;
-                const int t = tc + S;
-                const bool vt = active && t < t_end;
-                consume<(S + 3) & 3>(W, gcw, P, row_of(t + 3), kPitch, rvc[S], t + 3 < t_last, true,
-                                     active && t + 3 < t_end);
-                float2 d2[2];
-                conv_t<S>(W, P, d2);
-                const unsigned char* b = row_of(t);
-                const uint2 yq = lds64(b), hq = lds64(b + kPitch), vq = lds64(b + 2 * kPitch);
-                const uint2 Hq = lds64(b + 3 * kPitch), kq = lds64(b + 4 * kPitch);
-                const float2 rv2 = splat2(rvt[S]);
-                const float2 zero = make_float2(0.f, 0.f);
-                float2 s1 = zero, s3 = zero, s4 = zero, s5 = zero;
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const float2 dy = bf2(i == 0 ? yq.x : yq.y), vh = bf2(i == 0 ? hq.x : hq.y);
-                    const float2 vv = bf2(i == 0 ? vq.x : vq.y);
-                    const float2 h = bf2(i == 0 ? Hq.x : Hq.y), kk = bf2(i == 0 ? kq.x : kq.y);
-                    const float2 wdu = mul2(P.wv[i], d2[i]);
-                    s1 = fma2(fma2(rv2, wdu, dy), vv, s1);
-                    s3 = fma2(vh, vv, s3);
-                    s4 = fma2(wdu, vh, s4);
-                    s5 = fma2(mul2(h, kk), P.wh2[i], s5);
-                    const float2 g = mul2(d2[i], mul2(vh, rv2));
-                    gwv[i] = add2(gwv[i], vt ? g : zero);
-                    du[S][i] = d2[i];
-                }
-                sums[4 * S + 0] = s1.x + s1.y;
-                sums[4 * S + 1] = s3.x + s3.y;
-                sums[4 * S + 2] = s4.x + s4.y;
-                sums[4 * S + 3] = s5.x + s5.y;
-            };
-            out1(std::integral_constant<int, 0>());
-            out1(std::integral_constant<int, 1>());
-            out1(std::integral_constant<int, 2>());
-            out1(std::integral_constant<int, 3>());
-            val = gc::warp_reduce16(sums, lane);
+        if (active) {
+            float* o = p.partial + static_cast<long long>(q) * 6 * d + c0;
+            stg_f4(o, gwh[0].x, gwh[0].y, gwh[1].x, gwh[1].y);
         }
-        // ---------------- hand in chunk c (as in the forward: warp totals to
-        // shared memory, the last warp sends the CTA's total to every CTA)
-        if (k1) {
-            local[(buf * 8 + warp) * gc::kVals + (lane >> 1)] = val;
-            __syncwarp();
-            unsigned int last = 0u;
-            if (lane == 0) {
-                __threadfence_block();
-                if (atomicAdd(&arrived[buf], 1u) == static_cast<unsigned int>(nw - 1)) {
-                    arrived[buf] = 0u;
-                    __threadfence_block();
-                    last = 1u;
-                }
-            }
-            last = __shfl_sync(kFullMask, last, 0);
-            if (last) {
-                __syncwarp();
-                const float* lp = local + buf * 8 * gc::kVals + (lane & 15);
-                float cta = 0.f;
-                for (int w = 0; w < nw; ++w) cta += lp[w * gc::kVals];
-                const uint32_t dst = smem_addr(tot + (buf * 8 + static_cast<int>(rank)) * gc::kVals + (lane & 15));
-                const uint32_t bar = smem_addr(xbar + buf);
-                for (uint32_t r = static_cast<uint32_t>(lane >> 4); r < C; r += 2)
-                    st_async_f32(map_to_rank(dst, r), cta, map_to_rank(bar, r));
-            }
-        }
-        if (k2) release(tp, min(kChunk, t_end - tp));
-    };
-    iteration(std::true_type(), std::false_type(), 0);
-    for (int c = 1; c < nchunks; ++c) iteration(std::true_type(), std::true_type(), c);
-    iteration(std::false_type(), std::true_type(), nchunks);
-
-    // per-range weight-gradient partial: [dwh | dwv | dcw0..3], each d wide
-    if (active) {
-        float* o = p.partial + static_cast<long long>(q) * 6 * d + c0;
-        stg_f4(o, gwh[0].x, gwh[0].y, gwh[1].x, gwh[1].y);
-        stg_f4(o + d, gwv[0].x, gwv[0].y, gwv[1].x, gwv[1].y);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            stg_f4(o + (2 + j) * d, gcw[j][0].x, gcw[j][0].y, gcw[j][1].x, gcw[j][1].y);
     }
     if (failed) {
         atomicOr(p.err, kErrTimeout);
         if (tid == 0)
-            for (int j = ntok > kStages ? ntok - kStages : 0; j < ntok; ++j)
-                (void)mbar_wait(&full[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
+            for (int k = nstream > kSlots ? nstream - kSlots : 0; k < nstream; ++k)
+                (void)mbar_wait(&full[k & (kSlots - 1)], static_cast<uint32_t>((k / kSlots) & 1));
     }
     cluster_sync();
 }
@@ -504,7 +546,17 @@ __global__ void __launch_bounds__(256) gc_wreduce_kernel(const GateWReduceParams
 
 int gateconv_bwd_smem() { return kSmem; }
 
+int gateconv_bwd_threads() { return kWsThreads; }
+
 cudaError_t gateconv_bwd_prepare(int smem_bytes) {
+    // The phase-1 warps raise their registers to kP1Regs and the phase-2 warps
+    // lower theirs to kP2Regs (setmaxnreg).  That split must add up to what the
+    // CTA is launched with, or the raise would wait forever: refuse to run a
+    // build whose register count differs.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, gateconv_bwd_kernel);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * kWsThreads != kGroupWarps * 32 * (kP1Regs + kP2Regs)) return cudaErrorInvalidConfiguration;
     if (smem_bytes <= 0) return cudaSuccess;
     return cudaFuncSetAttribute(gateconv_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
