@@ -9,363 +9,405 @@
 //   y = SiLU(c) + vhat
 //   new cache = the last max_len rows of [zeros, cache, bf16(u_t)]
 //
-// Kernel 1 (projection): a CTA owns 128 columns of d and a slice of the d_mem
-// rows of both weight matrices, for up to 8 batch rows; each lane keeps two
-// columns' running sums for every batch row (W read once from HBM per batch
-// chunk, e staged in shared memory), the CTA's eight warps are summed in
-// shared memory in a fixed order and the slice's partial k and v go to the
-// workspace; the projection CTAs also shift the cache by one token (rows
-// r + 1 -> r), which depends on nothing else.  Kernel 2 (a cluster of 8 CTAs
-// per batch row, each owning an eighth of the columns): sums the slices in a
-// fixed order, forms the row statistics (block reduction, then an exchange
-// across the cluster through distributed shared memory), and writes y and the
-// cache's new last row.
+// Two kernels, each a single short chain of dependent memory round trips:
+//  1 (projection): a CTA owns a 32-column tile of d and up to 8 batch rows,
+//    over all d_mem rows, so its k and v are final (no split partials).  The
+//    tile's weight rows arrive by 2-D TMA (16 KB boxes of 256 rows x 32
+//    columns, which the copy engine gathers from the 64-byte row segments)
+//    and the matching e values by cp.async, into a ring of four stages of 256
+//    rows, all issued up front for d_mem <= 1024.  The sums run on mma.sync
+//    (the batch of 8 is the n of an m16n8k16 product; the work is a pass over
+//    the weights, so this only cuts the instruction count): eight warps each
+//    take 32 rows of a stage, then add their sums in warp order.  The CTA
+//    writes its v to the workspace together with the
+//    tile's four row sums per batch row (sum h^2, sum k^2, sum h k w_h^2,
+//    sum v^2; k is needed only there), and also shifts the cache by one token
+//    (independent work).
+//  2 (output): a CTA per (batch row, 256-column block).  It loads its inputs
+//    that do not depend on kernel 1 (w_v, the conv taps, the cached u of each
+//    tap) before it waits for kernel 1's grid, then adds the tiles' row sums
+//    in a fixed tree (every thread loads some, warp butterflies, the warp
+//    totals in warp order), forms the scalars and writes y and the new cache
+//    row.
 #include "common.cuh"
 #include "engram_internal.h"
 
 namespace eg {
 namespace {
 
-// Programmatic dependent launch: the row kernel is scheduled while the
-// projection runs and waits for the projection grid only where it reads the
-// partial sums.  The projection is itself launched that way: it waits for the
-// preceding kernel (e.g. the previous decode step, which wrote the cache it
-// shifts) before reading anything, so only its launch overlaps that kernel's
-// tail.  Each kernel lets its successor be scheduled only after its own wait.
+// Programmatic dependent launch: each kernel waits for the preceding kernel of
+// the stream (griddepcontrol.wait) before it reads anything that kernel may
+// write, and only then lets its successor be scheduled.
 EG_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 EG_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// The two halves of a cluster barrier (every thread of every CTA; release on
-// arrive, acquire on wait), so that work can run between them.
-EG_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-EG_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+EG_DEV void cp_async16(void* smem_dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(src) : "memory");
+}
+EG_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+EG_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// waits until at most n (0 <= n <= 15) of this thread's most recent groups are pending
+EG_DEV void cp_async_wait_n(int n) {
+    switch (n) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 4: cp_async_wait<4>(); break;
+        case 5: cp_async_wait<5>(); break;
+        case 6: cp_async_wait<6>(); break;
+        case 7: cp_async_wait<7>(); break;
+        case 8: cp_async_wait<8>(); break;
+        case 9: cp_async_wait<9>(); break;
+        case 10: cp_async_wait<10>(); break;
+        case 11: cp_async_wait<11>(); break;
+        case 12: cp_async_wait<12>(); break;
+        case 13: cp_async_wait<13>(); break;
+        case 14: cp_async_wait<14>(); break;
+        default: cp_async_wait<15>(); break;
+    }
+}
 
-// Asynchronous 16-byte store into the shared memory of a CTA of this cluster,
-// completing 16 bytes on that CTA's mbarrier.
-EG_DEV void st_async_f4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
+constexpr int kTile = 32;          // columns per projection CTA, of each of W_K and W_V
+constexpr int kBc = 8;             // batch rows per projection CTA (the mma's n)
+constexpr int kWarps1 = 8;         // one per batch row in the row sums
+constexpr int kChunkRows = 256;    // weight rows per ring stage (the TMA box height)
+constexpr int kRing = 4;           // ring stages
+constexpr int kRowsPerWarp = kChunkRows / kWarps1;     // 32 rows: two k-steps of 16
+// one stage: [2 matrices][256 rows][32 columns] bf16 (two TMA boxes, 64-byte
+// rows in the 64-byte swizzle), then [8 batch][256 rows] bf16 of e at a row
+// pitch of 528 bytes (the 8 rows of an ldmatrix land on distinct banks)
+constexpr int kBoxBytes = kChunkRows * kTile * 2;     // 16 KB
+constexpr int kWBytes = 2 * kBoxBytes;
+constexpr int kEPitch = kChunkRows * 2 + 16;
+constexpr int kEBytes = kBc * kEPitch;
+constexpr int kStageB = (kWBytes + kEBytes + 1023) / 1024 * 1024;
+constexpr int kOffBar = 0;                             // [kRing] stage mbarriers
+constexpr int kOffRing = 1024;
+constexpr int kOffRed = kOffRing + kRing * kStageB;    // [8 warps][2][8 batch][32] fp32
+constexpr int kOffKv = kOffRed + kWarps1 * 2 * kBc * kTile * 4;  // [2][8 batch][32] final k, v of the tile
+constexpr int kSmem1 = kOffKv + 2 * kBc * kTile * 4 + 1024;     // + the alignment of the base to 1024
+static_assert(kSmem1 <= 227 * 1024, "projection shared memory");
+static_assert(kRowsPerWarp == 32 && kWarps1 == kBc, "two k-steps per warp and stage; a warp per batch row");
+
+// 2-D TMA load of box (x, y) of a tensor map into shared memory, completing on `bar`
+EG_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-            remote_addr),
-        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
         : "memory");
 }
 
-constexpr int kCols = 128;   // columns per projection CTA (32 lanes x 4 columns)
-constexpr int kWarps1 = 8;   // warps of a projection CTA (interleaved 4-row groups)
-constexpr int kBc = 8;       // batch rows per projection CTA
-constexpr int kUnroll = 4;   // weight rows per warp iteration
+// four 8x8 b16 matrices from shared memory (lanes 8i..8i+7 give the row
+// addresses of matrix i); .trans hands each thread a column pair instead of a row pair
+EG_DEV void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+EG_DEV void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+// D (16x8 fp32) += A (16x16 bf16, row) B (16x8 bf16, col)
+EG_DEV void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
-// Kernel 1: CTA (x: 128-column tile, y: d_mem row split, z: batch chunk).
-// Lane l owns columns tile + 4l .. 4l+3 of both matrices (8-byte loads; a
-// warp reads 256 contiguous bytes of each weight row); warp w takes the row
-// groups m0 + 4w + 32k; the next group's weights are loaded while the
-// current one is used.  The eight warps' sums are added in warp order.
-__global__ void __launch_bounds__(32 * kWarps1, 2) decode_proj_kernel(const DecodeParams p) {
-    extern __shared__ __align__(16) float sm[];
-    float* es = sm;                                   // [kBc][rows] e of this slice
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int col = blockIdx.x * kCols + 4 * lane;
-    const int rows = p.rows_per_split;
-    const int m0 = blockIdx.y * rows;
-    const int m1 = min(p.dmem, m0 + rows);
-    const int b0 = blockIdx.z * kBc;
+// the cache shift for 16-byte chunks [q0, q1): row r < max_len - 1 of the new
+// cache is row r + 1 of the left-padded old one (I: the index type, 32-bit
+// whenever the chunk count fits)
+template <typename I>
+EG_DEV void shift_cache(const DecodeParams& p, I q0, I q1, I tid, I nthreads) {
+    const I pad = p.max_len - p.L;
+    const I per_row = p.d / 8, per_b = static_cast<I>(p.max_len - 1) * per_row;
+    for (I q = q0 + tid; q < q1; q += nthreads) {
+        const I bb = q / per_b, rem = q - bb * per_b;
+        const I r = rem / per_row, i = (rem - r * per_row) * 8;
+        const I src = r + 1 - pad;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (src >= 0 && src < p.L)
+            val = __ldg(reinterpret_cast<const uint4*>(p.state + (static_cast<long long>(bb) * p.L + src) * p.d + i));
+        *reinterpret_cast<uint4*>(p.new_state + (static_cast<long long>(bb) * p.max_len + r) * p.d + i) = val;
+    }
+}
+
+// Kernel 1: CTA (x: chunk of 8 batch rows, y: 32-column tile).  The weight
+// boxes come by TMA (the tensor maps cover (d_mem, d) row-major; rows past
+// d_mem read as zero), e by cp.async.  The contraction runs on mma.sync
+// m16n8k16: m = 16 output columns, n = the 8 batch rows, k = 16 rows of d_mem;
+// warp w takes rows [32w, 32w + 32) of every stage for all four 16-column
+// blocks (k and v, two each).
+__global__ void __launch_bounds__(32 * kWarps1, 1) decode_proj_kernel(const __grid_constant__ DecodeParams p) {
+    extern __shared__ __align__(128) unsigned char sm_raw[];
+    // the 64-byte swizzle is a function of the shared address: base at 1024
+    unsigned char* sm = sm_raw + ((1024u - (smem_addr(sm_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tile = blockIdx.y;
+    const int ntiles = gridDim.y;
+    const int c0 = tile * kTile;
+    const int b0 = blockIdx.x * kBc;
     const int nb = min(kBc, p.B - b0);
+    const int nchunk = (p.dmem + kChunkRows - 1) / kChunkRows;
+
+    // inputs only: h and w_h of this warp's batch row and lane's column (row sums)
+    const int hb = warp;
+    const float hval = hb < nb ? __uint_as_float(static_cast<uint32_t>(__ldg(p.h + static_cast<long long>(b0 + hb) * p.d + c0 + lane)) << 16) : 0.f;
+    const float whv = __ldg(p.wh + c0 + lane);
+    if (tid == 0) {
+        for (int i = 0; i < kRing; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    // chunk k of the weight rows (and of e) into ring stage k % kRing
+    auto issue = [&](int k) {
+        unsigned char* st = sm + kOffRing + (k % kRing) * kStageB;
+        const int m0 = k * kChunkRows;
+        if (tid == 0) {
+            uint64_t* bar = &bars[k % kRing];
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kWBytes));
+            tma_load_2d(st, &p.tmk, c0, m0, bar);
+            tma_load_2d(st + kBoxBytes, &p.tmv, c0, m0, bar);
+        }
+        // e: 8 batch rows x 256 values as bf16, [batch][row] (a 16-byte copy
+        // holds 8 consecutive values of one batch row); d_mem is a multiple of 8
+        {
+            const int b = tid >> 5, part = tid & 31;
+            unsigned char* dst = st + kWBytes + b * kEPitch + part * 16;
+            const int m = m0 + part * 8;
+            if (b < nb && m < p.dmem)
+                cp_async16(dst, p.e + static_cast<long long>(b0 + b) * p.dmem + m);
+            else
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+        cp_async_commit();
+    };
+    __syncthreads();   // the barriers exist before any copy completes on them
     grid_dep_wait();
     grid_dep_launch();
-    // the cache shift (independent of the projection), spread over all CTAs:
-    // row r < max_len - 1 of the new cache is row r + 1 of the left-padded old one
+    const int pro = nchunk < kRing ? nchunk : kRing;
+    for (int k = 0; k < pro; ++k) issue(k);
+
+    // the cache shift (independent of the projection), spread over all CTAs
     {
         const long long nq = static_cast<long long>(p.B) * (p.max_len - 1) * (p.d / 8);  // 16-byte chunks
-        const long long ncta = static_cast<long long>(gridDim.x) * gridDim.y * gridDim.z;
-        const long long cta = (static_cast<long long>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        const long long ncta = static_cast<long long>(gridDim.x) * gridDim.y;
+        const long long cta = static_cast<long long>(blockIdx.x) * gridDim.y + blockIdx.y;
         const long long q0 = nq * cta / ncta, q1 = nq * (cta + 1) / ncta;
-        const int pad = p.max_len - p.L;
-        const long long per_row = p.d / 8, per_b = static_cast<long long>(p.max_len - 1) * per_row;
-        for (long long q = q0 + threadIdx.x; q < q1; q += blockDim.x) {
-            const long long bb = q / per_b, rem = q - bb * per_b;
-            const long long r = rem / per_row, i = (rem - r * per_row) * 8;
-            const long long src = r + 1 - pad;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (src >= 0 && src < p.L)
-                val = __ldg(reinterpret_cast<const uint4*>(p.state + (bb * p.L + src) * p.d + i));
-            *reinterpret_cast<uint4*>(p.new_state + (bb * p.max_len + r) * p.d + i) = val;
-        }
+        if (nq <= 0x7fffffffLL)
+            shift_cache<int>(p, static_cast<int>(q0), static_cast<int>(q1), tid, blockDim.x);
+        else
+            shift_cache<long long>(p, q0, q1, tid, blockDim.x);
     }
-    for (int i = threadIdx.x; i < kBc * rows; i += blockDim.x) {
-        const int b = i / rows, m = i - b * rows;
-        es[i] = (b < nb && m0 + m < m1)
-            ? __uint_as_float(static_cast<uint32_t>(__ldg(p.e + static_cast<long long>(b0 + b) * p.dmem + m0 + m)) << 16)
-            : 0.f;
-    }
-    __syncthreads();
 
-    float2 ak[kBc][2], av[kBc][2];
+    float acc[4][4];
 #pragma unroll
-    for (int b = 0; b < kBc; ++b) ak[b][0] = ak[b][1] = av[b][0] = av[b][1] = make_float2(0.f, 0.f);
-    const uint2* wk = reinterpret_cast<const uint2*>(p.WK + col);
-    const uint2* wv = reinterpret_cast<const uint2*>(p.WV + col);
-    const long long rs = p.d / 4;  // row stride in 4-column units
-    uint2 qk[kUnroll], qv[kUnroll], nk[kUnroll], nv[kUnroll];
-    const bool colok = col < p.d;  // the last tile may be partly outside d (d % 64 == 0)
-    auto load = [&](int m, uint2 (&k4)[kUnroll], uint2 (&v4)[kUnroll]) {
+    for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-        for (int r = 0; r < kUnroll; ++r) {
-            const bool ok = colok && m + r < m1;
-            k4[r] = ok ? __ldg(wk + (m + r) * rs) : make_uint2(0u, 0u);
-            v4[r] = ok ? __ldg(wv + (m + r) * rs) : make_uint2(0u, 0u);
-        }
-    };
-    // the next row group is in flight while the current one is used
-    constexpr int kStep = kWarps1 * kUnroll;
-    int m = m0 + warp * kUnroll;
-    if (m < m1) load(m, qk, qv);
-    for (; m < m1; m += kStep) {
-        if (m + kStep < m1) load(m + kStep, nk, nv);
+        for (int j = 0; j < 4; ++j) acc[mt][j] = 0.f;
+    // ldmatrix row of this lane: B (e, [n][k]) matrix lane >> 3 = k-step
+    // half lane >> 4, k offset 8 (lane >> 3 & 1); A (weights, [k][m]) row k =
+    // lane & 7 (+ 8 for lanes 16..31), 8-column chunk (lane >> 3) & 1
+    const int kr = warp * kRowsPerWarp;
+    const uint32_t e_off = static_cast<uint32_t>((lane & 7) * kEPitch + (kr + (lane >> 3) * 8) * 2);
+    const int ka = (lane & 7) + ((lane >> 4) << 3);
+    const int ca = (lane >> 3) & 1;
+    bool failed = false;
+    for (int k = 0; k < nchunk; ++k) {
+        // chunk k's e has landed once no more than the groups committed after
+        // it (chunks k + 1 .. min(nchunk, k + kRing) - 1) are pending; its
+        // weights once its stage barrier completes
+        cp_async_wait_n(min(nchunk - 1 - k, kRing - 1));
+        if (!failed && !mbar_wait(&bars[k % kRing], static_cast<uint32_t>((k / kRing) & 1))) failed = true;
+        __syncthreads();
+        const uint32_t sA = smem_addr(sm + kOffRing + (k % kRing) * kStageB);
+        uint32_t bf[4];
+        ldsm_x4(bf, sA + kWBytes + e_off);
 #pragma unroll
-        for (int b = 0; b < kBc; ++b) {
-            const float4 e4 = *reinterpret_cast<const float4*>(es + b * rows + (m - m0));
-            const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+        for (int ks = 0; ks < 2; ++ks) {
+            const int kk = kr + ks * 16 + ka;                 // row of the stage
+            const uint32_t row = sA + static_cast<uint32_t>(kk * (kTile * 2));
+            const int sw = (kk >> 1) & 3;                     // 64-byte swizzle of this row
 #pragma unroll
-            for (int r = 0; r < kUnroll; ++r) {
-                const float2 e2 = splat2(ev[r]);
-                ak[b][0] = fma2(e2, bf2(qk[r].x), ak[b][0]);
-                ak[b][1] = fma2(e2, bf2(qk[r].y), ak[b][1]);
-                av[b][0] = fma2(e2, bf2(qv[r].x), av[b][0]);
-                av[b][1] = fma2(e2, bf2(qv[r].y), av[b][1]);
+            for (int mt = 0; mt < 4; ++mt) {
+                const int c = ((mt & 1) << 1) + ca;           // 16-byte chunk of the 64-byte row
+                uint32_t af[4];
+                ldsm_x4_trans(af, row + (mt >> 1) * kBoxBytes + ((c ^ sw) << 4));
+                mma_16816(acc[mt], af, bf[2 * ks], bf[2 * ks + 1]);
             }
         }
-#pragma unroll
-        for (int r = 0; r < kUnroll; ++r) {
-            qk[r] = nk[r];
-            qv[r] = nv[r];
+        if (k + kRing < nchunk) {
+            __syncthreads();   // every warp is done with stage k % kRing
+            fence_proxy_async();
+            issue(k + kRing);
         }
     }
-    // the eight warps' sums, in warp order
-    __syncthreads();
-    float4* red = reinterpret_cast<float4*>(sm);      // [kWarps1][kBc][2][32]
+    if (failed) atomicOr(p.err, kErrTimeout);
+    // the warps' sums, in warp order; accumulator (mt, j): column
+    // 16 (mt & 1) + lane / 4 (+ 8 for j >= 2), batch row 2 (lane % 4) + (j & 1)
+    float* red = reinterpret_cast<float*>(sm + kOffRed);    // [warp][mat][batch][32 columns]
+    {
+        const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int b = 0; b < kBc; ++b) {
-        red[((warp * kBc + b) * 2 + 0) * 32 + lane] = make_float4(ak[b][0].x, ak[b][0].y, ak[b][1].x, ak[b][1].y);
-        red[((warp * kBc + b) * 2 + 1) * 32 + lane] = make_float4(av[b][0].x, av[b][0].y, av[b][1].x, av[b][1].y);
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = ((mt & 1) << 4) + g + ((j >> 1) << 3);
+                const int bb = 2 * t + (j & 1);
+                red[((warp * 2 + (mt >> 1)) * kBc + bb) * kTile + col] = acc[mt][j];
+            }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < kBc * 2 * 32; i += blockDim.x) {
-        const int b = i / 64, kvsel = (i >> 5) & 1, ln = i & 31;
-        if (b >= nb || blockIdx.x * kCols + 4 * ln >= p.d) continue;
-        float4 s = red[((0 * kBc + b) * 2 + kvsel) * 32 + ln];
-        for (int w = 1; w < kWarps1; ++w) {
-            const float4 q = red[((w * kBc + b) * 2 + kvsel) * 32 + ln];
-            s.x += q.x;
-            s.y += q.y;
-            s.z += q.z;
-            s.w += q.w;
+    float* kv = reinterpret_cast<float*>(sm + kOffKv);      // [mat][batch][32]
+    for (int i = tid; i < 2 * kBc * kTile; i += blockDim.x) {
+        float s = red[i];
+#pragma unroll
+        for (int w = 1; w < kWarps1; ++w) s += red[w * 2 * kBc * kTile + i];
+        kv[i] = s;
+        // v goes to the workspace for kernel 2 (k enters it only through the row sums)
+        const int m2 = i / (kBc * kTile), b = (i / kTile) % kBc, col = i % kTile;
+        if (m2 == 1 && b < nb) p.vbuf[static_cast<long long>(b0 + b) * p.d + c0 + col] = s;
+    }
+    __syncthreads();
+    // the tile's row sums: warp = batch row, lane = column
+    if (hb < nb) {
+        const float kk = kv[hb * kTile + lane];
+        const float vv = kv[(kBc + hb) * kTile + lane];
+        float4 a = make_float4(hval * hval, kk * kk, hval * kk * (whv * whv), vv * vv);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            a.x += __shfl_xor_sync(kFullMask, a.x, off);
+            a.y += __shfl_xor_sync(kFullMask, a.y, off);
+            a.z += __shfl_xor_sync(kFullMask, a.z, off);
+            a.w += __shfl_xor_sync(kFullMask, a.w, off);
         }
-        float* dst = p.part + ((static_cast<long long>(kvsel) * p.splits + blockIdx.y) * p.B + b0 + b) * p.d +
-                     blockIdx.x * kCols + 4 * ln;
-        *reinterpret_cast<float4*>(dst) = s;
+        if (lane == 0)
+            *reinterpret_cast<float4*>(p.stats + (static_cast<long long>(b0 + hb) * ntiles + tile) * 4) = a;
     }
 }
 
 constexpr int kThreads2 = 256;
-constexpr int kCluster2 = 8;   // CTAs per batch row in kernel 2
-constexpr int kCache = 4;      // columns per thread whose v is kept between the passes
+constexpr int kMaxTaps2 = 8;   // taps whose cached u is loaded before the grid wait
 
-// Kernel 2: a cluster of kCluster2 CTAs per batch row, CTA `rank` owning
-// d / kCluster2 columns.  Each CTA sums its columns' row statistics and stores
-// the four partial sums into slot `rank` of every CTA of the cluster
-// (asynchronous remote stores completing on that CTA's mbarrier); each CTA
-// adds the eight slots in rank order, so all form identical scalars, then
-// writes y and the new cache for its columns.  Every CTA waits for all eight
-// slots before it goes on, so none leaves while a store to it is in flight.
-__global__ void __launch_bounds__(kThreads2) decode_row_kernel(const DecodeParams p) {
-    __shared__ float4 sh[kThreads2 / 32];
-    __shared__ float4 cta_sum;
-    __shared__ float4 slots[kCluster2];
-    __shared__ uint64_t xbar;
-    if (threadIdx.x == 0) {
-        mbar_init(&xbar, 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(&xbar, kCluster2 * 16u);
-    }
-    // the barrier is initialised before any peer stores into this CTA (the
-    // matching wait comes just before the stores)
-    cluster_arrive();
-    const uint32_t rank = cluster_rank();
-    const int b = static_cast<int>(cluster_index());
+// Kernel 2: CTA (x: batch row, y: 256-column block).
+__global__ void __launch_bounds__(kThreads2) decode_row_kernel(const __grid_constant__ DecodeParams p) {
+    __shared__ float4 red[kThreads2 / 32];
+    const int b = blockIdx.x;
     const int d = p.d;
-    const int ncol = d / kCluster2;
-    const int c0 = static_cast<int>(rank) * ncol;
-    const long long pk = static_cast<long long>(p.splits) * p.B * d;  // offset of the v partials
-    // k, v of column i: the splits summed in order (loads issued 8 at a time)
-    auto kv_at = [&](int i, float& kk, float& vv) {
-        kk = 0.f;
-        vv = 0.f;
-        const float* src = p.part + static_cast<long long>(b) * d + i;
-        const long long ss = static_cast<long long>(p.B) * d;  // split stride
-        for (int s0 = 0; s0 < p.splits; s0 += 8) {
-            float a[8], c[8];
+    const int i = blockIdx.y * kThreads2 + threadIdx.x;
+    const bool ok = i < d;
+    const int ntiles = d / kTile;
+    // inputs only, before the wait: w_v, the taps and the cached u of each tap
+    const uint16_t* st = p.state + static_cast<long long>(b) * p.L * d;
+    float wv = 0.f, cwv[kMaxTaps2], uj[kMaxTaps2];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const bool ok = s0 + u < p.splits;
-                a[u] = ok ? __ldg(src + (s0 + u) * ss) : 0.f;
-                c[u] = ok ? __ldg(src + pk + (s0 + u) * ss) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                kk += a[u];
-                vv += c[u];
-            }
+    for (int j = 0; j < kMaxTaps2; ++j) {
+        cwv[j] = 0.f;
+        uj[j] = 0.f;
+        if (ok && j < p.w) {
+            const int lag = (p.w - 1 - j) * p.dil;
+            cwv[j] = __ldg(p.cw + static_cast<long long>(j) * d + i);
+            if (lag > 0 && lag <= p.L)
+                uj[j] = __uint_as_float(static_cast<uint32_t>(__ldg(st + static_cast<long long>(p.L - lag) * d + i)) << 16);
         }
-    };
-    auto bf = [](const uint16_t* q, long long i) { return __uint_as_float(static_cast<uint32_t>(__ldg(q + i)) << 16); };
-
-    // ---- this CTA's share of the row statistics (v of the first kCache
-    // columns of each thread kept for the second pass).  h and w_h of those
-    // columns are inputs, read before waiting for the projection grid.
-    float vc[kCache], hc[kCache], wc[kCache];
-#pragma unroll
-    for (int q = 0; q < kCache; ++q) {
-        const int i = c0 + threadIdx.x + q * static_cast<int>(blockDim.x);
-        const bool ok = i < c0 + ncol;
-        hc[q] = ok ? bf(p.h, static_cast<long long>(b) * d + i) : 0.f;
-        wc[q] = ok ? __ldg(p.wh + i) : 0.f;
     }
+    if (ok) wv = __ldg(p.wv + i);
     grid_dep_wait();
     grid_dep_launch();   // the next decode step's projection may be scheduled (it waits for this grid)
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // sum h^2, k^2, h k w_h^2, v^2
-    int it = 0;
-    for (int i = c0 + threadIdx.x; i < c0 + ncol; i += blockDim.x, ++it) {
-        float kk, vv;
-        kv_at(i, kk, vv);
-        float hh = 0.f, w = 0.f;
-        if (it < kCache) {
-#pragma unroll
-            for (int q = 0; q < kCache; ++q)
-                if (q == it) {
-                    vc[q] = vv;
-                    hh = hc[q];
-                    w = wc[q];
-                }
-        } else {
-            hh = bf(p.h, static_cast<long long>(b) * d + i);
-            w = __ldg(p.wh + i);
+    const float vv = ok ? __ldcg(p.vbuf + static_cast<long long>(b) * d + i) : 0.f;
+    // the row sums of batch row b: thread j loads the sums of tiles j, j + 256,
+    // ... (one L2 round trip for d <= 8192), a butterfly adds them within each
+    // warp, then every thread adds the eight warp totals in warp order
+    {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int t = threadIdx.x; t < ntiles; t += kThreads2) {
+            const float4 q = __ldcg(reinterpret_cast<const float4*>(p.stats + (static_cast<long long>(b) * ntiles + t) * 4));
+            a.x += q.x;
+            a.y += q.y;
+            a.z += q.z;
+            a.w += q.w;
         }
-        acc.x = fmaf(hh, hh, acc.x);
-        acc.y = fmaf(kk, kk, acc.y);
-        acc.z = fmaf(hh * kk, w * w, acc.z);
-        acc.w = fmaf(vv, vv, acc.w);
-    }
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        acc.x += __shfl_xor_sync(kFullMask, acc.x, off);
-        acc.y += __shfl_xor_sync(kFullMask, acc.y, off);
-        acc.z += __shfl_xor_sync(kFullMask, acc.z, off);
-        acc.w += __shfl_xor_sync(kFullMask, acc.w, off);
-    }
-    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = acc;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float4 t = sh[0];
-        for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) {
-            t.x += sh[w].x;
-            t.y += sh[w].y;
-            t.z += sh[w].z;
-            t.w += sh[w].w;
+        for (int off = 16; off >= 1; off >>= 1) {
+            a.x += __shfl_xor_sync(kFullMask, a.x, off);
+            a.y += __shfl_xor_sync(kFullMask, a.y, off);
+            a.z += __shfl_xor_sync(kFullMask, a.z, off);
+            a.w += __shfl_xor_sync(kFullMask, a.w, off);
         }
-        cta_sum = t;
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
     }
     __syncthreads();
-    cluster_wait();
-    if (threadIdx.x < kCluster2) {
-        const uint32_t dst = static_cast<uint32_t>(threadIdx.x);
-        st_async_f4(map_to_rank(smem_addr(&slots[rank]), dst), cta_sum, map_to_rank(smem_addr(&xbar), dst));
-    }
-    if (!mbar_wait_cluster(&xbar, 0u) && threadIdx.x == 0) atomicOr(p.err, kErrTimeout);
-    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 tsum = red[0];
 #pragma unroll
-    for (int r = 0; r < kCluster2; ++r) {
-        const float4 q = slots[r];
-        t.x += q.x;
-        t.y += q.y;
-        t.z += q.z;
-        t.w += q.w;
+    for (int w = 1; w < kThreads2 / 32; ++w) {
+        tsum.x += red[w].x;
+        tsum.y += red[w].y;
+        tsum.z += red[w].z;
+        tsum.w += red[w].w;
     }
     const float inv_d = 1.0f / static_cast<float>(d);
-    const float rh = rsqrtf(fmaf(t.x, inv_d, p.eps));
-    const float rk = rsqrtf(fmaf(t.y, inv_d, p.eps));
-    const float z = rh * rk * t.z * p.inv_sqrt_d;
+    const float rh = rsqrtf(fmaf(tsum.x, inv_d, p.eps));
+    const float rk = rsqrtf(fmaf(tsum.y, inv_d, p.eps));
+    const float z = rh * rk * tsum.z * p.inv_sqrt_d;
     const float alpha = __fdividef(1.0f, 1.0f + __expf(-z));
-    const float rv = rsqrtf(fmaf(alpha * alpha * t.w, inv_d, p.eps));
-
-    // ---- conv, SiLU, output and the new cache row for this CTA's columns
-    const uint16_t* st = p.state + static_cast<long long>(b) * p.L * d;
-    uint16_t* ns = p.new_state + static_cast<long long>(b) * p.max_len * d;
-    it = 0;
-    for (int i = c0 + threadIdx.x; i < c0 + ncol; i += blockDim.x, ++it) {
-        float vv = 0.f;
-        if (it < kCache) {
+    const float rv = rsqrtf(fmaf(alpha * alpha * tsum.w, inv_d, p.eps));
+    if (!ok) return;
+    const float vh = alpha * vv;
+    const float u = vh * rv * wv;
+    float c = 0.f;
 #pragma unroll
-            for (int q = 0; q < kCache; ++q)
-                if (q == it) vv = vc[q];
-        } else {
-            float kk;
-            kv_at(i, kk, vv);
-        }
-        const float vh = alpha * vv;
-        const float u = vh * rv * __ldg(p.wv + i);
-        float c = 0.f;
-        for (int j = 0; j < p.w; ++j) {
-            const int lag = (p.w - 1 - j) * p.dil;
-            const float uj = lag == 0 ? u : (lag <= p.L ? bf(st, static_cast<long long>(p.L - lag) * d + i) : 0.f);
-            c = fmaf(__ldg(p.cw + static_cast<long long>(j) * d + i), uj, c);
-        }
-        const float y = __fdividef(c, 1.0f + __expf(-c)) + vh;
-        p.y[static_cast<long long>(b) * d + i] = static_cast<uint16_t>(pack_bf16x2(y, 0.f) & 0xffffu);
-        ns[static_cast<long long>(p.max_len - 1) * d + i] = static_cast<uint16_t>(pack_bf16x2(u, 0.f) & 0xffffu);
+    for (int j = 0; j < kMaxTaps2; ++j)
+        if (j < p.w) c = fmaf(cwv[j], (p.w - 1 - j) * p.dil == 0 ? u : uj[j], c);
+    for (int j = kMaxTaps2; j < p.w; ++j) {   // taps beyond those loaded early
+        const int lag = (p.w - 1 - j) * p.dil;
+        const float u2 = lag == 0 ? u
+                                  : (lag <= p.L ? __uint_as_float(static_cast<uint32_t>(__ldg(st + static_cast<long long>(p.L - lag) * d + i)) << 16)
+                                                : 0.f);
+        c = fmaf(__ldg(p.cw + static_cast<long long>(j) * d + i), u2, c);
     }
+    const float y = __fdividef(c, 1.0f + __expf(-c)) + vh;
+    p.y[static_cast<long long>(b) * d + i] = static_cast<uint16_t>(pack_bf16x2(y, 0.f) & 0xffffu);
+    p.new_state[(static_cast<long long>(b) * p.max_len + p.max_len - 1) * d + i] =
+        static_cast<uint16_t>(pack_bf16x2(u, 0.f) & 0xffffu);
 }
 
 }  // namespace
 
-int decode_proj_smem(int rows_per_split) {
-    const int a = kBc * rows_per_split * 4;
-    const int b = kWarps1 * kBc * 2 * 32 * 16;
-    return a > b ? a : b;
-}
-
 cudaError_t decode_prepare() {
-    return cudaFuncSetAttribute(decode_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    return cudaFuncSetAttribute(decode_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1);
 }
 
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s) {
-    const dim3 g1(static_cast<unsigned>((p.d + kCols - 1) / kCols), static_cast<unsigned>(p.splits),
-                  static_cast<unsigned>((p.B + kBc - 1) / kBc));
     cudaLaunchConfig_t cfg1 = {};
     cudaLaunchAttribute attr1[1];
     attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr1[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg1.gridDim = g1;
+    cfg1.gridDim = dim3(static_cast<unsigned>((p.B + kBc - 1) / kBc), static_cast<unsigned>(p.d / kTile), 1);
     cfg1.blockDim = dim3(32 * kWarps1, 1, 1);
-    cfg1.dynamicSmemBytes = static_cast<size_t>(decode_proj_smem(p.rows_per_split));
+    cfg1.dynamicSmemBytes = kSmem1;
     cfg1.stream = s;
     cfg1.attrs = attr1;
     cfg1.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg1, decode_proj_kernel, p);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(p.B) * kCluster2, 1, 1);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(p.B), static_cast<unsigned>((p.d + kThreads2 - 1) / kThreads2), 1);
     cfg.blockDim = dim3(kThreads2, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_row_kernel, p);
 }
 

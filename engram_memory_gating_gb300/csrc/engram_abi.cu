@@ -399,24 +399,30 @@ const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
     return &e.g;
 }
 
-// Decode: d_mem rows per projection split (a multiple of 32, at most 2048)
-// and the number of splits, chosen from the shape alone (the workspace size
-// depends on it): enough CTAs for about two per SM of a 152-SM part.
-void decode_split(int64_t B, int64_t dmem, int64_t d, int& splits, int& rows) {
-    const int64_t tiles = ((d + 127) / 128) * ((B + 7) / 8);
-    int64_t s = (304 + tiles - 1) / tiles;
-    // at least 32 rows per split, and partial sums of at most a quarter of
-    // the weight bytes (splits * B * d * 8 <= 2 * d_mem * d * 2 / 4)
-    int64_t max_s = dmem / 32;
-    const int64_t cap = dmem / (8 * B);
-    if (cap < max_s) max_s = cap;
-    if (s > max_s) s = max_s;
-    if (s < 1) s = 1;
-    int64_t r = (dmem + s - 1) / s;
-    r = (r + 31) / 32 * 32;
-    if (r > 2048) r = 2048;
-    rows = static_cast<int>(r);
-    splits = static_cast<int>((dmem + r - 1) / r);
+// Tensor map of a (rows, cols) row-major bf16 matrix with 32-column x
+// 256-row boxes (rows past the end read as zero; the 64-byte rows land in
+// shared memory in the 64-byte swizzle), through the driver entry point (no
+// link-time dependence on libcuda).
+bool encode_weight_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        looked_up = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        (void)cudaGetLastError();
+    }
+    if (!encode) return false;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {32, 256};
+    const cuuint32_t estride[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool decode_shape_ok(int64_t B, int64_t dmem, int64_t d) {
@@ -806,9 +812,8 @@ engram_status_t engram_fused_weight_bwd(const float* grad_w_partial, int64_t nbl
 
 size_t engram_decode_workspace_size(int64_t B, int64_t d_mem, int64_t d) {
     if (!decode_shape_ok(B, d_mem, d)) return 0;
-    int splits, rows;
-    decode_split(B, d_mem, d, splits, rows);
-    return static_cast<size_t>(2) * splits * static_cast<size_t>(B) * static_cast<size_t>(d) * 4;
+    // [(B, d) fp32 v | (B, d / 32, 4) fp32 row sums of the 32-column tiles]
+    return static_cast<size_t>(B) * static_cast<size_t>(d) * 4 + static_cast<size_t>(B) * (d / 32) * 16;
 }
 
 engram_status_t engram_decode_fwd(const void* e, const void* h, const void* state, int64_t L,
@@ -858,8 +863,11 @@ engram_status_t engram_decode_fwd(const void* e, const void* h, const void* stat
     p.cw = conv_w;
     p.y = static_cast<uint16_t*>(y);
     p.new_state = static_cast<uint16_t*>(new_state);
-    p.part = static_cast<float*>(workspace);
+    p.vbuf = static_cast<float*>(workspace);
+    p.stats = reinterpret_cast<float*>(static_cast<char*>(workspace) + static_cast<size_t>(B) * d * 4);
     p.err = st->err;
+    if (!encode_weight_map(&p.tmk, W_K, d_mem, d) || !encode_weight_map(&p.tmv, W_V, d_mem, d))
+        return ENGRAM_ERR_DEVICE;
     p.B = static_cast<int>(B);
     p.dmem = static_cast<int>(d_mem);
     p.d = static_cast<int>(d);
@@ -867,7 +875,6 @@ engram_status_t engram_decode_fwd(const void* e, const void* h, const void* stat
     p.max_len = static_cast<int>(max_len);
     p.w = static_cast<int>(w);
     p.dil = static_cast<int>(dilation);
-    decode_split(B, d_mem, d, p.splits, p.rows_per_split);
     p.eps = eps;
     p.inv_sqrt_d = static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
     return launch_status(decode_launch(p, stream));

@@ -2,6 +2,7 @@
 // translation units.  Plain structs of device pointers and sizes.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -152,8 +153,12 @@ struct FusedWeightParams {
     long long nblocks;
 };
 
-// GateConv decode step (one token per batch row).
+// GateConv decode step (one token per batch row).  The weight matrices are
+// also described by 2-D tensor maps (box 32 columns x 256 rows), encoded on
+// the host per call.
 struct DecodeParams {
+    CUtensorMap tmk;          // W_K as (d_mem, d) bf16
+    CUtensorMap tmv;          // W_V
     const uint16_t* e;        // (B, dmem) bf16
     const uint16_t* h;        // (B, d) bf16
     const uint16_t* state;    // (B, L, d) bf16, may be null when L == 0
@@ -164,10 +169,10 @@ struct DecodeParams {
     const float* cw;          // (w, d)
     uint16_t* y;              // (B, d) bf16
     uint16_t* new_state;      // (B, max_len, d) bf16
-    float* part;              // workspace: (2, splits, B, d) fp32 partial k, v
+    float* vbuf;              // workspace: (B, d) fp32 projected v
+    float* stats;             // workspace: (B, d / 32, 4) fp32 row sums of each 32-column tile
     unsigned int* err;        // sticky device error word
     int B, dmem, d, L, max_len, w, dil;
-    int splits, rows_per_split;
     float eps, inv_sqrt_d;
 };
 
@@ -195,7 +200,6 @@ cudaError_t gate_wreduce_launch(const GateWReduceParams& p, cudaStream_t s);
 cudaError_t fused_weight_launch(const FusedWeightParams& p, cudaStream_t s);
 cudaError_t fused_weight_bwd_launch(const FusedWeightParams& p, cudaStream_t s);
 
-int decode_proj_smem(int rows_per_split);
 cudaError_t decode_prepare();
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);
 
