@@ -1,20 +1,19 @@
-// Shared-memory layout and cluster exchange of the GateConv kernels.
+// Constants and warp-level pieces shared by the GateConv kernels.
 //
 // A GateConv token row is cut into C column slices, one per CTA of a thread
 // block cluster; each thread owns 4 consecutive columns of its CTA's slice.
 // The per-token quantities both kernels need (RMS statistics, the gate logit,
 // the gradient sums of the backward) are sums over the whole row, so each CTA
-// forms partial sums over its slice and the cluster exchanges them.  Tokens go
-// in chunks of kChunk: every warp reduces the 4 x kChunk partial sums of a
-// chunk across its lanes and writes them into a slot of every CTA of the
-// cluster with asynchronous remote stores (st.async) that complete on that
-// CTA's exchange mbarrier.  A CTA reads the totals of chunk c - 1 only after
-// it has finished the row work of chunk c, so the exchange latency overlaps a
-// chunk of work and no cluster-wide barrier runs inside the token loop.
-//
-// Two slot buffers suffice: a CTA writes chunk c + 1 into a peer only after it
-// has received chunk c from every warp of that peer, and every warp reads
-// chunk c - 1 before it sends chunk c.
+// forms partial sums over its slice and the cluster exchanges them, per chunk
+// of kChunk tokens.  Every warp reduces the 4 x kChunk partial sums of a
+// chunk across its lanes (warp_reduce16) and leaves them in shared memory;
+// the last warp of the CTA to hand in adds the warps' totals in warp order
+// and sends the CTA total into slot `rank` of every CTA of the cluster with
+// asynchronous remote stores (st.async) that complete on that CTA's exchange
+// mbarrier.  A receiver adds the C slots in rank order, so every CTA forms
+// the same total.  The kernels read the totals of chunk c - 1 only after the
+// row work of chunk c, so the exchange overlaps a chunk of work and no
+// cluster-wide barrier runs inside the token loop.
 #pragma once
 
 #include "common.cuh"
@@ -45,12 +44,6 @@ constexpr int kVals = 4 * kChunk; // partial sums per warp and chunk
 constexpr int kThreads = 256;     // threads per CTA (4 columns each)
 constexpr int kStages = 16;       // ring stages (one token each)
 
-// Byte offsets in dynamic shared memory.
-constexpr int kOffFull = 0;    // [kStages] stage mbarriers
-constexpr int kOffXbar = 128;  // [2] exchange mbarriers
-constexpr int kOffRel = 192;   // [kStages] per-stage release counters
-constexpr int kOffXch = 256;   // [2][parts][kVals] fp32 exchange slots
-
 // Sum of 16 values over the 32 lanes of a warp (reduce-scatter): lane l ends
 // with the warp total of value l >> 1 (lanes l and l ^ 1 hold the same total).
 EG_DEV float warp_reduce16(const float (&v)[16], int lane) {
@@ -76,25 +69,6 @@ EG_DEV float warp_reduce16(const float (&v)[16], int lane) {
     }
     const float e = (b1 ? c[1] : c[0]) + __shfl_xor_sync(kFullMask, b1 ? c[0] : c[1], 2);
     return e + __shfl_xor_sync(kFullMask, e, 1);
-}
-
-// Sends this warp's chunk totals (value l >> 1 in lane l) into slot `part` of
-// buffer `buf` of every CTA of the cluster; lanes l and l ^ 1 split the CTAs.
-EG_DEV void xch_send(float* xch, uint64_t* xbar, int buf, int parts, int part, float val, int lane,
-                     uint32_t C) {
-    const uint32_t dst = smem_addr(xch + (buf * parts + part) * kVals + (lane >> 1));
-    const uint32_t bar = smem_addr(xbar + buf);
-    for (uint32_t rr = static_cast<uint32_t>(lane & 1); rr < C; rr += 2)
-        st_async_f32(map_to_rank(dst, rr), val, map_to_rank(bar, rr));
-}
-
-// Total over all parts of value (lane & 15) of buffer `buf`, in a fixed order
-// (even parts, odd parts, then their sum), the same in every warp.
-EG_DEV float xch_total(const float* xch, int buf, int parts, int lane) {
-    const float* s = xch + buf * parts * kVals + (lane & 15);
-    float acc = 0.f;
-    for (int p = lane >> 4; p < parts; p += 2) acc += s[p * kVals];
-    return acc + __shfl_xor_sync(kFullMask, acc, 16);
 }
 
 }  // namespace gc

@@ -331,10 +331,9 @@ engram_status_t engram_decode_fwd(const void* e, const void* h, const void* stat
  * have no counterpart to this entry point.
  *
  * Some callers cannot call cudaMalloc (or any allocator, PyTorch's included)
- * at the point where they run the backward: code that runs while a stream
- * is being captured into a CUDA graph, plug-ins embedded in a host framework
- * that owns all device memory and forbids outside allocations, and runtimes
- * that work from a fixed, pre-planned memory budget.  They can pass inputs
+ * at the point where they run the backward: plug-ins embedded in a host
+ * framework that owns all device memory and forbids outside allocations, and
+ * runtimes that work from a fixed, pre-planned memory budget.  They can pass inputs
  * and outputs they already own, but no workspace.  This call is
  * engram_gate_bwd with its workspace taken from a fixed array inside the
  * library (ENGRAM_GATE_BWD_NOALLOC_SCRATCH_BYTES, enough for N up to
@@ -344,9 +343,9 @@ engram_status_t engram_decode_fwd(const void* e, const void* h, const void* stat
  *   N: 64 <= N <= ENGRAM_GATE_BWD_NOALLOC_MAX_TOKENS, N % 64 == 0; a larger N
  *      returns ENGRAM_ERR_SHAPE and enqueues nothing (use engram_gate_bwd
  *      with a caller-provided workspace instead).
- *   The first call on each device looks up the array's device address with
- *   that device current (one-time set-up); make that first call before any
- *   stream capture.  The call itself allocates nothing.
+ *   The first call on each device (and the first after the device's context
+ *   was replaced) looks up the array's device address with that device
+ *   current, a one-time set-up.  The call itself allocates nothing.
  *   All calls share the one array, which keeps the previous call's contents;
  *   nothing in it needs to start at zero (each call writes every slot it
  *   reads before reading it).  Calls whose kernels can overlap on the GPU

@@ -2,8 +2,8 @@
 
 engram_gate_bwd_noalloc runs the same backward as engram_gate_bwd, with its
 workspace taken from a fixed array inside the library instead of a buffer the
-caller allocates (for callers inside a graph capture, inside a framework that
-owns all device memory, or on a fixed memory budget).  Checked through the C
+caller allocates (for callers inside a framework that owns all device memory,
+or on a fixed memory budget).  Checked through the C
 ABI: two calls in a row give the same bits as the workspace entry point (the
 same deterministic kernels run, only the workspace's address differs, so any
 difference would mean a misplaced workspace slot), they change the device's
