@@ -339,6 +339,14 @@ def f64_inputs(inp):
             inp["mask"].numpy().astype("uint8"), f(inp["grad_out"]))
 
 
+def run_config(world):
+    """The workload description both arms print (identical, so that the two
+    lines can be compared key for key)."""
+    return {"workload": WORKLOAD, "N": N_TOK, "S": S, "d": D,
+            "l2": "inputs larger than L2 (1.85 GB read+written per step); no flush",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -374,8 +382,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "N": N_TOK, "S": S, "d": D,
-                       "sample_tokens_per_step": n},
+            "config": run_config(world),
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s",
                              "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": f"{n} tokens of the workload per step"},
@@ -615,9 +622,8 @@ def main():
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "N": N_TOK, "S": S, "d": D,
-                   "l2": "inputs larger than L2 (1.85 GB read+written per step); no flush",
-                   "parallelism": f"replicas x{world}", "launch": launch},
+        "config": run_config(world),
+        "launch": launch,
         "hbm_GB_s": round(step_bytes / (ms * 1e-3) / 1e9, 1),
         "roofline": {"kernel": "engram_gate_bwd (gate_bwd_coef_kernel + gate_bwd_main_kernel + wreduce_kernel), N=8192",
                      "bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak,
