@@ -539,7 +539,7 @@ def main():
     fwd_gbs = fwd_bytes / (fwd_ms * 1e-3) / 1e9
     csrc = "engram_memory_gating_gb300/csrc/"
     hdrs = [csrc + "common.cuh", csrc + "engram_internal.h"]
-    traffic = profile_traffic("gate_bwd_n8192.md", [csrc + "gate_bwd.cu"] + hdrs)
+    traffic = profile_traffic("gate_bwd_n8192.md", [csrc + "gate_bwd.cu", csrc + "gate_bwd_fused.cu"] + hdrs)
     traffic_fwd = profile_traffic("gate_fwd_n8192.md", [csrc + "gate_fwd.cu"] + hdrs)
 
     # ---- end to end through the public API with host buffers (pinned).  Every
@@ -625,7 +625,9 @@ def main():
         "config": run_config(world),
         "launch": launch,
         "hbm_GB_s": round(step_bytes / (ms * 1e-3) / 1e9, 1),
-        "roofline": {"kernel": "engram_gate_bwd (gate_bwd_coef_kernel + gate_bwd_main_kernel + wreduce_kernel), N=8192",
+        "roofline": {"kernel": ("engram_gate_bwd (gate_bwd_fused_kernel + wreduce_kernel), N=8192"
+                                if launch["bwd"]["kernels"] == 2 else
+                                "engram_gate_bwd (gate_bwd_coef_kernel + gate_bwd_main_kernel + wreduce_kernel), N=8192"),
                      "bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(bwd_gbs / peak, 4),
                      "peak_nominal": NOMINAL_GBS, "frac_nominal": round(bwd_gbs / NOMINAL_GBS, 4),
@@ -638,7 +640,10 @@ def main():
         "e2e": {"value": round(job_throughput(N_TOK, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 4 * K,  # forward + backward coefficients, elementwise, grad_weight merge
+        # kernels per step as the library reports them for this N: the forward,
+        # and the backward's (one pass + grad_weight merge, or coefficients,
+        # elementwise and merge)
+        "gpu_launches": (launch["fwd"]["kernels"] + launch["bwd"]["kernels"]) * K,
         "clocks": clk.summary(),
         "device_error_flags": err,
     }

@@ -67,7 +67,8 @@ class EngramError(RuntimeError):
 class _LaunchInfo(ctypes.Structure):
     _fields_ = [("cluster", ctypes.c_int), ("threads", ctypes.c_int),
                 ("clusters", ctypes.c_int), ("stages", ctypes.c_int),
-                ("smem_bytes", ctypes.c_int), ("resident", ctypes.c_int)]
+                ("smem_bytes", ctypes.c_int), ("resident", ctypes.c_int),
+                ("kernels", ctypes.c_int)]
 
 
 _lock = threading.Lock()

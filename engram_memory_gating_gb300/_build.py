@@ -17,8 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libengram.so")
-SOURCES = ["engram_abi.cu", "gate_fwd.cu", "gate_bwd.cu", "fused_weight.cu", "gateconv_fwd.cu",
-           "gateconv_bwd.cu", "decode.cu"]
+SOURCES = ["engram_abi.cu", "gate_fwd.cu", "gate_bwd.cu", "gate_bwd_fused.cu", "fused_weight.cu",
+           "gateconv_fwd.cu", "gateconv_bwd.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -63,6 +64,7 @@ struct DeviceState {
     int n = 0;
     GcCacheEntry gc_last[2];  // forward, backward
     bool decode_ready = false;
+    int fused_clusters = -1;  // co-resident clusters of the one-pass backward (-1: not asked yet)
 };
 
 std::mutex g_mu;
@@ -294,6 +296,30 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
     const int64_t need1 = blocks ? (N + 7) / 8 : (N + 3) / 4;
     c.aux_blocks = static_cast<int>(need1 < mc1 ? need1 : mc1);
     return true;
+}
+
+// The one-pass gate backward (gate_bwd_fused.cu) runs G clusters of two
+// CTAs, one per SM; each writes its grad_weight pair as 4 x 5120 fp32 hi
+// words and 4 x 5120 bf16 lo words (122,880 bytes).  With the per-token
+// scalars kept on chip the whole workspace is slot space: the hi slots, then
+// the lo rows.  G is fixed by N and the device alone (not by the buffer a
+// caller passes), and the call keeps the three-kernel backward when G would
+// leave too many SMs idle (small N: its workspace is small).  Measured at
+// N = 8192: 60 clusters 391 us, 67 clusters 351 us, 76 clusters 314 us, the
+// three kernels 359 us.
+constexpr int kFusedMinClusters = 64;
+constexpr size_t kFusedSlotBytes = 4 * kGateD * (4 + 2);
+
+int gate_bwd_fused_groups(DeviceState& st, int64_t N) {
+    if (st.fused_clusters < 0) {
+        int mc = 0;
+        if (gate_bwd_fused_prepare() != cudaSuccess || gate_bwd_fused_max_clusters(&mc) != cudaSuccess) mc = 0;
+        (void)cudaGetLastError();
+        st.fused_clusters = mc;
+    }
+    const int64_t slots = static_cast<int64_t>(engram_gate_bwd_workspace_size(N) / kFusedSlotBytes);
+    const int64_t G = std::min<int64_t>(st.fused_clusters, slots);
+    return G >= kFusedMinClusters ? static_cast<int>(G) : 0;
 }
 
 bool gc_shape_ok(int64_t M, int64_t T, int64_t d) {
@@ -531,6 +557,50 @@ engram_status_t gate_bwd_impl(const void* x, const void* kv, const float* weight
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState* st = device_state();
     if (!st) return ENGRAM_ERR_DEVICE;
+    const int G = gate_bwd_fused_groups(*st, N);
+    if (G > 0) {
+        // one pass: the workspace holds only the grad_weight words (G fp32 hi
+        // slots, then G bf16 lo rows)
+        float* partial = static_cast<float*>(workspace);
+        uint16_t* partial_lo = reinterpret_cast<uint16_t*>(partial + static_cast<size_t>(G) * 4 * kGateD);
+        GateBwdParams p = {};
+        p.x = static_cast<const uint16_t*>(x);
+        p.key = static_cast<const uint16_t*>(kv);
+        p.v = static_cast<const uint16_t*>(kv) + 4 * kGateD;
+        p.key_ts = p.v_ts = 5LL * kGateD;
+        p.w = weight;
+        p.saved = saved;
+        p.gout = static_cast<const uint16_t*>(grad_out);
+        p.gx = static_cast<uint16_t*>(grad_x);
+        p.gkey = static_cast<uint16_t*>(grad_kv);
+        p.gv = static_cast<uint16_t*>(grad_kv) + 4 * kGateD;
+        p.gkey_ts = p.gv_ts = 5LL * kGateD;
+        p.partial = partial;
+        p.partial_lo = partial_lo;
+        p.err = st->err;
+        p.N = N;
+        p.d = kGateD;
+        p.pair_slots = 1;
+        p.packed = 1;
+        p.clamp = ENGRAM_GATE_CLAMP;
+        engram_status_t s = launch_status(gate_bwd_fused_launch(p, G, stream));
+        if (s != ENGRAM_OK) return s;
+        GateWReduceParams r = {};
+        r.partial = partial;
+        r.out = grad_weight;
+        r.nblocks = G;
+        r.n = 4 * kGateD;
+        r.stride = 4 * kGateD;
+        r.pairs = 2;
+        r.lo16 = partial_lo;
+        if (prod) {
+            r.wh = static_cast<const uint16_t*>(wh);
+            r.we = static_cast<const uint16_t*>(we);
+            r.grad_wh = grad_wh;
+            r.grad_we = grad_we;
+        }
+        return launch_status(gate_wreduce_launch(r, stream));
+    }
     LaunchCfg c = {};
     int ncols;
     int group_tokens = 0;
@@ -1046,7 +1116,21 @@ engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
             break;
         case 1: {
             int gt = 0;
-            ok = engram_gate_bwd_workspace_size(n0) > 0 && gate_bwd_cfg(*st, n0, kGateD, false, c, ncols, gt);
+            ok = engram_gate_bwd_workspace_size(n0) > 0;
+            const int G = ok ? gate_bwd_fused_groups(*st, n0) : 0;
+            if (G > 0) {
+                // one-pass backward: clusters of two CTAs (column halves) per
+                // token range, plus the grad_weight merge
+                info->cluster = 2;
+                info->threads = gate_bwd_fused_threads();
+                info->clusters = G;
+                info->stages = 4;
+                info->smem_bytes = gate_bwd_fused_smem();
+                info->resident = st->fused_clusters;
+                info->kernels = 2;
+                return ENGRAM_OK;
+            }
+            ok = ok && gate_bwd_cfg(*st, n0, kGateD, false, c, ncols, gt);
             // CTAs sharing a token row = column slices; "clusters" = token groups
             if (ok) {
                 c.cluster = c.clusters;
@@ -1073,6 +1157,9 @@ engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
     // co-resident CTA groups: CTAs for the gate kernels, clusters for GateConv
     info->resident = op == 1 ? max_clusters(*st, op, 1, c.threads, c.smem) / c.cluster
                              : max_clusters(*st, op, op >= 2 ? c.cluster : 1, c.threads, c.smem);
+    // kernels a call launches: gate fwd 1; gate bwd coefficients, elementwise,
+    // merge; GateConv fwd 1; GateConv bwd main + three merges
+    info->kernels = op == 0 ? 1 : op == 1 ? 3 : op == 2 ? 1 : 4;
     return ENGRAM_OK;
 }
 

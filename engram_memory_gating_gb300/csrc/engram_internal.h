@@ -60,6 +60,7 @@ struct GateBwdParams {
     long long gkey_ts, gv_ts;
     float* coef;     // (N, 4, 4) fp32 per-token scalars: A hi, A lo, -B, -Ck
     float* partial;  // grad_weight slots (4, d) fp32 each
+    uint16_t* partial_lo;  // one-pass backward: the low words of its (hi, lo) pairs, bf16 (4, d) each
     unsigned int* err;
     long long N;
     int d;
@@ -77,7 +78,8 @@ struct GateWReduceParams {
     int nblocks;
     int n;
     int stride;
-    int pairs;  // slots come as (hi, lo) pairs
+    int pairs;  // 1: slots come as (hi, lo) pairs; 2: slot b holds hi, lo16 + b * n holds lo (bf16)
+    const uint16_t* lo16;
     // product rule of a fused weight w = wh * we (null: not written):
     // grad_wh = grad_w * we, grad_we = grad_w * wh, wh and we bf16 (n)
     const uint16_t* wh;
@@ -195,6 +197,12 @@ cudaError_t gate_fwd_launch(const GateFwdParams& p, const LaunchCfg& c, cudaStre
 cudaError_t gate_bwd_prepare(int smem_bytes);
 cudaError_t gate_bwd_max_clusters(int cluster, int threads, int smem, int* out);
 cudaError_t gate_bwd_launch(const GateBwdParams& p, const LaunchCfg& c, cudaStream_t s);
+// the one-pass backward (packed layout): G clusters of two CTAs
+cudaError_t gate_bwd_fused_prepare();
+cudaError_t gate_bwd_fused_max_clusters(int* out);
+int gate_bwd_fused_threads();
+int gate_bwd_fused_smem();
+cudaError_t gate_bwd_fused_launch(const GateBwdParams& p, int G, cudaStream_t s);
 cudaError_t gate_wreduce_launch(const GateWReduceParams& p, cudaStream_t s);
 
 cudaError_t fused_weight_launch(const FusedWeightParams& p, cudaStream_t s);

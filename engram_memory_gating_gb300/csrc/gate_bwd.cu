@@ -533,7 +533,8 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
 // grad_weight[i] from the group partials with error-free additions, in a fixed
 // order (bitwise reproducible): warp g of a CTA merges the g-th eighth of the
 // slots for 32 consecutive columns, then warp 0 merges the eight results in
-// ascending g.  pairs: slot 2b = hi, 2b+1 = lo of group b.
+// ascending g.  pairs 1: slot 2b = hi, 2b+1 = lo of group b; pairs 2 (the
+// one-pass backward): slot b = hi, row b of lo16 = lo in bf16.
 constexpr int kRedGroups = 8;
 
 __global__ void __launch_bounds__(32 * kRedGroups) wreduce_kernel(const GateWReduceParams p) {
@@ -546,13 +547,18 @@ __global__ void __launch_bounds__(32 * kRedGroups) wreduce_kernel(const GateWRed
     const int lane = threadIdx.x & 31;
     const int g = threadIdx.x >> 5;
     const int i = blockIdx.x * 32 + lane;
-    const int nslot = p.pairs ? p.nblocks / 2 : p.nblocks;
+    const int nslot = p.pairs == 1 ? p.nblocks / 2 : p.nblocks;
     const int per = (nslot + kRedGroups - 1) / kRedGroups;
     const int b0 = min(nslot, g * per), b1 = min(nslot, b0 + per);
     float hi = 0.f, lo = 0.f;
     if (i < p.n) {
         const float* src = p.partial + i;
-        if (p.pairs) {
+        if (p.pairs == 2) {
+            // hi in fp32 slots, lo as bf16 (one-pass backward)
+            for (int b = b0; b < b1; ++b)
+                cacc_merge(hi, lo, __ldg(src + static_cast<size_t>(b) * p.stride),
+                           __uint_as_float(static_cast<uint32_t>(__ldg(p.lo16 + static_cast<size_t>(b) * p.n + i)) << 16));
+        } else if (p.pairs) {
             int b = b0;
             for (; b + 4 <= b1; b += 4) {
                 float h[4], l[4];

@@ -372,9 +372,10 @@ engram_status_t engram_device_error(uint32_t* flags);
 /* Launch geometry chosen for a call, for tests and benchmarks: CTAs that
  * share one token row (thread-block cluster size, or column slices), threads
  * per CTA, number of such CTA groups, ring stages and dynamic shared memory
- * bytes of the main kernel, and how many of those CTA groups the device runs
- * at once (occupancy).  `op`: 0 gate fwd, 1 gate bwd, 2 gateconv fwd,
- * 3 gateconv bwd.  n0, n1, n2 = (N) for the gate, (M, T, d) for GateConv. */
+ * bytes of the main kernel, how many of those CTA groups the device runs at
+ * once (occupancy), and how many kernels the call launches.  `op`: 0 gate
+ * fwd, 1 gate bwd, 2 gateconv fwd, 3 gateconv bwd.  n0, n1, n2 = (N) for the
+ * gate, (M, T, d) for GateConv. */
 typedef struct {
     int cluster;
     int threads;
@@ -382,6 +383,7 @@ typedef struct {
     int stages;
     int smem_bytes;
     int resident;
+    int kernels;
 } engram_launch_info_t;
 engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
                                    engram_launch_info_t* info);

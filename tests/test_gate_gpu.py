@@ -299,17 +299,27 @@ def test_launch_geometry():
     warps, rows = 8 * f8["clusters"], 4 * 8192
     rpw = -(-rows // warps)
     assert warps * rpw - rows < 8 * rpw
-    # backward: token rows split across a cluster; at most one cluster per two
-    # 64-token blocks, so each cluster's (hi, lo) grad_weight pair fits
-    bwd = eg.engram_launch_info(1, 8192)
-    assert bwd["cluster"] >= 2 and 5120 % (8 * bwd["cluster"]) == 0
-    assert bwd["clusters"] <= 8192 // 128
-    # token groups of at most 256 tokens (their scalars are staged in shared
-    # memory), and their (hi, lo) grad_weight pairs fit the workspace's slots
+    # backward.  Large N: the one-pass kernel (two kernels a call), clusters of
+    # two CTAs (a column half each), each cluster's grad_weight pair (4 x 5120
+    # fp32 hi and bf16 lo words) within the workspace, no more clusters than
+    # run at once.  Otherwise: token rows split across column slices, at
+    # most one group per two 64-token blocks, groups of at most 256 tokens
+    # (their scalars are staged in shared memory).
     for N in (64, 128, 192, 4096, 8192, 11520, 65536, 65728, 1 << 20):
-        groups = eg.engram_launch_info(1, N)["clusters"]
-        assert -(-N // groups) <= 256
-        assert N // 64 < 2 or 2 * groups <= N // 64
+        b = eg.engram_launch_info(1, N)
+        if b["kernels"] == 2:
+            assert b["cluster"] == 2 and b["threads"] >= 640 and b["threads"] % 32 == 0
+            assert 1 <= b["clusters"] <= b["resident"]
+            assert b["clusters"] * 4 * 5120 * (4 + 2) <= eg.engram_gate_bwd_workspace_size(N)
+        else:
+            assert b["kernels"] == 3
+            assert b["cluster"] >= 2 and 5120 % (8 * b["cluster"]) == 0
+            groups = b["clusters"]
+            assert -(-N // groups) <= 256
+            assert N // 64 < 2 or 2 * groups <= N // 64
+    # the full batch takes the one-pass kernel on this device, small batches not
+    assert eg.engram_launch_info(1, 8192)["kernels"] == 2
+    assert eg.engram_launch_info(1, 1024)["kernels"] == 3
 
 
 def test_chained_steps_without_host_sync_match_synchronised_ones():
@@ -321,8 +331,8 @@ def test_chained_steps_without_host_sync_match_synchronised_ones():
     completed data, against the same chain with a device synchronisation after
     every call (no overlap at all).  The kernels are deterministic, so the two
     chains must agree bit for bit.  N = 4096 also spans a full wave of the
-    elementwise kernel's token groups."""
-    for N in (256, 4096):
+    elementwise kernel's token groups; N = 8192 runs the one-pass backward."""
+    for N in (256, 4096, 8192):
         _chain_check(N)
 
 
