@@ -15,7 +15,7 @@
 // halves of a token's row are in the shared memory of two SMs of one TPC.
 //
 // Per CTA, 20 column warps (thread i: columns 4i .. 4i+3 of the half, all four
-// streams) and one scalar warp.  In iteration t the column warps
+// streams) and four scalar warps.  In iteration t the column warps
 //   A  form the partial dgate of each stream of token t + 2 over their columns
 //      from the g and v rows in the ring (products exact in fp32, summed
 //      without rounding loss as (hi, lo) pairs) and reduce them over the warp;
@@ -25,27 +25,29 @@
 //   B  take token t's scalars from the scalar warp and write grad_x, grad_key
 //      and grad_v from the x, key and g rows in the ring, accumulating grad_w
 //      per thread as a (hi, lo) pair.
-// The scalar warp waits for each token's two halves, adds them in rank order
-// (both CTAs form the same total), evaluates the scalars in fp64 (lane s =
-// stream s, as the coefficient kernel does) and hands them to the column
-// warps through shared memory.  The two-token lag between A and B covers the
-// exchange and the fp64 evaluation.
+// Scalar warp k takes the tokens t = k (mod 4): it waits for a token's two
+// halves, adds them in rank order (both CTAs form the same total), evaluates
+// the scalars in fp64 (lane s = stream s, as the coefficient kernel does) and
+// hands them to the column warps through shared memory.  One token's fp64
+// chain on the narrow fp64 pipe takes about as long as a token's column work,
+// hence four warps; the two-token lag between A and B covers the exchange and
+// that chain.
 //
 // Rings (1-D bulk copies): g and v rows of 4 tokens, x and key rows of 2; the
-// last column warp to finish B(t) refills them with tokens t + 4 and t + 2.
+// last column warp to finish B(t) refills them with tokens t + 4 and t + 2
+// (no x and key rows for a token whose saved gates are all 0).
 // The weights of the thread's columns wait in shared memory (each thread
 // reads back only what it wrote), which keeps a thread within the 80
 // registers that 21 warps allow.
-// Slot reuse needs no acknowledgements.  In iteration t a column warp hands
-// in A(t + 2) after its B(t - 1), which waited for the scalars of t - 1.  The
-// scalar warp forms scalars in token order, each after its token's exchange
-// has completed, and an exchange completes only once every column warp of
-// both CTAs has handed the token in (token j in iteration j - 2, after that
-// warp's B(j - 3)).  So at A(t + 2): the exchanges of all tokens up to t - 1
-// are complete, and the hand-in slot of t - 2, which t + 2 reuses, has been
-// read (4 hand-in slots); the scalar warp writes token j only after every
-// column warp's B(j - 3) (4 scalar slots); and the peer's column warps
-// finished B(t - 4), so the peer formed the scalars of t - 4 and has read its
+// Slot reuse needs no acknowledgements.  A column warp hands in token j in
+// iteration j - 2, after its B(j - 3); B(j) waits for the scalars of j, which
+// are formed only after j's exchange has completed, i.e. after every column
+// warp of both CTAs handed j in.  So when a column warp hands in t + 2 it has
+// finished B(t - 2): the exchange of t - 2 is complete and its hand-in slot,
+// which t + 2 reuses, has been read (4 hand-in slots).  A scalar warp writes
+// the slot of token j only after every column warp's B(j - 3) (4 scalar
+// slots, one per scalar warp).  And the peer's column warps, having handed in
+// t - 1 (needed for our B(t - 1)), finished B(t - 6), so the peer has read its
 // exchange slot of t - 6, which t + 2 reuses (8 exchange slots).
 // grad_w: cluster q writes the hi word of its (hi, lo) pair to fp32 slot q
 // and the lo word, renormalised, as bf16 to row q of a second area (1.5 slots
@@ -61,7 +63,8 @@ constexpr int kS = 4;
 constexpr int kD = kGateHidden;           // 5120
 constexpr int kHalf = kD / 2;             // columns per CTA
 constexpr int kColWarps = kHalf / 4 / 32; // 20
-constexpr int kThreads = 32 * (kColWarps + 1);
+constexpr int kScalarWarps = 4;           // warp k forms the scalars of tokens t = k (mod 4)
+constexpr int kThreads = 32 * (kColWarps + kScalarWarps);
 constexpr int kLag = 2;                   // A runs this many tokens ahead of B
 constexpr int kRowB = kHalf * 2;          // bytes of a half row (5120)
 constexpr int kGvStages = 4, kXkStages = 2;
@@ -76,6 +79,7 @@ constexpr int kOffReady = 128;                              // [4] scalars ready
 constexpr int kOffRel = 160;                                // [4] release counters
 constexpr int kOffArr = 176;                                // [4] hand-in counters
 constexpr int kOffSz = 192;                                 // [4] all scalars zero
+constexpr int kOffSkip = 208;                               // [4] all four gates zero (x, key rows not copied)
 constexpr int kOffLocal = 256;                              // [4][20 warps][4] float2
 constexpr int kOffXch = kOffLocal + kHslots * kColWarps * kS * 8;   // [8 slots][2 ranks][4] float2
 constexpr int kOffSc = kOffXch + kXslots * 2 * kS * 8;               // [4][4] float4
@@ -88,6 +92,7 @@ static_assert(kOffSg + kSslots * kS * 4 <= kOffW, "header");
 static_assert(kSmem <= 232448, "shared memory");
 static_assert(kColWarps * 32 * 4 == kHalf, "thread mapping");
 static_assert(kGvStages >= kLag + 2 && kXkStages >= 2, "ring depths");
+static_assert(kSslots == kScalarWarps && kXslots % kScalarWarps == 0, "a scalar warp owns its slots");
 
 EG_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 EG_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -109,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_bwd_fused_kernel(const GateB
     unsigned int* rel = reinterpret_cast<unsigned int*>(smem + kOffRel);
     unsigned int* arrived = reinterpret_cast<unsigned int*>(smem + kOffArr);
     unsigned int* sz = reinterpret_cast<unsigned int*>(smem + kOffSz);
+    unsigned int* skip = reinterpret_cast<unsigned int*>(smem + kOffSkip);
     float2* local = reinterpret_cast<float2*>(smem + kOffLocal);
     float2* xch = reinterpret_cast<float2*>(smem + kOffXch);
     float4* sc = reinterpret_cast<float4*>(smem + kOffSc);
@@ -154,10 +160,16 @@ __global__ void __launch_bounds__(kThreads, 1) gate_bwd_fused_kernel(const GateB
             bulk_g2s(dst + s * kRowB, p.gout + (n * kS + s) * kD + col0, kRowB, &gv_full[b]);
         bulk_g2s(dst + kS * kRowB, p.v + n * (5LL * kD) + col0, kRowB, &gv_full[b]);
     };
-    auto issue_xk = [&](int t) {
+    // x and key rows of token t; none for a token whose four saved gates are
+    // 0 (a masked token needs only grad_out: its scalars are all zero)
+    auto issue_xk = [&](int t, bool rows) {
         const long long n = n0 + t;
         const int b = t % kXkStages;
         unsigned char* dst = xk_ring + b * kXkStageB;
+        if (!rows) {
+            mbar_arrive(&xk_full[b]);
+            return;
+        }
         mbar_arrive_expect_tx(&xk_full[b], static_cast<uint32_t>(kXkStageB));
 #pragma unroll
         for (int s = 0; s < kS; ++s) {
@@ -170,16 +182,22 @@ __global__ void __launch_bounds__(kThreads, 1) gate_bwd_fused_kernel(const GateB
     grid_dep_wait();
     if (tid == 0) {
         for (int t = 0; t < kGvStages && t < ntok; ++t) issue_gv(t);
-        for (int t = 0; t < kXkStages && t < ntok; ++t) issue_xk(t);
+        for (int t = 0; t < kXkStages && t < ntok; ++t) issue_xk(t, true);
     }
     grid_dep_launch();
     bool failed = false;
 
-    if (warp == kColWarps) {
-        // ------------------------------------------------ scalar warp
+    if (warp >= kColWarps) {
+        // ------------------------------------------------ scalar warps
+        const int k = warp - kColWarps;
         float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);   // saved record of (token, lane), one token ahead
-        if (lane < kS && ntok > 0) sv = __ldg(reinterpret_cast<const float4*>(p.saved + (n0 * kS + lane) * 4));
-        for (int t = 0; t < ntok; ++t) {
+        if (lane < kS && k < ntok) sv = __ldg(reinterpret_cast<const float4*>(p.saved + ((n0 + k) * kS + lane) * 4));
+        // saved gate of (token t + kXkStages, lane): whether that token's x and
+        // key rows are copied is published with the scalars of token t, before
+        // the refill that copies them (after every column warp's B(t))
+        float gnext = 0.f;
+        if (lane < kS && k + kXkStages < ntok) gnext = __ldg(p.saved + ((n0 + k + kXkStages) * kS + lane) * 4);
+        for (int t = k; t < ntok; t += kScalarWarps) {
             const int xs = t % kXslots, ss = t % kSslots;
             bool zero = true;
             if (!failed && !mbar_wait(&xbar[xs], static_cast<uint32_t>((t / kXslots) & 1))) failed = true;
@@ -190,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1) gate_bwd_fused_kernel(const GateB
                 cacc_merge(hs, ls, b.x, b.y);
                 const float gate = sv.x;
                 const double dot = sv.y, rx = sv.z, rk = sv.w;
-                if (t + 1 < ntok)
-                    sv = __ldg(reinterpret_cast<const float4*>(p.saved + ((n0 + t + 1) * kS + lane) * 4));
+                if (t + kScalarWarps < ntok)
+                    sv = __ldg(reinterpret_cast<const float4*>(p.saved + ((n0 + t + kScalarWarps) * kS + lane) * 4));
                 const double ad = fabs(dot);
                 double ddot = 0.0;
                 if (ad >= static_cast<double>(p.clamp) && gate != 0.f) {
@@ -217,7 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1) gate_bwd_fused_kernel(const GateB
                 zero = c.x == 0.f && c.y == 0.f && c.z == 0.f && c.w == 0.f;
             }
             zero = __all_sync(kFullMask, zero);
-            if (lane == 0) sz[ss] = zero ? 1u : 0u;
+            const bool masked = __all_sync(kFullMask, lane >= kS || gnext == 0.f);
+            if (lane < kS && t + kXkStages + kScalarWarps < ntok)
+                gnext = __ldg(p.saved + ((n0 + t + kXkStages + kScalarWarps) * kS + lane) * 4);
+            if (lane == 0) {
+                sz[ss] = zero ? 1u : 0u;
+                skip[(t + kXkStages) & 3] = masked ? 1u : 0u;
+            }
             __syncwarp();
             if (lane == 0) {
                 // slot xs is read: arm it for token t + kXslots (whose data may already be arriving)
@@ -371,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_bwd_fused_kernel(const GateB
                     rel[t % kRslots] = 0u;
                     fence_proxy_async();
                     if (t + kGvStages < ntok) issue_gv(t + kGvStages);
-                    if (t + kXkStages < ntok) issue_xk(t + kXkStages);
+                    if (t + kXkStages < ntok) issue_xk(t + kXkStages, skip[(t + kXkStages) & 3] == 0u);
                 }
             }
             stg_cs8(p.gv + n * (5LL * kD) + col, make_uint2(pack2(gv0), pack2(gv1)));
