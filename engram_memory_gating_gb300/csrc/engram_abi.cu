@@ -304,10 +304,11 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
 // scalars kept on chip the whole workspace is slot space: the hi slots, then
 // the lo rows.  G is fixed by N and the device alone (not by the buffer a
 // caller passes), and the call keeps the three-kernel backward when G would
-// leave too many SMs idle (small N: its workspace is small).  Measured at
-// N = 8192: 60 clusters 391 us, 67 clusters 351 us, 76 clusters 314 us, the
-// three kernels 359 us.
-constexpr int kFusedMinClusters = 64;
+// leave too many SMs idle (small N: its workspace is small).  The one-pass
+// kernel's time is close to (N / G) x 2.64 us (measured at N = 4096, 6144 and
+// 8192 with G from 32 to 76), and the three kernels took 236 us at N = 4096:
+// the one pass wins from about 48 clusters (N of about 4400) on.
+constexpr int kFusedMinClusters = 48;
 constexpr size_t kFusedSlotBytes = 4 * kGateD * (4 + 2);
 
 int gate_bwd_fused_groups(DeviceState& st, int64_t N) {
