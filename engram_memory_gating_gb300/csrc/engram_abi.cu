@@ -396,12 +396,26 @@ const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
         // fixed layouts (2048-byte row slots; the backward's with the staged
         // saved scalars of up to kGcBwdMaxRange + 7 streamed tokens); a
         // backward CTA has two warp groups over its column slice
-        g.c.smem = op == 0 ? gateconv_fwd_smem() : gateconv_bwd_smem();
+        g.c.smem = op == 0 ? gateconv_fwd_smem(g.c.threads) : gateconv_bwd_smem();
         if (op == 1) g.c.threads = gateconv_bwd_threads();
     };
     GcGeom g;
     const int C0 = static_cast<int>((d + 1023) / 1024);
     shape(C0, g);
+    if (op == 0 && d > 1024) {
+        // the forward also has 512-thread CTAs (one per SM, up to 2048
+        // columns): half as many CTAs a row, kept when they cover more SMs
+        // (d = 4096: clusters of four 256-thread CTAs fill 144 SMs, pairs
+        // of 512-thread CTAs all 152)
+        const int Cw = static_cast<int>((d + 2047) / 2048);
+        GcGeom gw;
+        shape(Cw, gw);
+        if (gw.c.threads > 256) {
+            const int kn = max_clusters(st, 2, g.c.cluster, g.c.threads, g.c.smem);
+            const int kw = max_clusters(st, 2, gw.c.cluster, gw.c.threads, gw.c.smem);
+            if (2 * kw * Cw > kn * C0) g = gw;
+        }
+    }
     if (op == 1) {
         const int p2 = C0 <= 1 ? 1 : C0 <= 2 ? 2 : C0 <= 4 ? 4 : 8;
         const int64_t cols = 4 * static_cast<int64_t>(round_up(static_cast<int>((d / 4 + p2 - 1) / p2), 32));

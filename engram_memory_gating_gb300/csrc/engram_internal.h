@@ -211,7 +211,7 @@ cudaError_t fused_weight_bwd_launch(const FusedWeightParams& p, cudaStream_t s);
 cudaError_t decode_prepare();
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t s);
 
-int gateconv_fwd_smem();  // dynamic shared memory of the forward kernel (fixed layout)
+int gateconv_fwd_smem(int threads);  // dynamic shared memory of the forward kernel of that CTA size (fixed layout)
 int gateconv_bwd_smem();  // dynamic shared memory of the backward kernel (fixed layout)
 int gateconv_bwd_threads();  // threads of a backward CTA (two warp groups over one column slice)
 cudaError_t gateconv_fwd_prepare(int smem_bytes);

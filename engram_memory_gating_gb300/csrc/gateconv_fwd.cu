@@ -33,27 +33,37 @@ namespace {
 
 using gc::kChunk;
 
-// Shared memory: a fixed layout, so that every ring address of a token is a
-// chunk base plus an immediate.  Each row slot is 2048 bytes (the widest
-// column slice, 1024 columns); a narrower slice leaves the slot's tail zero,
-// which the threads without columns read.
+// Two CTA shapes: kW = 8 warps (at most 1024 columns, two CTAs per SM) and
+// kW = 16 warps (at most 2048 columns, one CTA per SM, for rows that then
+// split over fewer CTAs).  Shared memory: a fixed layout, so that every ring
+// address of a token is a chunk base plus an immediate.  Each row slot holds
+// the widest column slice of the shape (8 kW 32 bytes); a narrower slice
+// leaves the slot's tail zero, which the threads without columns read.
 constexpr int kRows = 3;                         // H, k, v
-constexpr int kPitch = 2048;                     // bytes per row slot
-constexpr int kStageBytes = kRows * kPitch;
 constexpr int kStages = gc::kStages;             // 16 one-token stages
 constexpr int kSlots = kStages / kChunk;         // 4 chunk slots of the ring
 constexpr int kOffFull = 0;                      // [kSlots] chunk-slot mbarriers
 constexpr int kOffXbar = 128;                    // [2] cluster-exchange mbarriers
 constexpr int kOffRel = 160;                     // [kStages] stage release counters
 constexpr int kOffArr = 224;                     // [2] per-chunk arrival counters
-constexpr int kOffLocal = 256;                   // [2][8 warps][16] warp totals
-constexpr int kOffTot = kOffLocal + 2 * 8 * gc::kVals * 4;   // [2][8 ranks][16] CTA totals
-constexpr int kRingOff = kOffTot + 2 * 8 * gc::kVals * 4;
-constexpr int kSmem = kRingOff + kStages * kStageBytes;
-static_assert(kRingOff % 128 == 0, "ring alignment");
+constexpr int kOffLocal = 256;                   // [2][kW warps][16] warp totals
+template <int kW>
+struct FwdShape {
+    static constexpr int kPitch = 256 * kW;      // bytes per row slot
+    static constexpr int kStageBytes = kRows * kPitch;
+    static constexpr int kOffTot = kOffLocal + 2 * kW * gc::kVals * 4;   // [2][8 ranks][16] CTA totals
+    static constexpr int kRingOff = (kOffTot + 2 * 8 * gc::kVals * 4 + 127) / 128 * 128;
+    static constexpr int kSmem = kRingOff + kStages * kStageBytes;
+    static_assert(kSmem <= 232448 / (kW == 8 ? 2 : 1) - 1024, "shared memory of the CTAs an SM holds");
+};
 static_assert(kStages % kChunk == 0, "a chunk must not wrap around the ring");
 
-__global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const GateConvFwdParams p) {
+template <int kW>
+__global__ void __launch_bounds__(32 * kW, kW == 8 ? 2 : 1) gateconv_fwd_kernel(const GateConvFwdParams p) {
+    constexpr int kPitch = FwdShape<kW>::kPitch;
+    constexpr int kStageBytes = FwdShape<kW>::kStageBytes;
+    constexpr int kOffTot = FwdShape<kW>::kOffTot;
+    constexpr int kRingOff = FwdShape<kW>::kRingOff;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffFull);
     uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + kOffXbar);
@@ -278,7 +288,7 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
         // warp order and sends the CTA's total into slot `rank` of every CTA of
         // the cluster (st.async, completing on that CTA's exchange barrier)
         if (kA) {
-            local[(buf * 8 + warp) * gc::kVals + (lane >> 1)] = val;
+            local[(buf * kW + warp) * gc::kVals + (lane >> 1)] = val;
             __syncwarp();
             unsigned int last = 0u;
             if (lane == 0) {
@@ -292,7 +302,7 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
             last = __shfl_sync(kFullMask, last, 0);
             if (last) {
                 __syncwarp();   // the other warps' totals, seen by lane 0, to every lane
-                const float* lp = local + buf * 8 * gc::kVals + (lane & 15);
+                const float* lp = local + buf * kW * gc::kVals + (lane & 15);
                 float cta = 0.f;
                 for (int w = 0; w < nw; ++w) cta += lp[w * gc::kVals];
                 const uint32_t dst = smem_addr(tot + (buf * 8 + static_cast<int>(rank)) * gc::kVals + (lane & 15));
@@ -331,11 +341,13 @@ __global__ void __launch_bounds__(gc::kThreads, 2) gateconv_fwd_kernel(const Gat
 
 }  // namespace
 
-int gateconv_fwd_smem() { return kSmem; }
+int gateconv_fwd_smem(int threads) { return threads > 256 ? FwdShape<16>::kSmem : FwdShape<8>::kSmem; }
 
 cudaError_t gateconv_fwd_prepare(int smem_bytes) {
     if (smem_bytes <= 0) return cudaSuccess;
-    return cudaFuncSetAttribute(gateconv_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    cudaError_t e = cudaFuncSetAttribute(gateconv_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gateconv_fwd_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
 cudaError_t gateconv_fwd_max_clusters(int cluster, int threads, int smem, int* out) {
@@ -350,7 +362,8 @@ cudaError_t gateconv_fwd_max_clusters(int cluster, int threads, int smem, int* o
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(out, gateconv_fwd_kernel, &cfg);
+    return threads > 256 ? cudaOccupancyMaxActiveClusters(out, gateconv_fwd_kernel<16>, &cfg)
+                         : cudaOccupancyMaxActiveClusters(out, gateconv_fwd_kernel<8>, &cfg);
 }
 
 cudaError_t gateconv_fwd_launch(const GateConvFwdParams& p, const LaunchCfg& c, cudaStream_t s) {
@@ -366,7 +379,8 @@ cudaError_t gateconv_fwd_launch(const GateConvFwdParams& p, const LaunchCfg& c, 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gateconv_fwd_kernel, p);
+    return c.threads > 256 ? cudaLaunchKernelEx(&cfg, gateconv_fwd_kernel<16>, p)
+                           : cudaLaunchKernelEx(&cfg, gateconv_fwd_kernel<8>, p);
 }
 
 }  // namespace eg

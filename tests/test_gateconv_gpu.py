@@ -203,17 +203,19 @@ def test_full_config_m8_t8192_d7168():
 
 
 def test_launch_geometry():
-    """C CTAs per row with ceil(d/1024) <= C <= 8; forward CTAs of at most 256
-    threads (4 columns each), every CTA's column slice non-empty; backward CTAs
-    of 512 threads (two warp groups of 256 over a slice of at most 1024
-    columns); at least one cluster per row."""
+    """C CTAs per row with ceil(d/1024) <= C <= 8 (forward: ceil(d/2048) <= C
+    for its 512-thread CTAs); forward CTAs of at most 512 threads (4 columns
+    each), every CTA's column slice non-empty; backward CTAs of 512 threads
+    (two warp groups of 256 over a slice of at most 1024 columns); at least one
+    cluster per row."""
     for (M, T, d) in ((4, 4096, 4096), (8, 8192, 7168), (2, 45, 1032), (1, 40, 8192), (1, 5, 64)):
         for op in (2, 3):
             info = eg.engram_launch_info(op, M, T, d)
             C = info["cluster"]
-            assert -(-d // 1024) <= C <= 8
+            assert -(-d // (2048 if op == 2 else 1024)) <= C <= 8
             if op == 2:
-                assert info["threads"] % 32 == 0 and info["threads"] <= 256
+                assert info["threads"] % 32 == 0 and info["threads"] <= 512
+                assert info["threads"] <= 256 or C == -(-d // 2048)
                 assert 4 * info["threads"] * C >= d > 4 * info["threads"] * (C - 1)
             else:
                 assert info["threads"] == 512
