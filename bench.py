@@ -55,6 +55,14 @@ def source_hash(files):
     return h.hexdigest()[:16]
 
 
+def scaled_traffic(profile_md, sources, factor):
+    """A committed summary's per-launch DRAM bytes for a smaller case of the
+    same kernels, scaled to this launch by the units processed (the kernels'
+    traffic grows in proportion to tokens or rows)."""
+    t = profile_traffic(profile_md, sources)
+    return None if t is None else int(round(t * factor))
+
+
 def profile_traffic(profile_md, sources):
     """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
     the current kernel sources (the kernel's file and the headers it
@@ -188,6 +196,11 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
     time_region(torch, g.replay, 3, s)
     ms = time_region(torch, g.replay, 10, s)
     ops["gate_fwd_N262144"] = op_entry(ms, N * FWD_BYTES_PER_TOKEN + FWD_FIXED, peak)
+    csrc = "engram_memory_gating_gb300/csrc/"
+    hdrs = [csrc + "common.cuh", csrc + "engram_internal.h"]
+    ops["gate_fwd_N262144"]["traffic"] = scaled_traffic(
+        "gate_fwd_row_n36864.md", [csrc + "gate_fwd.cu"] + hdrs, N / 36864)
+    ops["gate_fwd_N262144"]["traffic_from"] = "N = 36,864 capture of the same kernel and input recipe, x 262144/36864"
     del inp, out, saved, g
     torch.cuda.empty_cache()
     # backward past the 8192-token cap: N = 65536, mask Bernoulli(0.9)
@@ -205,6 +218,9 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
     time_region(torch, g.replay, 3, s)
     ms = time_region(torch, g.replay, 10, s)
     ops["gate_bwd_N65536"] = op_entry(ms, N * BWD_BYTES_PER_TOKEN + BWD_FIXED, peak)
+    ops["gate_bwd_N65536"]["traffic"] = scaled_traffic(
+        "gate_bwd_n16384.md", [csrc + "gate_bwd.cu", csrc + "gate_bwd_fused.cu"] + hdrs, N / 16384)
+    ops["gate_bwd_N65536"]["traffic_from"] = "N = 16,384 capture of the same kernels and input recipe, x 4"
     del inp, saved, gx, gkv, gw, ws, g
     torch.cuda.empty_cache()
     # separate-tensor gate (tile-kernels layout), N = 8192, H = 4096
@@ -227,6 +243,10 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
                                                N * (26 * H + 64) + 16 * H, peak)
     ops["gate_sep_bwd_N8192_H4096"] = op_entry(time_region(torch, gb.replay, 10, s),
                                                N * (44 * H + 64) + 16 * H + (N // 64) * 16 * H, peak)
+    ops["gate_sep_fwd_N8192_H4096"]["traffic"] = profile_traffic(
+        "gate_sep_fwd_n8192_h4096.md", [csrc + "gate_fwd.cu"] + hdrs)
+    ops["gate_sep_bwd_N8192_H4096"]["traffic"] = profile_traffic(
+        "gate_sep_bwd_n8192_h4096.md", [csrc + "gate_bwd.cu"] + hdrs)
     del inp, k, v, out, sv, gx, gk, gv, gwp, ws, gf, gb
     torch.cuda.empty_cache()
     # GateConv decode step, B = 8, d_mem = 1024, d = 4096, full cache of 16, w = 4, dilation 3,
@@ -300,13 +320,18 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
                                       tok * (10 * d + 16) + 24 * d, peak)
         ops[name + "_bwd"] = op_entry(time_region(torch, gb.replay, 10, s),
                                       tok * (16 * d + 16) + 48 * d, peak)
-        if M == 4:  # DRAM bytes per launch from the committed ncu summaries
-            csrc = "engram_memory_gating_gb300/csrc/"
-            common = [csrc + "gateconv_xch.cuh", csrc + "common.cuh", csrc + "engram_internal.h"]
-            ops[name + "_fwd"]["traffic"] = profile_traffic(
-                "gateconv_fwd_m4_t4096_d4096.md", [csrc + "gateconv_fwd.cu"] + common)
-            ops[name + "_bwd"]["traffic"] = profile_traffic(
-                "gateconv_bwd_m4_t4096_d4096.md", [csrc + "gateconv_bwd.cu"] + common)
+        # DRAM bytes per launch from the committed ncu summaries (M8: the
+        # M = 1 capture of the same kernels, scaled by the rows)
+        csrc = "engram_memory_gating_gb300/csrc/"
+        common = [csrc + "gateconv_xch.cuh", csrc + "common.cuh", csrc + "engram_internal.h"]
+        tag, factor = ("m4_t4096_d4096", 1.0) if M == 4 else ("m1_t8192_d7168", float(M))
+        ops[name + "_fwd"]["traffic"] = scaled_traffic(
+            f"gateconv_fwd_{tag}.md", [csrc + "gateconv_fwd.cu"] + common, factor)
+        ops[name + "_bwd"]["traffic"] = scaled_traffic(
+            f"gateconv_bwd_{tag}.md", [csrc + "gateconv_bwd.cu"] + common, factor)
+        if M != 4:
+            ops[name + "_fwd"]["traffic_from"] = ops[name + "_bwd"]["traffic_from"] = \
+                f"M = 1 capture of the same kernels, x {M}"
         del ci, res, grads, ws, gf, gb
         torch.cuda.empty_cache()
     return ops
@@ -391,26 +416,52 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-GC_WORKLOADS = {"m4": (4, 4096, 4096, 1.0, 1.0), "m8": (8, 8192, 7168, 10.0, 0.1 ** 0.5)}
+GC_WORKLOADS = {"m4": (4, 4096, 4096, 1.0, 1.0), "m8": (8, 8192, 7168, 10.0, 0.1 ** 0.5),
+                "m1": (1, 8192, 7168, 10.0, 0.1 ** 0.5)}
 
 
 def run_single_op(args):
     """One entry point alone, `warmup` + `steps` plain calls on one stream, for
-    profiler captures: the gate at the step's N = 8192 inputs, GateConv at
-    --gc-workload (m4: M=4, T=4096, d=4096; m8: M=8, T=8192, d=7168).  Prints
-    the mean event-timed call.  Launches per call: gate_fwd 1, gate_bwd 3,
-    gateconv_fwd 1, gateconv_bwd 4, decode 2 (B = 8, d_mem = 1024, d = 4096,
-    a full cache of 16, w = 4, dilation 3; back to back, weights L2-warm)."""
+    profiler captures: the gate at --n tokens (default the step's 8192) with the
+    step's input recipe, or the forward sweep's with --sweep-inputs; the
+    separate-tensor gate at --n tokens, H = 4096; GateConv at --gc-workload
+    (m4: M=4, T=4096, d=4096; m8: M=8, T=8192, d=7168; m1: M=1, T=8192,
+    d=7168); decode at B = 8, d_mem = 1024, d = 4096, a full cache of 16, w = 4,
+    dilation 3 (back to back, weights L2-warm).  Prints the mean event-timed
+    call.  Launches per call: gate_fwd 1, gate_bwd 2 (the one-pass kernel and
+    the merge) or 3 (coefficients, elementwise, merge), gate_sep_fwd 1,
+    gate_sep_bwd 2, gateconv_fwd 1, gateconv_bwd 4, decode 2."""
     import torch
     import engram_memory_gating_gb300 as eg
     from engram_memory_gating_gb300 import inputs as inputs_mod
     s = torch.cuda.Stream()
-    if args.op.startswith("gate_"):
-        inp = inputs_mod.gate_inputs(N_TOK, 1, device="cuda", mask="bern0.9")
+    if args.op.startswith("gate_sep_"):
+        N, H = args.n, 4096
+        inp = inputs_mod.gate_inputs(N, 105, device="cuda", d=H)
+        k = inp["kv"][:, :4 * H].reshape(N, 4, H).contiguous()
+        v = inp["kv"][:, 4 * H:].contiguous()
+        del inp["kv"]
+        out = torch.empty_like(inp["x"])
+        sv = [torch.empty((N, 4), device="cuda") for _ in range(4)]
+        eg.engram_gate_sep_fwd(inp["x"], k, v, inp["weight"], out, *sv, stream=s)
+        gx, gk, gv = torch.empty_like(inp["x"]), torch.empty_like(k), torch.empty_like(v)
+        gwp = torch.empty(((N + 63) // 64, 4, H), device="cuda")
+        ws = torch.empty(eg.engram_gate_sep_bwd_workspace_size(N), device="cuda", dtype=torch.uint8)
+        if args.op == "gate_sep_fwd":
+            fn = lambda: eg.engram_gate_sep_fwd(inp["x"], k, v, inp["weight"], out, *sv, stream=s)
+        else:
+            fn = lambda: eg.engram_gate_sep_bwd(inp["grad_out"], inp["x"], k, v, inp["weight"], *sv, gx, gk,
+                                                gv, gwp, ws, stream=s)
+    elif args.op.startswith("gate_"):
+        N = args.n
+        if args.sweep_inputs:
+            inp = inputs_mod.gate_inputs(N, 103, device="cuda", mask="bern0.5", sigma="loguniform")
+        else:
+            inp = inputs_mod.gate_inputs(N, 1, device="cuda", mask="bern0.9")
         out, saved = eg.gate_forward(inp["x"], inp["kv"], inp["weight"], inp["mask"])
         gx, gkv, gw = (torch.empty_like(inp["x"]), torch.empty_like(inp["kv"]),
                        torch.empty_like(inp["weight"]))
-        ws = torch.empty(eg.engram_gate_bwd_workspace_size(N_TOK), device="cuda", dtype=torch.uint8)
+        ws = torch.empty(eg.engram_gate_bwd_workspace_size(N), device="cuda", dtype=torch.uint8)
         if args.op == "gate_fwd":
             fn = lambda: eg.engram_gate_fwd(inp["x"], inp["kv"], inp["weight"], inp["mask"], out,
                                             saved, stream=s)
@@ -455,9 +506,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-op sweep")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
-    ap.add_argument("--op", choices=["step", "gate_fwd", "gate_bwd", "gateconv_fwd", "gateconv_bwd", "decode"],
+    ap.add_argument("--op", choices=["step", "gate_fwd", "gate_bwd", "gate_sep_fwd", "gate_sep_bwd", "gateconv_fwd",
+                                     "gateconv_bwd", "decode"],
                     default="step", help="time one entry point alone (profiler captures)")
     ap.add_argument("--gc-workload", choices=sorted(GC_WORKLOADS), default="m4")
+    ap.add_argument("--n", type=int, default=N_TOK, help="tokens of the gate ops (--op)")
+    ap.add_argument("--sweep-inputs", action="store_true",
+                    help="--op gate_*: the forward sweep's inputs (LogUniform row scales, mask Bernoulli(0.5))")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
