@@ -184,18 +184,41 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
     larger than L2 (no flush needed)."""
     ops = {}
     s = stream
-    # forward sweep, N = 262144, per-token sigma ~ LogUniform(1e-2, 1e2), mask Bernoulli(0.5)
-    N = 262144
-    inp = inputs_mod.gate_inputs(N, 103, device="cuda", mask="bern0.5", sigma="loguniform",
-                                 with_grad=False)
+    # the smallest configuration: forward + backward of N = 64 tokens (mask all
+    # true), one CUDA graph of both calls, latency per call pair
+    N = 64
+    inp = inputs_mod.gate_inputs(N, 0, device="cuda", mask="all")
     out = torch.empty_like(inp["x"])
     saved = torch.empty((N, 4, 4), device="cuda", dtype=torch.float32)
-    fn = lambda: eg.engram_gate_fwd(inp["x"], inp["kv"], inp["weight"], inp["mask"], out, saved,
-                                    stream=s)
-    g = graph_of(torch, fn, s)
-    time_region(torch, g.replay, 3, s)
-    ms = time_region(torch, g.replay, 10, s)
-    ops["gate_fwd_N262144"] = op_entry(ms, N * FWD_BYTES_PER_TOKEN + FWD_FIXED, peak)
+    gx, gkv, gw = torch.empty_like(inp["x"]), torch.empty_like(inp["kv"]), torch.empty_like(inp["weight"])
+    ws = torch.empty(eg.engram_gate_bwd_workspace_size(N), device="cuda", dtype=torch.uint8)
+
+    def small_step():
+        eg.engram_gate_fwd(inp["x"], inp["kv"], inp["weight"], inp["mask"], out, saved, stream=s)
+        eg.engram_gate_bwd(inp["x"], inp["kv"], inp["weight"], saved, inp["grad_out"], gx, gkv, gw, ws, stream=s)
+
+    g = graph_of(torch, small_step, s)
+    time_region(torch, g.replay, 20, s)
+    ms = time_region(torch, g.replay, 200, s)
+    ops["gate_step_N64"] = op_entry(ms, N * (FWD_BYTES_PER_TOKEN + BWD_BYTES_PER_TOKEN) + FWD_FIXED + BWD_FIXED, peak)
+    ops["gate_step_N64"]["us"] = round(1000 * ms, 2)
+    del inp, out, saved, gx, gkv, gw, ws, g
+    # forward sweep, N in {4096, 65536, 262144}, per-token sigma ~ LogUniform(1e-2, 1e2),
+    # mask Bernoulli(0.5), CUDA-graph replays
+    for N in (4096, 65536, 262144):
+        inp = inputs_mod.gate_inputs(N, 103, device="cuda", mask="bern0.5", sigma="loguniform",
+                                     with_grad=False)
+        out = torch.empty_like(inp["x"])
+        saved = torch.empty((N, 4, 4), device="cuda", dtype=torch.float32)
+        fn = lambda: eg.engram_gate_fwd(inp["x"], inp["kv"], inp["weight"], inp["mask"], out, saved,
+                                        stream=s)
+        g = graph_of(torch, fn, s)
+        time_region(torch, g.replay, 3, s)
+        ms = time_region(torch, g.replay, 10 if N > 4096 else 40, s)
+        ops[f"gate_fwd_N{N}"] = op_entry(ms, N * FWD_BYTES_PER_TOKEN + FWD_FIXED, peak)
+        if N != 262144:
+            del inp, out, saved, g
+            torch.cuda.empty_cache()
     csrc = "engram_memory_gating_gb300/csrc/"
     hdrs = [csrc + "common.cuh", csrc + "engram_internal.h"]
     ops["gate_fwd_N262144"]["traffic"] = scaled_traffic(

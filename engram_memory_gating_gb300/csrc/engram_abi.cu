@@ -257,15 +257,19 @@ bool gate_fwd_cfg(DeviceState& st, int64_t N, LaunchCfg& c) {
 // workspace's block slots (a single-block problem uses one slot).
 bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg& c, int& ncols,
                   int& group_tokens) {
-    // slices of 64 column groups: 8 warps x (8 groups x 4 streams)
+    // slices of 64 column groups: 8 warps x (8 groups x 4 streams); a warp
+    // covers 64 columns of the four streams, a slice ncols / 64 warps
     ncols = 512;
-    const int C = static_cast<int>((d + ncols - 1) / ncols);
+    int C = static_cast<int>((d + ncols - 1) / ncols);
     c.cluster = 1;
     c.threads = 256;
     c.stages = kGateBwdStages;
     // barriers, (packed layout, blocks == false) the token group's scalars
     // (64 B a token) and zero flags, the ring
-    c.smem = 256 + (blocks ? 0 : kGateBwdTableTokens * (64 + 1)) + c.stages * (12 * ncols * 2 + 128);
+    auto smem_of = [&](int nc) {
+        return 256 + (blocks ? 0 : kGateBwdTableTokens * (64 + 1)) + c.stages * (12 * nc * 2 + 128);
+    };
+    c.smem = smem_of(ncols);
     if (max_clusters(st, 1, 1, c.threads, c.smem) <= 0) return false;
     const int mc1 = max_clusters(st, 1, 1, 256, 0);
     if (mc1 <= 0) return false;
@@ -289,8 +293,23 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
         if (groups < least) groups = least;
         group_tokens = static_cast<int>((N + groups - 1) / groups);
     }
-    c.clusters = C;
     c.grid_y = static_cast<int>((N + group_tokens - 1) / group_tokens);
+    if (!blocks) {
+        // short batches have few token groups (one per two 64-token blocks of
+        // the workspace): narrower column slices spread them over the SMs, and
+        // a narrower slice's stages are small, so the ring deepens with it (a
+        // group streams its tokens one after another; at N = 64 a single
+        // group on 10 CTAs of a 4-stage ring took 62 us)
+        while (ncols > 64 && static_cast<int64_t>(C) * c.grid_y < st.sm_count) {
+            ncols /= 2;
+            C = static_cast<int>((d + ncols - 1) / ncols);
+            c.threads = ncols / 2;
+            c.stages = std::min(kMaxStages, 2 * c.stages);
+            c.smem = smem_of(ncols);
+        }
+        if (max_clusters(st, 1, 1, c.threads, c.smem) <= 0) return false;
+    }
+    c.clusters = C;
     // coefficient kernel: a warp pair per token (packed, d = 5120) or a warp per
     // token (runtime d, the separate-tensor layout)
     const int64_t need1 = blocks ? (N + 7) / 8 : (N + 3) / 4;
