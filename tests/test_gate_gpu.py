@@ -217,6 +217,21 @@ def test_fwd_bwd_full_batch_8192(seed):
     assert torch.all(gkv.cpu()[m][:, :4 * D].float() == 0)
 
 
+@pytest.mark.parametrize("N,kernels", [(4352, 3), (4608, 2)])
+def test_bwd_either_side_of_the_one_pass_threshold(N, kernels):
+    """The backward takes the one-pass kernel from 48 clusters on (the
+    workspace of N = 4608 holds 50: token ranges of 92 and 93 tokens) and the
+    three kernels below (N = 4352 holds 47).  Both against the oracle, every
+    element, mask Bernoulli(0.9)."""
+    assert eg.engram_launch_info(1, N)["kernels"] == kernels
+    inp = gate_inputs(N, 9, device=DEV, mask="bern0.9")
+    _, saved = eg.gate_forward(inp["x"], inp["kv"], inp["weight"], inp["mask"])
+    gx, gkv, gw = eg.gate_backward(inp["x"], inp["kv"], inp["weight"], saved, inp["grad_out"])
+    torch.cuda.synchronize()
+    host = {k: v.cpu() for k, v in inp.items()}
+    check_bwd(gx, gkv, gw, oracle_bwd(host, saved.double().cpu().numpy()))
+
+
 def test_bwd_long_batch():
     """N = 65,728 (1,027 blocks of 64: an odd count, so three-block token
     groups and a one-block last group), past the cuDNN page's 8192 cap.  The
