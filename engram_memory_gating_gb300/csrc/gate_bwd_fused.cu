@@ -22,7 +22,7 @@
 //      the last warp of the CTA to hand in adds the 20 warp totals in warp
 //      order and sends the CTA's four pairs into slot `rank` of both CTAs of
 //      the cluster (st.async, completing on that CTA's exchange mbarrier);
-//   B  take token t's scalars from the scalar warp and write grad_x, grad_key
+//   B  take token t's scalars from its scalar warp and write grad_x, grad_key
 //      and grad_v from the x, key and g rows in the ring, accumulating grad_w
 //      per thread as a (hi, lo) pair.
 // Scalar warp k takes the tokens t = k (mod 4): it waits for a token's two
@@ -38,7 +38,7 @@
 // (no x and key rows for a token whose saved gates are all 0).
 // The weights of the thread's columns wait in shared memory (each thread
 // reads back only what it wrote), which keeps a thread within the 80
-// registers that 21 warps allow.
+// registers that 24 warps (six per scheduler) allow.
 // Slot reuse needs no acknowledgements.  A column warp hands in token j in
 // iteration j - 2, after its B(j - 3); B(j) waits for the scalars of j, which
 // are formed only after j's exchange has completed, i.e. after every column
@@ -47,8 +47,9 @@
 // which t + 2 reuses, has been read (4 hand-in slots).  A scalar warp writes
 // the slot of token j only after every column warp's B(j - 3) (4 scalar
 // slots, one per scalar warp).  And the peer's column warps, having handed in
-// t - 1 (needed for our B(t - 1)), finished B(t - 6), so the peer has read its
-// exchange slot of t - 6, which t + 2 reuses (8 exchange slots).
+// t - 1 (needed for our B(t - 1)), finished B(t - 4) and so B(t - 6): the peer
+// has formed the scalars of t - 6 and read its exchange slot, which t + 2
+// reuses (8 exchange slots).
 // grad_w: cluster q writes the hi word of its (hi, lo) pair to fp32 slot q
 // and the lo word, renormalised, as bf16 to row q of a second area (1.5 slots
 // a cluster, so that one cluster per TPC fits the workspace); wreduce_kernel
