@@ -294,19 +294,22 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
         group_tokens = static_cast<int>((N + groups - 1) / groups);
     }
     c.grid_y = static_cast<int>((N + group_tokens - 1) / group_tokens);
-    if (!blocks) {
-        // short batches have few token groups (one per two 64-token blocks of
-        // the workspace): narrower column slices spread them over the SMs, and
-        // a narrower slice's stages are small, so the ring deepens with it (a
-        // group streams its tokens one after another; at N = 64 a single
-        // group on 10 CTAs of a 4-stage ring took 62 us)
-        while (ncols > 64 && static_cast<int64_t>(C) * c.grid_y < st.sm_count) {
-            ncols /= 2;
-            C = static_cast<int>((d + ncols - 1) / ncols);
-            c.threads = ncols / 2;
-            c.stages = std::min(kMaxStages, 2 * c.stages);
-            c.smem = smem_of(ncols);
-        }
+    c.token_split = 0;
+    static_assert(kMaxStages % 8 == 0, "token mode: a stage's tokens go to one of 8 warps");
+    if (!blocks && 10LL * c.grid_y < 8LL * st.sm_count) {
+        // up to a few thousand tokens the groups (one per two 64-token blocks
+        // of the workspace) are few and each is walked token by token: there
+        // the CTAs take 64-column slices and their 8 warps split the group's
+        // tokens, with a ring of 16 stages (a multiple of the warps, so each
+        // stage has one consumer).  Measured (backward alone): N = 64 93.5 ->
+        // 25.0 us, 320 217.7 -> 51.1, 1024 265.8 -> 87.4, 2048 277.3 -> 147.9,
+        // 4096 292.5 -> 266.9.  Larger batches take the one-pass kernel.
+        ncols = 64;
+        C = static_cast<int>((d + ncols - 1) / ncols);
+        c.threads = 256;
+        c.stages = kMaxStages;
+        c.smem = smem_of(ncols);
+        c.token_split = 1;
         if (max_clusters(st, 1, 1, c.threads, c.smem) <= 0) return false;
     }
     c.clusters = C;
@@ -663,6 +666,7 @@ engram_status_t gate_bwd_impl(const void* x, const void* kv, const float* weight
     p.stages = c.stages;
     p.group_tokens = group_tokens;
     p.pair_slots = (N / 64) >= 2 ? 1 : 0;
+    p.token_split = c.token_split;
     p.packed = 1;
     p.clamp = ENGRAM_GATE_CLAMP;
     engram_status_t s = launch_status(gate_bwd_launch(p, c, stream));

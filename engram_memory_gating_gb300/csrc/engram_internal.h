@@ -68,6 +68,7 @@ struct GateBwdParams {
     int stages;
     int group_tokens; // tokens per token group (one grad_weight partial each)
     int pair_slots;   // 1: group g writes (hi, lo) to slots 2g, 2g+1
+    int token_split;  // 1: a CTA's warps all cover its 64 columns and split its group's tokens
     int packed;       // 1: packed KV / grad_kv and saved records, d = 5120
     float clamp;
 };
@@ -186,6 +187,7 @@ struct LaunchCfg {
     int smem;
     int grid_y;     // second grid dimension (1 unless stated)
     int aux_blocks; // CTAs of a preceding helper kernel, if any
+    int token_split;  // gate backward: the warps of a CTA split its tokens (see GateBwdParams)
 };
 
 // Kernel launchers (defined next to their kernels).  Each returns the launch

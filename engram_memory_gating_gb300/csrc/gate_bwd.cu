@@ -296,7 +296,14 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     const int lane = tid & 31;
     const int W = blockDim.x >> 5;
     const int s = lane >> 3;                               // stream
-    const int cg = (tid >> 5) * 8 + (lane & 7);           // column group in the slice
+    // Column mode: warp w owns column groups 8w .. 8w+7 and every warp takes
+    // every token of the group.  Token mode (p.token_split, a 64-column
+    // slice): every warp owns the slice's 8 column groups and the warps split
+    // the group's tokens (warp w: tokens w, w + W, ...), so that a short
+    // group's tokens are not walked one after another by a single warp.
+    const bool tsplit = p.token_split != 0;
+    const int warp = tid >> 5;
+    const int cg = (tsplit ? 0 : warp * 8) + (lane & 7);  // column group in the slice
     const int d = kPacked ? kGateHidden : p.d;
     const long long key_ts = kPacked ? 5LL * kGateHidden : p.key_ts;
     const long long gkey_ts = kPacked ? 5LL * kGateHidden : p.gkey_ts;
@@ -411,9 +418,11 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
 #pragma unroll
     for (int e = 0; e < 4; ++e) phi[e] = plo[e] = make_float2(0.f, 0.f);
 
-    int st = 0;
-    uint32_t phase = 0;
-    for (int j = 0; j < ntok; ++j) {
+    // token mode: a stage's tokens (j, j + stages, ...) all go to one warp,
+    // as stages is a multiple of W; it refills the stage with its next token
+    for (int j = tsplit ? warp : 0; j < ntok; j += tsplit ? W : 1) {
+        const int st = j % stages;
+        const uint32_t phase = static_cast<uint32_t>((j / stages) & 1);
         const long long n = t0 + j;
         if (!failed && !mbar_wait(&full[st], phase)) failed = true;
         const unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
@@ -467,7 +476,7 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
         __syncwarp();
         if (lane == 0) {
             __threadfence_block();
-            if (atomicAdd(&released[st], 1u) == static_cast<unsigned int>(W - 1)) {
+            if (atomicAdd(&released[st], 1u) == static_cast<unsigned int>(tsplit ? 0 : W - 1)) {
                 released[st] = 0u;
                 if (j + stages < ntok) {
                     fence_proxy_async();
@@ -475,10 +484,6 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
                     issue_gates(j + stages, st);
                 }
             }
-        }
-        if (++st == stages) {
-            st = 0;
-            phase ^= 1u;
         }
         // grad_v = (g0 + g1) + (g2 + g3) over the four streams' lanes
 #pragma unroll
@@ -497,9 +502,33 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
                        make_uint4(pack2(gv[0]), pack2(gv[1]), pack2(gv[2]), pack2(gv[3])));
         }
     }
+    // token mode: the warps' pairs for the same columns are merged in warp
+    // order (every issued copy has been consumed, so the ring is free)
+    if (tsplit) {
+        __syncthreads();
+        float* mine = reinterpret_cast<float*>(ring) + (warp * 32 + lane) * 16;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            mine[4 * e + 0] = phi[e].x;
+            mine[4 * e + 1] = phi[e].y;
+            mine[4 * e + 2] = plo[e].x;
+            mine[4 * e + 3] = plo[e].y;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            for (int w = 1; w < W; ++w) {
+                const float* o = reinterpret_cast<const float*>(ring) + (w * 32 + lane) * 16;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    cacc_merge(phi[e].x, plo[e].x, o[4 * e + 0], o[4 * e + 2]);
+                    cacc_merge(phi[e].y, plo[e].y, o[4 * e + 1], o[4 * e + 3]);
+                }
+            }
+        }
+    }
     // this group's grad_w for the columns: (hi, lo) in slots 2g, 2g+1, or
     // hi + lo in slot 0 when a single group covers a single block
-    if (active && ntok > 0) {
+    if (active && ntok > 0 && (!tsplit || warp == 0)) {
         float* o = p.partial + ((p.pair_slots ? 2 * grp : grp) * kS + s) * d + col;
         if (p.pair_slots) {
             float* ol = o + static_cast<long long>(kS) * d;
