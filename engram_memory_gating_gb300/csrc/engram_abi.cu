@@ -303,7 +303,9 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
         // tokens, with a ring of 16 stages (a multiple of the warps, so each
         // stage has one consumer).  Measured (backward alone): N = 64 93.5 ->
         // 25.0 us, 320 217.7 -> 51.1, 1024 265.8 -> 87.4, 2048 277.3 -> 147.9,
-        // 4096 292.5 -> 266.9.  Larger batches take the one-pass kernel.
+        // 4096 292.5 -> 266.9.  From N = 3712 the one-pass kernel runs.  The
+        // separate-tensor layout stays in column mode: its 64-token groups are
+        // many already (N = 8192, H = 4096: 363.7 us, token mode 1495.5).
         ncols = 64;
         C = static_cast<int>((d + ncols - 1) / ncols);
         c.threads = 256;
@@ -327,10 +329,11 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
 // the lo rows.  G is fixed by N and the device alone (not by the buffer a
 // caller passes), and the call keeps the three-kernel backward when G would
 // leave too many SMs idle (small N: its workspace is small).  The one-pass
-// kernel's time is close to (N / G) x 2.64 us (measured at N = 4096, 6144 and
-// 8192 with G from 32 to 76), and the three kernels took 236 us at N = 4096:
-// the one pass wins from about 48 clusters (N of about 4400) on.
-constexpr int kFusedMinClusters = 48;
+// kernel's time is close to (N / G) x 2.64 us (measured at N = 3072 to 8192
+// with G from 32 to 76).  Against the three kernels: N = 3584 (G = 39) 234.7
+// against 235.3 us, 3840 (G = 42) 234.8 against 252.6, 4096 (G = 44) 242.0
+// against 266.8; so the one pass runs from 40 clusters (N = 3712) on.
+constexpr int kFusedMinClusters = 40;
 constexpr size_t kFusedSlotBytes = 4 * kGateD * (4 + 2);
 
 int gate_bwd_fused_groups(DeviceState& st, int64_t N) {

@@ -217,11 +217,11 @@ def test_fwd_bwd_full_batch_8192(seed):
     assert torch.all(gkv.cpu()[m][:, :4 * D].float() == 0)
 
 
-@pytest.mark.parametrize("N,kernels", [(4352, 3), (4608, 2)])
+@pytest.mark.parametrize("N,kernels", [(3648, 3), (3712, 2)])
 def test_bwd_either_side_of_the_one_pass_threshold(N, kernels):
-    """The backward takes the one-pass kernel from 48 clusters on (the
-    workspace of N = 4608 holds 50: token ranges of 92 and 93 tokens) and the
-    three kernels below (N = 4352 holds 47).  Both against the oracle, every
+    """The backward takes the one-pass kernel from 40 clusters on (the
+    workspace of N = 3712 holds 40: token ranges of 92 and 93 tokens) and the
+    three kernels below (N = 3648 holds 39).  Both against the oracle, every
     element, mask Bernoulli(0.9)."""
     assert eg.engram_launch_info(1, N)["kernels"] == kernels
     inp = gate_inputs(N, 9, device=DEV, mask="bern0.9")
@@ -320,7 +320,7 @@ def test_launch_geometry():
     # run at once.  Otherwise: token rows split across column slices, at
     # most one group per two 64-token blocks, groups of at most 256 tokens
     # (their scalars are staged in shared memory).
-    for N in (64, 128, 192, 4096, 8192, 11520, 65536, 65728, 1 << 20):
+    for N in (64, 128, 192, 3648, 3712, 4096, 8192, 11520, 65536, 65728, 1 << 20):
         b = eg.engram_launch_info(1, N)
         if b["kernels"] == 2:
             assert b["cluster"] == 2 and b["threads"] >= 640 and b["threads"] % 32 == 0
@@ -345,9 +345,9 @@ def test_chained_steps_without_host_sync_match_synchronised_ones():
     predecessor finishes; this checks that every kernel still reads only
     completed data, against the same chain with a device synchronisation after
     every call (no overlap at all).  The kernels are deterministic, so the two
-    chains must agree bit for bit.  N = 4096 also spans a full wave of the
-    elementwise kernel's token groups; N = 8192 runs the one-pass backward."""
-    for N in (256, 4096, 8192):
+    chains must agree bit for bit.  N = 3584 runs the three-kernel backward
+    (its elementwise kernel in token mode), N = 8192 the one-pass backward."""
+    for N in (256, 3584, 8192):
         _chain_check(N)
 
 
