@@ -31,6 +31,10 @@ constexpr int kGcStages = 16;
 constexpr int kGcMinRange = 16;    // tokens; bounds the 3-token halo overhead
 constexpr int kGcRangeCost = 8;    // per-range set-up, in token-steps, for the range split
 constexpr int64_t kGcBwdSlots = 256;  // backward weight-gradient slots (one per range)
+// backward exchange records (two 128-byte slots per CTA) for up to
+// kGcBwdMaxCtas CTAs, after the weight-gradient slots of the workspace
+constexpr int kGcBwdMaxCtas = 1024;
+constexpr size_t kGcXrecBytes = static_cast<size_t>(kGcBwdMaxCtas) * 2 * 128;
 
 struct OccKey {
     int op, cluster, threads, smem;
@@ -44,6 +48,7 @@ struct GcGeom {
     int sc_off;  // backward: byte offset of the staged per-token scalars
     int range_len;
     int rpr;  // ranges per batch row
+    int groups;  // backward: CTA groups launched (each takes ranges in turn)
 };
 
 struct GcCacheEntry {
@@ -100,9 +105,16 @@ int max_clusters(DeviceState& st, int op, int cluster, int threads, int smem) {
                 e = gateconv_fwd_prepare(lim);
                 if (e == cudaSuccess) e = gateconv_fwd_max_clusters(cluster, threads, smem, &v);
                 break;
-            default:
+            case 3:
                 e = gateconv_bwd_prepare(lim);
                 if (e == cudaSuccess) e = gateconv_bwd_max_clusters(cluster, threads, smem, &v);
+                break;
+            default:
+                // the backward's cooperative launch: groups of `cluster`
+                // CTAs that fit the device at once
+                e = gateconv_bwd_prepare(lim);
+                if (e == cudaSuccess) e = gateconv_bwd_blocks_per_sm(threads, smem, &v);
+                v = e == cudaSuccess ? v * st.sm_count / cluster : 0;
                 break;
         }
     }
@@ -410,10 +422,10 @@ const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
     if (e.M == M && e.T == T && e.d == d) return &e.g;
     // C = ceil(d / 1024): measured on GB300, larger clusters (more, smaller
     // CTAs) did not run faster even where they packed onto more SMs.  The
-    // backward (one CTA per SM) also tries C rounded up to a power of two,
-    // where every CTA still gets columns, and keeps it if more CTAs are
-    // co-resident: at d = 7168 clusters of 7 fill 105 SMs and clusters of 8
-    // fill 120 (1.8% faster); at d = 5120 clusters of 5 fill more than 8 do.
+    // backward also tries C rounded up to a power of two, where every CTA
+    // still gets columns, and keeps it if more CTAs are co-resident: at
+    // d = 7168 clusters of 7 fill 105 SMs and clusters of 8 fill 120 (1.8%
+    // faster); at d = 5120 clusters of 5 fill more than 8 do.
     const int rows = op == 0 ? 3 : 5;
     auto shape = [&](int C, GcGeom& g) {
         g = {};
@@ -452,12 +464,34 @@ const GcGeom* gc_cfg(DeviceState& st, int op, int64_t M, int64_t T, int64_t d) {
             if (k2 * p2 > k0 * C0) g = g2;
         }
     }
-    const int K = max_clusters(st, op == 0 ? 2 : 3, g.c.cluster, g.c.threads, g.c.smem);
+    int K = max_clusters(st, op == 0 ? 2 : 3, g.c.cluster, g.c.threads, g.c.smem);
+    if (op == 1) {
+        // Groups of C0 CTAs exchanging through global memory (a cooperative
+        // launch) are not confined to a GPC as clusters are, and fill the
+        // device where clusters pack poorly.  A CTA's time per token follows
+        // its columns, and a group's exchange through L2 costs about 1/16 of
+        // that (measured: 2.39 against 2.24 us a chunk of 1024 columns), so
+        // the groups are taken when G * 15/16 / ncols beats K / ncols of the
+        // clusters: d = 7168, 21 groups of 7 x 1024 columns against 15
+        // clusters of 8 x 896 (2.26 -> 1.93 ms at M = 8, T = 8192); d = 4096
+        // keeps 36 clusters of 4 (144 SMs) against 38 groups.
+        GcGeom gg;
+        shape(C0, gg);
+        int G = max_clusters(st, 4, C0, gg.c.threads, gg.c.smem);
+        if (G * C0 > kGcBwdMaxCtas) G = kGcBwdMaxCtas / C0;
+        if (G > 0 && (K <= 0 || 15LL * G * g.ncols > 16LL * K * gg.ncols)) {
+            g = gg;
+            K = G;
+            g.groups = G;
+        }
+    }
     if (K <= 0) return nullptr;
-    if (op == 0)
+    if (op == 0) {
         gc_ranges(M, T, K, int64_t(1) << 31, int64_t(1) << 31, g);
-    else
+    } else {
         gc_ranges(M, T, K, gc_bwd_slots(M, T), kGcBwdMaxRange, g);
+        if (g.groups > 0 && g.c.clusters < g.groups) g.groups = g.c.clusters;
+    }
     e.M = M;
     e.T = T;
     e.d = d;
@@ -993,7 +1027,7 @@ engram_status_t engram_decode_fwd(const void* e, const void* h, const void* stat
 
 size_t engram_gateconv_bwd_workspace_size(int64_t M, int64_t T, int64_t d) {
     if (!gc_shape_ok(M, T, d)) return 0;
-    return static_cast<size_t>(gc_bwd_slots(M, T)) * 6 * static_cast<size_t>(d) * 4;
+    return static_cast<size_t>(gc_bwd_slots(M, T)) * 6 * static_cast<size_t>(d) * 4 + kGcXrecBytes;
 }
 
 engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k,
@@ -1032,6 +1066,8 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
     const GcGeom* g = gc_cfg(*st, 1, M, T, d);
     if (!g) return ENGRAM_ERR_DEVICE;
     float* partial = static_cast<float*>(workspace);
+    unsigned long long* xrec =
+        reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + (need - kGcXrecBytes));
     GateConvBwdParams p;
     p.dY = static_cast<const uint16_t*>(dY);
     p.H = static_cast<const uint16_t*>(H);
@@ -1049,10 +1085,13 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
     p.dk = static_cast<uint16_t*>(dk);
     p.dv = static_cast<uint16_t*>(dv);
     p.partial = partial;
+    p.xrec = xrec;
     p.err = st->err;
     p.M = static_cast<int>(M);
     p.T = static_cast<int>(T);
     p.d = static_cast<int>(d);
+    p.group = g->c.cluster;
+    p.nranges = g->c.clusters;
     p.ncols = g->ncols;
     p.ring_off = g->ring_off;
     p.sc_off = g->sc_off;
@@ -1060,7 +1099,14 @@ engram_status_t engram_gateconv_bwd(const void* dY, const void* H, const void* k
     p.ranges_per_row = g->rpr;
     p.eps = eps;
     p.inv_sqrt_d = static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
-    engram_status_t s = launch_status(gateconv_bwd_launch(p, g->c, stream));
+    engram_status_t s = ENGRAM_OK;
+    if (g->groups > 0) {
+        // the exchange records start at zero (sequence 0 is never awaited)
+        const size_t xbytes = static_cast<size_t>(g->groups) * g->c.cluster * 2 * 128;
+        s = launch_status(cudaMemsetAsync(xrec, 0, xbytes, stream));
+        if (s != ENGRAM_OK) return s;
+    }
+    s = launch_status(gateconv_bwd_launch(p, g->c, g->groups, stream));
     if (s != ENGRAM_OK) return s;
     const int R = g->c.clusters;
     float* outs3[3] = {drms_w_h, drms_w_v, dconv_w};
@@ -1184,6 +1230,18 @@ engram_status_t engram_launch_info(int op, int64_t n0, int64_t n1, int64_t n2,
             const GcGeom* g = gc_shape_ok(n0, n1, n2) ? gc_cfg(*st, op - 2, n0, n1, n2) : nullptr;
             ok = g != nullptr;
             if (ok) c = g->c;
+            if (ok && g->groups > 0) {
+                // the backward's cooperative launch: groups of c.cluster CTAs,
+                // each taking token ranges in turn
+                info->cluster = c.cluster;
+                info->threads = c.threads;
+                info->clusters = c.clusters;
+                info->stages = c.stages;
+                info->smem_bytes = c.smem;
+                info->resident = g->groups;
+                info->kernels = 4;
+                return ENGRAM_OK;
+            }
             break;
         }
         default:

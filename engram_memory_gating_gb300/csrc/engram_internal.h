@@ -131,8 +131,11 @@ struct GateConvBwdParams {
     uint16_t* dk;
     uint16_t* dv;
     float* partial;  // (ranges, 6, d): dwh, dwv, dcw[0..3]
+    unsigned long long* xrec;  // exchange records, 2 slots x 16 words per CTA, zero at launch
     unsigned int* err;
     int M, T, d;
+    int group;       // CTAs per token range (column slices), at most 8; cluster launch: unused
+    int nranges;     // token ranges (M * ranges_per_row)
     int ncols;
     int ring_off;
     int sc_off;      // byte offset of the per-token saved scalars in shared memory
@@ -222,7 +225,8 @@ cudaError_t gateconv_fwd_launch(const GateConvFwdParams& p, const LaunchCfg& c, 
 
 cudaError_t gateconv_bwd_prepare(int smem_bytes);
 cudaError_t gateconv_bwd_max_clusters(int cluster, int threads, int smem, int* out);
-cudaError_t gateconv_bwd_launch(const GateConvBwdParams& p, const LaunchCfg& c, cudaStream_t s);
+cudaError_t gateconv_bwd_blocks_per_sm(int threads, int smem, int* out);
+cudaError_t gateconv_bwd_launch(const GateConvBwdParams& p, const LaunchCfg& c, int groups, cudaStream_t s);
 cudaError_t gateconv_wreduce_launch(const GateWReduceParams& p, cudaStream_t s);
 
 }  // namespace eg

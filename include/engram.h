@@ -276,8 +276,13 @@ size_t engram_gateconv_bwd_workspace_size(int64_t M, int64_t T, int64_t d);
  *   workspace  >= engram_gateconv_bwd_workspace_size(M, T, d) bytes, 16-B
  *              aligned: per-range fp32 weight-gradient partials (6 d floats
  *              per token range, at most max(M, 256) ranges), summed in a fixed
- *              order by a second kernel (bitwise reproducible); nothing in it
+ *              order by a second kernel (bitwise reproducible), then 256 KiB
+ *              of exchange records for the CTAs that share a token row, which
+ *              the call clears on `stream` before its kernels; nothing in it
  *              needs to start at zero
+ * The main kernel is a cooperative launch of at most one 512-thread CTA per
+ * SM (the CTAs of a token row exchange per-token sums while they run); the
+ * call returns ENGRAM_ERR_LAUNCH if the runtime refuses that launch.
  * The backward reads the saved bf16 vhat (not alpha * v) wherever the forward
  * used the gated value, and recomputes the gate's logit from H, k, rrms_h and
  * rrms_k.  Same size limits as the forward.

@@ -52,14 +52,16 @@ def test_gate_bwd_workspace_size_formula():
 
 def test_gateconv_bwd_workspace_size():
     # one 6*d fp32 slot per token range: up to 256 ranges of >= 16 tokens, but
-    # at least enough for ranges of at most 1024 tokens
+    # at least enough for ranges of at most 1024 tokens; then the exchange
+    # records of up to 1024 CTAs (2 x 16 eight-byte words each)
     def slots(M, T):
         return max(M * ((T + 1023) // 1024), min(256, M * ((T + 15) // 16)))
 
+    xrec = 1024 * 2 * 16 * 8
     for M, T, d in ((4, 4096, 4096), (8, 8192, 7168), (1, 1, 8), (2, 96, 512), (300, 4, 64),
                     (1, 5, 8192), (2, 300000, 64)):
-        assert eg.engram_gateconv_bwd_workspace_size(M, T, d) == slots(M, T) * 6 * d * 4
-    assert eg.engram_gateconv_bwd_workspace_size(8, 8192, 7168) == 256 * 6 * 7168 * 4
+        assert eg.engram_gateconv_bwd_workspace_size(M, T, d) == slots(M, T) * 6 * d * 4 + xrec
+    assert eg.engram_gateconv_bwd_workspace_size(8, 8192, 7168) == 256 * 6 * 7168 * 4 + 262144
     for shape in ((0, 4, 64), (1, 0, 64), (1, 4, 12), (1, 4, 0), (1, 4, 8200), (1, 4, 8 * 1031)):
         assert eg.engram_gateconv_bwd_workspace_size(*shape) == 0
 

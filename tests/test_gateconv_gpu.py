@@ -59,11 +59,15 @@ def check_bwd(res, exact, sums=True):
 
 
 # shapes span one-warp CTAs (d = 8, 64), ragged last column slices (d = 1032:
-# 640 + 392 columns), the largest d (8 CTAs of 1024 columns), rows shorter
-# than the conv (T = 1, 2) and rows cut into several token ranges with halos
+# 640 + 392 columns; d = 6152: 6 x 896 + 776), the largest d (8 CTAs of 1024
+# columns), rows shorter than the conv (T = 1, 2) and rows cut into several
+# token ranges with halos.  The backward runs d = 6152, 7168 and 8192 as
+# groups of CTAs exchanging through global memory (M = 32, T = 64: 32 ranges
+# on 21 groups, so groups take a second range), the others as clusters.
 SMALL = [(1, 1, 8, 0), (2, 37, 64, 1), (3, 129, 512, 2), (1, 1000, 64, 3), (2, 300, 4096, 4),
          (1, 70, 7168, 5), (1, 5, 5120, 6), (2, 45, 1032, 7), (1, 40, 8192, 8), (3, 2, 264, 9),
-         (1, 2500, 64, 10), (1, 40, 4200, 11), (2, 33, 6144, 12)]
+         (1, 2500, 64, 10), (1, 40, 4200, 11), (2, 33, 6144, 12), (2, 45, 6152, 15),
+         (32, 64, 7168, 16)]
 
 
 @pytest.mark.parametrize("M,T,d,seed", SMALL)
@@ -200,6 +204,16 @@ def test_full_config_m8_t8192_d7168():
         for name, got, e in (("dH", g[0], eb[0]), ("dk", g[1], eb[1]), ("dv", g[2], eb[2])):
             check_bf16(name, bf16_bits(got[m:m + 1, a:b]), e[:, o0:o1],
                        floor="all" if name != "dv" else "row")
+
+
+def test_bwd_group_geometry():
+    """At d = 7168 the backward's CTAs of a token row work as cooperative
+    groups of 7 (1024 columns each) on at least 140 SMs, where clusters of 8
+    packed onto 120, and the groups take the M = 8, T = 8192 batch's token
+    ranges in turn."""
+    m8 = eg.engram_launch_info(3, 8, 8192, 7168)
+    assert m8["cluster"] == 7 and m8["cluster"] * m8["resident"] >= 140
+    assert m8["clusters"] > m8["resident"]
 
 
 def test_launch_geometry():

@@ -137,8 +137,11 @@ def test_fused_weight(n, nblocks):
         same_bits(x.t, r, name)
 
 
-@pytest.mark.parametrize("M,T,d", [(2, 45, 1032), (4, 4096, 4096)])
+@pytest.mark.parametrize("M,T,d", [(2, 45, 1032), (4, 4096, 4096), (3, 70, 7168)])
 def test_gateconv_fwd_bwd(M, T, d):
+    """Guard bands around every output and the workspace; d = 7168 runs the
+    backward as groups of CTAs exchanging through the workspace's records,
+    the other shapes as thread-block clusters."""
     ci = gateconv_inputs(M, T, d, 80, device=DEV)
     ref = eg.gateconv_forward(ci["H"], ci["k"], ci["v"], ci["rms_w_h"], ci["rms_w_v"], ci["conv_w"])
     gf = [like(t, 40 + i) for i, t in enumerate(ref)]
