@@ -283,8 +283,9 @@ static_assert(kRing2Off<true> % 128 == 0, "ring alignment");
 // col0 + 8 * (8w + g) of one stream.  The four streams of a column group sit
 // in one warp, so grad_v (a sum over streams) is two shuffles.
 // kPacked: d = 5120, packed KV / grad_kv rows and saved records, all strides
-// known at compile time; otherwise runtime d and strides.
-template <bool kPacked>
+// known at compile time; otherwise runtime d and strides.  kTsplit: token
+// mode (packed layout only; the host sets p.token_split to match).
+template <bool kPacked, bool kTsplit>
 __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);                            // [stages]
@@ -301,7 +302,8 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     // slice): every warp owns the slice's 8 column groups and the warps split
     // the group's tokens (warp w: tokens w, w + W, ...), so that a short
     // group's tokens are not walked one after another by a single warp.
-    const bool tsplit = p.token_split != 0;
+    constexpr bool tsplit = kTsplit;
+    static_assert(kPacked || !kTsplit, "token mode serves the packed layout");
     const int warp = tid >> 5;
     const int cg = (tsplit ? 0 : warp * 8) + (lane & 7);  // column group in the slice
     const int d = kPacked ? kGateHidden : p.d;
@@ -419,10 +421,12 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
     for (int e = 0; e < 4; ++e) phi[e] = plo[e] = make_float2(0.f, 0.f);
 
     // token mode: a stage's tokens (j, j + stages, ...) all go to one warp,
-    // as stages is a multiple of W; it refills the stage with its next token
-    for (int j = tsplit ? warp : 0; j < ntok; j += tsplit ? W : 1) {
-        const int st = j % stages;
-        const uint32_t phase = static_cast<uint32_t>((j / stages) & 1);
+    // as stages is a multiple of W; it refills the stage with its next token.
+    // The stage and its phase parity follow j incrementally (no division).
+    const int jstep = tsplit ? W : 1;
+    int st = tsplit ? warp : 0;
+    uint32_t phase = 0;
+    for (int j = st; j < ntok; j += jstep) {
         const long long n = t0 + j;
         if (!failed && !mbar_wait(&full[st], phase)) failed = true;
         const unsigned char* b = ring + static_cast<size_t>(st) * stage_bytes;
@@ -484,6 +488,11 @@ __global__ void __launch_bounds__(256, 3) gate_bwd_main_kernel(const GateBwdPara
                     issue_gates(j + stages, st);
                 }
             }
+        }
+        st += jstep;
+        if (st >= stages) {
+            st -= stages;
+            phase ^= 1u;
         }
         // grad_v = (g0 + g1) + (g2 + g3) over the four streams' lanes
 #pragma unroll
@@ -626,20 +635,18 @@ __global__ void __launch_bounds__(32 * kRedGroups) wreduce_kernel(const GateWRed
 }  // namespace
 
 cudaError_t gate_bwd_prepare(int smem_bytes) {
+    const void* mains[3] = {reinterpret_cast<const void*>(gate_bwd_main_kernel<true, false>),
+                            reinterpret_cast<const void*>(gate_bwd_main_kernel<true, true>),
+                            reinterpret_cast<const void*>(gate_bwd_main_kernel<false, false>)};
     cudaError_t e = cudaSuccess;
-    if (smem_bytes > 0)  // 0: only the coefficient kernel is being set up
-        e = cudaFuncSetAttribute(gate_bwd_main_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes);
-    if (e == cudaSuccess && smem_bytes > 0)
-        e = cudaFuncSetAttribute(gate_bwd_main_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gate_bwd_main_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gate_bwd_main_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
+    for (const void* k : mains) {
+        if (smem_bytes > 0)  // 0: only the coefficient kernel is being set up
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+    }
     e = cudaFuncSetAttribute(gate_bwd_coef_kernel<kGateHidden>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(gate_bwd_coef_kernel<0>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
@@ -651,7 +658,7 @@ cudaError_t gate_bwd_max_clusters(int, int threads, int smem, int* out) {
     int per_sm = 0, dev = 0, sms = 0;
     cudaError_t e = smem == 0
         ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_bwd_coef_kernel<kGateHidden>, threads, 0)
-        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_bwd_main_kernel<true>, threads, smem);
+        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_bwd_main_kernel<true, false>, threads, smem);
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     *out = per_sm * sms;
@@ -682,8 +689,9 @@ cudaError_t gate_bwd_launch(const GateBwdParams& p, const LaunchCfg& c, cudaStre
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return p.packed ? cudaLaunchKernelEx(&cfg, gate_bwd_main_kernel<true>, p)
-                    : cudaLaunchKernelEx(&cfg, gate_bwd_main_kernel<false>, p);
+    if (!p.packed) return cudaLaunchKernelEx(&cfg, gate_bwd_main_kernel<false, false>, p);
+    return p.token_split ? cudaLaunchKernelEx(&cfg, gate_bwd_main_kernel<true, true>, p)
+                         : cudaLaunchKernelEx(&cfg, gate_bwd_main_kernel<true, false>, p);
 }
 
 cudaError_t gate_wreduce_launch(const GateWReduceParams& p, cudaStream_t s) {
