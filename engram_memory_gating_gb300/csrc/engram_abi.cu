@@ -315,7 +315,7 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
         // tokens, with a ring of 16 stages (a multiple of the warps, so each
         // stage has one consumer).  Measured (backward alone): N = 64 93.5 ->
         // 25.0 us, 320 217.7 -> 51.1, 1024 265.8 -> 87.4, 2048 277.3 -> 147.9,
-        // 4096 292.5 -> 266.9.  From N = 3712 the one-pass kernel runs.  The
+        // 4096 292.5 -> 266.9.  From N = 3840 the one-pass kernel runs.  The
         // separate-tensor layout stays in column mode: its 64-token groups are
         // many already (N = 8192, H = 4096: 363.7 us, token mode 1495.5).
         ncols = 64;
@@ -342,10 +342,11 @@ bool gate_bwd_cfg(DeviceState& st, int64_t N, int64_t d, bool blocks, LaunchCfg&
 // caller passes), and the call keeps the three-kernel backward when G would
 // leave too many SMs idle (small N: its workspace is small).  The one-pass
 // kernel's time is close to (N / G) x 2.64 us (measured at N = 3072 to 8192
-// with G from 32 to 76).  Against the three kernels: N = 3584 (G = 39) 234.7
-// against 235.3 us, 3840 (G = 42) 234.8 against 252.6, 4096 (G = 44) 242.0
-// against 266.8; so the one pass runs from 40 clusters (N = 3712) on.
-constexpr int kFusedMinClusters = 40;
+// with G from 32 to 76).  Against the three kernels (token mode): N = 3712
+// (G = 40) 238.3 against 236.5 us, 3840 (G = 42) 234.4 against 235.4, 3968
+// (G = 43) 235.4 against 246.5, 4096 (G = 44) 241.7 against 249.1; so the one
+// pass runs from 42 clusters (N = 3840) on.
+constexpr int kFusedMinClusters = 42;
 constexpr size_t kFusedSlotBytes = 4 * kGateD * (4 + 2);
 
 int gate_bwd_fused_groups(DeviceState& st, int64_t N) {

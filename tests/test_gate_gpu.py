@@ -217,11 +217,11 @@ def test_fwd_bwd_full_batch_8192(seed):
     assert torch.all(gkv.cpu()[m][:, :4 * D].float() == 0)
 
 
-@pytest.mark.parametrize("N,kernels", [(3648, 3), (3712, 2)])
+@pytest.mark.parametrize("N,kernels", [(3776, 3), (3840, 2)])
 def test_bwd_either_side_of_the_one_pass_threshold(N, kernels):
-    """The backward takes the one-pass kernel from 40 clusters on (the
-    workspace of N = 3712 holds 40: token ranges of 92 and 93 tokens) and the
-    three kernels below (N = 3648 holds 39).  Both against the oracle, every
+    """The backward takes the one-pass kernel from 42 clusters on (the
+    workspace of N = 3840 holds 42: token ranges of 91 and 92 tokens) and the
+    three kernels below (N = 3776 holds 41).  Both against the oracle, every
     element, mask Bernoulli(0.9)."""
     assert eg.engram_launch_info(1, N)["kernels"] == kernels
     inp = gate_inputs(N, 9, device=DEV, mask="bern0.9")
@@ -320,7 +320,7 @@ def test_launch_geometry():
     # run at once.  Otherwise: token rows split across column slices, at
     # most one group per two 64-token blocks, groups of at most 256 tokens
     # (their scalars are staged in shared memory).
-    for N in (64, 128, 192, 3648, 3712, 4096, 8192, 11520, 65536, 65728, 1 << 20):
+    for N in (64, 128, 192, 3776, 3840, 4096, 8192, 11520, 65536, 65728, 1 << 20):
         b = eg.engram_launch_info(1, N)
         if b["kernels"] == 2:
             assert b["cluster"] == 2 and b["threads"] >= 640 and b["threads"] % 32 == 0
