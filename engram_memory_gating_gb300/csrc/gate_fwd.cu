@@ -241,14 +241,24 @@ EG_DEV void quad_sync(int q) {
 // parity, one quad barrier per row) and every warp merges them in part order,
 // so all four form the same gate.  kPacked: packed KV and saved records with
 // d = 5120 at compile time; otherwise runtime d and strides, saved arrays.
+// In the packed layout a warp's quarters of a row (2560 contiguous bytes of X,
+// 2560 of key) arrive by two 1-D bulk copies into the warp's own shared
+// buffer, issued as soon as the warp has taken the previous row's quarters into
+// registers, so the next row's loads are in flight for a whole row of work.
 constexpr int kParts = 4;
 constexpr int kPerLane = kGateHidden / 8 / kParts / 32;  // 5
 constexpr int kQuadMaxHidden = kParts * kPerLane * 32 * 8;  // 5120
+constexpr int kQuarter = kPerLane * 32;                   // 16-byte chunks of a packed quarter
+constexpr uint32_t kQuarterBytes = kQuarter * 16;         // 2560
 
 template <bool kPacked>
 __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdParams p) {
     grid_dep_start();
     __shared__ float4 xch[2][2][kParts];   // [quad][row parity][part]: sum x^2, sum k^2, hi, lo
+    // packed layout: each warp's (X, key) quarters of its next row, and the
+    // warp's mbarrier
+    __shared__ __align__(128) uint4 stage[kPacked ? 8 : 1][2][kPacked ? kQuarter : 1];
+    __shared__ uint64_t sbar[8];
     const int d = kPacked ? kGateHidden : p.d;
     const long long key_ts = kPacked ? 5LL * kGateHidden : p.key_ts;
     const long long v_ts = kPacked ? 5LL * kGateHidden : p.v_ts;
@@ -265,6 +275,30 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
     const int cnt = kPacked ? per : max(0, min(per, nch - cbeg));       // this part's chunks
     const int ch0 = cbeg + lane;
     auto has = [&](int m) { return kPacked || lane + 32 * m < cnt; };
+    uint4* const bx = stage[kPacked ? warp : 0][0];
+    uint4* const bk = stage[kPacked ? warp : 0][1];
+    uint64_t* const bar = &sbar[warp];
+    // lane 0: the quarters of row r into this warp's buffer (copy k of the
+    // warp completes the barrier's phase k)
+    uint32_t issued = 0;
+    auto issue = [&](long long r) {
+        ++issued;
+        const long long nn = r >> 2;
+        const int ss = static_cast<int>(r & 3);
+        mbar_arrive_expect_tx(bar, 2 * kQuarterBytes);
+        bulk_g2s(bx, p.x + r * d + cbeg * 8, kQuarterBytes, bar);
+        bulk_g2s(bk, p.key + nn * key_ts + static_cast<long long>(ss) * d + cbeg * 8, kQuarterBytes, bar);
+    };
+    bool failed = false;
+    uint32_t ph = 0;
+    if (kPacked) {
+        if (lane == 0) {
+            mbar_init(bar, 1);
+            fence_mbar_init();
+            if (gq < rows) issue(gq);
+        }
+        __syncwarp();
+    }
     int par = 0;
     for (long long row = gq; row < rows; row += nq, par ^= 1) {
         const long long n = row >> 2;
@@ -275,10 +309,28 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
         const float4* wr = reinterpret_cast<const float4*>(p.w + static_cast<long long>(s) * d) + 2 * ch0;
         const bool on = (p.mask == nullptr) || (__ldg(p.mask + n) != 0);
         uint4 xq[kPerLane], kq[kPerLane];
+        if (kPacked) {
+            // this row's quarters have landed; take them into registers, then
+            // free the buffer for the next row
+            if (!failed && !mbar_wait(bar, ph)) failed = true;
+            failed = __any_sync(kFullMask, failed);
+            ph ^= 1u;
 #pragma unroll
-        for (int m = 0; m < kPerLane; ++m) {
-            xq[m] = has(m) ? ldg16(xr + 32 * m) : make_uint4(0, 0, 0, 0);
-            kq[m] = has(m) ? ldg16_na(kr + 32 * m) : make_uint4(0, 0, 0, 0);
+            for (int m = 0; m < kPerLane; ++m) {
+                xq[m] = bx[lane + 32 * m];
+                kq[m] = bk[lane + 32 * m];
+            }
+            __syncwarp();
+            if (lane == 0 && !failed && row + nq < rows) {
+                fence_proxy_async();
+                issue(row + nq);
+            }
+        } else {
+#pragma unroll
+            for (int m = 0; m < kPerLane; ++m) {
+                xq[m] = has(m) ? ldg16(xr + 32 * m) : make_uint4(0, 0, 0, 0);
+                kq[m] = has(m) ? ldg16_na(kr + 32 * m) : make_uint4(0, 0, 0, 0);
+            }
         }
 
         // ---- pass 1 over this part: sum x^2, sum k^2, sum x w k (compensated)
@@ -364,12 +416,21 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
             if (has(m)) stg_cs(o + 32 * m, ov);
         }
     }
+    // the last copy, which may still be in flight only after a wait gave up
+    // (no copy is issued after that), lands or times out before the CTA leaves
+    if (kPacked && failed && lane == 0) {
+        atomicOr(p.err, kErrTimeout);
+        if (issued > 0) (void)mbar_wait(bar, (issued - 1u) & 1u);
+    }
 }
 
 }  // namespace
 
 cudaError_t gate_fwd_prepare(int) {
-    cudaError_t e = cudaFuncSetAttribute(gate_fwd_quad_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
+    // the packed quad kernel's row buffers (41 KB a CTA, two CTAs an SM) in
+    // shared memory, the rest of the unified cache as L1 for the 80 KB weight;
+    // the other kernels use no shared memory beyond the exchange slots
+    cudaError_t e = cudaFuncSetAttribute(gate_fwd_quad_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 40);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gate_fwd_quad_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
     if (e == cudaSuccess)
