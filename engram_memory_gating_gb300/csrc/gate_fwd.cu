@@ -18,9 +18,10 @@
 //    and v, two groups in flight, and writes `out` with streaming stores.  The
 //    four rows of a token go to four warps of the same CTA, so v is read from
 //    HBM once and from L1/L2 after.
-//  * gate_fwd_quad_kernel (batches up to kGateQuadMaxTokens, d <= 5120):
-//    the four warps of a quad share a row, each owning a quarter of the
-//    columns (five chunks per lane).  A warp keeps its X chunks in registers
+//  * gate_fwd_quad_kernel (4096 <= d <= 5120, any batch): the four warps of
+//    a quad share a row, each owning a quarter of the columns (five chunks
+//    per lane).  A warp's quarters of X and key arrive by bulk copies into
+//    its own shared buffer a row ahead; it keeps its X chunks in registers
 //    from the reduction to the output pass, issues its v loads before the
 //    exchange, and the quad adds the four partial sums through shared memory
 //    in a fixed order.  Splitting rows four ways evens out the work of short
@@ -48,11 +49,6 @@ EG_DEV void grid_dep_start() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
-// Largest batch (tokens) the packed forward runs with four warps per row.
-// Measured on GB300 with 10% and 50% of the tokens masked: the quad kernel is
-// faster up to 32,768 tokens (by 5-8% at 4,096-16,384), the row kernel on
-// long, heavily masked batches (5% at 262,144 tokens, half masked).
-constexpr long long kGateQuadMaxTokens = 32768;
 constexpr int kGroup = 4;   // 16-byte chunks per lane per load group
 
 // 16-byte loads: read-only path; `_na` does not allocate in L1 (data used once).
@@ -241,23 +237,22 @@ EG_DEV void quad_sync(int q) {
 // parity, one quad barrier per row) and every warp merges them in part order,
 // so all four form the same gate.  kPacked: packed KV and saved records with
 // d = 5120 at compile time; otherwise runtime d and strides, saved arrays.
-// In the packed layout a warp's quarters of a row (2560 contiguous bytes of X,
-// 2560 of key) arrive by two 1-D bulk copies into the warp's own shared
-// buffer, issued as soon as the warp has taken the previous row's quarters into
-// registers, so the next row's loads are in flight for a whole row of work.
+// A warp's quarters of a row (up to 2560 contiguous bytes of X and as many of
+// key; 16-byte multiples at 16-byte offsets, as d % 8 == 0) arrive by two 1-D
+// bulk copies into the warp's own shared buffer, issued as soon as the warp
+// has taken the previous row's quarters into registers, so the next row's
+// loads are in flight for a whole row of work.
 constexpr int kParts = 4;
 constexpr int kPerLane = kGateHidden / 8 / kParts / 32;  // 5
 constexpr int kQuadMaxHidden = kParts * kPerLane * 32 * 8;  // 5120
 constexpr int kQuarter = kPerLane * 32;                   // 16-byte chunks of a packed quarter
-constexpr uint32_t kQuarterBytes = kQuarter * 16;         // 2560
 
 template <bool kPacked>
 __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdParams p) {
     grid_dep_start();
     __shared__ float4 xch[2][2][kParts];   // [quad][row parity][part]: sum x^2, sum k^2, hi, lo
-    // packed layout: each warp's (X, key) quarters of its next row, and the
-    // warp's mbarrier
-    __shared__ __align__(128) uint4 stage[kPacked ? 8 : 1][2][kPacked ? kQuarter : 1];
+    // each warp's (X, key) quarters of its next row, and the warp's mbarrier
+    __shared__ __align__(128) uint4 stage[8][2][kQuarter];
     __shared__ uint64_t sbar[8];
     const int d = kPacked ? kGateHidden : p.d;
     const long long key_ts = kPacked ? 5LL * kGateHidden : p.key_ts;
@@ -275,8 +270,9 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
     const int cnt = kPacked ? per : max(0, min(per, nch - cbeg));       // this part's chunks
     const int ch0 = cbeg + lane;
     auto has = [&](int m) { return kPacked || lane + 32 * m < cnt; };
-    uint4* const bx = stage[kPacked ? warp : 0][0];
-    uint4* const bk = stage[kPacked ? warp : 0][1];
+    uint4* const bx = stage[warp][0];
+    uint4* const bk = stage[warp][1];
+    const uint32_t qbytes = 16u * static_cast<uint32_t>(cnt);   // this part's quarter (0 if it has none)
     uint64_t* const bar = &sbar[warp];
     // lane 0: the quarters of row r into this warp's buffer (copy k of the
     // warp completes the barrier's phase k)
@@ -285,13 +281,15 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
         ++issued;
         const long long nn = r >> 2;
         const int ss = static_cast<int>(r & 3);
-        mbar_arrive_expect_tx(bar, 2 * kQuarterBytes);
-        bulk_g2s(bx, p.x + r * d + cbeg * 8, kQuarterBytes, bar);
-        bulk_g2s(bk, p.key + nn * key_ts + static_cast<long long>(ss) * d + cbeg * 8, kQuarterBytes, bar);
+        mbar_arrive_expect_tx(bar, 2 * qbytes);
+        if (qbytes > 0) {
+            bulk_g2s(bx, p.x + r * d + cbeg * 8, qbytes, bar);
+            bulk_g2s(bk, p.key + nn * key_ts + static_cast<long long>(ss) * d + cbeg * 8, qbytes, bar);
+        }
     };
     bool failed = false;
     uint32_t ph = 0;
-    if (kPacked) {
+    {
         if (lane == 0) {
             mbar_init(bar, 1);
             fence_mbar_init();
@@ -303,34 +301,24 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
     for (long long row = gq; row < rows; row += nq, par ^= 1) {
         const long long n = row >> 2;
         const int s = static_cast<int>(row & 3);
-        const uint4* xr = reinterpret_cast<const uint4*>(p.x + row * d) + ch0;
-        const uint4* kr = reinterpret_cast<const uint4*>(p.key + n * key_ts + static_cast<long long>(s) * d) + ch0;
         const uint4* vr = reinterpret_cast<const uint4*>(p.v + n * v_ts) + ch0;
         const float4* wr = reinterpret_cast<const float4*>(p.w + static_cast<long long>(s) * d) + 2 * ch0;
         const bool on = (p.mask == nullptr) || (__ldg(p.mask + n) != 0);
         uint4 xq[kPerLane], kq[kPerLane];
-        if (kPacked) {
-            // this row's quarters have landed; take them into registers, then
-            // free the buffer for the next row
-            if (!failed && !mbar_wait(bar, ph)) failed = true;
-            failed = __any_sync(kFullMask, failed);
-            ph ^= 1u;
+        // this row's quarters have landed; take them into registers, then free
+        // the buffer for the next row
+        if (!failed && !mbar_wait(bar, ph)) failed = true;
+        failed = __any_sync(kFullMask, failed);
+        ph ^= 1u;
 #pragma unroll
-            for (int m = 0; m < kPerLane; ++m) {
-                xq[m] = bx[lane + 32 * m];
-                kq[m] = bk[lane + 32 * m];
-            }
-            __syncwarp();
-            if (lane == 0 && !failed && row + nq < rows) {
-                fence_proxy_async();
-                issue(row + nq);
-            }
-        } else {
-#pragma unroll
-            for (int m = 0; m < kPerLane; ++m) {
-                xq[m] = has(m) ? ldg16(xr + 32 * m) : make_uint4(0, 0, 0, 0);
-                kq[m] = has(m) ? ldg16_na(kr + 32 * m) : make_uint4(0, 0, 0, 0);
-            }
+        for (int m = 0; m < kPerLane; ++m) {
+            xq[m] = has(m) ? bx[lane + 32 * m] : make_uint4(0, 0, 0, 0);
+            kq[m] = has(m) ? bk[lane + 32 * m] : make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+        if (lane == 0 && !failed && row + nq < rows) {
+            fence_proxy_async();
+            issue(row + nq);
         }
 
         // ---- pass 1 over this part: sum x^2, sum k^2, sum x w k (compensated)
@@ -418,7 +406,7 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
     }
     // the last copy, which may still be in flight only after a wait gave up
     // (no copy is issued after that), lands or times out before the CTA leaves
-    if (kPacked && failed && lane == 0) {
+    if (failed && lane == 0) {
         atomicOr(p.err, kErrTimeout);
         if (issued > 0) (void)mbar_wait(bar, (issued - 1u) & 1u);
     }
@@ -427,12 +415,12 @@ __global__ void __launch_bounds__(256, 2) gate_fwd_quad_kernel(const GateFwdPara
 }  // namespace
 
 cudaError_t gate_fwd_prepare(int) {
-    // the packed quad kernel's row buffers (41 KB a CTA, two CTAs an SM) in
-    // shared memory, the rest of the unified cache as L1 for the 80 KB weight;
-    // the other kernels use no shared memory beyond the exchange slots
+    // the quad kernel's row buffers (41 KB a CTA, two CTAs an SM) in shared
+    // memory, the rest of the unified cache as L1 for the 80 KB weight; the
+    // row kernel uses no shared memory
     cudaError_t e = cudaFuncSetAttribute(gate_fwd_quad_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 40);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gate_fwd_quad_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
+        e = cudaFuncSetAttribute(gate_fwd_quad_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 40);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gate_fwd_kernel<kGateHidden>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
     if (e != cudaSuccess) return e;
@@ -458,13 +446,13 @@ cudaError_t gate_fwd_max_clusters(int, int threads, int, int* out) {
     return e;
 }
 
-// Four warps per row up to kGateQuadMaxTokens tokens for 4096 <= d <= 5120
-// (narrower rows leave most lanes of a quarter idle; at d = 4096 the two
-// kernels time the same); otherwise one warp per row, whose output pass gets
-// cheap on masked rows and streams a little faster on long, heavily masked
-// batches.
+// Four warps per row for 4096 <= d <= 5120, at every batch size: with its
+// quarters prefetched a row ahead the quad kernel is faster than one warp per
+// row from 2,048 to 262,144 tokens, masked or not (N = 65,536: 1.26 against
+// 1.50 ms; 262,144: 5.29 against 5.99 ms); narrower and wider rows take one
+// warp per row (narrower rows leave most lanes of a quarter idle).
 cudaError_t gate_fwd_launch(const GateFwdParams& p, const LaunchCfg& c, cudaStream_t s) {
-    const bool quad = p.N <= kGateQuadMaxTokens && p.d >= 4096 && p.d <= kQuadMaxHidden;
+    const bool quad = p.d >= 4096 && p.d <= kQuadMaxHidden;
     // programmatic stream serialisation (each kernel waits for its predecessor first)
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];

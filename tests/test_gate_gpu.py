@@ -137,9 +137,9 @@ def test_fwd_graph_capture_matches_eager():
 def test_fwd_full_size_sweep_graph(N):
     """Full-size forward sweep: per-token sigma ~ LogUniform(1e-2, 1e2), mask
     Bernoulli(0.5), CUDA-graph captured execute.  Sampled tokens are checked
-    against the oracle; the masked identity is checked on every token.  32768
-    and 32769 sit on either side of the switch from four warps per row to one
-    warp per row."""
+    against the oracle; the masked identity is checked on every token.  The
+    sizes give the persistent grid's quads whole and ragged last rounds of
+    rows (32768, 32769) and rows far more than the grid (262144)."""
     inp = gate_inputs(N, 100 + N % 97, device=DEV, mask="bern0.5", sigma="loguniform",
                       with_grad=False)
     out = torch.empty_like(inp["x"])
