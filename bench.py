@@ -222,7 +222,7 @@ def extra_ops(torch, eg, inputs_mod, stream, peak):
     csrc = "engram_memory_gating_gb300/csrc/"
     hdrs = [csrc + "common.cuh", csrc + "engram_internal.h"]
     ops["gate_fwd_N262144"]["traffic"] = scaled_traffic(
-        "gate_fwd_row_n36864.md", [csrc + "gate_fwd.cu"] + hdrs, N / 36864)
+        "gate_fwd_n36864.md", [csrc + "gate_fwd.cu"] + hdrs, N / 36864)
     ops["gate_fwd_N262144"]["traffic_from"] = "N = 36,864 capture of the same kernel and input recipe, x 262144/36864"
     del inp, out, saved, g
     torch.cuda.empty_cache()
@@ -447,7 +447,8 @@ def run_single_op(args):
     """One entry point alone, `warmup` + `steps` plain calls on one stream, for
     profiler captures: the gate at --n tokens (default the step's 8192) with the
     step's input recipe, or the forward sweep's with --sweep-inputs; the
-    separate-tensor gate at --n tokens, H = 4096; GateConv at --gc-workload
+    separate-tensor gate at --n tokens and hidden size --h (default 4096; the
+    quad kernel for 4096 <= H <= 5120, one warp per row otherwise); GateConv at --gc-workload
     (m4: M=4, T=4096, d=4096; m8: M=8, T=8192, d=7168; m1: M=1, T=8192,
     d=7168); decode at B = 8, d_mem = 1024, d = 4096, a full cache of 16, w = 4,
     dilation 3 (back to back, weights L2-warm).  Prints the mean event-timed
@@ -459,7 +460,7 @@ def run_single_op(args):
     from engram_memory_gating_gb300 import inputs as inputs_mod
     s = torch.cuda.Stream()
     if args.op.startswith("gate_sep_"):
-        N, H = args.n, 4096
+        N, H = args.n, args.h
         inp = inputs_mod.gate_inputs(N, 105, device="cuda", d=H)
         k = inp["kv"][:, :4 * H].reshape(N, 4, H).contiguous()
         v = inp["kv"][:, 4 * H:].contiguous()
@@ -534,6 +535,7 @@ def main():
                     default="step", help="time one entry point alone (profiler captures)")
     ap.add_argument("--gc-workload", choices=sorted(GC_WORKLOADS), default="m4")
     ap.add_argument("--n", type=int, default=N_TOK, help="tokens of the gate ops (--op)")
+    ap.add_argument("--h", type=int, default=4096, help="hidden size of the separate-tensor ops (--op)")
     ap.add_argument("--sweep-inputs", action="store_true",
                     help="--op gate_*: the forward sweep's inputs (LogUniform row scales, mask Bernoulli(0.5))")
     args = ap.parse_args()
