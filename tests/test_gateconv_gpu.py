@@ -206,6 +206,42 @@ def test_full_config_m8_t8192_d7168():
                        floor="all" if name != "dv" else "row")
 
 
+def test_bwd_group_mode_graph_replays_match_eager():
+    """The backward at d = 7168 runs as cooperative groups that exchange row
+    sums through records in the workspace, which every call clears before its
+    kernels.  Captured in a CUDA graph (the clearing with it) and replayed
+    twice, it gives the eager call's outputs bit for bit; M = 32, T = 64 has
+    more token ranges than groups, so groups take ranges in turn."""
+    M, T, d = 32, 64, 7168
+    inp = gateconv_inputs(M, T, d, 17, device=DEV)
+    res = eg.gateconv_forward(inp["H"], inp["k"], inp["v"], inp["rms_w_h"], inp["rms_w_v"],
+                              inp["conv_w"])
+    args = (inp["dY"], inp["H"], inp["k"], inp["v"], inp["rms_w_h"], inp["rms_w_v"],
+            inp["conv_w"], *res[1:])
+    eager = eg.gateconv_backward(*args)
+    outs = [torch.empty_like(t) for t in eager]
+    ws = torch.empty(eg.engram_gateconv_bwd_workspace_size(M, T, d), device=DEV, dtype=torch.uint8)
+    eg.engram_gateconv_bwd(*args, *outs, ws)   # set-up outside the capture
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            eg.engram_gateconv_bwd(*args, *outs, ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        for t in outs:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for x, y in zip(outs, eager):
+            if x.dtype == torch.bfloat16:
+                assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+            else:
+                assert torch.equal(x, y)
+    assert eg.engram_device_error() == 0
+
+
 def test_bwd_group_geometry():
     """At d = 7168 the backward's CTAs of a token row work as cooperative
     groups of 7 (1024 columns each) on at least 140 SMs, where clusters of 8
