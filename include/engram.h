@@ -125,9 +125,9 @@ size_t engram_gate_bwd_workspace_size(int64_t N);
  *                               gate_s * grad_out_s, summed in FP32 (stream
  *                               order 0..3) before its one BF16 rounding
  *   grad_weight fp32 (4, 5120)  out: sum over tokens of ddot * xh * kh, formed
- *                               as per-64-token partials in the workspace and
- *                               reduced in ascending block order (bitwise
- *                               reproducible run to run)
+ *                               as per-token-range partials in the workspace
+ *                               and reduced in a fixed order (bitwise
+ *                               reproducible run to run on a device)
  *   workspace  >= engram_gate_bwd_workspace_size(N) bytes, 16-B aligned,
  *              contents need no initialisation and are left undefined
  *   N        64 <= N <= ENGRAM_GATE_BWD_MAX_TOKENS, N % 64 == 0.  The cuDNN
@@ -135,7 +135,9 @@ size_t engram_gate_bwd_workspace_size(int64_t N);
  *            workspace grows by 1,344 bytes per token and the grad_weight
  *            merge reads N/64 slots per column, so any multiple of 64 up to
  *            the forward's maximum is accepted.
- * Three kernels on `stream`, no host synchronisation between them.
+ * Two kernels on `stream` from N = 3840 (one pass over the rows, then the
+ * grad_weight merge), three below (per-token scalars, the elementwise pass,
+ * the merge), no host synchronisation between them.
  */
 engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weight,
                                 const float* saved, const void* grad_out, void* grad_x,
@@ -157,7 +159,7 @@ engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weig
  *   grad_weight fp32 (4, 5120)  out, or NULL to skip it
  *   grad_wh, grad_we fp32 (4, 5120)  out
  * Every other argument, limit and error as engram_gate_bwd; outputs must not
- * overlap anything.  Three kernels on `stream`.
+ * overlap anything.  The kernels of engram_gate_bwd on `stream`.
  */
 engram_status_t engram_gate_bwd_fused_weight(const void* x, const void* kv, const float* weight,
                                              const float* saved, const void* grad_out,
@@ -278,11 +280,13 @@ size_t engram_gateconv_bwd_workspace_size(int64_t M, int64_t T, int64_t d);
  *              per token range, at most max(M, 256) ranges), summed in a fixed
  *              order by a second kernel (bitwise reproducible), then 256 KiB
  *              of exchange records for the CTAs that share a token row, which
- *              the call clears on `stream` before its kernels; nothing in it
- *              needs to start at zero
- * The main kernel is a cooperative launch of at most one 512-thread CTA per
- * SM (the CTAs of a token row exchange per-token sums while they run); the
- * call returns ENGRAM_ERR_LAUNCH if the runtime refuses that launch.
+ *              the call clears on `stream` before its kernels when it uses
+ *              them; nothing in it needs to start at zero
+ * The CTAs of a token row (one 512-thread CTA per SM) exchange per-token sums
+ * while they run: as a thread-block cluster, or, at widths where clusters
+ * would leave SMs idle (d = 7168, for instance), as a cooperative launch of
+ * CTA groups exchanging through the workspace's records; the call returns
+ * ENGRAM_ERR_LAUNCH if the runtime refuses either launch.
  * The backward reads the saved bf16 vhat (not alpha * v) wherever the forward
  * used the gated value, and recomputes the gate's logit from H, k, rrms_h and
  * rrms_k.  Same size limits as the forward.
