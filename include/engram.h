@@ -135,9 +135,11 @@ size_t engram_gate_bwd_workspace_size(int64_t N);
  *            workspace grows by 1,344 bytes per token and the grad_weight
  *            merge reads N/64 slots per column, so any multiple of 64 up to
  *            the forward's maximum is accepted.
- * Two kernels on `stream` from N = 3840 (one pass over the rows, then the
- * grad_weight merge), three below (per-token scalars, the elementwise pass,
- * the merge), no host synchronisation between them.
+ * Two kernels on `stream` when the workspace holds 42 or more of the one-pass
+ * kernel's clusters and the device runs them at once (N >= 3840 on GB300:
+ * one pass over the rows, then the grad_weight merge), three otherwise
+ * (per-token scalars, the elementwise pass, the merge), no host
+ * synchronisation between them.
  */
 engram_status_t engram_gate_bwd(const void* x, const void* kv, const float* weight,
                                 const float* saved, const void* grad_out, void* grad_x,
