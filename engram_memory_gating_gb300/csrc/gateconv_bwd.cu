@@ -120,25 +120,31 @@ EG_DEV void conv_t(const Windows& W, const Weights& P, float2 (&du)[2]) {
 // kP1Regs registers a thread, phase-2 warps kP2Regs, by setmaxnreg) where one
 // warp doing both phases needed 236.
 //
-// Groups and the exchange.  The launch is cooperative (every CTA resident at
-// once, one per SM).  CTAs g*C .. g*C + C - 1 form group g, CTA `rank` of a
-// group owns column slice `rank`, and group g takes token ranges g, g + G,
-// g + 2G, ... one after another.  A CTA's totals of a chunk's 16 row sums go
-// to its own exchange record in global memory, slot s mod 2 for the chunk's
-// running index s, each value in one 64-bit word {sequence s + 1, value}; one
-// warp of a reader polls the C records of its group until every word carries
-// the sequence it wants, adds
-// the C values in rank order, so every CTA of the group forms the same total.
-// The host clears the records before the launch, and a word is written and
-// read whole, so a reader never pairs a stale value with a new sequence.
-// Unlike a thread-block cluster the group need not sit in one GPC: at d = 7168
-// 21 groups of 7 CTAs fill 147 SMs where clusters of 8 packed onto 120.
+// The exchange, two ways (kGroups).  A CTA's totals of a chunk's 16 row sums
+// reach every CTA of its token row, and each adds the C values in rank order,
+// so all form the same total.
+//  * Clusters: CTA `rank` of a thread-block cluster owns column slice `rank`,
+//    one cluster per token range; the last phase-1 warp to hand in stores the
+//    CTA's totals into slot `rank` of every CTA's shared memory with
+//    `st.async`, completing on that CTA's exchange mbarrier.
+//  * Groups: the launch is cooperative (every CTA resident at once, one per
+//    SM); CTAs g*C .. g*C + C - 1 form group g and take token ranges g, g + G,
+//    g + 2G, ... one after another.  The totals go to the CTA's own exchange
+//    record in global memory, slot s mod 2 for the chunk's running index s,
+//    each value in one 64-bit word {sequence s + 1, value}; the first phase-2
+//    warp of each CTA polls its group's C records until every word carries
+//    the sequence it wants and leaves the totals in shared memory for the
+//    others.  The host clears the records before the launch, and a word is
+//    written and read whole, so a reader never pairs a stale value with a new
+//    sequence.  Unlike a cluster the group need not sit in one GPC: at
+//    d = 7168 21 groups of 7 CTAs fill 147 SMs where clusters of 8 packed
+//    onto 120.
 //
 // Ordering: phase-1 warps hand in chunk s only after this CTA's phase-2 warps
 // have read the totals of chunk s - 1 (barrier `tread`).  Those totals are
-// complete only once every CTA of the group has handed in s - 1, which each
-// did after its own phase-2 warps had read chunk s - 2; so a record slot
-// (shared by chunks s and s - 2) has been read by the whole group before it is
+// complete only once every CTA of the row has handed in s - 1, which each
+// did after its own phase-2 warps had read chunk s - 2; so an exchange slot
+// (shared by chunks s and s - 2) has been read by the whole row before it is
 // rewritten, and phase 1 never runs more than two chunks ahead, so three t1
 // slots suffice.  The ring completes per chunk of four streamed tokens (one
 // mbarrier per chunk slot); phase-2 warps release a chunk's stages once they
